@@ -1,0 +1,78 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check that a pin catches each.
+
+Every mutation is applied with monkeypatch to a copy of one oracle function and
+one pin test body is re-run; the pin must fail.  This shows the pins are not
+vacuous: a dropped term, a wrong rounding, a transposed operand or a sign on the
+wrong side would not slip through.
+"""
+import numpy as np
+import pytest
+
+from oracle import quant, attention, output, rotations
+import test_oracle_quant as tq
+import test_oracle_attention as ta
+import test_oracle_output as to
+import test_oracle_rotations as tr
+
+
+def _floor_quantize(x, clip):
+    x = np.asarray(x, np.float64)
+    lo, hi = clip * x.min(-1), clip * x.max(-1)
+    s = quant.fp16_rne((hi - lo) / 3)
+    z = quant.fp16_rne(lo)
+    c = np.clip(np.floor((x - z[..., None]) / np.where(s > 0, s, 1)[..., None]), 0, 3).astype(np.uint8)
+    return c, s, z
+
+
+def _unrounded_scale_quantize(x, clip):
+    x = np.asarray(x, np.float64)
+    lo, hi = clip * x.min(-1), clip * x.max(-1)
+    s_exact = (hi - lo) / 3
+    z = quant.fp16_rne(lo)
+    c = np.clip(np.rint((x - z[..., None]) / np.where(s_exact > 0, s_exact, 1)[..., None]), 0, 3).astype(np.uint8)
+    return c, quant.fp16_rne(s_exact), z
+
+
+def _msb_first_pack(codes):
+    c4 = np.asarray(codes, np.uint32).reshape(codes.shape[:-1] + (32, 4))
+    return (c4[..., 3] | (c4[..., 2] << 2) | (c4[..., 1] << 4) | (c4[..., 0] << 6)).astype(np.uint8)
+
+
+def _no_scale_softmax_decode(q, k_hat, v_hat, r_k, gqa):
+    qr = attention.rotate_queries(q, r_k, gqa)
+    return np.stack([attention.softmax(k_hat[:, j // gqa] @ qr[j]) @ v_hat[:, j // gqa] for j in range(len(qr))])
+
+
+def _transposed_fold(w_o, r_v, gqa):
+    w = np.asarray(w_o, np.float64).copy()
+    for j in range(w.shape[1] // 128):
+        w[:, j * 128:(j + 1) * 128] = w[:, j * 128:(j + 1) * 128] @ r_v[j // gqa].T
+    return w
+
+
+def _output_side_signs(signs):
+    s = np.asarray(signs, np.float64)
+    return rotations.sylvester_hadamard(len(s)) * s[None, :] / np.sqrt(len(s))
+
+
+MUTATIONS = [
+    ("floor instead of round", quant, "quantize_groups", _floor_quantize,
+     lambda: tq.test_codes_equal_nearest_level_brute_force(1.0)),
+    ("codes from the unrounded scale", quant, "quantize_groups", _unrounded_scale_quantize,
+     lambda: [tq.test_hand_worked_groups(e) for e in tq._golden()]),
+    ("reversed bit order", quant, "pack_codes", _msb_first_pack,
+     lambda: [tq.test_hand_worked_groups(e) for e in tq._golden()]),
+    ("missing 1/sqrt(d)", attention, "decode_attention", _no_scale_softmax_decode,
+     ta.test_decode_attention_matches_brute_force_loops),
+    ("W_O folded with R^T", output, "fold_wo", _transposed_fold,
+     to.test_folded_wo_reproduces_unrotated_output),
+    ("signs on the output side", rotations, "signed_hadamard", _output_side_signs,
+     tr.test_signed_hadamard_orthogonal_and_equals_fwht_of_signed_input),
+]
+
+
+@pytest.mark.parametrize("name,module,attr,bad,pin", MUTATIONS, ids=[m[0] for m in MUTATIONS])
+def test_pin_catches_planted_mistake(monkeypatch, name, module, attr, bad, pin):
+    monkeypatch.setattr(module, attr, bad)
+    with pytest.raises(AssertionError):
+        pin()
