@@ -1,0 +1,219 @@
+/*
+ * kvq.h -- C ABI of libkvq: rotated INT2 KV-cache attention on NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow "Output-Aware Rotation for INT2 KV-Cache Quantization"
+ * (OptR) and the "Output-aware INT2 KV-cache rotation evaluation" page:
+ *
+ *   write path   keys are centred by a per-channel mean mu (§4.1, Eq. 19), rotated
+ *                per KV head (k - mu) R_K = k R_K - mu R_K (Eq. 20), values rotated
+ *                v R_V (Eq. 27), then quantized per token in groups of 128 channels
+ *                to 4 levels (§3.1 Eq. 4, §5 implementation details, Table A) and
+ *                packed into a paged cache.
+ *   read path    q is rotated once, q R_K (Eqs. 21-22, 26); scores, softmax and the
+ *                value readout run straight off the packed pages; the readout stays
+ *                in the rotated-V basis o' = o R_V (Eq. 27) and meets the folded
+ *                W_O-bar_j = W_O,j R_V,h(j) (Eqs. 29-31) in the output projection.
+ *   calibration  post-W_O NMSE (Eq. 10) of every candidate rotation x clip ratio,
+ *                as in the evaluation page's candidate search.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller unless the
+ *     argument says "host".  The library never allocates device memory; calls
+ *     that need scratch take a caller-provided workspace sized by the matching
+ *     *_workspace_size function.
+ *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
+ *     and performs no implicit synchronisation, except kvq_device_check.
+ *   - Every tensor is dense, row-major, with the shapes given below.  Pointers
+ *     must be 16-byte aligned; otherwise KVQ_EINVAL.
+ *   - head_dim must be 128 (the group size of the method); anything else returns
+ *     KVQ_EUNSUPPORTED.  There is no fallback path of any kind.
+ *   - A non-OK status leaves outputs unspecified; kvq_last_error() returns a
+ *     thread-local, human-readable reason.
+ *   - Data-dependent indices that cannot be checked on the host without a
+ *     synchronisation (block-table entries, sequence lengths) are bounds-checked
+ *     in the kernels: an out-of-range entry is skipped and recorded in a device
+ *     error word, which kvq_device_check() reads back as KVQ_EDEVICE_FLAG.
+ */
+#ifndef KVQ_H
+#define KVQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t. */
+typedef struct CUstream_st* kvq_stream;
+
+typedef enum {
+  KVQ_OK = 0,
+  KVQ_EINVAL = -1,        /* bad argument: null pointer, bad shape, misalignment, bad clip */
+  KVQ_EUNSUPPORTED = -2,  /* valid request outside what is implemented (head_dim != 128, ...) */
+  KVQ_ECUDA = -3,         /* a CUDA runtime call failed (launch error, no device, ...) */
+  KVQ_EDEVICE_FLAG = -4   /* a kernel met an out-of-range block-table entry or length */
+} kvq_status;
+
+typedef enum {
+  KVQ_ROT_IDENTITY = 0,         /* R = I */
+  KVQ_ROT_SIGNED_HADAMARD = 1,  /* R_h = diag(s_h) H_128 / sqrt(128), H Sylvester-ordered */
+  KVQ_ROT_DENSE = 2             /* R_h given explicitly (e.g. exp(A - A^T), OptR Eq. 11) */
+} kvq_rot_kind;
+
+typedef enum {
+  KVQ_F32 = 0,
+  KVQ_BF16 = 1
+} kvq_dtype;
+
+/* One orthogonal rotation per KV head.  A row vector x is rotated as x R_h.
+ *   signs: [n_heads][128] float, each +1 or -1       (KVQ_ROT_SIGNED_HADAMARD)
+ *   dense: [n_heads][128][128] float, R_h[c][d] at c*128 + d, row = input channel
+ *                                                      (KVQ_ROT_DENSE)
+ * Unused pointers may be NULL. */
+typedef struct {
+  int kind;             /* kvq_rot_kind */
+  const float* signs;
+  const float* dense;
+} kvq_rot;
+
+/* Paged cache geometry.
+ * The pool is uint8 [num_blocks][n_kv_heads][72 * page_tokens]: one record per
+ * (physical page, KV head), laid out as
+ *   [0, 32P)     K codes: token slot o at 32*o, 128 two-bit codes, channel i in
+ *                byte i/4 at bits 2*(i%4)
+ *   [32P, 64P)   V codes, same layout
+ *   [64P, 68P)   K meta: slot o at 64P + 4*o = fp16 scale, fp16 zero
+ *   [68P, 72P)   V meta
+ * Position pos of sequence b lives in page block_table[b * max_blocks_per_seq + pos / P],
+ * slot pos % P.  A dequantized value is zero + scale * code. */
+typedef struct {
+  int head_dim;            /* must be 128 */
+  int page_tokens;         /* P: 8 or 16 */
+  int n_kv_heads;          /* H_kv >= 1 */
+  int n_q_heads;           /* H_q, a multiple of H_kv; query head j reads KV head j / (H_q/H_kv) */
+  int num_blocks;          /* physical pages in the pool */
+  int max_blocks_per_seq;  /* row stride of block_table */
+} kvq_layout;
+
+/* Size in bytes of the pool described by `layout`. */
+size_t kvq_pool_bytes(const kvq_layout* layout);
+
+/* Thread-local message describing the last non-OK status returned on this thread. */
+const char* kvq_last_error(void);
+
+/* Synchronise `stream`, then read and clear the device error word.
+ * KVQ_OK if no kernel recorded an out-of-range index since the last check,
+ * KVQ_EDEVICE_FLAG otherwise (the message names the first recorded error). */
+kvq_status kvq_device_check(kvq_stream stream);
+
+/* Key mean (OptR appendix, "Key-mean estimation and application", Eq. 19):
+ *   mu[h][c] = (1/n_tok) sum_t k[t][h][c]
+ * k: [n_tok][n_kv_heads][128] of dtype; mu: [n_kv_heads][128] float (written). */
+kvq_status kvq_key_mean(int n_tok, int n_kv_heads, const void* k, kvq_dtype dtype,
+                        float* mu, kvq_stream stream);
+
+/* Per-head rotation of row vectors (Eq. 20's precomputed mu R_K; Eq. 22's q R_K):
+ *   y[r][j] = x[r][j] R_{j / heads_per_rot}
+ * x, y: [n_rows][n_heads][128] float (may not alias); rot covers
+ * n_heads / heads_per_rot heads. */
+kvq_status kvq_rotate_heads(int n_rows, int n_heads, int heads_per_rot, const float* x,
+                            kvq_rot rot, float* y, kvq_stream stream);
+
+/* Quantize-append (OptR §6 "Efficiency Analysis" cache-write kernel; Eqs. 4, 20, 21, 27):
+ * for every new token t of sequence b at position pos = start_pos[b] + (t - cu_new[b]),
+ * and every KV head h,
+ *   x_K = k[t][h] R_K,h - mu_rot_k[h]      (= (k - mu) R_K; mu_rot_k NULL means mu = 0)
+ *   x_V = v[t][h] R_V,h
+ * each x is quantized as one group of 128: lo = c*min(x), hi = c*max(x),
+ * scale = fp16_rn((hi - lo)/3), zero = fp16_rn(lo),
+ * code = clamp(rint((x - zero)/scale), 0, 3) (code 0 where scale == 0),
+ * and written to the token's page slot (see kvq_layout).
+ *   k, v:        [n_new_total][n_kv_heads][128] of dtype
+ *   cu_new:      int32 [n_seqs + 1], cu_new[0] = 0, non-decreasing, cu_new[n_seqs] = n_new_total
+ *   start_pos:   int32 [n_seqs]
+ *   block_table: int32 [n_seqs][max_blocks_per_seq]
+ *   mu_rot_k:    float [n_kv_heads][128] or NULL
+ *   clip_k, clip_v in (0, 1]
+ *   pool:        uint8, kvq_pool_bytes(layout) bytes, written in place
+ * Pages referenced by an out-of-range block-table entry or position are skipped
+ * and flagged (kvq_device_check). */
+kvq_status kvq_quantize_append(const kvq_layout* layout, int n_seqs, int n_new_total,
+                               const void* k, const void* v, kvq_dtype dtype,
+                               const int32_t* cu_new, const int32_t* start_pos,
+                               const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v,
+                               const float* mu_rot_k, float clip_k, float clip_v,
+                               uint8_t* pool, kvq_stream stream);
+
+/* Workspace bytes needed by kvq_decode_attention for this many sequences and
+ * splits (n_splits = 0: the count the library would choose for max_seq_len). */
+kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int max_seq_len,
+                                     int n_splits, size_t* bytes);
+
+/* Split-K decode attention straight off the packed cache (OptR Eqs. 1-2, 5, 22, 26, 27):
+ * for sequence b and query head j with KV head h = j / (H_q / H_kv),
+ *   q'_j   = q[b][j] R_K,h
+ *   a_s    = q'_j . (zero_s + scale_s * codeK_s) / sqrt(128),   s < seq_lens[b]
+ *   p      = softmax(a)
+ *   o_rot[b][j] = sum_s p_s (zero_s + scale_s * codeV_s)      (rotated-V basis)
+ * computed as n_splits partial softmaxes over contiguous page ranges merged by a
+ * log-sum-exp combine.  A sequence of length 0 yields a zero vector.
+ *   q:       [n_seqs][n_q_heads][128] of q_dtype
+ *   seq_lens int32 [n_seqs]; max_seq_len (host) >= every seq_lens[b]
+ *   o_rot:   float [n_seqs][n_q_heads][128] (written)
+ *   workspace: >= kvq_decode_workspace_size bytes, 16-byte aligned. */
+kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void* q,
+                                kvq_dtype q_dtype, const int32_t* seq_lens, int max_seq_len,
+                                const int32_t* block_table, kvq_rot rot_k, const uint8_t* pool,
+                                int n_splits, void* workspace, size_t workspace_bytes,
+                                float* o_rot, kvq_stream stream);
+
+/* W_O folding (OptR Eqs. 29-31): for query head j with KV head h = j / (H_q / H_kv),
+ *   w_folded[:, j*128:(j+1)*128] = w_o[:, j*128:(j+1)*128] R_V,h
+ * w_o: [d_model][n_q_heads*128] of w_dtype; w_folded: same shape, out_dtype
+ * (bf16 output is rounded to nearest even). */
+kvq_status kvq_fold_wo(int d_model, int n_q_heads, int n_kv_heads, const void* w_o,
+                       kvq_dtype w_dtype, kvq_rot rot_v, void* w_folded, kvq_dtype out_dtype,
+                       kvq_stream stream);
+
+/* Output projection (OptR Eqs. 3, 7, 31): y[r] = sum_k x[r][k] w[n][k] for n < d_model,
+ * i.e. y = x W^T with x = o_rot viewed as [n_rows][n_q_heads*128] and W = the folded W_O.
+ *   x: float [n_rows][k_dim]; w: [d_model][k_dim] of w_dtype; y: float [n_rows][d_model]. */
+kvq_status kvq_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
+                        kvq_dtype w_dtype, float* y, kvq_stream stream);
+
+/* Workspace bytes for kvq_calib_nmse. */
+kvq_status kvq_calib_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint,
+                                    size_t* bytes);
+
+/* Candidate x clip sweep scored by post-W_O NMSE ("Output-aware INT2 KV-cache rotation
+ * evaluation": candidate search on calibration queries; OptR Eq. 10 and the appendix
+ * calibration details: final query positions, per-KV-head selection).
+ * For candidate i (rotation R_i applied to the keys and values of every head) and
+ * clip ratio c (applied to both):
+ *   keys  k~ = Q_2((k - mu) R_i; c) (mu NULL: no centring),  values v~ = Q_2(v R_i; c)
+ *   queries at positions t = n_tok - n_qpos .. n_tok - 1, causal (s <= t), rotated by R_i
+ *   o~'   = attention readout (rotated basis), y~_h = sum_{j in G_h} o~'_j (W_O,j R_i)^T
+ *   y_h   = the same with unquantized, unrotated, uncentred k, v
+ *   nmse[i][c][h] = sum_t ||y~_h - y_h||^2 / ref[h],  ref[h] = sum_t ||y_h||^2
+ * With joint != 0 the outputs are summed over KV heads before the norms (one column).
+ *   q: [n_qpos][n_kv_heads*gqa][128]; k, v: [n_tok][n_kv_heads][128]   (dtype)
+ *   w_o: [d_model][n_kv_heads*gqa*128] (w_dtype, unfolded)
+ *   cand: HOST array of n_cand rotations (their signs/dense pointers are device pointers)
+ *   clips: HOST array of n_clip ratios in (0, 1]
+ *   mu: float [n_kv_heads][128] or NULL
+ *   nmse: double [n_cand][n_clip][joint ? 1 : n_kv_heads]; ref: double [joint ? 1 : n_kv_heads]
+ *   workspace: >= kvq_calib_workspace_size bytes.
+ * Selection (argmin) is left to the caller. */
+kvq_status kvq_calib_nmse(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model,
+                          const void* q, const void* k, const void* v, kvq_dtype dtype,
+                          const void* w_o, kvq_dtype w_dtype, int n_cand, const kvq_rot* cand,
+                          int n_clip, const float* clips, const float* mu, int joint,
+                          double* nmse, double* ref, void* workspace, size_t workspace_bytes,
+                          kvq_stream stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H */

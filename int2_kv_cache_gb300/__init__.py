@@ -1,0 +1,212 @@
+"""Python binding of libkvq (rotated INT2 KV-cache attention for GB300).
+
+Argument marshalling only: every computation runs in the CUDA kernels of
+``libkvq.so`` behind the C ABI declared in ``include/kvq.h``.  PyTorch supplies
+device memory and streams.  There is no CPU path: if the library has not been
+built, importing the binding functions raises.
+
+Functions carry the C names (``kvq_quantize_append``, ``kvq_decode_attention``,
+``kvq_out_proj``, ``kvq_calib_nmse`` and helpers) and take torch tensors.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from ._build import LIB as LIB_PATH
+
+KVQ_OK, KVQ_EINVAL, KVQ_EUNSUPPORTED, KVQ_ECUDA, KVQ_EDEVICE_FLAG = 0, -1, -2, -3, -4
+ROT_KIND = {"identity": 0, "signed_hadamard": 1, "dense": 2}
+KVQ_F32, KVQ_BF16 = 0, 1
+HEAD_DIM = 128
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"kvq status {status}: {message}")
+        self.status = status
+
+
+class KvqLayout(ctypes.Structure):
+    _fields_ = [("head_dim", ctypes.c_int), ("page_tokens", ctypes.c_int),
+                ("n_kv_heads", ctypes.c_int), ("n_q_heads", ctypes.c_int),
+                ("num_blocks", ctypes.c_int), ("max_blocks_per_seq", ctypes.c_int)]
+
+
+class KvqRot(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int), ("signs", ctypes.c_void_p), ("dense", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load libkvq.so (built in-tree by ``_build.build()``); raise if it is missing."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"libkvq.so not built ({LIB_PATH}); run __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        vp, i, f, st, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
+        lp = ctypes.POINTER(KvqLayout)
+        sigs = {
+            "kvq_last_error": ([], ctypes.c_char_p),
+            "kvq_pool_bytes": ([lp], sz),
+            "kvq_device_check": ([vp], st),
+            "kvq_key_mean": ([i, i, vp, i, vp, vp], st),
+            "kvq_rotate_heads": ([i, i, i, vp, KvqRot, vp, vp], st),
+            "kvq_quantize_append": ([lp, i, i, vp, vp, i, vp, vp, vp, KvqRot, KvqRot, vp, f, f, vp, vp], st),
+            "kvq_decode_workspace_size": ([lp, i, i, i, ctypes.POINTER(sz)], st),
+            "kvq_decode_attention": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, sz, vp, vp], st),
+            "kvq_fold_wo": ([i, i, i, vp, i, KvqRot, vp, i, vp], st),
+            "kvq_out_proj": ([i, i, i, vp, vp, i, vp, vp], st),
+            "kvq_calib_workspace_size": ([i, i, i, i, i, ctypes.POINTER(sz)], st),
+            "kvq_calib_nmse": ([i, i, i, i, i, vp, vp, vp, i, vp, i, i, ctypes.POINTER(KvqRot), i,
+                                ctypes.POINTER(ctypes.c_float), vp, i, vp, vp, vp, sz, vp], st),
+        }
+        for name, (argtypes, restype) in sigs.items():
+            fn = getattr(L, name)
+            fn.argtypes = argtypes
+            fn.restype = restype
+        _lib = L
+    return _lib
+
+
+EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mean", "kvq_rotate_heads",
+            "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_fold_wo",
+            "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse")
+
+
+def _check(status: int) -> None:
+    if status != KVQ_OK:
+        raise KvqError(status, lib().kvq_last_error().decode())
+
+
+def _ptr(t) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return getattr(stream, "cuda_stream", stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+    if t.dtype == torch.float32:
+        return KVQ_F32
+    if t.dtype == torch.bfloat16:
+        return KVQ_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _contig(t, name):
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+class DeviceRot:
+    """A rotation spec with its device tensors kept alive."""
+
+    def __init__(self, kind: str, signs=None, dense=None):
+        self.kind = kind
+        self.signs = signs
+        self.dense = dense
+
+    @classmethod
+    def from_spec(cls, rot, device="cuda"):
+        import torch
+        s = torch.as_tensor(rot.signs, dtype=torch.float32, device=device).contiguous() if rot.signs is not None else None
+        d = torch.as_tensor(rot.dense, dtype=torch.float32, device=device).contiguous() if rot.dense is not None else None
+        return cls(rot.kind, s, d)
+
+    @property
+    def c(self) -> KvqRot:
+        return KvqRot(ROT_KIND[self.kind], _ptr(self.signs), _ptr(self.dense))
+
+
+def make_layout(page_tokens: int, n_kv_heads: int, n_q_heads: int, num_blocks: int,
+                max_blocks_per_seq: int) -> KvqLayout:
+    return KvqLayout(HEAD_DIM, page_tokens, n_kv_heads, n_q_heads, num_blocks, max_blocks_per_seq)
+
+
+def kvq_pool_bytes(layout: KvqLayout) -> int:
+    return int(lib().kvq_pool_bytes(ctypes.byref(layout)))
+
+
+def kvq_device_check(stream=None) -> None:
+    _check(lib().kvq_device_check(_stream(stream)))
+
+
+def kvq_key_mean(k, mu, stream=None) -> None:
+    n_tok, h, d = k.shape
+    _check(lib().kvq_key_mean(n_tok, h, _ptr(_contig(k, "k")), _dtype_code(k), _ptr(mu), _stream(stream)))
+
+
+def kvq_rotate_heads(x, rot: DeviceRot, y, heads_per_rot: int = 1, stream=None) -> None:
+    n_rows, n_heads, _ = x.shape
+    _check(lib().kvq_rotate_heads(n_rows, n_heads, heads_per_rot, _ptr(_contig(x, "x")), rot.c, _ptr(y),
+                                  _stream(stream)))
+
+
+def kvq_quantize_append(layout: KvqLayout, k, v, cu_new, start_pos, block_table, rot_k: DeviceRot,
+                        rot_v: DeviceRot, mu_rot_k, clip_k: float, clip_v: float, pool, stream=None) -> None:
+    n_new = k.shape[0]
+    n_seqs = start_pos.shape[0]
+    _check(lib().kvq_quantize_append(ctypes.byref(layout), n_seqs, n_new, _ptr(_contig(k, "k")),
+                                     _ptr(_contig(v, "v")), _dtype_code(k), _ptr(cu_new), _ptr(start_pos),
+                                     _ptr(block_table), rot_k.c, rot_v.c, _ptr(mu_rot_k), clip_k, clip_v,
+                                     _ptr(pool), _stream(stream)))
+
+
+def kvq_decode_workspace_size(layout: KvqLayout, n_seqs: int, max_seq_len: int, n_splits: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().kvq_decode_workspace_size(ctypes.byref(layout), n_seqs, max_seq_len, n_splits, ctypes.byref(out)))
+    return int(out.value)
+
+
+def kvq_decode_attention(layout: KvqLayout, q, seq_lens, max_seq_len: int, block_table, rot_k: DeviceRot,
+                         pool, workspace, o_rot, n_splits: int = 0, stream=None) -> None:
+    n_seqs = q.shape[0]
+    _check(lib().kvq_decode_attention(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _dtype_code(q),
+                                      _ptr(seq_lens), max_seq_len, _ptr(block_table), rot_k.c, _ptr(pool),
+                                      n_splits, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                      _ptr(o_rot), _stream(stream)))
+
+
+def kvq_fold_wo(w_o, n_q_heads: int, n_kv_heads: int, rot_v: DeviceRot, w_folded, stream=None) -> None:
+    d_model = w_o.shape[0]
+    _check(lib().kvq_fold_wo(d_model, n_q_heads, n_kv_heads, _ptr(_contig(w_o, "w_o")), _dtype_code(w_o),
+                             rot_v.c, _ptr(w_folded), _dtype_code(w_folded), _stream(stream)))
+
+
+def kvq_out_proj(x, w, y, stream=None) -> None:
+    n_rows, k_dim = x.shape[0], x.numel() // max(1, x.shape[0])
+    d_model = w.shape[0]
+    _check(lib().kvq_out_proj(n_rows, d_model, k_dim, _ptr(_contig(x, "x")), _ptr(_contig(w, "w")),
+                              _dtype_code(w), _ptr(y), _stream(stream)))
+
+
+def kvq_calib_workspace_size(n_tok: int, n_qpos: int, n_kv_heads: int, gqa: int, joint: bool) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().kvq_calib_workspace_size(n_tok, n_qpos, n_kv_heads, gqa, int(joint), ctypes.byref(out)))
+    return int(out.value)
+
+
+def kvq_calib_nmse(q, k, v, w_o, cands, clips, mu, joint: bool, nmse, ref, workspace, stream=None) -> None:
+    n_qpos, hq, _ = q.shape
+    n_tok, hkv, _ = k.shape
+    gqa = hq // hkv
+    d_model = w_o.shape[0]
+    rot_arr = (KvqRot * len(cands))(*[c.c for c in cands])
+    clip_arr = (ctypes.c_float * len(clips))(*[float(c) for c in clips])
+    _check(lib().kvq_calib_nmse(n_tok, n_qpos, hkv, gqa, d_model, _ptr(_contig(q, "q")), _ptr(_contig(k, "k")),
+                                _ptr(_contig(v, "v")), _dtype_code(k), _ptr(_contig(w_o, "w_o")), _dtype_code(w_o),
+                                len(cands), rot_arr, len(clips), clip_arr, _ptr(mu), int(joint), _ptr(nmse),
+                                _ptr(ref), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                _stream(stream)))

@@ -1,0 +1,103 @@
+// Internal helpers shared by the libkvq translation units (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "kvq.h"
+
+namespace kvq {
+
+constexpr int D = 128;            // head dimension = quantization group size
+constexpr int GROUP_BYTES = 32;   // 128 two-bit codes
+constexpr int META_BYTES = 4;     // fp16 scale + fp16 zero
+
+// Device error word bits (read back by kvq_device_check).
+enum : unsigned {
+  ERR_BLOCK_RANGE = 1u,   // block-table entry outside [0, num_blocks)
+  ERR_POS_RANGE = 2u,     // position beyond max_blocks_per_seq * page_tokens
+  ERR_SEQ_RANGE = 4u,     // cu_new / seq_lens inconsistent (negative, decreasing, too long)
+};
+
+struct RotDev {
+  int kind;
+  const float* signs;
+  const float* dense;
+};
+
+inline RotDev to_dev(const kvq_rot& r) { return RotDev{r.kind, r.signs, r.dense}; }
+
+struct PageGeom {
+  int page_tokens;
+  int n_kv_heads;
+  int num_blocks;
+  int max_blocks;
+  int record;  // 72 * page_tokens
+};
+
+__device__ __forceinline__ void flag_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// Load 4 consecutive channels (16-byte aligned for f32, 8-byte for bf16) as float.
+__device__ __forceinline__ float4 load4(const void* base, size_t elem, int dtype) {
+  if (dtype == KVQ_F32) {
+    return __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(base) + elem));
+  }
+  uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(base) + elem));
+  float4 r;
+  r.x = __uint_as_float(w.x << 16);
+  r.y = __uint_as_float(w.x & 0xFFFF0000u);
+  r.z = __uint_as_float(w.y << 16);
+  r.w = __uint_as_float(w.y & 0xFFFF0000u);
+  return r;
+}
+
+__device__ __forceinline__ float load1(const void* base, size_t elem, int dtype) {
+  if (dtype == KVQ_F32) return __ldg(static_cast<const float*>(base) + elem);
+  return __bfloat162float(static_cast<const __nv_bfloat16*>(base)[elem]);
+}
+
+}  // namespace kvq
+
+// ---- launchers implemented in the kernel translation units (C++ linkage, internal) ----
+namespace kvq {
+
+// quantize.cu
+cudaError_t launch_key_mean(int n_tok, int n_heads, const void* k, int dtype, float* mu,
+                            cudaStream_t s);
+cudaError_t launch_rotate_heads(int n_rows, int n_heads, int heads_per_rot, const float* x,
+                                RotDev rot, float* y, bool transpose, cudaStream_t s);
+cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* src,
+                                   int dtype, const int32_t* cu_new, const int32_t* start_pos,
+                                   const int32_t* table, RotDev rot, const float* mu_rot,
+                                   float clip, int codes_off, int meta_off, uint8_t* pool,
+                                   unsigned* err, cudaStream_t s);
+cudaError_t launch_quant_dequant(int n_groups, const float* x, float clip, float* out,
+                                 cudaStream_t s);
+
+// decode.cu
+int decode_auto_splits(int n_seqs, int n_kv_heads, int max_seq_len, int page_tokens);
+size_t decode_workspace_bytes(int n_seqs, int n_q_heads, int n_splits);
+cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q,
+                          int q_dtype, const int32_t* seq_lens, int max_seq_len,
+                          const int32_t* table, RotDev rot_k, const uint8_t* pool, int n_splits,
+                          void* ws, float* o_rot, unsigned* err, cudaStream_t s);
+
+// outproj.cu
+cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, int w_dtype,
+                           RotDev rot_v, void* out, int out_dtype, cudaStream_t s);
+cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
+                            int w_dtype, float* y, cudaStream_t s);
+
+// calib.cu
+size_t calib_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint);
+cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model,
+                         const void* q, const void* k, const void* v, int dtype, const void* w_o,
+                         int w_dtype, int n_cand, const kvq_rot* cand, int n_clip,
+                         const float* clips, const float* mu, int joint, double* nmse,
+                         double* ref, void* ws, cudaStream_t s);
+
+}  // namespace kvq

@@ -1,0 +1,155 @@
+"""The C-ABI library loads, exports every entry point declared in include/kvq.h,
+and its host-side validation rejects bad arguments before touching the GPU.
+No kernel is launched here (these run without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+H = os.path.join(ROOT, "include", "kvq.h")
+
+
+@pytest.fixture(scope="module")
+def kvq():
+    from int2_kv_cache_gb300 import _build
+    _build.build()
+    import int2_kv_cache_gb300 as m
+    m.lib()
+    return m
+
+
+def declared_functions():
+    text = open(H).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_every_declared_symbol_is_exported(kvq):
+    names = declared_functions()
+    assert len(names) >= 12
+    lib = kvq.lib()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(kvq.EXPORTED) | {"kvq_last_error"}
+
+
+def test_binding_names_match_c_names(kvq):
+    for n in kvq.EXPORTED:
+        if n in ("kvq_last_error",):
+            continue
+        assert callable(getattr(kvq, n)), n
+
+
+def _layout(kvq, **kw):
+    d = dict(page_tokens=16, n_kv_heads=8, n_q_heads=32, num_blocks=100, max_blocks_per_seq=10)
+    d.update(kw)
+    lay = kvq.make_layout(**d)
+    return lay
+
+
+def test_pool_bytes(kvq):
+    lay = _layout(kvq, num_blocks=256, n_kv_heads=4, n_q_heads=4)
+    assert kvq.kvq_pool_bytes(lay) == 256 * 4 * 1152
+    lay8 = _layout(kvq, page_tokens=8, num_blocks=3, n_kv_heads=2, n_q_heads=2)
+    assert kvq.kvq_pool_bytes(lay8) == 3 * 2 * 576
+
+
+def test_decode_workspace_size(kvq):
+    lay = _layout(kvq)
+    assert kvq.kvq_decode_workspace_size(lay, 16, 160, 5) == 16 * 32 * 5 * 130 * 4
+    auto = kvq.kvq_decode_workspace_size(lay, 16, 160, 0)
+    assert auto % (16 * 32 * 130 * 4) == 0 and auto > 0
+
+
+def _status(kvq, fn, *args):
+    return fn(*args)
+
+
+def test_unsupported_head_dim_and_page_size(kvq):
+    lib = kvq.lib()
+    lay = _layout(kvq)
+    lay.head_dim = 64
+    out = ctypes.c_size_t(0)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(lay), 1, 16, 1, ctypes.byref(out)) == kvq.KVQ_EUNSUPPORTED
+    assert b"head_dim" in lib.kvq_last_error()
+    lay = _layout(kvq, page_tokens=32)
+    assert lib.kvq_decode_workspace_size(ctypes.byref(lay), 1, 16, 1, ctypes.byref(out)) == kvq.KVQ_EUNSUPPORTED
+    lay = _layout(kvq, n_q_heads=24)  # 3 query heads per KV head
+    assert lib.kvq_decode_workspace_size(ctypes.byref(lay), 1, 16, 1, ctypes.byref(out)) == kvq.KVQ_EUNSUPPORTED
+    lay = _layout(kvq, n_q_heads=12)  # not a multiple
+    assert lib.kvq_decode_workspace_size(ctypes.byref(lay), 1, 16, 1, ctypes.byref(out)) == kvq.KVQ_EINVAL
+
+
+def test_quantize_append_rejects_bad_arguments(kvq):
+    lib = kvq.lib()
+    lay = _layout(kvq)
+    ident = kvq.KvqRot(0, None, None)
+    fake = 0x10000  # aligned but never dereferenced: validation fails first
+    # bad clip
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, fake, fake, 0, fake, fake, fake, ident, ident, None,
+                                 1.5, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL and b"clip" in lib.kvq_last_error()
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, fake, fake, 0, fake, fake, fake, ident, ident, None,
+                                 0.0, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL
+    # null pointer
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, None, fake, 0, fake, fake, fake, ident, ident, None,
+                                 1.0, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL and b"k is NULL" in lib.kvq_last_error()
+    # misaligned pointer
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, fake + 4, fake, 0, fake, fake, fake, ident, ident, None,
+                                 1.0, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL and b"aligned" in lib.kvq_last_error()
+    # signed Hadamard without signs
+    bad = kvq.KvqRot(1, None, None)
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, fake, fake, 0, fake, fake, fake, bad, ident, None,
+                                 1.0, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL and b"signs" in lib.kvq_last_error()
+    # unknown rotation kind / dtype
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, fake, fake, 0, fake, fake, fake, kvq.KvqRot(7, None, None),
+                                 ident, None, 1.0, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 4, fake, fake, 5, fake, fake, fake, ident, ident, None,
+                                 1.0, 1.0, fake, None)
+    assert st == kvq.KVQ_EINVAL
+    # nothing to do is OK without touching any pointer
+    st = lib.kvq_quantize_append(ctypes.byref(lay), 1, 0, None, None, 0, None, None, None, ident, ident, None,
+                                 1.0, 1.0, None, None)
+    assert st == kvq.KVQ_OK
+
+
+def test_decode_rejects_bad_arguments(kvq):
+    lib = kvq.lib()
+    lay = _layout(kvq)
+    ident = kvq.KvqRot(0, None, None)
+    fake = 0x10000
+    # max_seq_len beyond the block table
+    st = lib.kvq_decode_attention(ctypes.byref(lay), 1, fake, 0, fake, 161, fake, ident, fake, 1, fake, 1 << 20,
+                                  fake, None)
+    assert st == kvq.KVQ_EINVAL
+    # workspace too small
+    st = lib.kvq_decode_attention(ctypes.byref(lay), 2, fake, 0, fake, 160, fake, ident, fake, 4, fake, 16, fake, None)
+    assert st == kvq.KVQ_EINVAL and b"workspace" in lib.kvq_last_error()
+    # zero sequences is a no-op
+    assert lib.kvq_decode_attention(ctypes.byref(lay), 0, None, 0, None, 0, None, ident, None, 0, None, 0, None,
+                                    None) == kvq.KVQ_OK
+
+
+def test_calib_rejects_bad_arguments(kvq):
+    lib = kvq.lib()
+    fake = 0x10000
+    rots = (kvq.KvqRot * 1)(kvq.KvqRot(0, None, None))
+    clips = (ctypes.c_float * 2)(1.0, 1.2)
+    st = lib.kvq_calib_nmse(64, 4, 2, 2, 128, fake, fake, fake, 0, fake, 0, 1, rots, 2, clips, None, 0, fake, fake,
+                            fake, 1 << 30, None)
+    assert st == kvq.KVQ_EINVAL and b"clip" in lib.kvq_last_error()
+    clips = (ctypes.c_float * 1)(1.0)
+    st = lib.kvq_calib_nmse(20000, 4, 2, 2, 128, fake, fake, fake, 0, fake, 0, 1, rots, 1, clips, None, 0, fake, fake,
+                            fake, 1 << 30, None)
+    assert st == kvq.KVQ_EUNSUPPORTED
+    out = ctypes.c_size_t(0)
+    assert lib.kvq_calib_workspace_size(64, 65, 2, 2, 0, ctypes.byref(out)) == kvq.KVQ_EINVAL
+    assert lib.kvq_calib_workspace_size(64, 4, 2, 2, 0, ctypes.byref(out)) == kvq.KVQ_OK and out.value > 0
