@@ -1,0 +1,508 @@
+#!/usr/bin/env python3
+"""Benchmark of the rotated INT2 KV-cache decode step on GB300.
+
+Workload (default, the 32K-context configuration): 8B-class GQA layer, 32 query
+heads / 8 KV heads, head dim 128, hidden 4096, bf16 inputs, 16 sequences x
+32,768 tokens in a paged INT2 cache (16-token pages, shuffled block table),
+per-head dense learned-style rotations R = expm(A - A^T), key mean subtracted.
+
+One step = the whole hot path for one decode token of every sequence:
+  1. kvq_quantize_append  -- rotate, centre, clip, quantize, pack and write the new
+                              token's K and V (positions 32,767)
+  2. kvq_decode_attention -- rotated query, split-K attention over 32,768 packed
+                              tokens, log-sum-exp combine
+  3. kvq_out_proj         -- y = o' W_O-bar^T with R_V folded into W_O
+value = sequences x steps / time (decode tokens per second, one layer).
+
+--impl reference times the fp64 oracle (CPU) on a bounded sample of the same
+workload.  --case append_chunk / calib time the 4,096-token prefill append and
+the calibration sweep instead (for profiling; not the headline line).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "INT2 decode attention: KV-cache GB/s read (% of HBM peak), tokens/s at 32K ctx"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    p.add_argument("--case", choices=["decode_step", "append_chunk", "calib"], default="decode_step")
+    p.add_argument("--seqs", type=int, default=16)
+    p.add_argument("--ctx", type=int, default=32768)
+    p.add_argument("--splits", type=int, default=0)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-clocks", action="store_true")
+    return p.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class Clocks:
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, enabled: bool = True):
+        self.proc = None
+        self.gpu = gpu_index
+        if enabled:
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", "200"],
+                                             stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except Exception:
+                self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def traffic_record(kernel_file: str, key: str):
+    """Per-launch DRAM traffic from a committed ncu summary, valid only while the
+    kernel source is unchanged (the summary stores the source's sha256)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    src = os.path.join(ROOT, "int2_kv_cache_gb300", "csrc", kernel_file)
+    try:
+        digest = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        for line in open(path):
+            f = line.split()
+            if len(f) >= 3 and f[0] == key and f[2] == digest:
+                return float(f[1])
+    except OSError:
+        pass
+    return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def gen_parallel(fn, n):
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4)) as ex:
+        return list(ex.map(fn, range(n)))
+
+
+class DecodeStep:
+    """The decode-step workload resident on one GPU."""
+
+    def __init__(self, n_seqs: int, ctx: int, splits: int, device: str):
+        import torch
+        import int2_kv_cache_gb300 as kvq
+        from int2_kv_cache_gb300 import workloads as W
+
+        self.torch, self.kvq, self.dev = torch, kvq, device
+        c = W.gqa8b_32k(n_seqs=n_seqs, ctx=ctx)
+        self.case = c
+        self.B, self.L, self.hq, self.hkv, self.dm = n_seqs, ctx, c.n_q_heads, c.n_kv_heads, c.d_model
+        bf = torch.bfloat16
+        t = lambda x, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(device).to(dt)
+        self.t = t
+        self.layout = kvq.make_layout(c.page_tokens, c.n_kv_heads, c.n_q_heads, c.num_blocks, c.block_table.shape[1])
+        self.table = t(c.block_table, torch.int32)
+        self.rot_k = kvq.DeviceRot.from_spec(c.rot_k, device)
+        self.rot_v = kvq.DeviceRot.from_spec(c.rot_v, device)
+        # key mean (Eq. 19) and its rotation (Eq. 20), on the GPU
+        mu = torch.empty(c.n_kv_heads, 128, device=device)
+        kvq.kvq_key_mean(t(c.calibration_keys(), bf), mu)
+        self.mu_rot = torch.empty_like(mu)
+        kvq.kvq_rotate_heads(mu.reshape(1, c.n_kv_heads, 128), self.rot_k, self.mu_rot.reshape(1, c.n_kv_heads, 128))
+        # paged cache: positions 0 .. L-2 are history; every step writes position L-1
+        self.pool = torch.zeros(kvq.kvq_pool_bytes(self.layout), dtype=torch.uint8, device=device)
+        hist = ctx - 1
+        for b0 in range(0, n_seqs, 4):
+            kvs = gen_parallel(lambda i: c.kv(b0 + i), min(4, n_seqs - b0))
+            for i, (k, v) in enumerate(kvs):
+                b = b0 + i
+                kvq.kvq_quantize_append(self.layout, t(k[:hist], bf), t(v[:hist], bf), t(np.array([0, hist]), torch.int32),
+                                        t(np.array([0]), torch.int32), self.table[b:b + 1].contiguous(), self.rot_k,
+                                        self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
+        torch.cuda.synchronize()
+        kvq.kvq_device_check()
+        # folded W_O (Eqs. 29-31), bf16
+        self.w_fold = torch.empty(self.dm, self.hq * 128, dtype=bf, device=device)
+        kvq.kvq_fold_wo(t(c.w_o(), bf), self.hq, self.hkv, self.rot_v, self.w_fold)
+        # step inputs
+        kn, vn = zip(*[c.new_kv(b, 1) for b in range(n_seqs)])
+        self.host_q = torch.from_numpy(c.queries()).to(bf).pin_memory()
+        self.host_k = torch.from_numpy(np.concatenate(kn)).to(bf).pin_memory()
+        self.host_v = torch.from_numpy(np.concatenate(vn)).to(bf).pin_memory()
+        self.q = self.host_q.to(device)
+        self.k_new = self.host_k.to(device)
+        self.v_new = self.host_v.to(device)
+        self.cu_new = t(np.arange(n_seqs + 1), torch.int32)
+        self.start = t(np.full(n_seqs, hist), torch.int32)
+        self.lens = t(np.full(n_seqs, ctx), torch.int32)
+        self.splits = splits
+        ws = kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, splits)
+        self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.n_splits_used = ws // (n_seqs * self.hq * 130 * 4)
+        self.o = torch.empty(n_seqs, self.hq, 128, device=device)
+        self.y = torch.empty(n_seqs, self.dm, device=device)
+        self.host_y = torch.empty(n_seqs, self.dm).pin_memory()
+        self.launches_per_step = 2 + 2 + 1
+
+    def step(self, ev=None):
+        kvq = self.kvq
+        c = self.case
+        if ev is not None:
+            ev[0].record()
+        kvq.kvq_quantize_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.table, self.rot_k,
+                                self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
+        if ev is not None:
+            ev[1].record()
+        kvq.kvq_decode_attention(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.pool, self.ws,
+                                 self.o, n_splits=self.splits)
+        if ev is not None:
+            ev[2].record()
+        kvq.kvq_out_proj(self.o.reshape(self.B, -1), self.w_fold, self.y)
+        if ev is not None:
+            ev[3].record()
+
+    def step_e2e(self):
+        self.q.copy_(self.host_q, non_blocking=True)
+        self.k_new.copy_(self.host_k, non_blocking=True)
+        self.v_new.copy_(self.host_v, non_blocking=True)
+        self.step()
+        self.host_y.copy_(self.y, non_blocking=True)
+
+    def decode_bytes(self) -> dict:
+        B, L, hq, hkv = self.B, self.L, self.hq, self.hkv
+        s = self.n_splits_used
+        cache = B * L * hkv * 72
+        return {
+            "kv_cache": cache,
+            "q": B * hq * 128 * 2,
+            "block_table": B * ((L + 15) // 16) * 4,
+            "rotation": hkv * 128 * 128 * 4,
+            "partials_write_read": 2 * B * hq * s * 130 * 4,
+            "o_rot": B * hq * 128 * 4,
+        }
+
+
+def run_gpu(args):
+    import torch
+    from int2_kv_cache_gb300 import _build
+    _build.build()
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = f"cuda:{local}"
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    w = DecodeStep(args.seqs, args.ctx, args.splits, device)
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(args.warmup, 3)):
+        w.step()
+    barrier()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    clocks = Clocks(local, enabled=not args.no_clocks)
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    start.record(stream)
+    for i in range(args.steps):
+        w.step(evs[i])
+    stop.record(stream)
+    barrier()
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    t_app = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    t_out = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+
+    # end to end through the public API with host buffers
+    for _ in range(3):
+        w.step_e2e()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        w.step_e2e()
+    e1.record(stream)
+    barrier()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    w.kvq.kvq_device_check()
+
+    ms = torch.tensor([total_ms / args.steps, e2e_ms], device=device)
+    if world > 1:
+        torch.distributed.all_reduce(ms, op=torch.distributed.ReduceOp.MAX)
+    ms_step, e2e_step = float(ms[0]), float(ms[1])
+    if rank != 0:
+        return
+    peak, peak_kind = peaks()
+    by = w.decode_bytes()
+    alg = sum(by.values())
+    achieved = alg / (t_dec * 1e-3) / 1e9
+    traffic = traffic_record("decode.cu", "decode_step")
+    line = {
+        "metric": METRIC,
+        "value": world * w.B / (ms_step * 1e-3),
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic (seeded; bf16 q/K/V/W_O, 2-bit cache)",
+        "config": {
+            "workload": f"gqa8b decode step: B={w.B} x ctx {w.L}, Hq 32 / Hkv 8, d 128, hidden 4096, "
+                        "16-token pages (shuffled), dense expm(A-A^T) rotations, mu-centred keys, clip 1.0",
+            "batch": w.B, "ctx": w.L, "n_q_heads": w.hq, "n_kv_heads": w.hkv, "d_model": w.dm,
+            "n_splits": w.n_splits_used, "parallelism": f"replicas x{world}",
+            "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (w.pool.numel() / 1e6),
+        },
+        "kernel_ms": {"quantize_append": t_app, "decode_attention": t_dec, "out_proj": t_out},
+        "kv_cache_gbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9,
+        "kv_cache_pct_of_peak": {"measured": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / peak,
+                                 "nominal_8tbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / NOMINAL_HBM_GBS},
+        "roofline": {"kernel": "kvq_decode_attention (split + combine)", "bound": "hbm", "achieved": achieved,
+                     "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes": alg, "bytes": by},
+        "e2e": {"value": world * w.B / (e2e_step * 1e-3), "unit": "tokens/s",
+                "h2d_bytes_per_step": int(w.host_q.numel() * 2 + w.host_k.numel() * 2 + w.host_v.numel() * 2),
+                "d2h_bytes_per_step": int(w.host_y.numel() * 4)},
+        "gpu_launches": w.launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w.case, budget_s=12.0)
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline leg and --impl reference)
+# ---------------------------------------------------------------------------
+
+class OracleStep:
+    """The fp64 oracle doing one decode step for one sequence of the workload."""
+
+    def __init__(self, case, b: int = 0):
+        import oracle
+        self.o = oracle
+        c = case
+        self.c, self.b = c, b
+        self.r_k = oracle.rotations.rot_matrices(c.rot_k, c.n_kv_heads)
+        self.r_v = oracle.rotations.rot_matrices(c.rot_v, c.n_kv_heads)
+        self.mu = oracle.cache.key_mean(c.calibration_keys())
+        self.w_fold = oracle.output.fold_wo(c.w_o(), self.r_v, c.gqa)
+        k, v = c.kv(b)
+        self.L = int(c.seq_lens[b])
+        hist = self.L - 1
+        self.pool = np.zeros(oracle.cache.pool_bytes(c.num_blocks, c.n_kv_heads, c.page_tokens), np.uint8)
+        enc = oracle.cache.encode_tokens(k[:hist], v[:hist], self.r_k, self.r_v, self.mu, c.clip_k, c.clip_v)
+        oracle.cache.write_tokens(self.pool, c.n_kv_heads, c.page_tokens, c.block_table[b], 0, enc)
+        self.k_new, self.v_new = c.new_kv(b, 1)
+        self.q = c.queries()[b]
+
+    def step(self):
+        o, c = self.o, self.c
+        enc = o.cache.encode_tokens(self.k_new, self.v_new, self.r_k, self.r_v, self.mu, c.clip_k, c.clip_v)
+        o.cache.write_tokens(self.pool, c.n_kv_heads, c.page_tokens, c.block_table[self.b], self.L - 1, enc)
+        kh, vh = o.cache.dequantized_sequence(self.pool, c.n_kv_heads, c.page_tokens, c.block_table[self.b], self.L)
+        o_rot = o.attention.decode_attention(self.q, kh, vh, self.r_k, c.gqa)
+        return o.output.out_proj(o_rot, self.w_fold)
+
+
+def cpu_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(case, budget_s: float = 12.0) -> dict:
+    st = OracleStep(case, 0)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        st.step()
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or n >= 50:
+            break
+    return {"value": n / el, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{n} decode steps of sequence 0 of {case.n_seqs} (append 1 token, decode over "
+                      f"{int(case.seq_lens[0])} tokens, W_O) in numpy fp64; BLAS threads use the listed cores"}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    from int2_kv_cache_gb300 import workloads as W
+    case = W.gqa8b_32k(n_seqs=args.seqs, ctx=args.ctx)
+    st = OracleStep(case, 0)
+    for _ in range(max(args.warmup, 3)):
+        st.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        st.step()
+    el = time.perf_counter() - t0
+    value = args.steps / el
+    sample = f"each step = one decode step (append, decode over {args.ctx} tokens, W_O) of 1 of {args.seqs} sequences"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"gqa8b decode step: B={args.seqs} x ctx {args.ctx}, Hq 32 / Hkv 8, d 128, hidden 4096",
+                   "batch": args.seqs, "ctx": args.ctx},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Secondary cases (profiling only)
+# ---------------------------------------------------------------------------
+
+def run_append_chunk(args):
+    """4,096-token prefill append per sequence (4B-class layer, signed Hadamard, clip 0.9)."""
+    import torch
+    import int2_kv_cache_gb300 as kvq
+    from int2_kv_cache_gb300 import workloads as W
+    device = "cuda:0"
+    n_seq = 4
+    c = W.long4b_128k(n_seqs=n_seq, ctx=4096)
+    t = lambda x, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(device).to(dt)
+    lay = kvq.make_layout(16, 8, 32, c.num_blocks, c.block_table.shape[1])
+    pool = torch.zeros(kvq.kvq_pool_bytes(lay), dtype=torch.uint8, device=device)
+    kv = [c.kv(b) for b in range(n_seq)]
+    k = t(np.concatenate([x[0] for x in kv]), torch.bfloat16)
+    v = t(np.concatenate([x[1] for x in kv]), torch.bfloat16)
+    cu = t(np.arange(n_seq + 1) * 4096, torch.int32)
+    st = t(np.zeros(n_seq), torch.int32)
+    table = t(c.block_table, torch.int32)
+    rk, rv = kvq.DeviceRot.from_spec(c.rot_k, device), kvq.DeviceRot.from_spec(c.rot_v, device)
+    mu_rot = torch.zeros(8, 128, device=device)
+
+    def step():
+        kvq.kvq_quantize_append(lay, k, v, cu, st, table, rk, rv, mu_rot, c.clip_k, c.clip_v, pool)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    bytes_ = n_seq * 4096 * 8 * (2 * 256 + 72) + 8 * 128 * 4 * 2
+    peak, kind = peaks()
+    print(json.dumps({"case": "append_chunk", "ms": ms, "tokens": n_seq * 4096, "bytes": bytes_,
+                      "gbs": bytes_ / ms / 1e6, "frac": bytes_ / ms / 1e6 / peak, "peak_kind": kind}), flush=True)
+
+
+def run_calib(args):
+    import torch
+    import int2_kv_cache_gb300 as kvq
+    from int2_kv_cache_gb300 import workloads as W
+    device = "cuda:0"
+    cc = W.serve14b_calibration()
+    t = lambda x, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(device).to(dt)
+    bf = torch.bfloat16
+    mu = torch.empty(cc.n_kv_heads, 128, device=device)
+    kvq.kvq_key_mean(t(cc.k, bf), mu)
+    ws = torch.empty(kvq.kvq_calib_workspace_size(cc.n_tok, cc.n_qpos, cc.n_kv_heads, cc.gqa, False),
+                     dtype=torch.uint8, device=device)
+    nm = torch.empty(len(cc.cands), len(cc.clips), cc.n_kv_heads, dtype=torch.float64, device=device)
+    ref = torch.empty(cc.n_kv_heads, dtype=torch.float64, device=device)
+    cands = [kvq.DeviceRot.from_spec(x, device) for x in cc.cands]
+    q, k, v, w = t(cc.q, bf), t(cc.k, bf), t(cc.v, bf), t(cc.w_o, bf)
+
+    def step():
+        kvq.kvq_calib_nmse(q, k, v, w, cands, cc.clips, mu, False, nm, ref, ws)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    n = max(1, min(args.steps, 3))
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    print(json.dumps({"case": "calib", "ms": e0.elapsed_time(e1) / n, "candidates": len(cc.cands),
+                      "clips": len(cc.clips), "heads": cc.n_kv_heads}), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    elif args.case == "append_chunk":
+        run_append_chunk(args)
+    elif args.case == "calib":
+        run_calib(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -61,17 +61,27 @@ def key_mean(k_cal: np.ndarray) -> np.ndarray:
 def rotate_heads(x: np.ndarray, r: np.ndarray, heads_per_rot: int = 1) -> np.ndarray:
     """x [..., n_heads, 128] -> x_h @ R_{h // heads_per_rot} for every head."""
     x = np.asarray(x, np.float64)
-    n_heads = x.shape[-2]
-    idx = np.arange(n_heads) // heads_per_rot
-    return np.einsum("...hc,hcd->...hd", x, r[idx])
+    out = np.empty(x.shape, dtype=np.float64)
+    for h in range(x.shape[-2]):
+        out[..., h, :] = x[..., h, :] @ r[h // heads_per_rot]
+    return out
 
 
-def encode_tokens(k, v, r_k, r_v, mu, clip_k: float, clip_v: float) -> dict:
-    """Quantize new tokens k, v [T, H, 128] for the cache (Eqs. 19-21, 27)."""
+def encode_tokens(k, v, r_k, r_v, mu, clip_k: float, clip_v: float, mu_rot=None) -> dict:
+    """Quantize new tokens k, v [T, H, 128] for the cache (Eqs. 19-21, 27).
+
+    The key is centred before rotation, x_K = (k - mu) R_K, or -- when ``mu_rot``
+    (= mu R_K, [H, 128]) is given instead -- rotated then shifted,
+    x_K = k R_K - mu R_K, the implementation form of Eq. 20.
+    """
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
-    kc = k - (np.asarray(mu, np.float64)[None] if mu is not None else 0.0)
-    xk = rotate_heads(kc, r_k)
+    if mu_rot is not None:
+        assert mu is None, "give mu or mu_rot, not both"
+        xk = rotate_heads(k, r_k) - np.asarray(mu_rot, np.float64)[None]
+    else:
+        kc = k - (np.asarray(mu, np.float64)[None] if mu is not None else 0.0)
+        xk = rotate_heads(kc, r_k)
     xv = rotate_heads(v, r_v)
     ck, sk, zk = quantize_groups(xk, clip_k)
     cv, sv, zv = quantize_groups(xv, clip_v)
@@ -90,22 +100,22 @@ def write_tokens(pool: np.ndarray, n_kv_heads: int, page_tokens: int, table_row,
     rec = record_bytes(p)
     off = offsets(p)
     pool4 = pool.reshape(-1, n_kv_heads, rec)
-    pk = pack_codes(enc["ck"])
+    pk = pack_codes(enc["ck"])  # [T, H, 32]
     pv = pack_codes(enc["cv"])
-    mk = _meta_bytes(enc["sk"], enc["zk"])
+    mk = _meta_bytes(enc["sk"], enc["zk"])  # [T, H, 4]
     mv = _meta_bytes(enc["sv"], enc["zv"])
     n = pk.shape[0]
-    for t in range(n):
-        pos = start_pos + t
-        blk = int(table_row[pos // p])
-        o = pos % p
-        assert 0 <= blk < pool4.shape[0]
-        for h in range(n_kv_heads):
-            r = pool4[blk, h]
-            r[off["k_codes"] + 32 * o: off["k_codes"] + 32 * o + 32] = pk[t, h]
-            r[off["v_codes"] + 32 * o: off["v_codes"] + 32 * o + 32] = pv[t, h]
-            r[off["k_meta"] + 4 * o: off["k_meta"] + 4 * o + 4] = mk[t, h]
-            r[off["v_meta"] + 4 * o: off["v_meta"] + 4 * o + 4] = mv[t, h]
+    pos = start_pos + np.arange(n)
+    blk = np.asarray(table_row, np.int64)[pos // p]  # physical page of every token
+    assert np.all((blk >= 0) & (blk < pool4.shape[0]))
+    slot = pos % p
+    heads = np.arange(n_kv_heads)
+    b3 = blk[:, None, None]
+    h3 = heads[None, :, None]
+    for base, width, data in ((off["k_codes"], 32, pk), (off["v_codes"], 32, pv),
+                              (off["k_meta"], 4, mk), (off["v_meta"], 4, mv)):
+        col = base + width * slot[:, None, None] + np.arange(width)[None, None, :]
+        pool4[b3, h3, col] = data
 
 
 def read_sequence(pool: np.ndarray, n_kv_heads: int, page_tokens: int, table_row, length: int) -> dict:
@@ -142,15 +152,20 @@ def dequantized_sequence(pool, n_kv_heads, page_tokens, table_row, length):
     return kh, vh
 
 
-def build_pool(case, r_k, r_v, mu, lengths=None) -> np.ndarray:
-    """Encode every sequence of a workloads.DecodeCase into a fresh pool."""
+def build_pool(case, r_k, r_v, mu=None, lengths=None, mu_rot=None, keep=False):
+    """Encode every sequence of a workloads.DecodeCase into a fresh pool.
+
+    Returns the pool, or (pool, per-sequence encodings) when ``keep``."""
     h = case.n_kv_heads
     p = case.page_tokens
     pool = np.zeros(pool_bytes(case.num_blocks, h, p), dtype=np.uint8)
     lengths = case.seq_lens if lengths is None else lengths
+    encs = []
     for b in range(case.n_seqs):
         k, v = case.kv(b)
         n = int(lengths[b])
-        enc = encode_tokens(k[:n], v[:n], r_k, r_v, mu, case.clip_k, case.clip_v)
+        enc = encode_tokens(k[:n], v[:n], r_k, r_v, mu, case.clip_k, case.clip_v, mu_rot=mu_rot)
         write_tokens(pool, h, p, case.block_table[b], 0, enc)
-    return pool
+        if keep:
+            encs.append(enc)
+    return (pool, encs) if keep else pool

@@ -1,0 +1,61 @@
+"""GPU parity of kvq_fold_wo and kvq_out_proj against the fp64 oracle."""
+import numpy as np
+import pytest
+
+import gpu_util as gu
+from int2_kv_cache_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("rot,wdt,odt", [("dense", "bf16", "f32"), ("signed_hadamard", "f32", "f32"),
+                                         ("dense", "bf16", "bf16"), ("identity", "f32", "bf16")])
+def test_fold_wo(rot, wdt, odt):
+    import oracle
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    hq, hkv, dm = 8, 2, 320
+    w = W.draw_wo(31, dm, hq * 128, wdt)
+    spec = W.make_rot(rot, 31, 1, hkv)
+    r = oracle.rotations.rot_matrices(spec, hkv)
+    out = torch.empty(dm, hq * 128, device="cuda", dtype=torch.float32 if odt == "f32" else torch.bfloat16)
+    kvq.kvq_fold_wo(gu.dev(w, wdt), hq, hkv, kvq.DeviceRot.from_spec(spec), out)
+    ref = oracle.output.fold_wo(w, r, hq // hkv)
+    got = out.float().cpu().numpy()
+    if odt == "f32":
+        assert gu.normwise_err(got, ref) < 1e-6
+    else:
+        # bf16 output: within one bf16 rounding of the exact fold
+        assert np.all(np.abs(got - ref) <= np.abs(ref) * 2.0 ** -8 + 1e-6 * np.abs(ref).max())
+
+
+@pytest.mark.parametrize("rows,dm,hq,wdt", [(1, 128, 1, "f32"), (16, 4096, 32, "bf16"), (5, 200, 3, "bf16"),
+                                            (64, 640, 10, "f32")])
+def test_out_proj(rows, dm, hq, wdt):
+    import oracle
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    w = W.draw_wo(32, dm, hq * 128, wdt)
+    o = np.random.default_rng(1).standard_normal((rows, hq, 128)).astype(np.float32)
+    y = torch.empty(rows, dm, device="cuda")
+    kvq.kvq_out_proj(gu.dev(o).reshape(rows, -1), gu.dev(w, wdt), y)
+    ref = oracle.output.out_proj(o, w)
+    assert gu.normwise_err(y.cpu().numpy(), ref) <= gu.OUT_TOL
+
+
+def test_folded_projection_of_rotated_readout_equals_unrotated():
+    """Eq. 31 on the GPU: out_proj(o R_V, fold(W_O)) = o W_O^T."""
+    import oracle
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    hq, hkv, dm = 8, 4, 256
+    w = W.draw_wo(33, dm, hq * 128, "f32")
+    spec = W.make_rot("dense", 33, 2, hkv)
+    r = oracle.rotations.rot_matrices(spec, hkv)
+    o = np.random.default_rng(2).standard_normal((3, hq, 128))
+    o_rot = np.einsum("bjc,jcd->bjd", o, r[np.arange(hq) // 2]).astype(np.float32)
+    wf = torch.empty(dm, hq * 128, device="cuda")
+    kvq.kvq_fold_wo(gu.dev(w), hq, hkv, kvq.DeviceRot.from_spec(spec), wf)
+    y = torch.empty(3, dm, device="cuda")
+    kvq.kvq_out_proj(gu.dev(o_rot).reshape(3, -1), wf, y)
+    assert gu.normwise_err(y.cpu().numpy(), oracle.output.out_proj(o, w)) < 1e-4

@@ -1,0 +1,99 @@
+"""GPU parity of the write path: kvq_quantize_append, kvq_key_mean, kvq_rotate_heads."""
+import numpy as np
+import pytest
+
+import gpu_util as gu
+from int2_kv_cache_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # rot, dtype, page, lengths, clips
+    ("identity", "f32", 16, [1, 37, 300], (1.0, 1.0)),
+    ("signed_hadamard", "f32", 16, [16, 129, 5], (0.9, 0.95)),
+    ("signed_hadamard", "bf16", 8, [300, 17], (1.0, 0.85)),
+    ("dense", "f32", 8, [33, 250], (0.96, 0.92)),
+    ("dense", "bf16", 16, [511, 2, 64], (1.0, 1.0)),
+    ("identity", "bf16", 8, [7, 8, 9], (0.8, 0.8)),
+]
+
+
+@pytest.mark.parametrize("rot,dtype,page,lengths,clips", CASES, ids=lambda v: str(v))
+def test_quantize_append_matches_oracle(rot, dtype, page, lengths, clips):
+    case = W.decode_case(11, lengths, 4, 2, 256, rot, dtype, page_tokens=page, clip_k=clips[0], clip_v=clips[1],
+                         spare_blocks=3, n_cal=256)
+    g = gu.GpuCase(case)
+    pool = g.new_pool()
+    g.gpu_append_all(pool)
+    g.kvq.kvq_device_check()
+    ora_pool, encs = g.oracle_pool()
+    gpool = pool.cpu().numpy()
+    stats = gu.compare_codes(gpool, ora_pool, case.n_kv_heads, page, case.block_table, g.lengths, encs, clips,
+                             label=f"{rot}/{dtype}/P{page}")
+    # bytes of pages that no sequence owns stay untouched (zero) on both sides
+    used = np.zeros(case.num_blocks, bool)
+    for b, n in enumerate(g.lengths):
+        used[case.block_table[b, :(n + page - 1) // page]] = True
+    rec = gpool.reshape(case.num_blocks, -1)
+    assert rec[~used].sum() == 0
+    print("code parity", stats)
+
+
+@pytest.mark.parametrize("rot", ["signed_hadamard", "dense"])
+def test_chunked_append_equals_single_append(rot):
+    case = W.decode_case(12, [300, 45, 160], 8, 4, 128, rot, "bf16", page_tokens=16, clip_k=0.9, n_cal=128)
+    g = gu.GpuCase(case)
+    a = g.new_pool()
+    b = g.new_pool()
+    g.gpu_append_all(a, chunks=1)
+    g.gpu_append_all(b, chunks=3)  # chunk edges fall inside pages
+    assert g.torch.equal(a, b)
+
+
+def test_identity_rotation_equals_plain_int2_on_gpu():
+    # the benchmark spec pin: the identity rotation is plain INT2 (Eq. 4 with R = I); uncentred, clip 1
+    case = W.decode_case(13, [100], 1, 1, 128, "identity", "f32", n_off=0)
+    g = gu.GpuCase(case, mu_mode="none")
+    pool = g.new_pool()
+    g.gpu_append_all(pool)
+    import oracle
+    k, v = case.kv(0)
+    codes, s, z = oracle.quant.quantize_groups(k.astype(np.float64), 1.0)
+    ck, mk = gu.seq_codes_meta(pool.cpu().numpy(), 1, 16, case.block_table[0], 100, "k")
+    assert np.array_equal(ck, codes)
+    assert np.array_equal(mk[..., 0], oracle.quant.fp16_bits(s)) and np.array_equal(mk[..., 1], oracle.quant.fp16_bits(z))
+
+
+def test_out_of_range_block_is_skipped_and_flagged():
+    case = W.decode_case(14, [40], 2, 2, 128, "signed_hadamard", "f32", page_tokens=16, spare_blocks=1)
+    case.block_table[0, 1] = case.num_blocks + 5  # page 1 points outside the pool
+    g = gu.GpuCase(case)
+    pool = g.new_pool()
+    g.gpu_append_all(pool)
+    with pytest.raises(g.kvq.KvqError) as e:
+        g.kvq.kvq_device_check()
+    assert e.value.status == g.kvq.KVQ_EDEVICE_FLAG
+    g.kvq.kvq_device_check()  # the word was cleared
+    # pages 0 and 2 were written, nothing else
+    rec = pool.cpu().numpy().reshape(case.num_blocks, -1)
+    assert rec[case.block_table[0, 0]].any() and rec[case.block_table[0, 2]].any()
+
+
+def test_key_mean_and_rotate_heads_match_oracle():
+    import oracle
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    case = W.decode_case(15, [8], 8, 4, 128, "dense", "bf16", n_cal=1000)
+    kc = case.calibration_keys()
+    mu = torch.empty(4, 128, device="cuda")
+    kvq.kvq_key_mean(gu.dev(kc, "bf16"), mu)
+    ref = oracle.cache.key_mean(kc)
+    assert np.abs(mu.cpu().numpy() - ref).max() <= 1e-6 * np.abs(ref).max()
+    for rot in ("identity", "signed_hadamard", "dense"):
+        spec = W.make_rot(rot, 15, 3, 4)
+        r = oracle.rotations.rot_matrices(spec, 4)
+        x = np.random.default_rng(0).standard_normal((5, 8, 128)).astype(np.float32)
+        y = torch.empty(5, 8, 128, device="cuda")
+        kvq.kvq_rotate_heads(gu.dev(x), kvq.DeviceRot.from_spec(spec), y, heads_per_rot=2)
+        yr = oracle.cache.rotate_heads(x, r, heads_per_rot=2)
+        assert gu.normwise_err(y.cpu().numpy(), yr) < 1e-6, rot

@@ -102,3 +102,16 @@ def test_key_mean_and_rotate_heads():
     x = np.ones((4, 128))
     y = cache.rotate_heads(x, r, heads_per_rot=2)  # heads 0,1 -> R0; 2,3 -> R1
     assert np.array_equal(y[:2], np.ones((2, 128))) and np.array_equal(y[2:], 2 * np.ones((2, 128)))
+
+
+def test_rotate_then_subtract_form_equals_centre_then_rotate():
+    # Eq. 20: (k - mu) R = k R - mu R
+    g = np.random.default_rng(7)
+    h = 2
+    k = g.standard_normal((9, h, 128)) * 4
+    v = g.standard_normal((9, h, 128))
+    r = np.stack([rotations.expm_skew(g.normal(0, 0.05, (128, 128))) for _ in range(h)])
+    mu = g.standard_normal((h, 128))
+    a = cache.encode_tokens(k, v, r, r, mu, 1.0, 1.0)
+    b = cache.encode_tokens(k, v, r, r, None, 1.0, 1.0, mu_rot=np.einsum("hc,hcd->hd", mu, r))
+    assert np.abs(a["xk"] - b["xk"]).max() < 1e-12
