@@ -102,6 +102,13 @@ kvq::PageGeom geom(const kvq_layout* L) {
     if (st_ != KVQ_OK) return st_;  \
   } while (0)
 
+#define KVQ_IDX(p, name)                                                               \
+  do {                                                                                 \
+    if (!(p)) return fail(KVQ_EINVAL, "%s is NULL", name);                             \
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0)                                    \
+      return fail(KVQ_EINVAL, "%s is not 4-byte aligned", name);                       \
+  } while (0)
+
 #define KVQ_PTR(p, name)                                                         \
   do {                                                                           \
     if (!(p)) return fail(KVQ_EINVAL, "%s is NULL", name);                       \
@@ -176,9 +183,9 @@ kvq_status kvq_quantize_append(const kvq_layout* layout, int n_seqs, int n_new_t
   if (n_new_total == 0) return KVQ_OK;
   KVQ_PTR(k, "k");
   KVQ_PTR(v, "v");
-  KVQ_PTR(cu_new, "cu_new");
-  KVQ_PTR(start_pos, "start_pos");
-  KVQ_PTR(block_table, "block_table");
+  KVQ_IDX(cu_new, "cu_new");
+  KVQ_IDX(start_pos, "start_pos");
+  KVQ_IDX(block_table, "block_table");
   KVQ_PTR(pool, "pool");
   if (mu_rot_k && !aligned16(mu_rot_k)) return fail(KVQ_EINVAL, "mu_rot_k is not 16-byte aligned");
   unsigned* err = nullptr;
@@ -220,8 +227,8 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
   KVQ_CHECK(check_rot(rot_k, "rot_k"));
   if (n_seqs == 0) return KVQ_OK;
   KVQ_PTR(q, "q");
-  KVQ_PTR(seq_lens, "seq_lens");
-  KVQ_PTR(block_table, "block_table");
+  KVQ_IDX(seq_lens, "seq_lens");
+  KVQ_IDX(block_table, "block_table");
   KVQ_PTR(pool, "pool");
   KVQ_PTR(o_rot, "o_rot");
   KVQ_PTR(workspace, "workspace");

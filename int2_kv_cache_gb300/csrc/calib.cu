@@ -14,10 +14,10 @@
 
 namespace kvq {
 
-constexpr int CAL_MAX_TOK = 12288;  // keys that fit the score buffer (48 KB of shared memory)
+
 
 struct CalibWs {
-  float *qf, *qr, *kf, *vf, *xk, *xv, *kq, *vq, *o_rot, *o_ref, *o_un, *gram;
+  float *qf, *qr, *kf, *vf, *xk_hi, *xk_lo, *xv_hi, *xv_lo, *kq, *vq, *o_rot, *o_ref, *o_un, *gram;
 };
 
 static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
@@ -28,17 +28,17 @@ static CalibWs carve(void* ws, int n_tok, int n_qpos, int n_kv_heads, int gqa, i
   const size_t qn = (size_t)n_qpos * hq * D, kn = (size_t)n_tok * n_kv_heads * D;
   const size_t gd = joint ? hq * D : (size_t)gqa * D;
   const size_t gn = (joint ? 1 : (size_t)n_kv_heads) * gd * gd;
-  const size_t sizes[12] = {qn, qn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn};
+  const size_t sizes[14] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn};
   char* p = static_cast<char*>(ws);
-  float* ptrs[12];
+  float* ptrs[14];
   size_t off = 0;
-  for (int i = 0; i < 12; ++i) {
+  for (int i = 0; i < 14; ++i) {
     ptrs[i] = reinterpret_cast<float*>(p + off);
     off += align_up(sizes[i] * sizeof(float));
   }
   if (total) *total = off;
-  return CalibWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5],
-                 ptrs[6], ptrs[7], ptrs[8], ptrs[9], ptrs[10], ptrs[11]};
+  return CalibWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6],
+                 ptrs[7], ptrs[8], ptrs[9], ptrs[10], ptrs[11], ptrs[12], ptrs[13]};
 }
 
 size_t calib_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint) {
@@ -205,8 +205,6 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
   causal_attn_kernel<<<dim3(n_qpos, hq), 128, attn_smem, s>>>(n_tok, n_qpos, n_kv_heads, gqa, w.qf,
                                                               w.kf, w.vf, w.o_ref);
   KVQ_TRY(cudaSuccess);
-  // centre the keys (OptR §4.1; attention-equivalent)
-  to_f32_kernel<<<blocks(kn), 256, 0, s>>>(kn, n_kv_heads, k, dtype, mu, w.kf);
   gram_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype,
                                                                w.gram);
   zero_f64_kernel<<<1, 256, 0, s>>>(ref, n_groups);
@@ -219,12 +217,13 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
   KVQ_TRY(cudaSuccess);
   for (int i = 0; i < n_cand; ++i) {
     const RotDev r = to_dev(cand[i]);
-    KVQ_TRY(launch_rotate_heads(n_tok, n_kv_heads, 1, w.kf, r, w.xk, false, s));
-    KVQ_TRY(launch_rotate_heads(n_tok, n_kv_heads, 1, w.vf, r, w.xv, false, s));
+    // keys centred (OptR §4.1; attention-equivalent) then rotated; values rotated
+    KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, k, dtype, mu, r, w.xk_hi, w.xk_lo, s));
+    KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, v, dtype, nullptr, r, w.xv_hi, w.xv_lo, s));
     KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.qf, r, w.qr, false, s));
     for (int c = 0; c < n_clip; ++c) {
-      KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk, clips[c], w.kq, s));
-      KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv, clips[c], w.vq, s));
+      KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clips[c], w.kq, s));
+      KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clips[c], w.vq, s));
       causal_attn_kernel<<<dim3(n_qpos, hq), 128, attn_smem, s>>>(n_tok, n_qpos, n_kv_heads, gqa,
                                                                   w.qr, w.kq, w.vq, w.o_rot);
       KVQ_TRY(cudaSuccess);

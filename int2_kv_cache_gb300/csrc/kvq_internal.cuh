@@ -75,8 +75,10 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
                                    const int32_t* table, RotDev rot, const float* mu_rot,
                                    float clip, int codes_off, int meta_off, uint8_t* pool,
                                    unsigned* err, cudaStream_t s);
-cudaError_t launch_quant_dequant(int n_groups, const float* x, float clip, float* out,
-                                 cudaStream_t s);
+cudaError_t launch_rotate_df(int n_rows, int n_heads, const void* src, int dtype, const float* mu,
+                             RotDev rot, float* x_hi, float* x_lo, cudaStream_t s);
+cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x_lo, float clip,
+                                 float* out, cudaStream_t s);
 
 // decode.cu
 int decode_auto_splits(int n_seqs, int n_kv_heads, int max_seq_len, int page_tokens);

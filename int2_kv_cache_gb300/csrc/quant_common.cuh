@@ -6,41 +6,134 @@
 // the 2.32 bits-per-element accounting implies):
 //   lo = c * min(x), hi = c * max(x)
 //   scale = fp16_rn((hi - lo) / 3), zero = fp16_rn(lo)
-//   code  = clamp(rint((x - zero) / scale), 0, 3), 0 where scale == 0
-// Arithmetic is fp32; (x - zero) / scale is evaluated as (x - zero) * (1 / scale)
-// with an IEEE reciprocal (at most ~2 ulp from the quotient).
+//   code  = clamp(round_half_even((x - zero) / scale), 0, 3), 0 where scale == 0
+//
+// Every decision that turns floating point into an integer (the fp16 rounding of
+// scale and zero, the code of each channel) is taken on x carried as an unevaluated
+// sum of two floats ("double-float", ~48 significant bits) and decided exactly:
+// the fp16 roundings look at the low word at exact midpoints, and codes come from
+// exact comparisons of x - zero with the rounding midpoints 0.5, 1.5 and 2.5 times
+// scale.  The rotations that produce x carry their rounding errors the same way
+// (compensated butterflies for the Walsh-Hadamard transform, error-free products
+// and sums for dense matrices; Ogita, Rump & Oishi, "Accurate sum and dot
+// product", 2005).  The result equals the decision on the exact real x except
+// within ~1e-13 (relative) of a rounding boundary.
 #pragma once
 
 #include "kvq_internal.cuh"
 
 namespace kvq {
 
-struct QParams {
-  unsigned short s_bits, z_bits;
-  float s, z, r;  // fp16-rounded scale and zero (as float), reciprocal of s (0 if s == 0)
+// ---------------------------------------------------------------------------
+// double-float arithmetic (intrinsics keep the compiler from fusing or reordering)
+// ---------------------------------------------------------------------------
+struct DF {
+  float hi, lo;
 };
 
-__device__ __forceinline__ QParams qparams(float mn, float mx, float clip) {
-  float lo = clip * mn;
-  float hi = clip * mx;
-  float sc = __fdiv_rn(hi - lo, 3.0f);
-  __half s16 = __float2half_rn(sc);
-  __half z16 = __float2half_rn(lo);
+__device__ __forceinline__ DF two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  const float e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+  return DF{s, e};
+}
+
+// Renormalise hi + lo (any magnitudes) so that |lo| <= ulp(hi) / 2.
+__device__ __forceinline__ DF df_norm(float hi, float lo) { return two_sum(hi, lo); }
+
+__device__ __forceinline__ DF df_add(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  return df_norm(s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo)));
+}
+
+__device__ __forceinline__ DF df_add_f(DF a, float b) {
+  const DF s = two_sum(a.hi, b);
+  return df_norm(s.hi, __fadd_rn(s.lo, a.lo));
+}
+
+__device__ __forceinline__ DF df_mul_f(DF a, float b) {
+  const float p = __fmul_rn(a.hi, b);
+  float e = __fmaf_rn(a.hi, b, -p);
+  e = __fmaf_rn(a.lo, b, e);
+  return df_norm(p, e);
+}
+
+// 1 / sqrt(128) as a double-float.
+constexpr float INV_SQRT_D = 0.0883883461356163f;
+constexpr float INV_SQRT_D_LO = 1.512702185735293e-09f;
+
+__device__ __forceinline__ DF df_mul_inv_sqrt_d(DF a) {
+  const float p = __fmul_rn(a.hi, INV_SQRT_D);
+  float e = __fmaf_rn(a.hi, INV_SQRT_D, -p);
+  e = __fmaf_rn(a.hi, INV_SQRT_D_LO, e);
+  e = __fmaf_rn(a.lo, INV_SQRT_D, e);
+  return df_norm(p, e);
+}
+
+__device__ __forceinline__ bool df_less(DF a, DF b) {
+  return a.hi < b.hi || (a.hi == b.hi && a.lo < b.lo);
+}
+
+// fp16 rounding (to nearest, ties to even) of the exact value hi + lo.
+__device__ __forceinline__ __half df_to_half(DF v) {
+  __half h = __float2half_rn(v.hi);
+  const float hf = __half2float(h);
+  if (v.lo != 0.f && hf != v.hi && isfinite(hf)) {
+    // v.hi was rounded to h; only if v.hi sits exactly on the midpoint between h
+    // and its other neighbour can the low word change the result.
+    const unsigned short hb = __half_as_ushort(h);
+    const bool away = fabsf(v.hi) > fabsf(hf);  // v.hi lies further from zero than h
+    const unsigned short nb = away ? (unsigned short)(hb + 1) : (unsigned short)(hb - 1);
+    const float nf = __half2float(__ushort_as_half(nb));
+    if (__fsub_rn(v.hi, hf) == __fsub_rn(nf, v.hi)) {
+      const bool lo_toward_n = (nf > v.hi) == (v.lo > 0.f);
+      if (lo_toward_n) h = __ushort_as_half(nb);
+    }
+  }
+  return h;
+}
+
+struct QParams {
+  unsigned short s_bits, z_bits;
+  float s, z;           // fp16-rounded scale and zero (exact as float)
+  float t05, t15, t25;  // rounding midpoints 0.5 s, 1.5 s, 2.5 s (exact in fp32)
+};
+
+// Scale and zero from the group's (double-float) min and max.
+__device__ __forceinline__ QParams qparams_df(DF mn, DF mx, float clip) {
+  const DF lo = df_mul_f(mn, clip);
+  const DF hi = df_mul_f(mx, clip);
+  const DF range = df_add(hi, DF{-lo.hi, -lo.lo});
+  // range / 3 as a double-float: q = fl(range.hi / 3), remainder exact by FMA
+  const float q = __fdiv_rn(range.hi, 3.0f);
+  const float r = __fadd_rn(__fmaf_rn(-q, 3.0f, range.hi), range.lo);
+  const DF third = df_norm(q, __fdiv_rn(r, 3.0f));
+  const __half s16 = df_to_half(third);
+  const __half z16 = df_to_half(lo);
   QParams p;
   p.s_bits = __half_as_ushort(s16);
   p.z_bits = __half_as_ushort(z16);
   p.s = __half2float(s16);
   p.z = __half2float(z16);
-  p.r = p.s > 0.f ? __frcp_rn(p.s) : 0.f;
+  p.t05 = 0.5f * p.s;
+  p.t15 = 1.5f * p.s;
+  p.t25 = 2.5f * p.s;
   return p;
 }
 
-__device__ __forceinline__ unsigned qcode(float x, const QParams& p) {
-  int c = __float2int_rn((x - p.z) * p.r);
-  c = c < 0 ? 0 : (c > 3 ? 3 : c);
-  return p.s > 0.f ? (unsigned)c : 0u;
+// round_half_even((x - zero) / scale) clamped to [0, 3], decided exactly on x = hi + lo.
+__device__ __forceinline__ unsigned qcode_df(DF x, const QParams& p) {
+  if (!(p.s > 0.f)) return 0u;
+  const DF d = df_add_f(x, -p.z);
+  const unsigned a = (d.hi > p.t05 || (d.hi == p.t05 && d.lo > 0.f)) ? 1u : 0u;   // tie at .5 -> 0
+  const unsigned b = (d.hi > p.t15 || (d.hi == p.t15 && d.lo >= 0.f)) ? 1u : 0u;  // tie at 1.5 -> 2
+  const unsigned c = (d.hi > p.t25 || (d.hi == p.t25 && d.lo > 0.f)) ? 1u : 0u;   // tie at 2.5 -> 2
+  return a + b + c;
 }
 
+// ---------------------------------------------------------------------------
+// warp helpers
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_min(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
@@ -57,34 +150,113 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// Warp-cooperative Walsh-Hadamard transform of 128 values, lane l holding
-// channels 4l..4l+3 (Sylvester order, unnormalised): two butterfly stages in
-// registers, five across lanes.
-__device__ __forceinline__ void warp_fwht128(float4& v, int lane) {
-  float a0 = v.x + v.y, a1 = v.x - v.y, a2 = v.z + v.w, a3 = v.z - v.w;
-  v.x = a0 + a2; v.z = a0 - a2; v.y = a1 + a3; v.w = a1 - a3;
+__device__ __forceinline__ DF shfl_xor_df(DF v, int m) {
+  return DF{__shfl_xor_sync(0xffffffffu, v.hi, m), __shfl_xor_sync(0xffffffffu, v.lo, m)};
+}
+
+// min and max over the 128 double-float values of a warp (4 per lane).
+__device__ __forceinline__ void warp_minmax_df(const DF x[4], DF& mn, DF& mx) {
+  mn = x[0];
+  mx = x[0];
 #pragma unroll
-  for (int m = 1; m < 32; m <<= 1) {
-    float px = __shfl_xor_sync(0xffffffffu, v.x, m);
-    float py = __shfl_xor_sync(0xffffffffu, v.y, m);
-    float pz = __shfl_xor_sync(0xffffffffu, v.z, m);
-    float pw = __shfl_xor_sync(0xffffffffu, v.w, m);
-    if (lane & m) { v.x = px - v.x; v.y = py - v.y; v.z = pz - v.z; v.w = pw - v.w; }
-    else          { v.x = v.x + px; v.y = v.y + py; v.z = v.z + pz; v.w = v.w + pw; }
+  for (int i = 1; i < 4; ++i) {
+    if (df_less(x[i], mn)) mn = x[i];
+    if (df_less(mx, x[i])) mx = x[i];
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const DF a = shfl_xor_df(mn, o), b = shfl_xor_df(mx, o);
+    if (df_less(a, mn)) mn = a;
+    if (df_less(mx, b)) mx = b;
   }
 }
 
-// 1 / sqrt(128) rounded to fp32.
-constexpr float INV_SQRT_D = 0.08838834764831845f;
+// ---------------------------------------------------------------------------
+// Rotations of one head vector held by a warp (lane l owns channels 4l..4l+3).
+// ---------------------------------------------------------------------------
 
-// Rotate one head vector held by a warp (lane l owns channels 4l..4l+3):
+// Compensated Walsh-Hadamard transform (Sylvester order, unnormalised): every
+// butterfly keeps its rounding error in the low word.
+__device__ __forceinline__ DF df_bfly_add(DF a, DF b) {
+  const DF s = two_sum(a.hi, b.hi);
+  return DF{s.hi, __fadd_rn(s.lo, __fadd_rn(a.lo, b.lo))};
+}
+__device__ __forceinline__ DF df_bfly_sub(DF a, DF b) {
+  const DF s = two_sum(a.hi, -b.hi);
+  return DF{s.hi, __fadd_rn(s.lo, __fsub_rn(a.lo, b.lo))};
+}
+
+__device__ __forceinline__ void warp_fwht128_df(DF v[4], int lane) {
+  DF a0 = df_bfly_add(v[0], v[1]), a1 = df_bfly_sub(v[0], v[1]);
+  DF a2 = df_bfly_add(v[2], v[3]), a3 = df_bfly_sub(v[2], v[3]);
+  v[0] = df_bfly_add(a0, a2);
+  v[2] = df_bfly_sub(a0, a2);
+  v[1] = df_bfly_add(a1, a3);
+  v[3] = df_bfly_sub(a1, a3);
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const DF p = shfl_xor_df(v[i], m);
+      v[i] = upper ? df_bfly_sub(p, v[i]) : df_bfly_add(v[i], p);
+    }
+  }
+}
+
+// x (4 channels per lane, double-float) -> x R_head as double-float.
+//   signed Hadamard: R = diag(s) H / sqrt(128)
+//   dense:           y_d = sum_c x_c R[c][d], error-free products and sums
+__device__ __forceinline__ void rotate_df_warp(DF x[4], const RotDev& rot, int head, int lane) {
+  if (rot.kind == KVQ_ROT_SIGNED_HADAMARD) {
+    const float4 s = __ldg(reinterpret_cast<const float4*>(rot.signs + (size_t)head * D) + lane);
+    x[0].hi *= s.x; x[0].lo *= s.x; x[1].hi *= s.y; x[1].lo *= s.y;
+    x[2].hi *= s.z; x[2].lo *= s.z; x[3].hi *= s.w; x[3].lo *= s.w;
+    warp_fwht128_df(x, lane);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = df_mul_inv_sqrt_d(x[i]);
+  } else if (rot.kind == KVQ_ROT_DENSE) {
+    const float* R = rot.dense + (size_t)head * D * D;
+    float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 2
+    for (int c = 0; c < D; ++c) {
+      const int src = c >> 2, k = c & 3;
+      const float xh = __shfl_sync(0xffffffffu, k == 0 ? x[0].hi : k == 1 ? x[1].hi : k == 2 ? x[2].hi : x[3].hi, src);
+      const float xl = __shfl_sync(0xffffffffu, k == 0 ? x[0].lo : k == 1 ? x[1].lo : k == 2 ? x[2].lo : x[3].lo, src);
+      const float4 r4 = __ldg(reinterpret_cast<const float4*>(R + (size_t)c * D) + lane);
+      const float r[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __fmul_rn(xh, r[i]);
+        float pe = __fmaf_rn(xh, r[i], -p);
+        pe = __fmaf_rn(xl, r[i], pe);
+        const DF t = two_sum(sh[i], p);
+        sh[i] = t.hi;
+        sl[i] = __fadd_rn(sl[i], __fadd_rn(t.lo, pe));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = df_norm(sh[i], sl[i]);
+  }
+}
+
+// Plain fp32 rotation of a warp-held vector (query rotation and the inverse
+// rotation of calibration readouts, which feed continuous outputs only):
 // y = x R_head, or y = x R_head^T when `transpose`.
 __device__ __forceinline__ float4 rotate_vec_warp(float4 v, const RotDev& rot, int head, int lane,
                                                   bool transpose) {
   if (rot.kind == KVQ_ROT_SIGNED_HADAMARD) {
     const float4 s = __ldg(reinterpret_cast<const float4*>(rot.signs + (size_t)head * D) + lane);
     if (!transpose) { v.x *= s.x; v.y *= s.y; v.z *= s.z; v.w *= s.w; }
-    warp_fwht128(v, lane);
+    float a0 = v.x + v.y, a1 = v.x - v.y, a2 = v.z + v.w, a3 = v.z - v.w;
+    v.x = a0 + a2; v.z = a0 - a2; v.y = a1 + a3; v.w = a1 - a3;
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {
+      const float px = __shfl_xor_sync(0xffffffffu, v.x, m), py = __shfl_xor_sync(0xffffffffu, v.y, m);
+      const float pz = __shfl_xor_sync(0xffffffffu, v.z, m), pw = __shfl_xor_sync(0xffffffffu, v.w, m);
+      if (lane & m) { v.x = px - v.x; v.y = py - v.y; v.z = pz - v.z; v.w = pw - v.w; }
+      else          { v.x = v.x + px; v.y = v.y + py; v.z = v.z + pz; v.w = v.w + pw; }
+    }
     v.x *= INV_SQRT_D; v.y *= INV_SQRT_D; v.z *= INV_SQRT_D; v.w *= INV_SQRT_D;
     if (transpose) { v.x *= s.x; v.y *= s.y; v.z *= s.z; v.w *= s.w; }
     return v;
@@ -93,26 +265,24 @@ __device__ __forceinline__ float4 rotate_vec_warp(float4 v, const RotDev& rot, i
     const float* R = rot.dense + (size_t)head * D * D;
     float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
     if (!transpose) {
-      // y_d = sum_c x_c R[c][d], lane owns d = 4*lane .. 4*lane+3
 #pragma unroll 4
       for (int c = 0; c < D; ++c) {
-        float src = (c & 3) == 0 ? v.x : (c & 3) == 1 ? v.y : (c & 3) == 2 ? v.z : v.w;
-        float xc = __shfl_sync(0xffffffffu, src, c >> 2);
-        float4 r = __ldg(reinterpret_cast<const float4*>(R + (size_t)c * D) + lane);
+        const float src = (c & 3) == 0 ? v.x : (c & 3) == 1 ? v.y : (c & 3) == 2 ? v.z : v.w;
+        const float xc = __shfl_sync(0xffffffffu, src, c >> 2);
+        const float4 r = __ldg(reinterpret_cast<const float4*>(R + (size_t)c * D) + lane);
         y.x = fmaf(xc, r.x, y.x); y.y = fmaf(xc, r.y, y.y);
         y.z = fmaf(xc, r.z, y.z); y.w = fmaf(xc, r.w, y.w);
       }
     } else {
-      // y_d = sum_c x_c R[d][c]
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float4* row = reinterpret_cast<const float4*>(R + (size_t)(4 * lane + i) * D);
         float part = 0.f;
         for (int c4 = 0; c4 < 32; ++c4) {
-          float4 r = __ldg(row + c4);
-          float x0 = __shfl_sync(0xffffffffu, v.x, c4), x1 = __shfl_sync(0xffffffffu, v.y, c4);
-          float x2 = __shfl_sync(0xffffffffu, v.z, c4), x3 = __shfl_sync(0xffffffffu, v.w, c4);
+          const float4 r = __ldg(row + c4);
+          const float x0 = __shfl_sync(0xffffffffu, v.x, c4), x1 = __shfl_sync(0xffffffffu, v.y, c4);
+          const float x2 = __shfl_sync(0xffffffffu, v.z, c4), x3 = __shfl_sync(0xffffffffu, v.w, c4);
           part = fmaf(x0, r.x, part); part = fmaf(x1, r.y, part);
           part = fmaf(x2, r.z, part); part = fmaf(x3, r.w, part);
         }
@@ -125,5 +295,13 @@ __device__ __forceinline__ float4 rotate_vec_warp(float4 v, const RotDev& rot, i
   return v;
 }
 
+// Quantize one warp-held group (4 double-float channels per lane): returns this
+// lane's packed byte (channels 4l..4l+3) and the group's fp16 meta.
+__device__ __forceinline__ unsigned quantize_warp_df(const DF x[4], float clip, QParams& qp) {
+  DF mn, mx;
+  warp_minmax_df(x, mn, mx);
+  qp = qparams_df(mn, mx, clip);
+  return qcode_df(x[0], qp) | (qcode_df(x[1], qp) << 2) | (qcode_df(x[2], qp) << 4) | (qcode_df(x[3], qp) << 6);
+}
 
 }  // namespace kvq

@@ -76,96 +76,13 @@ __device__ __forceinline__ bool locate(int t, int n_seqs, const int32_t* cu_new,
 }
 
 // ---------------------------------------------------------------------------
-// Identity / signed-Hadamard cache write: one thread per (token, head) group,
-// the 128 values and the Walsh-Hadamard transform held in registers.
-// grid = (ceil(n_new / 128), n_kv_heads), block = 128.
-// ---------------------------------------------------------------------------
-template <int DTYPE, bool HADAMARD>
-__global__ void __launch_bounds__(128) append_fwht_kernel(
-    PageGeom g, int n_seqs, int n_new, const void* __restrict__ src,
-    const int32_t* __restrict__ cu_new, const int32_t* __restrict__ start_pos,
-    const int32_t* __restrict__ table, const float* __restrict__ signs,
-    const float* __restrict__ mu_rot, float clip, int codes_off, int meta_off,
-    uint8_t* __restrict__ pool, unsigned* err) {
-  const int h = blockIdx.y;
-  __shared__ float s_sign[D];
-  __shared__ float s_mu[D];
-  s_sign[threadIdx.x] = HADAMARD ? signs[(size_t)h * D + threadIdx.x] : 1.f;
-  s_mu[threadIdx.x] = mu_rot ? mu_rot[(size_t)h * D + threadIdx.x] : 0.f;
-  __syncthreads();
-  const int t = blockIdx.x * 128 + threadIdx.x;
-  if (t >= n_new) return;
-  long long rec;
-  int slot;
-  if (!locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, h)) return;
-
-  float x[D];
-  const size_t row = ((size_t)t * g.n_kv_heads + h) * D;
-  if (DTYPE == KVQ_F32) {
-    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(src) + row);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      float4 f = __ldg(p + i);
-      x[4 * i] = f.x; x[4 * i + 1] = f.y; x[4 * i + 2] = f.z; x[4 * i + 3] = f.w;
-    }
-  } else {
-    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(src) + row);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      uint4 w = __ldg(p + i);
-      x[8 * i + 0] = __uint_as_float(w.x << 16); x[8 * i + 1] = __uint_as_float(w.x & 0xFFFF0000u);
-      x[8 * i + 2] = __uint_as_float(w.y << 16); x[8 * i + 3] = __uint_as_float(w.y & 0xFFFF0000u);
-      x[8 * i + 4] = __uint_as_float(w.z << 16); x[8 * i + 5] = __uint_as_float(w.z & 0xFFFF0000u);
-      x[8 * i + 6] = __uint_as_float(w.w << 16); x[8 * i + 7] = __uint_as_float(w.w & 0xFFFF0000u);
-    }
-  }
-  float scale = 1.f;
-  if (HADAMARD) {
-#pragma unroll
-    for (int i = 0; i < D; ++i) x[i] *= s_sign[i];
-#pragma unroll
-    for (int hs = 1; hs < D; hs <<= 1) {
-#pragma unroll
-      for (int i = 0; i < D; ++i) {
-        if ((i & hs) == 0) {
-          float a = x[i], b = x[i + hs];
-          x[i] = a + b;
-          x[i + hs] = a - b;
-        }
-      }
-    }
-    scale = INV_SQRT_D;
-  }
-  float mn = INFINITY, mx = -INFINITY;
-#pragma unroll
-  for (int i = 0; i < D; ++i) {
-    x[i] = fmaf(x[i], scale, -s_mu[i]);
-    mn = fminf(mn, x[i]);
-    mx = fmaxf(mx, x[i]);
-  }
-  const QParams qp = qparams(mn, mx, clip);
-  uint32_t w[8];
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    uint32_t acc = 0;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) acc |= qcode(x[16 * k + j], qp) << (2 * j);
-    w[k] = acc;
-  }
-  uint8_t* recp = pool + (size_t)rec * g.record;
-  uint4* dst = reinterpret_cast<uint4*>(recp + codes_off + GROUP_BYTES * slot);
-  dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-  dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-  *reinterpret_cast<uint32_t*>(recp + meta_off + META_BYTES * slot) =
-      (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
-}
-
-// ---------------------------------------------------------------------------
-// Dense-R cache write: one warp per (token, head) group; lane l owns channels
-// 4l..4l+3 and hence byte l of the packed group.
+// Cache write: one warp per (token, head) group.  Lane l owns channels 4l..4l+3
+// and hence byte l of the packed group.  x = k R - mu R is formed in
+// double-float (Eq. 20 with the rotation's rounding errors carried), so the
+// quantization decisions are exact.
 // grid = (ceil(n_new / 8), n_kv_heads), block = 256.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) append_dense_kernel(
+__global__ void __launch_bounds__(256) append_kernel(
     PageGeom g, int n_seqs, int n_new, const void* __restrict__ src, int dtype,
     const int32_t* __restrict__ cu_new, const int32_t* __restrict__ start_pos,
     const int32_t* __restrict__ table, RotDev rot, const float* __restrict__ mu_rot, float clip,
@@ -177,16 +94,16 @@ __global__ void __launch_bounds__(256) append_dense_kernel(
   long long rec;
   int slot;
   if (!locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, h)) return;
-  float4 v = load4(src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
-  v = rotate_vec_warp(v, rot, h, lane, false);
+  const float4 v = load4(src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
+  DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+  rotate_df_warp(x, rot, h, lane);
   if (mu_rot) {
-    float4 m = __ldg(reinterpret_cast<const float4*>(mu_rot + (size_t)h * D) + lane);
-    v.x -= m.x; v.y -= m.y; v.z -= m.z; v.w -= m.w;
+    const float4 m = __ldg(reinterpret_cast<const float4*>(mu_rot + (size_t)h * D) + lane);
+    x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
+    x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
   }
-  float mn = warp_min(fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
-  float mx = warp_max(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-  const QParams qp = qparams(mn, mx, clip);
-  unsigned byte = qcode(v.x, qp) | (qcode(v.y, qp) << 2) | (qcode(v.z, qp) << 4) | (qcode(v.w, qp) << 6);
+  QParams qp;
+  const unsigned byte = quantize_warp_df(x, clip, qp);
   uint8_t* recp = pool + (size_t)rec * g.record;
   recp[codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
   if (lane == 0)
@@ -200,54 +117,70 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
                                    float clip, int codes_off, int meta_off, uint8_t* pool,
                                    unsigned* err, cudaStream_t s) {
   if (n_new == 0) return cudaSuccess;
-  if (rot.kind == KVQ_ROT_DENSE) {
-    dim3 grid((n_new + 7) / 8, g.n_kv_heads);
-    append_dense_kernel<<<grid, 256, 0, s>>>(g, n_seqs, n_new, src, dtype, cu_new, start_pos,
-                                             table, rot, mu_rot, clip, codes_off, meta_off, pool,
-                                             err);
-    return cudaGetLastError();
-  }
-  dim3 grid((n_new + 127) / 128, g.n_kv_heads);
-  const bool had = rot.kind == KVQ_ROT_SIGNED_HADAMARD;
-#define KVQ_LAUNCH(DT, HAD)                                                                   \
-  append_fwht_kernel<DT, HAD><<<grid, 128, 0, s>>>(g, n_seqs, n_new, src, cu_new, start_pos, \
-                                                   table, rot.signs, mu_rot, clip, codes_off, \
-                                                   meta_off, pool, err)
-  if (dtype == KVQ_F32) {
-    if (had) KVQ_LAUNCH(KVQ_F32, true); else KVQ_LAUNCH(KVQ_F32, false);
-  } else {
-    if (had) KVQ_LAUNCH(KVQ_BF16, true); else KVQ_LAUNCH(KVQ_BF16, false);
-  }
-#undef KVQ_LAUNCH
+  dim3 grid((n_new + 7) / 8, g.n_kv_heads);
+  append_kernel<<<grid, 256, 0, s>>>(g, n_seqs, n_new, src, dtype, cu_new, start_pos, table, rot,
+                                     mu_rot, clip, codes_off, meta_off, pool, err);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Quantize-dequantize in place of a matrix of groups (calibration sweep):
-// out = zero + scale * code, one warp per group.
+// Calibration helpers.
+// rotate_df: x = (src - mu) R per (row, head), kept as double-float (hi, lo planes).
+// quant_dequant_df: out = zero + scale * code of each group of x.
+// One warp per group.
 // ---------------------------------------------------------------------------
-__global__ void quant_dequant_kernel(int n_groups, const float* __restrict__ x, float clip,
-                                     float* __restrict__ out) {
-  int gi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  int lane = threadIdx.x & 31;
+__global__ void rotate_df_kernel(int n_rows, int n_heads, const void* __restrict__ src, int dtype,
+                                 const float* __restrict__ mu, RotDev rot, float* __restrict__ x_hi,
+                                 float* __restrict__ x_lo) {
+  const int w = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= n_rows * n_heads) return;
+  const int h = w % n_heads;
+  const float4 v = load4(src, (size_t)w * D + 4 * lane, dtype);
+  DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+  if (mu) {
+    const float4 m = __ldg(reinterpret_cast<const float4*>(mu + (size_t)h * D) + lane);
+    x[0] = two_sum(v.x, -m.x); x[1] = two_sum(v.y, -m.y);
+    x[2] = two_sum(v.z, -m.z); x[3] = two_sum(v.w, -m.w);
+  }
+  rotate_df_warp(x, rot, h, lane);
+  reinterpret_cast<float4*>(x_hi + (size_t)w * D)[lane] = make_float4(x[0].hi, x[1].hi, x[2].hi, x[3].hi);
+  reinterpret_cast<float4*>(x_lo + (size_t)w * D)[lane] = make_float4(x[0].lo, x[1].lo, x[2].lo, x[3].lo);
+}
+
+cudaError_t launch_rotate_df(int n_rows, int n_heads, const void* src, int dtype, const float* mu,
+                             RotDev rot, float* x_hi, float* x_lo, cudaStream_t s) {
+  const long long warps = (long long)n_rows * n_heads;
+  if (warps == 0) return cudaSuccess;
+  rotate_df_kernel<<<(unsigned)((warps * 32 + 255) / 256), 256, 0, s>>>(n_rows, n_heads, src, dtype, mu, rot,
+                                                                      x_hi, x_lo);
+  return cudaGetLastError();
+}
+
+__global__ void quant_dequant_df_kernel(int n_groups, const float* __restrict__ x_hi,
+                                        const float* __restrict__ x_lo, float clip,
+                                        float* __restrict__ out) {
+  const int gi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
   if (gi >= n_groups) return;
-  float4 v = reinterpret_cast<const float4*>(x + (size_t)gi * D)[lane];
-  float mn = warp_min(fminf(fminf(v.x, v.y), fminf(v.z, v.w)));
-  float mx = warp_max(fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-  const QParams qp = qparams(mn, mx, clip);
+  const float4 a = reinterpret_cast<const float4*>(x_hi + (size_t)gi * D)[lane];
+  const float4 b = reinterpret_cast<const float4*>(x_lo + (size_t)gi * D)[lane];
+  const DF x[4] = {{a.x, b.x}, {a.y, b.y}, {a.z, b.z}, {a.w, b.w}};
+  QParams qp;
+  const unsigned byte = quantize_warp_df(x, clip, qp);
   float4 o;
-  o.x = fmaf(qp.s, (float)qcode(v.x, qp), qp.z);
-  o.y = fmaf(qp.s, (float)qcode(v.y, qp), qp.z);
-  o.z = fmaf(qp.s, (float)qcode(v.z, qp), qp.z);
-  o.w = fmaf(qp.s, (float)qcode(v.w, qp), qp.z);
+  o.x = fmaf(qp.s, (float)(byte & 3u), qp.z);
+  o.y = fmaf(qp.s, (float)((byte >> 2) & 3u), qp.z);
+  o.z = fmaf(qp.s, (float)((byte >> 4) & 3u), qp.z);
+  o.w = fmaf(qp.s, (float)((byte >> 6) & 3u), qp.z);
   reinterpret_cast<float4*>(out + (size_t)gi * D)[lane] = o;
 }
 
-cudaError_t launch_quant_dequant(int n_groups, const float* x, float clip, float* out,
-                                 cudaStream_t s) {
+cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x_lo, float clip,
+                                 float* out, cudaStream_t s) {
   if (n_groups == 0) return cudaSuccess;
-  int blocks = (int)(((long long)n_groups * 32 + 255) / 256);
-  quant_dequant_kernel<<<blocks, 256, 0, s>>>(n_groups, x, clip, out);
+  const int blocks = (int)(((long long)n_groups * 32 + 255) / 256);
+  quant_dequant_df_kernel<<<blocks, 256, 0, s>>>(n_groups, x_hi, x_lo, clip, out);
   return cudaGetLastError();
 }
 
