@@ -166,6 +166,37 @@ __global__ void __launch_bounds__(256) gram_form_kernel(int n_qpos, int n_groups
   }
 }
 
+// out[slot] += sum over (position, group) of ||du W_g^T||^2 computed directly
+// (used when d_model <= the group width, where it is also the cheaper form).
+// One warp per output row n of W; grid = (n_qpos, n_groups), block = 256.
+__global__ void __launch_bounds__(256) proj_err_kernel(int n_qpos, int n_groups, int gd, int d_model,
+                                                       const float* __restrict__ a,
+                                                       const float* __restrict__ b,
+                                                       const void* __restrict__ w, int w_dtype,
+                                                       double* __restrict__ out) {
+  extern __shared__ float du[];  // [gd]
+  __shared__ double red[8];
+  const int qi = blockIdx.x, grp = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const size_t base = ((size_t)qi * n_groups + grp) * gd;
+  for (int i = tid; i < gd; i += 256) du[i] = b ? a[base + i] - b[base + i] : a[base + i];
+  __syncthreads();
+  const size_t total_cols = (size_t)n_groups * gd, col0 = (size_t)grp * gd;
+  double part = 0.0;
+  for (int n = warp; n < d_model; n += 8) {
+    float y = 0.f;
+    for (int k = lane; k < gd; k += 32) y = fmaf(du[k], load1(w, (size_t)n * total_cols + col0 + k, w_dtype), y);
+    y = warp_sum(y);
+    part += (double)y * (double)y;
+  }
+  if (lane == 0) red[warp] = part;
+  __syncthreads();
+  if (tid == 0) {
+    double s2 = 0.0;
+    for (int i = 0; i < 8; ++i) s2 += red[i];
+    atomicAdd(out + grp, s2);
+  }
+}
+
 __global__ void zero_f64_kernel(double* p, int n) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i < n) p[i] = 0.0;
@@ -205,15 +236,23 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
   causal_attn_kernel<<<dim3(n_qpos, hq), 128, attn_smem, s>>>(n_tok, n_qpos, n_kv_heads, gqa, w.qf,
                                                               w.kf, w.vf, w.o_ref);
   KVQ_TRY(cudaSuccess);
-  gram_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype,
-                                                               w.gram);
+  // ||du W^T||^2: directly when d_model <= gd, else through the group's Gram matrix
+  const bool direct = d_model <= gd;
+  if (!direct)
+    gram_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype, w.gram);
   zero_f64_kernel<<<1, 256, 0, s>>>(ref, n_groups);
   const int n_out = n_cand * n_clip * n_groups;
   zero_f64_kernel<<<(n_out + 255) / 256, 256, 0, s>>>(nmse, n_out);
   KVQ_TRY(cudaSuccess);
   const size_t form_smem = (size_t)gd * sizeof(float);
-  gram_form_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, w.o_ref,
-                                                                  nullptr, w.gram, ref);
+  auto out_err = [&](const float* a, const float* b, double* dst) {
+    if (direct)
+      proj_err_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, d_model, a, b, w_o,
+                                                                     w_dtype, dst);
+    else
+      gram_form_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, a, b, w.gram, dst);
+  };
+  out_err(w.o_ref, nullptr, ref);
   KVQ_TRY(cudaSuccess);
   for (int i = 0; i < n_cand; ++i) {
     const RotDev r = to_dev(cand[i]);
@@ -229,8 +268,7 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
       KVQ_TRY(cudaSuccess);
       KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.o_rot, r, w.o_un, true, s));
       double* slot = nmse + (size_t)(i * n_clip + c) * n_groups;
-      gram_form_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, w.o_un,
-                                                                      w.o_ref, w.gram, slot);
+      out_err(w.o_un, w.o_ref, slot);
       KVQ_TRY(cudaSuccess);
     }
   }

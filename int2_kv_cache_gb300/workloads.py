@@ -26,7 +26,14 @@ from dataclasses import dataclass, field
 import numpy as np
 
 HEAD_DIM = 128
-CLIPS_ENVELOPE = (1.00, 0.95, 0.90, 0.85, 0.80)
+
+
+def f32(x: float) -> float:
+    """A clip ratio as the kernels receive it (an IEEE float32 value)."""
+    return float(np.float32(x))
+
+
+CLIPS_ENVELOPE = tuple(f32(c) for c in (1.00, 0.95, 0.90, 0.85, 0.80))
 
 _TAG_Q, _TAG_K, _TAG_V, _TAG_PROFILE, _TAG_ROT, _TAG_WO, _TAG_TABLE, _TAG_CAL, _TAG_LENS, _TAG_NEW = range(10)
 
@@ -247,7 +254,7 @@ def decode_case(seed: int, seq_lens, n_q_heads: int, n_kv_heads: int, d_model: i
     table, nb = draw_block_table(seed, seq_lens, page_tokens, need + spare_blocks, shuffle)
     return DecodeCase(
         seed=seed, seq_lens=seq_lens, n_q_heads=n_q_heads, n_kv_heads=n_kv_heads, d_model=d_model,
-        dtype=dtype, page_tokens=page_tokens, clip_k=clip_k, clip_v=clip_v,
+        dtype=dtype, page_tokens=page_tokens, clip_k=f32(clip_k), clip_v=f32(clip_v),
         rot_k=make_rot(rot, seed, 0, n_kv_heads), rot_v=make_rot(rot, seed, 1, n_kv_heads),
         profile=draw_profile(seed, n_kv_heads, n_off=n_off), block_table=table, num_blocks=nb,
         n_cal=n_cal, name=name)
@@ -357,4 +364,4 @@ def small_calibration(seed: int, n_tok: int, n_qpos: int, n_kv_heads: int, gqa: 
     w = draw_wo(seed, d_model, n_kv_heads * gqa * HEAD_DIM, dtype)
     cands = [make_rot(kd, seed, 700 + i, n_kv_heads) for i, kd in enumerate(kinds)]
     return CalibCase(seed, n_tok, n_qpos, n_kv_heads, gqa, d_model, dtype, k, v, q, w, cands,
-                     tuple(clips), joint=joint, name="small_calib")
+                     tuple(f32(c) for c in clips), joint=joint, name="small_calib")

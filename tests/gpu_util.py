@@ -183,3 +183,12 @@ class GpuCase:
             kh, vh = oracle.cache.dequantized_sequence(ora_pool, c.n_kv_heads, c.page_tokens, c.block_table[b], n)
             out[b] = oracle.attention.decode_attention(q[b], kh, vh, self.r_k, c.gqa)
         return out
+
+
+def assert_nmse_close(got, ref, label=""):
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    rel = np.abs(got - ref) / np.abs(ref)
+    i = np.unravel_index(np.argmax(rel), rel.shape)
+    assert rel.max() <= NMSE_TOL, f"{label}: worst NMSE rel err {rel.max():.3g} at {i}: gpu {got[i]} oracle {ref[i]}"
+    return float(rel.max())

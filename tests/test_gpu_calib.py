@@ -37,8 +37,8 @@ def test_small_sweep_matches_oracle(joint, dtype):
     mu = oracle.cache.key_mean(cc.k).astype(np.float32)
     nm, ref = run_gpu_calib(cc, mu)
     nm_o, _, ref_o = oracle_calib(cc, mu)
-    assert np.all(np.abs(ref - ref_o) <= gu.NMSE_TOL * ref_o)
-    assert np.all(np.abs(nm - nm_o) <= gu.NMSE_TOL * nm_o), (nm, nm_o)
+    gu.assert_nmse_close(ref, ref_o, "ref")
+    gu.assert_nmse_close(nm, nm_o, "nmse")
     # the selection the caller makes agrees (unique argmin here)
     assert oracle.calib.select(nm) == oracle.calib.select(nm_o)
 
@@ -51,7 +51,7 @@ def test_evaluation_page_envelope_sweep():
     mu = oracle.cache.key_mean(cc.k).astype(np.float32)
     nm, ref = run_gpu_calib(cc, mu)
     nm_o, _, ref_o = oracle_calib(cc, mu)
-    assert np.all(np.abs(nm - nm_o) <= gu.NMSE_TOL * nm_o)
+    gu.assert_nmse_close(nm, nm_o, "envelope nmse")
     sel_gpu = oracle.calib.select(nm)[0]
     sel_ora = oracle.calib.select(nm_o)[0]
     # selections agree, or the GPU's pick is within tolerance of the oracle's minimum

@@ -126,7 +126,7 @@ def test_envelope_selection_then_fresh_queries():
         n_gpu.append(oracle.output.nmse(y[i], y_ref[0]))
         n_ora.append(oracle.output.nmse(y_o[0], y_ref[0]))
     n_gpu, n_ora = np.array(n_gpu), np.array(n_ora)
-    assert np.all(np.abs(n_gpu - n_ora) <= gu.NMSE_TOL * n_ora)
+    gu.assert_nmse_close(n_gpu, n_ora, "fresh-query nmse")
     m, sd = oracle.output.mean_popsd(n_gpu)
     tm, tsd = oracle.output.threshold_rate(n_gpu)
     print(f"envelope: selected candidate {ci} clip {clip}: NMSE {m:.6f} +- {sd:.6f}, threshold {tm:.2f} +- {tsd:.2f}")
@@ -204,5 +204,5 @@ def test_serve14b_calibration_sampled():
                       cc.w_o, [cc.cands[i] for i in sample], cc.clips, cc.joint)
     mats = [oracle.rotations.rot_matrices(x, cc.n_kv_heads) for x in sub.cands]
     nm_o, _, ref_o = oracle.calib.calib_sweep(sub.q, sub.k, sub.v, sub.w_o, mats, sub.clips, mu, sub.gqa, False)
-    assert np.all(np.abs(ref - ref_o) <= gu.NMSE_TOL * ref_o)
-    assert np.all(np.abs(nm[sample] - nm_o) <= gu.NMSE_TOL * nm_o)
+    gu.assert_nmse_close(ref, ref_o, "ref")
+    gu.assert_nmse_close(nm[sample], nm_o, "serve14b nmse")

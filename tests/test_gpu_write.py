@@ -28,7 +28,8 @@ def test_quantize_append_matches_oracle(rot, dtype, page, lengths, clips):
     g.kvq.kvq_device_check()
     ora_pool, encs = g.oracle_pool()
     gpool = pool.cpu().numpy()
-    stats = gu.compare_codes(gpool, ora_pool, case.n_kv_heads, page, case.block_table, g.lengths, encs, clips,
+    stats = gu.compare_codes(gpool, ora_pool, case.n_kv_heads, page, case.block_table, g.lengths, encs,
+                             (case.clip_k, case.clip_v),
                              label=f"{rot}/{dtype}/P{page}")
     # bytes of pages that no sequence owns stay untouched (zero) on both sides
     used = np.zeros(case.num_blocks, bool)
