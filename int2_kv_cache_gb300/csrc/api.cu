@@ -191,15 +191,10 @@ kvq_status kvq_quantize_append(const kvq_layout* layout, int n_seqs, int n_new_t
   unsigned* err = nullptr;
   KVQ_CHECK(device_error_word(&err));
   const kvq::PageGeom g = geom(layout);
-  const int P = layout->page_tokens;
-  cudaError_t e = kvq::launch_quantize_append(g, n_seqs, n_new_total, k, dtype, cu_new, start_pos,
-                                              block_table, kvq::to_dev(rot_k), mu_rot_k, clip_k,
-                                              0, 64 * P, pool, err, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "kvq_quantize_append (keys)");
-  e = kvq::launch_quantize_append(g, n_seqs, n_new_total, v, dtype, cu_new, start_pos, block_table,
-                                  kvq::to_dev(rot_v), nullptr, clip_v, 32 * P, 68 * P, pool, err,
-                                  stream);
-  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_quantize_append (values)");
+  cudaError_t e = kvq::launch_quantize_append(g, n_seqs, n_new_total, k, v, dtype, cu_new, start_pos,
+                                              block_table, kvq::to_dev(rot_k), kvq::to_dev(rot_v), mu_rot_k,
+                                              clip_k, clip_v, pool, err, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_quantize_append");
 }
 
 kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int max_seq_len,
@@ -263,6 +258,7 @@ kvq_status kvq_out_proj(int n_rows, int d_model, int k_dim, const float* x, cons
                         kvq_dtype w_dtype, float* y, kvq_stream stream) {
   if (n_rows < 0 || d_model < 1 || k_dim < 1)
     return fail(KVQ_EINVAL, "bad shape n_rows %d d_model %d k_dim %d", n_rows, d_model, k_dim);
+  if (k_dim % 32 != 0) return fail(KVQ_EUNSUPPORTED, "k_dim %d is not a multiple of 32", k_dim);
   if (!valid_dtype(w_dtype)) return fail(KVQ_EINVAL, "bad dtype %d", (int)w_dtype);
   if (n_rows == 0) return KVQ_OK;
   KVQ_PTR(x, "x");

@@ -70,11 +70,11 @@ cudaError_t launch_key_mean(int n_tok, int n_heads, const void* k, int dtype, fl
                             cudaStream_t s);
 cudaError_t launch_rotate_heads(int n_rows, int n_heads, int heads_per_rot, const float* x,
                                 RotDev rot, float* y, bool transpose, cudaStream_t s);
-cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* src,
-                                   int dtype, const int32_t* cu_new, const int32_t* start_pos,
-                                   const int32_t* table, RotDev rot, const float* mu_rot,
-                                   float clip, int codes_off, int meta_off, uint8_t* pool,
-                                   unsigned* err, cudaStream_t s);
+cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* k,
+                                   const void* v, int dtype, const int32_t* cu_new,
+                                   const int32_t* start_pos, const int32_t* table, RotDev rot_k,
+                                   RotDev rot_v, const float* mu_rot_k, float clip_k, float clip_v,
+                                   uint8_t* pool, unsigned* err, cudaStream_t s);
 cudaError_t launch_rotate_df(int n_rows, int n_heads, const void* src, int dtype, const float* mu,
                              RotDev rot, float* x_hi, float* x_lo, cudaStream_t s);
 cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x_lo, float clip,

@@ -79,48 +79,135 @@ __device__ __forceinline__ bool locate(int t, int n_seqs, const int32_t* cu_new,
 // Cache write: one warp per (token, head) group.  Lane l owns channels 4l..4l+3
 // and hence byte l of the packed group.  x = k R - mu R is formed in
 // double-float (Eq. 20 with the rotation's rounding errors carried), so the
-// quantization decisions are exact.
-// grid = (ceil(n_new / 8), n_kv_heads), block = 256.
+// quantization decisions are exact.  Keys and values are the two values of
+// blockIdx.z; a dense R_h is staged once per CTA in shared memory.
+// grid = (ceil(n_new / APPEND_TOK), n_kv_heads, 2), block = 256.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) append_kernel(
-    PageGeom g, int n_seqs, int n_new, const void* __restrict__ src, int dtype,
-    const int32_t* __restrict__ cu_new, const int32_t* __restrict__ start_pos,
-    const int32_t* __restrict__ table, RotDev rot, const float* __restrict__ mu_rot, float clip,
-    int codes_off, int meta_off, uint8_t* __restrict__ pool, unsigned* err) {
-  const int h = blockIdx.y;
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
-  if (t >= n_new) return;
-  long long rec;
-  int slot;
-  if (!locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, h)) return;
-  const float4 v = load4(src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
-  DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
-  rotate_df_warp(x, rot, h, lane);
-  if (mu_rot) {
-    const float4 m = __ldg(reinterpret_cast<const float4*>(mu_rot + (size_t)h * D) + lane);
-    x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
-    x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+constexpr int APPEND_TOK = 64;
+
+// x R for a dense R held in shared memory as [128 rows][32 float4], with four
+// independent compensated accumulation chains (terms c = 4m + u) per output.
+__device__ __forceinline__ void dense_rotate_df_smem(DF x[4], const float4* __restrict__ R4, int lane) {
+  float sh[4][4], sl[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sh[u][i] = sl[u][i] = 0.f;
+#pragma unroll 2
+  for (int m = 0; m < 32; ++m) {
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float xh = __shfl_sync(0xffffffffu, x[u].hi, m);  // channel 4m + u lives in lane m
+      const float xl = __shfl_sync(0xffffffffu, x[u].lo, m);
+      const float4 r4 = R4[(4 * m + u) * 32 + lane];
+      const float r[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __fmul_rn(xh, r[i]);
+        float pe = __fmaf_rn(xh, r[i], -p);
+        pe = __fmaf_rn(xl, r[i], pe);
+        const DF t = two_sum(sh[u][i], p);
+        sh[u][i] = t.hi;
+        sl[u][i] = __fadd_rn(sl[u][i], __fadd_rn(t.lo, pe));
+      }
+    }
   }
-  QParams qp;
-  const unsigned byte = quantize_warp_df(x, clip, qp);
-  uint8_t* recp = pool + (size_t)rec * g.record;
-  recp[codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
-  if (lane == 0)
-    *reinterpret_cast<uint32_t*>(recp + meta_off + META_BYTES * slot) =
-        (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const DF a = df_add(DF{sh[0][i], sl[0][i]}, DF{sh[1][i], sl[1][i]});
+    const DF b = df_add(DF{sh[2][i], sl[2][i]}, DF{sh[3][i], sl[3][i]});
+    x[i] = df_add(a, b);
+  }
 }
 
-cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* src,
-                                   int dtype, const int32_t* cu_new, const int32_t* start_pos,
-                                   const int32_t* table, RotDev rot, const float* mu_rot,
-                                   float clip, int codes_off, int meta_off, uint8_t* pool,
-                                   unsigned* err, cudaStream_t s) {
+struct AppendRole {
+  const void* src;
+  RotDev rot;
+  const float* mu_rot;
+  float clip;
+  int codes_off, meta_off;
+};
+struct AppendRoles {
+  AppendRole r[2];
+};
+
+template <bool DENSE>
+__global__ void __launch_bounds__(256, 1) append_kernel(
+    PageGeom g, int n_seqs, int n_new, int dtype, const int32_t* __restrict__ cu_new,
+    const int32_t* __restrict__ start_pos, const int32_t* __restrict__ table, AppendRoles roles,
+    uint8_t* __restrict__ pool, unsigned* err) {
+  extern __shared__ float4 s_r4[];  // dense only: R_h, 128 x 32 float4
+  const AppendRole ro = blockIdx.z ? roles.r[1] : roles.r[0];
+  const int h = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int t0 = blockIdx.x * APPEND_TOK;
+  const int t1 = min(n_new, t0 + APPEND_TOK);
+  if (DENSE) {
+    const float4* src = reinterpret_cast<const float4*>(ro.rot.dense + (size_t)h * D * D);
+    for (int i = threadIdx.x; i < D * D / 4; i += 256) s_r4[i] = __ldg(src + i);
+    __syncthreads();
+  }
+  for (int t = t0 + warp; t < t1; t += 8) {
+    long long rec;
+    int slot;
+    if (!locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, h)) continue;
+    const float4 v = load4(ro.src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
+    DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+    if (DENSE) dense_rotate_df_smem(x, s_r4, lane);
+    else rotate_df_warp(x, ro.rot, h, lane);
+    if (ro.mu_rot) {
+      const float4 m = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
+      x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
+      x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+    }
+    QParams qp;
+    const unsigned byte = quantize_warp_df(x, ro.clip, qp);
+    uint8_t* recp = pool + (size_t)rec * g.record;
+    recp[ro.codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
+    if (lane == 0)
+      *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
+          (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+  }
+}
+
+cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* k,
+                                   const void* v, int dtype, const int32_t* cu_new,
+                                   const int32_t* start_pos, const int32_t* table, RotDev rot_k,
+                                   RotDev rot_v, const float* mu_rot_k, float clip_k, float clip_v,
+                                   uint8_t* pool, unsigned* err, cudaStream_t s) {
   if (n_new == 0) return cudaSuccess;
-  dim3 grid((n_new + 7) / 8, g.n_kv_heads);
-  append_kernel<<<grid, 256, 0, s>>>(g, n_seqs, n_new, src, dtype, cu_new, start_pos, table, rot,
-                                     mu_rot, clip, codes_off, meta_off, pool, err);
-  return cudaGetLastError();
+  const int P = g.page_tokens;
+  AppendRoles roles;
+  roles.r[0] = AppendRole{k, rot_k, mu_rot_k, clip_k, 0, 64 * P};
+  roles.r[1] = AppendRole{v, rot_v, nullptr, clip_v, 32 * P, 68 * P};
+  const dim3 grid((n_new + APPEND_TOK - 1) / APPEND_TOK, g.n_kv_heads, 1);
+  const size_t smem = (size_t)D * D * sizeof(float);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(append_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  // keys and values may use different rotation kinds: one launch per kind
+  const bool kd = rot_k.kind == KVQ_ROT_DENSE, vd = rot_v.kind == KVQ_ROT_DENSE;
+  if (kd == vd) {
+    const dim3 g2(grid.x, grid.y, 2);
+    if (kd) append_kernel<true><<<g2, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
+    else append_kernel<false><<<g2, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
+    return cudaGetLastError();
+  }
+  for (int role = 0; role < 2; ++role) {
+    AppendRoles one;
+    one.r[0] = roles.r[role];
+    one.r[1] = roles.r[role];
+    if (role == 0 ? kd : vd)
+      append_kernel<true><<<grid, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
+    else
+      append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 // ---------------------------------------------------------------------------
