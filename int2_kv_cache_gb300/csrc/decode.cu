@@ -39,7 +39,11 @@ constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 4;
 constexpr int TILE_BYTES = 1152;  // 16 tokens x 72 bytes
 constexpr unsigned ERR_TIMEOUT = 8u;
-constexpr int WAIT_LIMIT = 1 << 22;
+constexpr uint32_t WAIT_HINT_NS = 100000;  // per try_wait: sleep up to 100 us
+constexpr int WAIT_LIMIT = 20000;          // then give up (>= 2 s): error flag, no hang
+// Lazy softmax rescaling: the running sums keep their reference maximum until a
+// tile's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
+constexpr float TAU = 6.f;
 // The fp16 remainder column carries (x - fp16(x)) * 2^11, keeping it out of the
 // subnormal range whenever the high part is normal.
 constexpr float LO_SCALE = 2048.f;
@@ -95,12 +99,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Waits (suspended, up to the time hint) for the phase with the given parity.
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n}"
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(WAIT_HINT_NS)
       : "memory");
   return ok != 0;
 }
@@ -175,6 +180,7 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
   __shared__ __align__(16) float qs[G][D];
   __shared__ float qsum[G], qexp[G];
   __shared__ float sm_m[DEC_WARPS][G], sm_l[DEC_WARPS][G];
+  __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit 0 / bit 1: first / second page copied
 
   int len = __ldg(seq_lens + b);
   if (len < 0 || len > g.max_blocks * g.page_tokens) {
@@ -189,40 +195,55 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
   const int my_tiles = t_end > t_begin + warp ? (t_end - t_begin - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
   const int32_t* trow = table + (size_t)b * g.max_blocks;
 
-  auto page_rec = [&](int page, bool* ok) -> const uint8_t* {
-    const int blk = __ldg(trow + page);
-    *ok = blk >= 0 && blk < g.num_blocks;
-    return pool + ((size_t)(*ok ? blk : 0) * g.n_kv_heads + h) * g.record;
-  };
-  // Issue the copy of the warp's i-th tile into its stage (lane 0 only).
-  auto issue = [&](int i) {
+  // Page ids of the warp's tiles, 32 tiles at a time in lane registers (lane l
+  // holds tile i0 + l); the producer reads them with shuffles.
+  int pc0 = -1, pc1 = -1;
+  auto fill_cache = [&](int i0) {
+    const int i = i0 + lane;
     const int tile = t_begin + warp + DEC_WARPS * i;
-    uint64_t* bar = &bars[warp][i % DEC_STAGES];
-    uint8_t* dst = stage[warp][i % DEC_STAGES];
-    fence_proxy_async();
-    if (P == 16) {
-      bool ok;
-      const uint8_t* src = page_rec(tile, &ok);
-      if (ok) {
-        mbar_arrive_expect_tx(bar, TILE_BYTES);
-        bulk_g2s(dst, src, TILE_BYTES, bar);
+    pc0 = -1;
+    pc1 = -1;
+    if (i < my_tiles) {
+      if (P == 16) {
+        pc0 = __ldg(trow + tile);
       } else {
-        flag_error(err, ERR_BLOCK_RANGE);
-        mbar_arrive(bar);
+        pc0 = __ldg(trow + 2 * tile);
+        pc1 = 2 * tile + 1 < n_pages ? __ldg(trow + 2 * tile + 1) : -2;  // -2: no second page
       }
-    } else {
-      bool ok0, ok1 = false;
-      const uint8_t* s0 = page_rec(2 * tile, &ok0);
-      const bool has1 = 2 * tile + 1 < n_pages;
-      const uint8_t* s1 = has1 ? page_rec(2 * tile + 1, &ok1) : nullptr;
-      if (!ok0 || (has1 && !ok1)) flag_error(err, ERR_BLOCK_RANGE);
-      const uint32_t bytes = (ok0 ? 576u : 0u) + (ok1 ? 576u : 0u);
-      if (bytes) {
-        mbar_arrive_expect_tx(bar, bytes);
-        if (ok0) bulk_g2s(dst, s0, 576, bar);
-        if (ok1) bulk_g2s(dst + 576, s1, 576, bar);
+    }
+  };
+  // Issue the copy of the warp's i-th tile into its stage.  Called by the whole warp.
+  auto issue = [&](int i) {
+    if (i % 32 == 0 && i > 0) fill_cache(i);
+    const int blk0 = __shfl_sync(0xffffffffu, pc0, i % 32);
+    const int blk1 = __shfl_sync(0xffffffffu, pc1, i % 32);
+    if (lane == 0) {
+      const int sidx = i % DEC_STAGES;
+      uint64_t* bar = &bars[warp][sidx];
+      uint8_t* dst = stage[warp][sidx];
+      const bool ok0 = blk0 >= 0 && blk0 < g.num_blocks;
+      const bool ok1 = P == 16 ? ok0 : (blk1 >= 0 && blk1 < g.num_blocks);
+      if (!ok0 || (P == 8 && blk1 != -2 && !ok1)) flag_error(err, ERR_BLOCK_RANGE);
+      sflag[warp][sidx] = (ok0 ? 1 : 0) | (ok1 ? 2 : 0);
+      fence_proxy_async();
+      const size_t stride = (size_t)g.n_kv_heads * g.record;
+      const uint8_t* base = pool + (size_t)h * g.record;
+      if (P == 16) {
+        if (ok0) {
+          mbar_arrive_expect_tx(bar, TILE_BYTES);
+          bulk_g2s(dst, base + (size_t)blk0 * stride, TILE_BYTES, bar);
+        } else {
+          mbar_arrive(bar);
+        }
       } else {
-        mbar_arrive(bar);
+        const uint32_t bytes = (ok0 ? 576u : 0u) + (ok1 ? 576u : 0u);
+        if (bytes) {
+          mbar_arrive_expect_tx(bar, bytes);
+          if (ok0) bulk_g2s(dst, base + (size_t)blk0 * stride, 576, bar);
+          if (ok1) bulk_g2s(dst + 576, base + (size_t)blk1 * stride, 576, bar);
+        } else {
+          mbar_arrive(bar);
+        }
       }
     }
   };
@@ -232,8 +253,8 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
     fence_mbar_init();
   }
   __syncwarp();
-  if (lane == 0)
-    for (int i = 0; i < DEC_STAGES && i < my_tiles; ++i) issue(i);
+  fill_cache(0);
+  for (int i = 0; i < DEC_STAGES && i < my_tiles; ++i) issue(i);
 
   // ---- prologue: q'_j = q_j R_K,h * log2(e)/sqrt(128) (Eq. 22) ----
   for (int jj = warp; jj < G; jj += DEC_WARPS) {
@@ -319,19 +340,8 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
     const uint8_t* st = stage[warp][sidx];
     // rows valid: position < len and its page's block id in range
     const int nv = min(16, len - tile * 16);
-    bool half_ok[2];
-    {
-      if (P == 16) {
-        const int blk = __ldg(trow + tile);
-        half_ok[0] = half_ok[1] = blk >= 0 && blk < g.num_blocks;
-      } else {
-        const int b0 = __ldg(trow + 2 * tile);
-        half_ok[0] = b0 >= 0 && b0 < g.num_blocks;
-        const bool has1 = 2 * tile + 1 < n_pages;
-        const int b1 = has1 ? __ldg(trow + 2 * tile + 1) : -1;
-        half_ok[1] = has1 && b1 >= 0 && b1 < g.num_blocks;
-      }
-    }
+    const int fl = sflag[warp][sidx];
+    const bool half_ok[2] = {(fl & 1) != 0, (fl & 2) != 0};
     const bool row0_ok = gi < nv && half_ok[0];
     const bool row1_ok = gi + 8 < nv && half_ok[1];
 
@@ -361,7 +371,6 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
     const float2 vm1 = meta_pair(st + TileLayout<P>::vm(gi + 8));
 
     uint32_t bp[NT][2];
-    float alphas[NT];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
       const float dot0 = fmaf(d[nt][1], LO_UNSCALE, d[nt][0]) * my_dscale[nt];
@@ -372,9 +381,10 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float mnew = fmaxf(m[nt], mx);
-      const float msafe = mnew == -INFINITY ? 0.f : mnew;
-      const float alpha = exp2f(m[nt] - msafe);
+      const bool need = mx > m[nt] + TAU;  // reference max moves only by > TAU
+      const float alpha = need ? exp2f(m[nt] - mx) : 1.f;
+      if (need) m[nt] = mx;
+      const float msafe = m[nt] == -INFINITY ? 0.f : m[nt];
       const float p0 = exp2f(sc0 - msafe), p1 = exp2f(sc1 - msafe);
       float ps = p0 + p1;
       float pz = (row0_ok ? p0 * fmaf(1.5f, vm0.x, vm0.y) : 0.f) + (row1_ok ? p1 * fmaf(1.5f, vm1.x, vm1.y) : 0.f);
@@ -386,8 +396,12 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
       pz += __shfl_xor_sync(0xffffffffu, pz, 16);
       l[nt] = fmaf(l[nt], alpha, ps);
       zacc[nt] = fmaf(zacc[nt], alpha, pz);
-      m[nt] = mnew;
-      alphas[nt] = alpha;
+      if (__any_sync(0xffffffffu, need)) {
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          acc[nt][r][0] *= alpha; acc[nt][r][1] *= alpha; acc[nt][r][2] *= alpha; acc[nt][r][3] *= alpha;
+        }
+      }
       // weights p_t s_t of this lane's rows, then gathered into the B fragment:
       // k = 2t, 2t+1, 2t+8, 2t+9 <-> tokens t, t+4, t+8, t+12; column g <-> head g/2, part g&1
       const float w0 = row0_ok ? p0 * vm0.x : 0.f;
@@ -434,17 +448,11 @@ __global__ void __launch_bounds__(128) decode_split_kernel(
           a[u] = centered_codes(src & mask, pp);
         }
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          // this tile's sum in a fresh accumulator, folded into the running sum in fp32
-          float dt[4] = {0.f, 0.f, 0.f, 0.f};
-          mma16816(dt, a[0], a[1], a[2], a[3], bp[nt][0], bp[nt][1]);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) acc[nt][r][u] = fmaf(acc[nt][r][u], alphas[nt], dt[u]);
-        }
+        for (int nt = 0; nt < NT; ++nt) mma16816(acc[nt][r], a[0], a[1], a[2], a[3], bp[nt][0], bp[nt][1]);
       }
     }
     __syncwarp();
-    if (lane == 0 && i + DEC_STAGES < my_tiles) issue(i + DEC_STAGES);
+    if (i + DEC_STAGES < my_tiles) issue(i + DEC_STAGES);
   }
   if (aborted) {
     // wait (bounded) for the copies still in flight before the stages go away
