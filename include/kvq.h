@@ -168,6 +168,28 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
                                 int n_splits, void* workspace, size_t workspace_bytes,
                                 float* o_rot, kvq_stream stream);
 
+/* The same decode attention for callers that cannot allocate device memory
+ * (the paper has no counterpart; this is a deployment convenience).
+ * Serving engines that reserve all device memory up front and forbid allocation
+ * while requests are in flight, and host frameworks that hand a plugin only the
+ * tensors it reads and writes, cannot provide kvq_decode_attention's workspace.
+ * This variant keeps the split partials in a fixed 4 MiB buffer inside the
+ * library (a __device__ array that every GPU loading the library holds until
+ * process exit) and allocates nothing.
+ *   - Arguments are those of kvq_decode_attention without the workspace.
+ *   - If the partials need more than 4 MiB (kvq_decode_workspace_size), it
+ *     returns KVQ_EUNSUPPORTED with a message naming both sizes.
+ *   - The first call on each device looks up the buffer's device address; make
+ *     that first call, with the device current, before any stream capture.
+ *   - All calls share the buffer: calls that overlap on the GPU (other streams,
+ *     other host threads) race and must be serialised by the caller.  Each call
+ *     writes every byte of scratch it reads, so nothing needs clearing. */
+kvq_status kvq_decode_attention_noalloc(const kvq_layout* layout, int n_seqs, const void* q,
+                                        kvq_dtype q_dtype, const int32_t* seq_lens, int max_seq_len,
+                                        const int32_t* block_table, kvq_rot rot_k,
+                                        const uint8_t* pool, int n_splits, float* o_rot,
+                                        kvq_stream stream);
+
 /* W_O folding (OptR Eqs. 29-31): for query head j with KV head h = j / (H_q / H_kv),
  *   w_folded[:, j*128:(j+1)*128] = w_o[:, j*128:(j+1)*128] R_V,h
  * w_o: [d_model][n_q_heads*128] of w_dtype; w_folded: same shape, out_dtype

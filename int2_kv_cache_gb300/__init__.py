@@ -58,6 +58,7 @@ def lib() -> ctypes.CDLL:
             "kvq_quantize_append": ([lp, i, i, vp, vp, i, vp, vp, vp, KvqRot, KvqRot, vp, f, f, vp, vp], st),
             "kvq_decode_workspace_size": ([lp, i, i, i, ctypes.POINTER(sz)], st),
             "kvq_decode_attention": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, sz, vp, vp], st),
+            "kvq_decode_attention_noalloc": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, vp], st),
             "kvq_fold_wo": ([i, i, i, vp, i, KvqRot, vp, i, vp], st),
             "kvq_out_proj": ([i, i, i, vp, vp, i, vp, vp], st),
             "kvq_calib_workspace_size": ([i, i, i, i, i, ctypes.POINTER(sz)], st),
@@ -73,7 +74,8 @@ def lib() -> ctypes.CDLL:
 
 
 EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mean", "kvq_rotate_heads",
-            "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention", "kvq_fold_wo",
+            "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention",
+            "kvq_decode_attention_noalloc", "kvq_fold_wo",
             "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse")
 
 
@@ -177,6 +179,16 @@ def kvq_decode_attention(layout: KvqLayout, q, seq_lens, max_seq_len: int, block
                                       _ptr(seq_lens), max_seq_len, _ptr(block_table), rot_k.c, _ptr(pool),
                                       n_splits, _ptr(workspace), workspace.numel() * workspace.element_size(),
                                       _ptr(o_rot), _stream(stream)))
+
+
+def kvq_decode_attention_noalloc(layout: KvqLayout, q, seq_lens, max_seq_len: int, block_table,
+                                 rot_k: DeviceRot, pool, o_rot, n_splits: int = 0, stream=None) -> None:
+    """Decode attention without a caller-provided workspace (for callers that may
+    not allocate device memory); the split partials live in a fixed library buffer."""
+    n_seqs = q.shape[0]
+    _check(lib().kvq_decode_attention_noalloc(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _dtype_code(q),
+                                              _ptr(seq_lens), max_seq_len, _ptr(block_table), rot_k.c, _ptr(pool),
+                                              n_splits, _ptr(o_rot), _stream(stream)))
 
 
 def kvq_fold_wo(w_o, n_q_heads: int, n_kv_heads: int, rot_v: DeviceRot, w_folded, stream=None) -> None:

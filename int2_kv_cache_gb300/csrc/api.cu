@@ -117,6 +117,8 @@ kvq::PageGeom geom(const kvq_layout* L) {
 
 }  // namespace
 
+kvq_status kvq::set_error(kvq_status st, const char* msg) { return fail(st, "%s", msg); }
+
 extern "C" {
 
 const char* kvq_last_error(void) { return g_last_error.c_str(); }

@@ -65,6 +65,9 @@ __device__ __forceinline__ float load1(const void* base, size_t elem, int dtype)
 // ---- launchers implemented in the kernel translation units (C++ linkage, internal) ----
 namespace kvq {
 
+// api.cu: record `msg` as this thread's kvq_last_error() text and return `st`.
+kvq_status set_error(kvq_status st, const char* msg);
+
 // quantize.cu
 cudaError_t launch_key_mean(int n_tok, int n_heads, const void* k, int dtype, float* mu,
                             cudaStream_t s);
