@@ -191,11 +191,11 @@ class DecodeStep:
         self.splits = splits
         ws = kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, splits)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
-        self.n_splits_used = ws // (n_seqs * self.hq * 130 * 4)
+        self.n_splits_used = (ws // (n_seqs * self.hq * 4) - 128) // 130
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
         self.y = torch.empty(n_seqs, self.dm, device=device)
         self.host_y = torch.empty(n_seqs, self.dm).pin_memory()
-        self.launches_per_step = 2 + 2 + 1
+        self.launches_per_step = 1 + 3 + 1  # append (K and V), qprep + split + combine, W_O
 
     def step(self, ev=None):
         kvq = self.kvq
@@ -231,6 +231,7 @@ class DecodeStep:
             "block_table": B * ((L + 15) // 16) * 4,
             "rotation": hkv * 128 * 128 * 4,
             "partials_write_read": 2 * B * hq * s * 130 * 4,
+            "rotated_q_write_read": 2 * B * hq * 128 * 4,
             "o_rot": B * hq * 128 * 4,
         }
 

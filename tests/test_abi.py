@@ -59,9 +59,9 @@ def test_pool_bytes(kvq):
 
 def test_decode_workspace_size(kvq):
     lay = _layout(kvq)
-    assert kvq.kvq_decode_workspace_size(lay, 16, 160, 5) == 16 * 32 * 5 * 130 * 4
+    assert kvq.kvq_decode_workspace_size(lay, 16, 160, 5) == 16 * 32 * (5 * 130 + 128) * 4
     auto = kvq.kvq_decode_workspace_size(lay, 16, 160, 0)
-    assert auto % (16 * 32 * 130 * 4) == 0 and auto > 0
+    assert (auto // (16 * 32 * 4) - 128) % 130 == 0 and auto > 0
 
 
 def _status(kvq, fn, *args):
