@@ -41,8 +41,8 @@ FALLBACK_HBM_GBS = 6800.0
 def parse():
     p = argparse.ArgumentParser()
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=20)
-    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     p.add_argument("--case", choices=["decode_step", "append_chunk", "calib"], default="decode_step")
     p.add_argument("--seqs", type=int, default=16)
@@ -67,22 +67,38 @@ def dist_env():
 
 
 class Clocks:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock and throttle reasons; only the samples
+    whose timestamps fall inside the timed region are reported."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int, enabled: bool = True):
+    def __init__(self, device_index: int, enabled: bool = True, interval_ms: int = 20):
         self.proc = None
-        self.gpu = gpu_index
+        self.t0 = self.t1 = None
         if enabled:
+            sel = str(device_index)
             try:
-                self.proc = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                                              "--format=csv,noheader,nounits", "-lms", "200"],
+                import torch
+                uuid = str(getattr(torch.cuda.get_device_properties(device_index), "uuid", "") or "")
+                if uuid:
+                    sel = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+            except Exception:
+                pass
+            try:
+                self.proc = subprocess.Popen(["nvidia-smi", "-i", sel, f"--query-gpu={self.FIELDS}",
+                                              "--format=csv,noheader,nounits", "-lms", str(interval_ms)],
                                              stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                time.sleep(0.5)  # let the sampler start before the timed region
             except Exception:
                 self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_stop(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -93,23 +109,30 @@ class Clocks:
         except Exception:
             self.proc.kill()
             out = ""
-        sm, mx, reasons = [], None, set()
+        import datetime
+        sm, mx, reasons, n_all = [], None, set(), 0
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                clk, cmax = float(f[1]), float(f[2])
             except ValueError:
                 continue
+            n_all += 1
+            if self.t0 is None or not (self.t0 <= ts <= self.t1):
+                continue
+            sm.append(clk)
+            mx = cmax
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
         if not sm:
             return None
-        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm), "window_s": round(self.t1 - self.t0, 3)}
 
 
 def traffic_record(kernel_file: str, key: str):
@@ -191,11 +214,13 @@ class DecodeStep:
         self.splits = splits
         ws = kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, splits)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
-        self.n_splits_used = (ws // (n_seqs * self.hq * 4) - 128) // 130
+        # thread blocks of the decode kernel (the library's choice when splits == 0)
+        self.n_ctas = splits or next(s for s in range(1, 1025)
+                                     if kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, s) == ws)
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
         self.y = torch.empty(n_seqs, self.dm, device=device)
         self.host_y = torch.empty(n_seqs, self.dm).pin_memory()
-        self.launches_per_step = 1 + 3 + 1  # append (K and V), qprep + split + combine, W_O
+        self.launches_per_step = 1 + 3 + 1  # append (K and V), query prep + decode + combine, W_O
 
     def step(self, ev=None):
         kvq = self.kvq
@@ -223,15 +248,19 @@ class DecodeStep:
 
     def decode_bytes(self) -> dict:
         B, L, hq, hkv = self.B, self.L, self.hq, self.hkv
-        s = self.n_splits_used
+        g = hq // hkv
+        units = B * hkv
+        # one partial (acc[128], m, l per query head) per (warp slice, unit) pair:
+        # at most 4 * n_ctas + units of them, written once and read once
+        pairs = min(4 * self.n_ctas + units, units * ((L + 31) // 32))
         cache = B * L * hkv * 72
         return {
             "kv_cache": cache,
             "q": B * hq * 128 * 2,
             "block_table": B * ((L + 15) // 16) * 4,
             "rotation": hkv * 128 * 128 * 4,
-            "partials_write_read": 2 * B * hq * s * 130 * 4,
-            "rotated_q_write_read": 2 * B * hq * 128 * 4,
+            "query_fragments_write_read": 2 * units * (((g + 3) // 4) * 16 * 32 * 4 + g * 16),
+            "partials_write_read": 2 * pairs * g * 130 * 4,
             "o_rot": B * hq * 128 * 4,
         }
 
@@ -261,11 +290,13 @@ def run_gpu(args):
     clocks = Clocks(local, enabled=not args.no_clocks)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
+    clocks.mark_start()
     start.record(stream)
     for i in range(args.steps):
         w.step(evs[i])
     stop.record(stream)
     barrier()
+    clocks.mark_stop()
     clk = clocks.stop()
     total_ms = start.elapsed_time(stop)
     t_app = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
@@ -313,14 +344,14 @@ def run_gpu(args):
             "workload": f"gqa8b decode step: B={w.B} x ctx {w.L}, Hq 32 / Hkv 8, d 128, hidden 4096, "
                         "16-token pages (shuffled), dense expm(A-A^T) rotations, mu-centred keys, clip 1.0",
             "batch": w.B, "ctx": w.L, "n_q_heads": w.hq, "n_kv_heads": w.hkv, "d_model": w.dm,
-            "n_splits": w.n_splits_used, "parallelism": f"replicas x{world}",
+            "decode_ctas": w.n_ctas, "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (w.pool.numel() / 1e6),
         },
         "kernel_ms": {"quantize_append": t_app, "decode_attention": t_dec, "out_proj": t_out},
         "kv_cache_gbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9,
         "kv_cache_pct_of_peak": {"measured": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / peak,
                                  "nominal_8tbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / NOMINAL_HBM_GBS},
-        "roofline": {"kernel": "kvq_decode_attention (split + combine)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": "kvq_decode_attention (query prep + decode + combine)", "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": alg, "bytes": by},
         "e2e": {"value": world * w.B / (e2e_step * 1e-3), "unit": "tokens/s",

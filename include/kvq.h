@@ -146,7 +146,8 @@ kvq_status kvq_quantize_append(const kvq_layout* layout, int n_seqs, int n_new_t
                                uint8_t* pool, kvq_stream stream);
 
 /* Workspace bytes needed by kvq_decode_attention for this many sequences and
- * splits (n_splits = 0: the count the library would choose for max_seq_len). */
+ * work partitions (n_splits = 0: the count the library would choose for
+ * max_seq_len).  Computed on the host from the arguments alone. */
 kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int max_seq_len,
                                      int n_splits, size_t* bytes);
 
@@ -156,10 +157,17 @@ kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int m
  *   a_s    = q'_j . (zero_s + scale_s * codeK_s) / sqrt(128),   s < seq_lens[b]
  *   p      = softmax(a)
  *   o_rot[b][j] = sum_s p_s (zero_s + scale_s * codeV_s)      (rotated-V basis)
- * computed as n_splits partial softmaxes over contiguous page ranges merged by a
- * log-sum-exp combine.  A sequence of length 0 yields a zero vector.
+ * The cached tokens of the batch, taken as one list of (sequence, KV head,
+ * 32-token chunk) entries, are cut into 4 * n_splits equal contiguous slices
+ * (n_splits thread blocks of 4 warps; 0 = the library's choice, one full wave
+ * of the GPU).  Each slice yields a partial softmax per (sequence, KV head) it
+ * touches, and the partials of a unit are merged by a log-sum-exp combine in
+ * slice order, so the result does not depend on timing.  A sequence of
+ * length 0 yields a zero vector.  Out-of-range lengths or block ids are
+ * flagged (kvq_device_check) and the affected outputs are unspecified.
  *   q:       [n_seqs][n_q_heads][128] of q_dtype
- *   seq_lens int32 [n_seqs]; max_seq_len (host) >= every seq_lens[b]
+ *   seq_lens int32 [n_seqs]; max_seq_len (host) >= every seq_lens[b];
+ *            n_seqs <= 65535 and n_seqs * n_kv_heads * ceil(max_seq_len / 32) < 2^30
  *   o_rot:   float [n_seqs][n_q_heads][128] (written)
  *   workspace: >= kvq_decode_workspace_size bytes, 16-byte aligned. */
 kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void* q,
@@ -177,8 +185,11 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
  * library (a __device__ array that every GPU loading the library holds until
  * process exit) and allocates nothing.
  *   - Arguments are those of kvq_decode_attention without the workspace.
- *   - If the partials need more than 4 MiB (kvq_decode_workspace_size), it
- *     returns KVQ_EUNSUPPORTED with a message naming both sizes.
+ *   - With n_splits = 0 it takes the largest number of work partitions, up
+ *     to the library's choice, whose partials fit in the buffer.  If the
+ *     partials still need more than 4 MiB (kvq_decode_workspace_size), or an
+ *     explicit n_splits needs more, it returns KVQ_EUNSUPPORTED with a
+ *     message naming both sizes.
  *   - The first call on each device looks up the buffer's device address; make
  *     that first call, with the device current, before any stream capture.
  *   - All calls share the buffer: calls that overlap on the GPU (other streams,

@@ -199,15 +199,28 @@ kvq_status kvq_quantize_append(const kvq_layout* layout, int n_seqs, int n_new_t
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_quantize_append");
 }
 
+// Index ranges the decode kernels keep in 32-bit integers.
+static kvq_status check_decode_size(const kvq_layout* layout, int n_seqs, int max_seq_len) {
+  if (n_seqs > 65535) return fail(KVQ_EUNSUPPORTED, "n_seqs %d > 65535", n_seqs);
+  const long long entries = (long long)n_seqs * layout->n_kv_heads * ((max_seq_len + 31) / 32);
+  if (entries >= (1ll << 30)) return fail(KVQ_EUNSUPPORTED, "%lld cached 32-token chunks per call", entries);
+  if ((long long)layout->num_blocks * layout->n_kv_heads >= (1ll << 31))
+    return fail(KVQ_EUNSUPPORTED, "num_blocks * n_kv_heads >= 2^31");
+  if ((long long)layout->max_blocks_per_seq * layout->page_tokens >= (1ll << 31))
+    return fail(KVQ_EUNSUPPORTED, "max_blocks_per_seq * page_tokens >= 2^31");
+  return KVQ_OK;
+}
+
 kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int max_seq_len,
                                      int n_splits, size_t* bytes) {
   KVQ_CHECK(check_layout(layout, true));
   if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");
   if (n_seqs < 0 || max_seq_len < 0 || n_splits < 0 || n_splits > 1024)
     return fail(KVQ_EINVAL, "bad n_seqs %d / max_seq_len %d / n_splits %d", n_seqs, max_seq_len, n_splits);
-  const int s = n_splits ? n_splits
-                         : kvq::decode_auto_splits(n_seqs, layout->n_kv_heads, max_seq_len, layout->page_tokens);
-  *bytes = kvq::decode_workspace_bytes(n_seqs, layout->n_q_heads, s);
+  KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
+  const int gqa = layout->n_q_heads / layout->n_kv_heads;
+  const int s = n_splits ? n_splits : kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, gqa, max_seq_len);
+  *bytes = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s);
   return KVQ_OK;
 }
 
@@ -229,9 +242,10 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
   KVQ_PTR(pool, "pool");
   KVQ_PTR(o_rot, "o_rot");
   KVQ_PTR(workspace, "workspace");
-  const int s = n_splits ? n_splits
-                         : kvq::decode_auto_splits(n_seqs, layout->n_kv_heads, max_seq_len, layout->page_tokens);
-  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_q_heads, s);
+  KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
+  const int gqa = layout->n_q_heads / layout->n_kv_heads;
+  const int s = n_splits ? n_splits : kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, gqa, max_seq_len);
+  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s);
   if (workspace_bytes < need)
     return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
   unsigned* err = nullptr;

@@ -1,5 +1,4 @@
-// Read path: split-K decode attention straight off the packed INT2 pages, and
-// the log-sum-exp combine of the split partials.
+// Read path: split-K decode attention straight off the packed INT2 pages.
 //
 // "Output-Aware Rotation for INT2 KV-Cache Quantization": Eqs. 1-2 and 5
 // (logits <q, k~>/sqrt(d), softmax over the cached positions, o = p^T V~),
@@ -11,25 +10,34 @@
 //   sum_t p_t (z_t + s_t c_t) = sum_t (p_t s_t) c_t + sum_t p_t z_t
 // so both contractions run on the codes c in {0,1,2,3}.
 //
-// Kernel structure (one CTA = one (sequence, KV head, split), 4 warps):
-// * each warp owns every 4th 32-token chunk of the split and streams its
-//   chunks through a ring of shared-memory stages with cp.async.bulk copies
-//   completed on mbarriers (two 1,152-byte page records per stage for 16-token
-//   pages, four 576-byte records for 8-token pages), one page per lane;
-// * q'.c and sum_t (p_t s_t) c_t are warp-level tensor-core products
-//   (mma.sync m16n8k16, fp16 inputs, fp32 accumulation).  A 2-bit field masked
-//   in place inside a 16-bit word is the fp16 value c * 2^(p-24) (a subnormal,
-//   p = the field's bit offset), so the operands need one logical operation per
-//   two codes, and the power-of-two factor is compensated exactly in the other
-//   operand.  The value codes are read transposed (ldmatrix .trans) so that
-//   each register holds two tokens of one channel group, as the product wants.
-//   The fp32 operand of each product (the rotated query, the weights p_t s_t)
-//   is split into an fp16 high part and an fp16 remainder occupying the two
-//   MMA columns of one head, which keeps ~22 significant bits;
-// * the softmax runs online in base 2 per warp with a lazy reference maximum;
-//   the four warps are merged in shared memory and the split's partial
-//   (m, l, unnormalised acc) is written.
-// A second kernel merges the splits.
+// Three kernels per call:
+// * qprep_kernel, one CTA per (sequence, KV head): rotates the query heads of
+//   the group (Eq. 22), folds in log2(e)/sqrt(128), and lays the result out as
+//   the tensor-core B fragments every decode warp loads as is;
+// * decode_split_kernel, a fixed grid of 4 CTAs (3 for 8 query heads per KV
+//   head) per SM.  The (sequence, KV head, 32-token chunk) list of the whole
+//   batch is cut into one contiguous, equal slice per warp, so every warp has
+//   the same work whatever the sequence lengths.  A warp streams its chunks
+//   through a ring of shared-memory stages (cp.async.bulk copies completed on
+//   mbarriers, one page record per lane), and for every (sequence, KV head)
+//   unit its slice touches it writes one partial softmax (m, l, unnormalised
+//   acc);
+// * decode_combine_kernel, one CTA per (unit, query head): the log-sum-exp
+//   merge of the unit's partials in a fixed order (deterministic).
+// The second and third kernels are programmatic dependent launches: the batch
+// scan and the first page copies overlap the query rotation, and the combine
+// blocks are scheduled as decode blocks retire.
+// Inside a warp, q'.c and sum_t (p_t s_t) c_t are tensor-core products
+// (mma.sync m16n8k16, fp16 inputs, fp32 accumulation).  A 2-bit field masked in
+// place inside a 16-bit word is the fp16 value c * 2^(p-24) (a subnormal, p =
+// the field's bit offset), so the operands need one logical operation per two
+// codes, and the power-of-two factor is compensated exactly in the other
+// operand.  The value codes are read transposed (ldmatrix .trans) so that each
+// register holds two tokens of one channel group, as the product wants.  The
+// fp32 operand of each product (the rotated query, the weights p_t s_t) is
+// split into an fp16 high part and an fp16 remainder occupying the two MMA
+// columns of one head, which keeps ~22 significant bits.  The softmax runs
+// online in base 2 with a lazy reference maximum.
 #include <type_traits>
 
 #include "quant_common.cuh"
@@ -39,50 +47,70 @@ namespace kvq {
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 4;
+constexpr int SM_COUNT = 152;  // GB300
 constexpr unsigned ERR_TIMEOUT = 8u;
 constexpr uint32_t WAIT_HINT_NS = 100000;  // per try_wait: sleep up to 100 us
 constexpr int WAIT_LIMIT = 20000;          // then give up (>= 2 s): error flag, no hang
 // Lazy softmax rescaling: the running sums keep their reference maximum until a
-// tile's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
+// chunk's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
 constexpr float TAU = 6.f;
 // The fp16 remainder column carries (x - fp16(x)) * 2^11, keeping it out of the
 // subnormal range whenever the high part is normal.
 constexpr float LO_SCALE = 2048.f;
 constexpr float LO_UNSCALE = 1.f / 2048.f;
+constexpr int PART = D + 4;  // floats per head in a partial: acc[128], m (log2 units), l, 2 pad (16-byte rows)
 
-struct Partials {
-  float* acc;  // [B][Hq][S][128]
-  float* ml;   // [B][Hq][S][2]: running max (log2 units), sum
+__host__ __device__ constexpr int ctas_per_sm(int gqa) { return gqa >= 8 ? 3 : 4; }
+__host__ __device__ constexpr int n_tiles(int gqa) { return (gqa + 3) / 4; }
+
+// Workspace regions (each 256-byte aligned):
+//   part   [n_slots][gqa][132] fp32 partials, n_slots = 4 * n_ctas + U; the
+//          partial of warp w for unit u lives in slot w + u (the units a warp
+//          slice touches are consecutive, so slots never collide)
+//   qfrag  [U][16 * NT][32] u32: query B fragments, lane-major
+//   qconst [U][gqa][4] fp32: dscale, sum(q')/dscale, TAU/dscale, 0
+//   span   [U] int2: the warp slices (k0, k1) that meet the unit, (1, 0) if none
+// with U = n_seqs * n_kv_heads units (sequence b, KV head h) -> u = b * n_kv_heads + h.
+struct DecWs {
+  float* part;
+  uint32_t* qfrag;
+  float* qconst;
+  int2* span;
 };
 
-__host__ __device__ inline Partials partials_from_ws(void* ws, int n_seqs, int n_q_heads, int n_splits) {
-  Partials p;
-  p.acc = static_cast<float*>(ws);
-  p.ml = p.acc + (size_t)n_seqs * n_q_heads * n_splits * D;
-  return p;
+__host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+__host__ __device__ inline size_t decode_ws_layout(void* base, int n_seqs, int n_kv_heads, int gqa, int n_ctas,
+                                                   DecWs* out) {
+  const size_t units = (size_t)n_seqs * n_kv_heads;
+  const size_t slots = (size_t)DEC_WARPS * n_ctas + units;
+  const size_t o_part = 0;
+  const size_t o_frag = align256(o_part + slots * gqa * PART * sizeof(float));
+  const size_t o_const = align256(o_frag + units * 16 * n_tiles(gqa) * 32 * sizeof(uint32_t));
+  const size_t o_span = align256(o_const + units * gqa * 4 * sizeof(float));
+  const size_t total = align256(o_span + units * sizeof(int2));
+  if (out) {
+    char* p = static_cast<char*>(base);
+    out->part = reinterpret_cast<float*>(p + o_part);
+    out->qfrag = reinterpret_cast<uint32_t*>(p + o_frag);
+    out->qconst = reinterpret_cast<float*>(p + o_const);
+    out->span = reinterpret_cast<int2*>(p + o_span);
+  }
+  return total;
 }
 
-// Workspace: partials acc [B][Hq][S][128], (m, l) [B][Hq][S][2], then the rotated,
-// pre-scaled queries q' [B][Hq][128] (fp32).
-__host__ __device__ inline float* rotated_q_from_ws(void* ws, int n_seqs, int n_q_heads, int n_splits) {
-  return static_cast<float*>(ws) + (size_t)n_seqs * n_q_heads * n_splits * (D + 2);
+size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas) {
+  return decode_ws_layout(nullptr, n_seqs, n_kv_heads, gqa, n_ctas, nullptr);
 }
 
-size_t decode_workspace_bytes(int n_seqs, int n_q_heads, int n_splits) {
-  return (size_t)n_seqs * n_q_heads * (n_splits * (D + 2) + D) * sizeof(float);
-}
-
-int decode_auto_splits(int n_seqs, int n_kv_heads, int max_seq_len, int page_tokens) {
-  (void)page_tokens;
-  const int chunks = (max_seq_len + 31) / 32;
-  const long long units = (long long)n_seqs * n_kv_heads;
-  const int target = 152 * 4;
-  int s = (int)((target + units - 1) / units);
-  const int cap = chunks / 8 > 1 ? chunks / 8 : 1;  // keep >= 8 chunks (2 per warp) per split
-  if (s > cap) s = cap;
-  if (s < 1) s = 1;
-  if (s > 256) s = 256;
-  return s;
+// Default grid: a full single wave (4 or 3 CTAs per SM), but no more warps than
+// slices of at least four chunks.
+int decode_auto_ctas(int n_seqs, int n_kv_heads, int gqa, int max_seq_len) {
+  const long long chunks = (long long)n_seqs * n_kv_heads * ((max_seq_len + 31) / 32);
+  const long long by_work = (chunks + 4 * DEC_WARPS - 1) / (4 * DEC_WARPS);
+  long long n = (long long)SM_COUNT * ctas_per_sm(gqa);
+  if (n > by_work) n = by_work;
+  return n < 1 ? 1 : (int)n;
 }
 
 // ---------------------------------------------------------------------------
@@ -161,10 +189,9 @@ struct ChunkLayout {
   static __device__ __forceinline__ int page(int u, int r) { return P == 16 ? u : 2 * u + (r >> 3); }
 };
 
+// (scale, zero) fp16 pair of one token -> fp32
 __device__ __forceinline__ float2 meta_pair(const uint8_t* p) {
-  const uint32_t m = *reinterpret_cast<const uint32_t*>(p);
-  return make_float2(__half2float(__ushort_as_half((unsigned short)(m & 0xFFFFu))),
-                     __half2float(__ushort_as_half((unsigned short)(m >> 16))));
+  return __half22float2(*reinterpret_cast<const __half2*>(p));
 }
 
 // Value codes are read with a transposing shared-memory load (ldmatrix .trans):
@@ -182,132 +209,244 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// Query rotation (Eq. 22): q'[b][j] = q[b][j] R_K,h(j) * log2(e)/sqrt(128), once
-// per decode call.  grid = (n_kv_heads, ceil(n_seqs / QP_SEQS)), block = 256.
-// A dense R_h is staged in shared memory; thread (d, half) produces channel d
-// of every other query vector of the CTA.
-// ---------------------------------------------------------------------------
-constexpr int QP_SEQS = 4;
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
-template <bool DENSE>
-__global__ void __launch_bounds__(256) qprep_kernel(int n_seqs, int n_q_heads, int gqa,
-                                                    const void* __restrict__ q, int q_dtype, RotDev rot,
-                                                    float* __restrict__ qr) {
-  extern __shared__ float sm[];  // dense: R [128][128], then q vectors [QP_SEQS * gqa][128]
-  const int h = blockIdx.x;
-  const int b0 = blockIdx.y * QP_SEQS;
-  const int nb = min(QP_SEQS, n_seqs - b0);
-  const int nv = nb * gqa;
+// ---------------------------------------------------------------------------
+// Query preparation (Eq. 22), one CTA per (KV head h, sequence b), 256 threads:
+// q'_j = q[b][h G + j] R_K,h * log2(e)/sqrt(128) for the G query heads of the
+// group, then per head the sum of q' and a power-of-two prescale e_j keeping
+// 256 |q'| well inside the fp16 range, and the B fragments of q'.c.  Also
+// marks the unit as not yet covered and writes o = 0 for an empty sequence.
+// ---------------------------------------------------------------------------
+constexpr int QP_THREADS = 256;
+
+template <int G, bool DENSE>
+__global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_kv_heads, const void* __restrict__ q,
+                                                           int q_dtype, RotDev rot, const int32_t* __restrict__ seq_lens,
+                                                           DecWs ws, float* __restrict__ o_rot) {
+  constexpr int NT = n_tiles(G);
+  constexpr int NW = QP_THREADS / 32;
+  pdl_launch_dependents();  // the decode kernel may start its batch scan and first copies
+  __shared__ __align__(16) float qv[G][D];
+  __shared__ __align__(16) float qr[G][D];
+  __shared__ __align__(16) float red[DENSE ? NW : 1][G][D];
+  __shared__ float qe[G];
+  const int h = blockIdx.x, b = blockIdx.y;
+  const int u = b * n_kv_heads + h;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float sc = LOG2E * INV_SQRT_D;
   if (DENSE) {
-    float* Rs = sm;
-    float* qv = sm + D * D;
-    const float4* src = reinterpret_cast<const float4*>(rot.dense + (size_t)h * D * D);
-    for (int i = threadIdx.x; i < D * D / 4; i += 256) reinterpret_cast<float4*>(Rs)[i] = __ldg(src + i);
-    for (int i = threadIdx.x; i < nv * D; i += 256) {
-      const int v = i / D, c = i % D;
-      const int b = b0 + v / gqa, j = h * gqa + v % gqa;
-      qv[i] = load1(q, ((size_t)b * n_q_heads + j) * D + c, q_dtype);
+    for (int i = tid; i < G * D; i += QP_THREADS)
+      qv[i / D][i % D] = load1(q, ((size_t)b * n_q_heads + h * G) * D + i, q_dtype);
+    __syncthreads();
+    // warp w: rows 16w .. 16w + 15 of R; lane: columns 4l .. 4l + 3 (all row loads in flight at once)
+    const float4* R = reinterpret_cast<const float4*>(rot.dense + (size_t)h * D * D) + lane;
+    float4 r[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) r[c] = __ldg(R + (size_t)(16 * warp + c) * (D / 4));
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float x = qv[j][16 * warp + c];
+        a.x = fmaf(x, r[c].x, a.x); a.y = fmaf(x, r[c].y, a.y); a.z = fmaf(x, r[c].z, a.z); a.w = fmaf(x, r[c].w, a.w);
+      }
+      reinterpret_cast<float4*>(red[warp][j])[lane] = a;
     }
     __syncthreads();
-    const int d = threadIdx.x & 127, half = threadIdx.x >> 7;
-    for (int v = half; v < nv; v += 2) {
-      const float* x = qv + v * D;
-      float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-#pragma unroll 8
-      for (int c = 0; c < D; c += 4) {
-        a0 = fmaf(x[c], Rs[c * D + d], a0);
-        a1 = fmaf(x[c + 1], Rs[(c + 1) * D + d], a1);
-        a2 = fmaf(x[c + 2], Rs[(c + 2) * D + d], a2);
-        a3 = fmaf(x[c + 3], Rs[(c + 3) * D + d], a3);
-      }
-      const int b = b0 + v / gqa, j = h * gqa + v % gqa;
-      qr[((size_t)b * n_q_heads + j) * D + d] = ((a0 + a1) + (a2 + a3)) * sc;
+    for (int i = tid; i < G * D; i += QP_THREADS) {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < NW; ++w) a += red[w][i / D][i % D];
+      qr[i / D][i % D] = a * sc;
     }
   } else {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int v = warp; v < nv; v += 8) {
-      const int b = b0 + v / gqa, j = h * gqa + v % gqa;
-      float4 x = load4(q, ((size_t)b * n_q_heads + j) * D + 4 * lane, q_dtype);
+    for (int j = warp; j < G; j += NW) {
+      float4 x = load4(q, ((size_t)b * n_q_heads + h * G + j) * D + 4 * lane, q_dtype);
       x = rotate_vec_warp(x, rot, h, lane, false);
       x.x *= sc; x.y *= sc; x.z *= sc; x.w *= sc;
-      reinterpret_cast<float4*>(qr + ((size_t)b * n_q_heads + j) * D)[lane] = x;
+      reinterpret_cast<float4*>(qr[j])[lane] = x;
     }
   }
+  __syncthreads();
+  for (int j = warp; j < G; j += NW) {
+    const float4 v = reinterpret_cast<const float4*>(qr[j])[lane];
+    const float tot = warp_sum(v.x + v.y + v.z + v.w);
+    const float mx = warp_max(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+    if (lane == 0) {
+      int e = 0;
+      while (e < 64 && mx * 256.f > 16384.f * exp2f((float)e)) ++e;
+      qe[j] = (float)e;
+      const float inv = exp2f(-16.f - (float)e);
+      reinterpret_cast<float4*>(ws.qconst)[(size_t)u * G + j] = make_float4(exp2f(16.f + (float)e), tot * inv, TAU * inv, 0.f);
+    }
+  }
+  __syncthreads();
+  // B fragment word (nt, s, r) of lane (g, t): column g <-> head j = 4nt + g/2,
+  // the fp16 high part (g even) or the remainder * 2^11 (g odd) of
+  // q'_j * 2^(8 - pe - e_j) at channels 32t + 16r + s and 32t + 16r + 8 + s, the
+  // key field of k-slice s sitting at bit pe = 2s (s <= 4) or 2s - 10.
+  uint32_t* fr = ws.qfrag + (size_t)u * NT * 16 * 32;
+  for (int wv = tid; wv < NT * 16 * 32; wv += QP_THREADS) {
+    const int w = wv >> 5, L = wv & 31;
+    const int nt = w >> 4, s = (w & 15) >> 1, r = w & 1;
+    const int gi = L >> 2, ti = L & 3;
+    const int j = 4 * nt + (gi >> 1);
+    const int pe = s <= 4 ? 2 * s : 2 * s - 10;
+    float v0 = 0.f, v1 = 0.f;
+    if (j < G) {
+      const float f = exp2f((float)(8 - pe) - qe[j]);
+      const float x0 = qr[j][32 * ti + 16 * r + s] * f, x1 = qr[j][32 * ti + 16 * r + 8 + s] * f;
+      const float h0 = half_rn(x0), h1 = half_rn(x1);
+      v0 = (gi & 1) ? (x0 - h0) * LO_SCALE : h0;
+      v1 = (gi & 1) ? (x1 - h1) * LO_SCALE : h1;
+    }
+    fr[wv] = pack_half2(v0, v1);
+  }
+  if (tid == 0) ws.span[u] = make_int2(1, 0);
+  if (__ldg(seq_lens + b) == 0)  // no cached tokens: the softmax is over nothing, o = 0
+    for (int i = tid; i < G * D; i += QP_THREADS) o_rot[((size_t)b * n_q_heads + h * G) * D + i] = 0.f;
 }
 
+// Position of a warp in the batch's chunk list: unit (sequence b, KV head h)
+// covering list entries [S, E), nb = chunks of b, len = cached tokens of b.
+struct ChunkWalker {
+  int b, h, len, nb, S, E;
+};
+
 // ---------------------------------------------------------------------------
-// The split kernel.  grid = (n_splits, n_kv_heads, n_seqs), block = 128.
+// The decode kernel.  grid = n_ctas, block = 128 (4 independent warps).
 // G = query heads per KV head; NT = n-tiles of 8 columns (2 columns per head).
-// A split is a range of 32-token chunks; warp w takes chunks w, w + 4, ...
-//
-// Scores are kept per lane in units of 1/dscale_j (dscale_j = 2^(16 + e_j), the
-// power of two that undoes the query prescale), so they come out of the
-// products with one multiply-add; the softmax exponent applies dscale_j.
-//
-// Centring of the value codes: tile 0 of a chunk enters as (c, +w) and tile 1
-// as (3 - c, -w), one logical operation per two codes either way.  The tensor
-// cores then accumulate sum_t w_t c_t - 3 sum_{t in tile 1} w_t, whose common
-// part 1.5 (sum_tile0 w - sum_tile1 w) cancels between neighbouring tiles
-// instead of growing with the context; 3 s_t is added back through the zero term.
 // ---------------------------------------------------------------------------
 template <int G, int P>
-__global__ void __launch_bounds__(128, (G >= 8 ? 3 : 5)) decode_split_kernel(
-    PageGeom g, int n_q_heads, const float* __restrict__ qr,
-    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ table,
-    const uint8_t* __restrict__ pool, int n_splits, Partials part, unsigned* err) {
-  constexpr int NT = (G + 3) / 4;
+__global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
+    PageGeom g, int n_seqs, int n_q_heads, const int32_t* __restrict__ seq_lens,
+    const int32_t* __restrict__ table, const uint8_t* __restrict__ pool, DecWs ws,
+    float* __restrict__ o_rot, unsigned* err) {
+  constexpr int NT = n_tiles(G);
   constexpr int PPC = 32 / P;       // pages per chunk
   constexpr int REC = 72 * P;       // bytes per page record
   constexpr int CHUNK = PPC * REC;  // 2304
-  constexpr int CPF = 32 / PPC;     // chunks per fill of the page-id cache
+  constexpr int CPF = 32 / PPC;     // chunks per fill of the page cache
   constexpr uint32_t ALL_PAGES = (1u << PPC) - 1u;
   constexpr unsigned FULLM = 0xffffffffu;
   using CL = ChunkLayout<P>;
-  const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, ti = lane & 3;  // MMA group id, thread id in group
+  const int Hkv = g.n_kv_heads;
+  const int max_len = g.max_blocks * P;
 
   __shared__ __align__(128) uint8_t stage[DEC_WARPS][DEC_STAGES][CHUNK];
   __shared__ __align__(8) uint64_t bars[DEC_WARPS][DEC_STAGES];
-  __shared__ __align__(16) float qs[G][D];
-  __shared__ float qsum[G], qexp[G];
-  __shared__ float sm_m[DEC_WARPS][G], sm_l[DEC_WARPS][G];
-  __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the chunk was copied
+  __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the staged chunk was copied
+  __shared__ int s_sum[DEC_WARPS];
+  __shared__ int s_start[DEC_WARPS][2];  // first sequence of each warp's slice, chunks before it
 
-  int len = __ldg(seq_lens + b);
-  if (len < 0 || len > g.max_blocks * g.page_tokens) {
-    if (threadIdx.x == 0) flag_error(err, ERR_SEQ_RANGE);
-    len = 0;
+  auto n_chunks_of = [&](int len) { return (len <= 0 || len > max_len) ? 0 : (len + 31) >> 5; };
+
+  // ---- the batch's chunk list: sequence b holds H_kv * nb_b entries, unit (b, h)
+  //      the nb_b entries from H_kv * prefix_b + h * nb_b on ----
+  int tot = 0;
+  for (int b = threadIdx.x; b < n_seqs; b += 128) {
+    const int len = __ldg(seq_lens + b);
+    if ((len < 0 || len > max_len) && blockIdx.x == 0) flag_error(err, ERR_SEQ_RANGE);
+    tot += n_chunks_of(len);
   }
-  const int n_pages = (len + P - 1) / P;
-  const int n_chunks = (len + 31) / 32;
-  const int cps = (n_chunks + n_splits - 1) / n_splits;
-  const int c_begin = split * cps;
-  const int c_end = min(n_chunks, c_begin + cps);
-  const int my_chunks = c_end > c_begin + warp ? (c_end - c_begin - warp + DEC_WARPS - 1) / DEC_WARPS : 0;
-  const int32_t* trow = table + (size_t)b * g.max_blocks;
-  const uint8_t* hbase = pool + (size_t)h * g.record;
-  const size_t bstride = (size_t)g.n_kv_heads * g.record;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULLM, tot, o);
+  if (lane == 0) s_sum[warp] = tot;
+  __syncthreads();
+  const int T = Hkv * (s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3]);
+  const int n_warps = gridDim.x * DEC_WARPS;
+  const int Ww = (T + n_warps - 1) / n_warps;  // entries per warp slice
+  const int gw = blockIdx.x * DEC_WARPS + warp;
+  const int ga = min(T, gw * Ww);
+  const int my_n = min(T, ga + Ww) - ga;
+  __syncthreads();
+  // exclusive prefix of chunk counts, tile by tile: the sequence holding each slice's first entry
+  int base = 0;
+  for (int b0 = 0; b0 < n_seqs; b0 += 128) {
+    const int b = b0 + threadIdx.x;
+    const int n = b < n_seqs ? n_chunks_of(__ldg(seq_lens + b)) : 0;
+    int inc = n;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(FULLM, inc, o);
+      if (lane >= o) inc += y;
+    }
+    if (lane == 31) s_sum[warp] = inc;
+    __syncthreads();
+    int before = base;
+    for (int w = 0; w < warp; ++w) before += s_sum[w];
+    const int excl = before + inc - n;
+    if (n > 0) {
+      for (int w = 0; w < DEC_WARPS; ++w) {
+        const int gs = (blockIdx.x * DEC_WARPS + w) * Ww;
+        if (gs < T && gs >= Hkv * excl && gs < Hkv * (excl + n)) {
+          s_start[w][0] = b;
+          s_start[w][1] = excl;
+        }
+      }
+    }
+    base += s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
+    __syncthreads();
+  }
+  auto walk_to = [&](ChunkWalker& w, int gq) {
+    while (gq >= w.E) {
+      if (++w.h == Hkv) {
+        w.h = 0;
+        ++w.b;
+        w.len = __ldg(seq_lens + w.b);
+        w.nb = n_chunks_of(w.len);
+      }
+      w.S = w.E;
+      w.E = w.S + w.nb;
+    }
+  };
+  ChunkWalker iw;  // issue side
+  if (my_n > 0) {
+    iw.b = s_start[warp][0];
+    iw.len = __ldg(seq_lens + iw.b);
+    iw.nb = n_chunks_of(iw.len);
+    const int sb = Hkv * s_start[warp][1];
+    iw.h = (ga - sb) / iw.nb;
+    iw.S = sb + iw.h * iw.nb;
+    iw.E = iw.S + iw.nb;
+  }
+  ChunkWalker cw = iw;  // consume side
 
-  // Page-id cache: lane l holds page l % PPC of the warp's chunk i0 + l / PPC;
-  // -2 marks a page past the end of the sequence.
-  int pid = -2;
+  // Page cache: lane l holds the record index (block * H_kv + h) of page l % PPC
+  // of the warp's chunk i0 + l / PPC; -2: past the sequence, -1: bad block id.
+  int rec = -2;
+  int n_issued = 0;  // chunks whose copies were issued
   auto fill_cache = [&](int i0) {
+    ChunkWalker w = iw;
     const int i = i0 + lane / PPC;
-    const int pg = (c_begin + warp + DEC_WARPS * i) * PPC + lane % PPC;
-    pid = (i < my_chunks && pg < n_pages) ? __ldg(trow + pg) : -2;
+    rec = -2;
+    if (i < my_n) {
+      walk_to(w, ga + i);
+      const int pg = (ga + i - w.S) * PPC + lane % PPC;
+      if (pg < (w.len + P - 1) / P) {
+        const int pid = __ldg(table + (size_t)w.b * g.max_blocks + pg);
+        rec = (pid >= 0 && pid < g.num_blocks) ? pid * Hkv + w.h : -1;
+      }
+    }
   };
   // Stage the warp's i-th chunk: lane 0 arms the stage's mbarrier with the byte
   // count, then each lane owning a valid page copies it.  Whole warp.
   auto issue = [&](int i) {
-    if (i % CPF == 0 && i > 0) fill_cache(i);
+    n_issued = i + 1;
+    walk_to(iw, ga + i);
+    if (i % CPF == 0) fill_cache(i);
     const int sidx = i % DEC_STAGES;
     const bool mine = lane / PPC == i % CPF;
-    const bool ok = mine && pid >= 0 && pid < g.num_blocks;
+    const bool ok = mine && rec >= 0;
     const unsigned okm = __ballot_sync(FULLM, ok);
-    const unsigned badm = __ballot_sync(FULLM, mine && pid != -2 && !ok);
+    const unsigned badm = __ballot_sync(FULLM, mine && rec == -1);
     const uint32_t bits = (okm >> ((i % CPF) * PPC)) & ALL_PAGES;
     uint64_t* bar = &bars[warp][sidx];
     if (lane == 0) {
@@ -318,88 +457,99 @@ __global__ void __launch_bounds__(128, (G >= 8 ? 3 : 5)) decode_split_kernel(
     __syncwarp();
     if (ok) {
       fence_proxy_async();
-      bulk_g2s(stage[warp][sidx] + (lane % PPC) * REC, hbase + (size_t)pid * bstride, REC, bar);
+      bulk_g2s(stage[warp][sidx] + (lane % PPC) * REC, pool + (size_t)rec * g.record, REC, bar);
     }
   };
 
-  if (lane == 0) {
-    for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[warp][s], 1);
-    fence_mbar_init();
-  }
-  __syncwarp();
-  fill_cache(0);
-  for (int i = 0; i < DEC_STAGES && i < my_chunks; ++i) issue(i);
-
-  // ---- prologue: the rotated, pre-scaled queries q'_j (Eq. 22, from qprep_kernel) ----
-  for (int jj = warp; jj < G; jj += DEC_WARPS) {
-    const float4 v = __ldg(reinterpret_cast<const float4*>(qr + ((size_t)b * n_q_heads + h * G + jj) * D) + lane);
-    reinterpret_cast<float4*>(qs[jj])[lane] = v;
-    const float tot = warp_sum(v.x + v.y + v.z + v.w);
-    const float mx = warp_max(fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  if (my_n > 0) {
     if (lane == 0) {
-      qsum[jj] = tot;
-      // power-of-two prescale keeping 256 * |q'| well inside the fp16 range
-      int e = 0;
-      while (e < 64 && mx * 256.f > 16384.f * exp2f((float)e)) ++e;
-      qexp[jj] = (float)e;
+      for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[warp][s], 1);
+      fence_mbar_init();
     }
+    __syncwarp();
+    for (int i = 0; i < DEC_STAGES && i < my_n; ++i) issue(i);
   }
-  __syncthreads();
+  pdl_wait();               // the query fragments and spans come from qprep_kernel
+  pdl_launch_dependents();  // the combine kernel may be scheduled as blocks retire
+  if (my_n <= 0) return;    // no block-level synchronisation follows
 
-  // B fragments of q'.c: k-slice s uses the 2-bit field at bit p = 2s of each
-  // 16-bit half of the key words; its fp16 value is c * 2^(pe-24) with
-  // pe = p (p <= 8) or p - 10 (read after a 10-bit shift).  Column 2j holds the
-  // fp16 high part of q'_j * 2^(8-pe-e_j), column 2j+1 the remainder * 2^11.
-  uint32_t bq[NT][8][2];
+  // ---- per-segment state (one segment = the warp's entries of one unit) ----
+  uint32_t bq[NT][8][2];  // B fragments of q'.c, k-slice s (see qprep_kernel)
+  float dsc[NT], qsum_s[NT], tau_s[NT], m_s[NT], thr[NT], nm[NT], lp[NT], zp[NT];
+  float acc[NT][8][4];
+  int cur_u = -1, cur_S = 0, cur_E = 0;
+
+  auto start_segment = [&](int u) {
+    const uint32_t* fr = ws.qfrag + (size_t)u * NT * 16 * 32 + lane;
 #pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int j = 4 * nt + (gi >> 1);
-    const bool lo_part = gi & 1;
+    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-    for (int s = 0; s < 8; ++s) {
-      const int pe = s <= 4 ? 2 * s : 2 * s - 10;
-      float vals[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int s = 0; s < 8; ++s) {
+        bq[nt][s][0] = __ldg(fr + (nt * 16 + 2 * s) * 32);
+        bq[nt][s][1] = __ldg(fr + (nt * 16 + 2 * s + 1) * 32);
+      }
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int j = 4 * nt + ti;
+      const float4 c = j < G ? __ldg(reinterpret_cast<const float4*>(ws.qconst) + (size_t)u * G + j)
+                             : make_float4(1.f, 0.f, TAU, 0.f);
+      dsc[nt] = c.x;
+      qsum_s[nt] = c.y;
+      tau_s[nt] = c.z;
+      m_s[nt] = -INFINITY;
+      thr[nt] = -INFINITY;
+      nm[nt] = 0.f;
+      lp[nt] = 0.f;
+      zp[nt] = 0.f;
+#pragma unroll
+      for (int f = 0; f < 8; ++f) acc[nt][f][0] = acc[nt][f][1] = acc[nt][f][2] = acc[nt][f][3] = 0.f;
+    }
+  };
+
+  // Write the warp's partial of the open segment (slot gw + unit).
+  auto finish_segment = [&]() {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        lp[nt] += __shfl_xor_sync(FULLM, lp[nt], o);
+        zp[nt] += __shfl_xor_sync(FULLM, zp[nt], o);
+      }
+    }
+    float* pp = ws.part + (size_t)(gw + cur_u) * G * PART;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int j = 4 * nt + ti;
       if (j < G) {
-        const float f = exp2f((float)(8 - pe) - qexp[j]);
-        const int ch[4] = {32 * ti + s, 32 * ti + 8 + s, 32 * ti + 16 + s, 32 * ti + 24 + s};
+        float o[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float x = qs[j][ch[u]] * f;
-          const float hi = half_rn(x);
-          vals[u] = lo_part ? (x - hi) * LO_SCALE : hi;
+        for (int f = 0; f < 8; ++f) {
+          const float sc = (float)(1 << (24 - v_pe(f)));
+          o[f] = fmaf(fmaf(acc[nt][f][1], LO_UNSCALE, acc[nt][f][0]), sc, zp[nt]);      // channel 8g + f
+          o[8 + f] = fmaf(fmaf(acc[nt][f][3], LO_UNSCALE, acc[nt][f][2]), sc, zp[nt]);  // channel 64 + 8g + f
+        }
+        float4* dst = reinterpret_cast<float4*>(pp + j * PART);
+        dst[2 * gi] = make_float4(o[0], o[1], o[2], o[3]);
+        dst[2 * gi + 1] = make_float4(o[4], o[5], o[6], o[7]);
+        dst[16 + 2 * gi] = make_float4(o[8], o[9], o[10], o[11]);
+        dst[16 + 2 * gi + 1] = make_float4(o[12], o[13], o[14], o[15]);
+        if (gi == 0) {
+          pp[j * PART + D] = m_s[nt] * dsc[nt];
+          pp[j * PART + D + 1] = lp[nt];
         }
       }
-      bq[nt][s][0] = pack_half2(vals[0], vals[1]);
-      bq[nt][s][1] = pack_half2(vals[2], vals[3]);
     }
-  }
-  // Per-lane softmax state of head 4nt + ti, scores in units of 1/dsc.
-  float dsc[NT], qsum_s[NT], tau_s[NT], m_s[NT], thr[NT], nm[NT], lp[NT], zp[NT];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int j = 4 * nt + ti;
-    dsc[nt] = j < G ? exp2f(16.f + qexp[j]) : 1.f;
-    qsum_s[nt] = j < G ? qsum[j] * exp2f(-16.f - qexp[j]) : 0.f;
-    tau_s[nt] = TAU / dsc[nt];
-    m_s[nt] = -INFINITY;
-    thr[nt] = -INFINITY;
-    nm[nt] = 0.f;
-    lp[nt] = 0.f;
-    zp[nt] = 0.f;
-  }
+    // the slice holding the unit's first entry records which slices meet the unit
+    if (lane == 0 && gw == cur_S / Ww) ws.span[cur_u] = make_int2(gw, (cur_E - 1) / Ww);
+  };
+
   const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;  // pick remainder / high halves
   const int srcA = 8 * ti + (gi >> 1);                // lanes holding tokens 2t, 2t + 8 of head 4nt + g/2
   // ldmatrix row address of this lane inside a staged chunk (tile 0); tile 1 is 1,152 bytes on
   const uint32_t vrow = smem_u32(stage[warp][0]) + CL::v(0, 8 * (lane >> 4) + (lane & 7)) + 16 * ((lane >> 3) & 1);
 
-  float acc[NT][8][4];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-    for (int f = 0; f < 8; ++f) acc[nt][f][0] = acc[nt][f][1] = acc[nt][f][2] = acc[nt][f][3] = 0.f;
-
   // One 32-token chunk from a staged stage.  FULL: every token valid and copied.
-  auto chunk = [&](auto full_tag, const uint8_t* st, uint32_t vaddr, int tok0, int bits) {
+  auto chunk = [&](auto full_tag, const uint8_t* st, uint32_t vaddr, int tok0, int len, int bits) {
     constexpr bool FULL = decltype(full_tag)::value;
     bool rok[4];
 #pragma unroll
@@ -499,6 +649,10 @@ __global__ void __launch_bounds__(128, (G >= 8 ? 3 : 5)) decode_split_kernel(
     }
 
     // ---- values (Eq. 5): D[channel][2j + {hi,lo}] += 2^(pe-24) sum_t code_t (+-w_t) ----
+    // Tile 0 enters as (c, +w) and tile 1 as (3 - c, -w), one logical operation
+    // per two codes either way: the accumulated common part 1.5 (sum_tile0 w -
+    // sum_tile1 w) cancels between neighbouring tiles instead of growing with the
+    // context, and the 3 s_t of tile 1 is restored through the zero term.
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       uint32_t rw[4], sw[4];  // element g / 8+g of tokens (2t, 2t+1) and (2t+8, 2t+9); byte-swapped
@@ -522,7 +676,7 @@ __global__ void __launch_bounds__(128, (G >= 8 ? 3 : 5)) decode_split_kernel(
 
   bool aborted = false;
   int consumed = 0;
-  for (int i = 0; i < my_chunks; ++i) {
+  for (int i = 0; i < my_n; ++i) {
     const int sidx = i % DEC_STAGES;
     bool ok = false;
     for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][sidx], (i / DEC_STAGES) & 1);
@@ -533,126 +687,133 @@ __global__ void __launch_bounds__(128, (G >= 8 ? 3 : 5)) decode_split_kernel(
       break;
     }
     consumed = i + 1;
+    walk_to(cw, ga + i);
+    const int u = cw.b * Hkv + cw.h;
+    if (u != cur_u) {
+      if (cur_u >= 0) finish_segment();
+      start_segment(u);
+      cur_u = u;
+      cur_S = cw.S;
+      cur_E = cw.E;
+    }
     const uint8_t* st = stage[warp][sidx];
     const uint32_t vaddr = vrow + sidx * CHUNK;
     const int bits = sflag[warp][sidx];
-    const int tok0 = (c_begin + warp + DEC_WARPS * i) * 32;
-    if (tok0 + 32 <= len && bits == (int)ALL_PAGES) chunk(std::true_type{}, st, vaddr, tok0, bits);
-    else chunk(std::false_type{}, st, vaddr, tok0, bits);
+    const int tok0 = (ga + i - cw.S) * 32;
+    if (tok0 + 32 <= cw.len && bits == (int)ALL_PAGES) chunk(std::true_type{}, st, vaddr, tok0, cw.len, bits);
+    else chunk(std::false_type{}, st, vaddr, tok0, cw.len, bits);
     __syncwarp();
-    if (i + DEC_STAGES < my_chunks) issue(i + DEC_STAGES);
+    if (i + DEC_STAGES < my_n) issue(i + DEC_STAGES);
   }
   if (aborted) {
-    // wait (bounded) for the copies still in flight before the stages go away
-    for (int i = consumed; i < my_chunks && i < consumed + DEC_STAGES; ++i) {
+    // wait (bounded) for the copies still in flight before the stages go away;
+    // the open segment is dropped (its unit's output is not written, the error flag is set)
+    for (int i = consumed; i < n_issued; ++i) {
       bool ok = false;
       for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][i % DEC_STAGES], (i / DEC_STAGES) & 1);
     }
+    return;
   }
-  // per-head sums over the lanes of one head (same t)
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-      lp[nt] += __shfl_xor_sync(FULLM, lp[nt], o);
-      zp[nt] += __shfl_xor_sync(FULLM, zp[nt], o);
-    }
-  }
-  __syncthreads();  // all warps done with their stages; reuse them for the merge
+  if (cur_u >= 0) finish_segment();
+}
 
-  // ---- per-warp results: head 4nt+t, channels 8g + f and 64 + 8g + f ----
-  float* sm_acc = reinterpret_cast<float*>(&stage[0][0][0]);  // [DEC_WARPS][G][128]
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) {
-    const int j = 4 * nt + ti;
-    if (j < G) {
-#pragma unroll
-      for (int f = 0; f < 8; ++f) {
-        const float sc = (float)(1 << (24 - v_pe(f)));
-        sm_acc[(warp * G + j) * D + 8 * gi + f] = fmaf(fmaf(acc[nt][f][1], LO_UNSCALE, acc[nt][f][0]), sc, zp[nt]);
-        sm_acc[(warp * G + j) * D + 64 + 8 * gi + f] = fmaf(fmaf(acc[nt][f][3], LO_UNSCALE, acc[nt][f][2]), sc, zp[nt]);
-      }
-      if (gi == 0) {
-        sm_m[warp][j] = m_s[nt] * dsc[nt];
-        sm_l[warp][j] = lp[nt];
-      }
-    }
+// ---------------------------------------------------------------------------
+// Combine: grid (U, G), 256 threads.  o_rot of query head j of unit u is the
+// log-sum-exp merge of the unit's partials (slots k + u, k0 <= k <= k1): warp w
+// folds slots k0 + w, k0 + w + 8, ... with a running maximum, then the eight
+// warp results are merged in warp order, so the result does not depend on timing.
+// ---------------------------------------------------------------------------
+constexpr int CB_WARPS = 8;
+
+template <int G>
+__global__ void __launch_bounds__(CB_WARPS * 32) decode_combine_kernel(int n_kv_heads, int n_q_heads, DecWs ws,
+                                                                       float* __restrict__ o_rot) {
+  __shared__ float sm_m[CB_WARPS], sm_l[CB_WARPS];
+  __shared__ __align__(16) float sm_a[CB_WARPS][D];
+  pdl_wait();  // the partials come from decode_split_kernel
+  const int u = blockIdx.x, j = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int2 sp = __ldcg(ws.span + u);
+  if (sp.x > sp.y) return;  // no cached tokens (o = 0 already) or an invalid length
+  float m = -INFINITY, l = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 2
+  for (int k = sp.x + warp; k <= sp.y; k += CB_WARPS) {
+    const float* pp = ws.part + ((size_t)(k + u) * G + j) * PART;
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + D));
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + lane);
+    if (ml.x == -INFINITY) continue;
+    const float mn = fmaxf(m, ml.x);
+    const float so = exp2f(m - mn), sn = exp2f(ml.x - mn);
+    l = fmaf(l, so, ml.y * sn);
+    a.x = fmaf(a.x, so, x.x * sn); a.y = fmaf(a.y, so, x.y * sn);
+    a.z = fmaf(a.z, so, x.z * sn); a.w = fmaf(a.w, so, x.w * sn);
+    m = mn;
   }
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_l[warp] = l;
+  }
+  reinterpret_cast<float4*>(sm_a[warp])[lane] = a;
   __syncthreads();
-  const int cch = threadIdx.x;
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
+  if (threadIdx.x < D) {
+    const int c = threadIdx.x;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < DEC_WARPS; ++w) M = fmaxf(M, sm_m[w][j]);
+    for (int w = 0; w < CB_WARPS; ++w) M = fmaxf(M, sm_m[w]);
     float A = 0.f, L = 0.f;
     if (M != -INFINITY) {
 #pragma unroll
-      for (int w = 0; w < DEC_WARPS; ++w) {
-        if (sm_m[w][j] == -INFINITY) continue;
-        const float e = exp2f(sm_m[w][j] - M);
-        A = fmaf(e, sm_acc[(w * G + j) * D + cch], A);
-        L = fmaf(e, sm_l[w][j], L);
+      for (int w = 0; w < CB_WARPS; ++w) {
+        if (sm_m[w] == -INFINITY) continue;
+        const float e = exp2f(sm_m[w] - M);
+        A = fmaf(e, sm_a[w][c], A);
+        L = fmaf(e, sm_l[w], L);
       }
     }
-    const size_t row = ((size_t)b * n_q_heads + h * G + j) * n_splits + split;
-    part.acc[row * D + cch] = A;
-    if (cch == 0) {
-      part.ml[row * 2] = M;
-      part.ml[row * 2 + 1] = L;
-    }
+    const int b = u / n_kv_heads, h = u % n_kv_heads;
+    o_rot[((size_t)b * n_q_heads + h * G + j) * D + c] = L > 0.f ? A / L : 0.f;
   }
 }
 
-// grid = (n_q_heads, n_seqs), block = 128: o = sum_s acc_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
-__global__ void __launch_bounds__(128) decode_combine_kernel(int n_q_heads, int n_splits,
-                                                             Partials part, float* __restrict__ o) {
-  const int j = blockIdx.x, b = blockIdx.y, c = threadIdx.x;
-  const size_t base = ((size_t)b * n_q_heads + j) * n_splits;
-  float M = -INFINITY;
-  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, part.ml[(base + s) * 2]);
-  float A = 0.f, L = 0.f;
-  if (M != -INFINITY) {
-    for (int s = 0; s < n_splits; ++s) {
-      const float ms = part.ml[(base + s) * 2];
-      if (ms == -INFINITY) continue;
-      const float e = exp2f(ms - M);
-      L = fmaf(e, part.ml[(base + s) * 2 + 1], L);
-      A = fmaf(e, part.acc[(base + s) * D + c], A);
-    }
-  }
-  o[((size_t)b * n_q_heads + j) * D + c] = L > 0.f ? A / L : 0.f;
-}
-
-cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q,
-                          int q_dtype, const int32_t* seq_lens, int max_seq_len,
-                          const int32_t* table, RotDev rot_k, const uint8_t* pool, int n_splits,
-                          void* ws, float* o_rot, unsigned* err, cudaStream_t s) {
+cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q, int q_dtype,
+                          const int32_t* seq_lens, int max_seq_len, const int32_t* table, RotDev rot_k,
+                          const uint8_t* pool, int n_ctas, void* ws_base, float* o_rot, unsigned* err,
+                          cudaStream_t s) {
   (void)max_seq_len;
   if (n_seqs == 0) return cudaSuccess;
   const int gqa = n_q_heads / g.n_kv_heads;
-  Partials part = partials_from_ws(ws, n_seqs, n_q_heads, n_splits);
-  float* qr = rotated_q_from_ws(ws, n_seqs, n_q_heads, n_splits);
-  {
-    const dim3 qg(g.n_kv_heads, (n_seqs + QP_SEQS - 1) / QP_SEQS);
-    if (rot_k.kind == KVQ_ROT_DENSE) {
-      const size_t smem = (size_t)(D * D + QP_SEQS * gqa * D) * sizeof(float);
-      static size_t attr = 0;
-      if (smem > attr) {
-        const cudaError_t e = cudaFuncSetAttribute(qprep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        attr = smem;
-      }
-      qprep_kernel<true><<<qg, 256, smem, s>>>(n_seqs, n_q_heads, gqa, q, q_dtype, rot_k, qr);
-    } else {
-      qprep_kernel<false><<<qg, 256, 0, s>>>(n_seqs, n_q_heads, gqa, q, q_dtype, rot_k, qr);
-    }
-    const cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+  DecWs ws;
+  decode_ws_layout(ws_base, n_seqs, g.n_kv_heads, gqa, n_ctas, &ws);
+  const dim3 qg(g.n_kv_heads, n_seqs);
+  const bool dense = rot_k.kind == KVQ_ROT_DENSE;
+#define KVQ_QPREP(GG)                                                                                     \
+  if (dense) qprep_kernel<GG, true><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k, seq_lens, ws, o_rot); \
+  else qprep_kernel<GG, false><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k, seq_lens, ws, o_rot)
+  switch (gqa) {
+    case 1: KVQ_QPREP(1); break;
+    case 2: KVQ_QPREP(2); break;
+    case 4: KVQ_QPREP(4); break;
+    case 8: KVQ_QPREP(8); break;
+    default: return cudaErrorInvalidValue;
   }
-  dim3 grid(n_splits, g.n_kv_heads, n_seqs);
+#undef KVQ_QPREP
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  // the decode kernel is a programmatic dependent of qprep_kernel
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_ctas);
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
 #define KVQ_DEC(GG, PP) \
-  decode_split_kernel<GG, PP><<<grid, 128, 0, s>>>(g, n_q_heads, qr, seq_lens, table, pool, n_splits, part, err)
+  e = cudaLaunchKernelEx(&cfg, decode_split_kernel<GG, PP>, g, n_seqs, n_q_heads, seq_lens, table, pool, ws, o_rot, err)
 #define KVQ_DEC_P(GG) \
   if (g.page_tokens == 16) KVQ_DEC(GG, 16); else KVQ_DEC(GG, 8)
   switch (gqa) {
@@ -664,9 +825,21 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   }
 #undef KVQ_DEC_P
 #undef KVQ_DEC
-  cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_combine_kernel<<<dim3(n_q_heads, n_seqs), 128, 0, s>>>(n_q_heads, n_splits, part, o_rot);
+
+  // the combine is a programmatic dependent of the decode kernel
+  cfg.gridDim = dim3(n_seqs * g.n_kv_heads, gqa);
+  cfg.blockDim = dim3(CB_WARPS * 32);
+#define KVQ_CB(GG) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<GG>, g.n_kv_heads, n_q_heads, ws, o_rot)
+  switch (gqa) {
+    case 1: KVQ_CB(1); break;
+    case 2: KVQ_CB(2); break;
+    case 4: KVQ_CB(4); break;
+    case 8: KVQ_CB(8); break;
+    default: return cudaErrorInvalidValue;
+  }
+#undef KVQ_CB
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

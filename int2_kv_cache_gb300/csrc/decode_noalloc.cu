@@ -41,6 +41,16 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_layout* layout, int
   size_t need = 0;
   kvq_status st = kvq_decode_workspace_size(layout, n_seqs, max_seq_len, n_splits, &need);
   if (st != KVQ_OK) return st;
+  if (n_splits == 0 && need > NOALLOC_SCRATCH_BYTES) {
+    // the library's choice of work partitions: take fewer until the partials fit
+    int s = kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, layout->n_q_heads / layout->n_kv_heads, max_seq_len);
+    while (need > NOALLOC_SCRATCH_BYTES && s > 1) {
+      s /= 2;
+      st = kvq_decode_workspace_size(layout, n_seqs, max_seq_len, s, &need);
+      if (st != KVQ_OK) return st;
+    }
+    n_splits = s;
+  }
   char msg[256];
   if (need > NOALLOC_SCRATCH_BYTES) {
     snprintf(msg, sizeof(msg),

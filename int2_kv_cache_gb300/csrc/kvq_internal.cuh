@@ -84,11 +84,11 @@ cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x
                                  float* out, cudaStream_t s);
 
 // decode.cu
-int decode_auto_splits(int n_seqs, int n_kv_heads, int max_seq_len, int page_tokens);
-size_t decode_workspace_bytes(int n_seqs, int n_q_heads, int n_splits);
+int decode_auto_ctas(int n_seqs, int n_kv_heads, int gqa, int max_seq_len);
+size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas);
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q,
                           int q_dtype, const int32_t* seq_lens, int max_seq_len,
-                          const int32_t* table, RotDev rot_k, const uint8_t* pool, int n_splits,
+                          const int32_t* table, RotDev rot_k, const uint8_t* pool, int n_ctas,
                           void* ws, float* o_rot, unsigned* err, cudaStream_t s);
 
 // outproj.cu

@@ -57,11 +57,25 @@ def test_pool_bytes(kvq):
     assert kvq.kvq_pool_bytes(lay8) == 3 * 2 * 576
 
 
+def _ws_bytes(n_seqs, hkv, gqa, n_ctas):
+    """Documented decode workspace: partials [4 n_ctas + U][gqa][132] f32, query
+    fragments [U][16 NT][32] u32, constants [U][gqa][4] f32, slice spans [U] int2,
+    each region rounded up to 256 bytes (U = n_seqs * hkv units)."""
+    a = lambda x: (x + 255) // 256 * 256
+    u = n_seqs * hkv
+    nt = (gqa + 3) // 4
+    return (a((4 * n_ctas + u) * gqa * 132 * 4) + a(u * 16 * nt * 32 * 4) + a(u * gqa * 16) + a(u * 8))
+
+
 def test_decode_workspace_size(kvq):
     lay = _layout(kvq)
-    assert kvq.kvq_decode_workspace_size(lay, 16, 160, 5) == 16 * 32 * (5 * 130 + 128) * 4
+    assert kvq.kvq_decode_workspace_size(lay, 16, 160, 5) == _ws_bytes(16, 8, 4, 5)
+    # library's choice: one full wave (4 blocks per SM), capped at 16 chunks per block
     auto = kvq.kvq_decode_workspace_size(lay, 16, 160, 0)
-    assert (auto // (16 * 32 * 4) - 128) % 130 == 0 and auto > 0
+    assert auto == _ws_bytes(16, 8, 4, (16 * 8 * 5 + 15) // 16)
+    lay8 = _layout(kvq, n_q_heads=64, max_blocks_per_seq=4096)
+    assert kvq.kvq_decode_workspace_size(lay8, 16, 32768, 0) == _ws_bytes(16, 8, 8, 3 * 152)
+    assert kvq.kvq_decode_workspace_size(lay, 16, 160, 1) < kvq.kvq_decode_workspace_size(lay, 16, 160, 2)
 
 
 def _status(kvq, fn, *args):
