@@ -280,7 +280,9 @@ kvq_status kvq_out_proj(int n_rows, int d_model, int k_dim, const float* x, cons
   KVQ_PTR(x, "x");
   KVQ_PTR(w, "w");
   KVQ_PTR(y, "y");
-  cudaError_t e = kvq::launch_out_proj(n_rows, d_model, k_dim, x, w, w_dtype, y, stream);
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
+  cudaError_t e = kvq::launch_out_proj(n_rows, d_model, k_dim, x, w, w_dtype, y, err, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_out_proj");
 }
 

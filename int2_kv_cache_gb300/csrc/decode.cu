@@ -40,6 +40,7 @@
 // online in base 2 with a lazy reference maximum.
 #include <type_traits>
 
+#include "async_copy.cuh"
 #include "quant_common.cuh"
 
 namespace kvq {
@@ -48,9 +49,6 @@ constexpr float LOG2E = 1.4426950408889634f;
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 4;
 constexpr int SM_COUNT = 152;  // GB300
-constexpr unsigned ERR_TIMEOUT = 8u;
-constexpr uint32_t WAIT_HINT_NS = 100000;  // per try_wait: sleep up to 100 us
-constexpr int WAIT_LIMIT = 20000;          // then give up (>= 2 s): error flag, no hang
 // Lazy softmax rescaling: the running sums keep their reference maximum until a
 // chunk's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
 constexpr float TAU = 6.f;
@@ -116,40 +114,6 @@ int decode_auto_ctas(int n_seqs, int n_kv_heads, int gqa, int max_seq_len) {
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void fence_mbar_init() {
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-// Waits (suspended, up to the time hint) for the phase with the given parity.
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\tselp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(WAIT_HINT_NS)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
@@ -202,12 +166,6 @@ __device__ __forceinline__ float2 meta_pair(const uint8_t* p) {
 __host__ __device__ constexpr int v_pe(int f) { return f == 0 ? 8 : (f <= 4 ? 2 * f : 2 * f - 8); }
 __host__ __device__ constexpr bool v_swapped(int f) { return f == 0 || f >= 5; }
 
-__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(addr)
-               : "memory");
-}
 
 __device__ __forceinline__ void pdl_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");

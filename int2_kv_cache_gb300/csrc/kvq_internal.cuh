@@ -19,6 +19,7 @@ enum : unsigned {
   ERR_BLOCK_RANGE = 1u,   // block-table entry outside [0, num_blocks)
   ERR_POS_RANGE = 2u,     // position beyond max_blocks_per_seq * page_tokens
   ERR_SEQ_RANGE = 4u,     // cu_new / seq_lens inconsistent (negative, decreasing, too long)
+  ERR_TIMEOUT = 8u,       // a bounded wait on a shared-memory copy gave up
 };
 
 struct RotDev {
@@ -95,7 +96,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
 cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, int w_dtype,
                            RotDev rot_v, void* out, int out_dtype, cudaStream_t s);
 cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
-                            int w_dtype, float* y, cudaStream_t s);
+                            int w_dtype, float* y, unsigned* err, cudaStream_t s);
 
 // calib.cu
 size_t calib_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint);

@@ -4,6 +4,7 @@
 // Inference Implementation", Eqs. 29-31: W_O-bar_j = W_O,j R_V,h(j), and
 // (o_j R_V) W_O-bar_j^T = o_j W_O,j^T; Eq. 3: the layer output sums the heads,
 // y = sum_j o_j W_O,j^T = o W_O^T with o the heads concatenated.
+#include "async_copy.cuh"
 #include "quant_common.cuh"
 
 namespace kvq {
@@ -170,14 +171,190 @@ __global__ void __launch_bounds__(256) out_proj_mma_kernel(int n_rows, int d_mod
   }
 }
 
+// bf16 weights, the decode-size case: W streamed through shared memory.
+//
+// A CTA owns BM = 16 MT rows of W and a pass of up to 8 NR activation rows.
+// W (row slices of OP_BK columns) and the matching x columns are staged in a
+// ring of shared-memory stages by bulk copies (one row per lane, completed on
+// an mbarrier), so tens of kilobytes per SM are in flight; rows are padded by
+// 16 (W) and 32 (x) bytes so the ldmatrix reads of W and the 8-byte reads of
+// x are free of bank conflicts.  Warp w takes columns 32w .. 32w + 31 of every stage; x is
+// split into bf16 high and remainder parts (two products into one fp32
+// accumulator); the eight warps are summed in a fixed order at the end.
+constexpr int OP_BK = 256;
+constexpr int OP_MAX_STAGES = 4;
+constexpr int OP_SMEM_TARGET = 110 * 1024;  // two CTAs per SM
+
+__host__ __device__ constexpr int op_stage_bytes(int mt, int nr) {
+  return 16 * mt * (OP_BK * 2 + 16) + 8 * nr * (OP_BK * 4 + 32);
+}
+__host__ __device__ constexpr int op_stages(int mt, int nr) {
+  return OP_SMEM_TARGET / op_stage_bytes(mt, nr) > OP_MAX_STAGES ? OP_MAX_STAGES
+         : OP_SMEM_TARGET / op_stage_bytes(mt, nr) < 2          ? 2
+                                                                  : OP_SMEM_TARGET / op_stage_bytes(mt, nr);
+}
+
+template <int MT, int NR>
+__global__ void __launch_bounds__(256) out_proj_stream_kernel(int n_rows, int d_model, int k_dim,
+                                                              const float* __restrict__ x,
+                                                              const __nv_bfloat16* __restrict__ w,
+                                                              float* __restrict__ y, unsigned* err) {
+  constexpr int BM = 16 * MT, XR = 8 * NR;
+  constexpr int WROW = OP_BK * 2 + 16;  // bytes per staged W row
+  constexpr int XROW = OP_BK * 4 + 32;  // bytes per staged x row
+  constexpr int STAGE = op_stage_bytes(MT, NR);
+  constexpr int S = op_stages(MT, NR);
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full[OP_MAX_STAGES];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gi = lane >> 2, ti = lane & 3;
+  const int n0 = blockIdx.x * BM;
+  const int w_rows = min(BM, d_model - n0);
+  const int n_k = (k_dim + OP_BK - 1) / OP_BK;
+
+  // One arrival per row copy: every copying thread arms the barrier with its own
+  // bytes, so the copies need no ordering among threads.
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&full[i], (uint32_t)(w_rows + n_rows));
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  // CTAs start at different column blocks, so at any moment they read different
+  // slices of x (all of them share x).
+  const int kc0 = blockIdx.x % n_k;
+  // The row this thread stages: W row `lane / 4 * 8 + warp` for lanes 0..3 of
+  // each warp (BM <= 32), x row `(lane - 4) * 8 + warp` for lanes 4..7 (<= 32
+  // rows), so the copies of a stage are spread over all eight warps.
+  const int my_wr = lane < 4 ? lane * 8 + warp : -1;
+  const int my_xr = (lane >= 4 && lane < 8) ? (lane - 4) * 8 + warp : -1;
+  const bool copies_w = my_wr >= 0 && my_wr < w_rows;
+  const bool copies_x = my_xr >= 0 && my_xr < n_rows;
+  auto issue = [&](int kc) {
+    if (!copies_w && !copies_x) return;
+    const int st = kc % S;
+    const int k0 = ((kc + kc0) % n_k) * OP_BK;
+    const int kw = min(OP_BK, k_dim - k0);
+    uint8_t* dst = smem + st * STAGE;
+    fence_proxy_async();
+    if (copies_w) {
+      mbar_arrive_expect_tx(&full[st], (uint32_t)kw * 2);
+      bulk_g2s(dst + my_wr * WROW, w + (size_t)(n0 + my_wr) * k_dim + k0, (uint32_t)kw * 2, &full[st]);
+    } else {
+      mbar_arrive_expect_tx(&full[st], (uint32_t)kw * 4);
+      bulk_g2s(dst + BM * WROW + my_xr * XROW, x + (size_t)my_xr * k_dim + k0, (uint32_t)kw * 4, &full[st]);
+    }
+  };
+  for (int kc = 0; kc < S && kc < n_k; ++kc) issue(kc);
+
+  float acc[MT][NR][4];
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NR; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
+  // ldmatrix row of this lane: matrices (rows 0-7 | 8-15) x (k 0-7 | 8-15) of an m-tile
+  const uint32_t a_off = ((lane & 7) + 8 * ((lane >> 3) & 1)) * WROW + 16 * (lane >> 4);
+
+  for (int kc = 0; kc < n_k; ++kc) {
+    const int st = kc % S;
+    const bool ok = mbar_wait_bounded(&full[st], (kc / S) & 1);
+    if (__syncthreads_or(!ok)) {
+      if (threadIdx.x == 0) flag_error(err, ERR_TIMEOUT);
+      // wait (bounded) for the copies in flight before the CTA retires
+      for (int k2 = kc; k2 < n_k && k2 < kc + S; ++k2) mbar_wait_bounded(&full[k2 % S], (k2 / S) & 1);
+      return;
+    }
+    const int kw = min(OP_BK, k_dim - ((kc + kc0) % n_k) * OP_BK);
+    if (32 * warp < kw) {
+      const uint8_t* sb = smem + st * STAGE;
+      const uint32_t sa = smem_u32(sb) + a_off;
+#pragma unroll
+      for (int ks = 0; ks < 2; ++ks) {
+        const int kb = 32 * warp + 16 * ks;
+        uint32_t a[MT][4];
+#pragma unroll
+        for (int mt = 0; mt < MT; ++mt) ldsm_x4(sa + 16 * mt * WROW + kb * 2, a[mt]);
+#pragma unroll
+        for (int nt = 0; nt < NR; ++nt) {
+          const float* xr = reinterpret_cast<const float*>(sb + BM * WROW + (8 * nt + gi) * XROW) + kb + 2 * ti;
+          const float2 p0 = *reinterpret_cast<const float2*>(xr);
+          const float2 p1 = *reinterpret_cast<const float2*>(xr + 8);
+          const float h0 = bf_rn(p0.x), h1 = bf_rn(p0.y), h2 = bf_rn(p1.x), h3 = bf_rn(p1.y);
+          const uint32_t bh0 = pack_bf2(h0, h1), bh1 = pack_bf2(h2, h3);
+          const uint32_t bl0 = pack_bf2(p0.x - h0, p0.y - h1), bl1 = pack_bf2(p1.x - h2, p1.y - h3);
+#pragma unroll
+          for (int mt = 0; mt < MT; ++mt) {
+            mma_bf16(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], bh0, bh1);
+            mma_bf16(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], bl0, bl1);
+          }
+        }
+      }
+    }
+    __syncthreads();  // stage st consumed by every warp
+    if (kc + S < n_k) issue(kc + S);
+  }
+
+  // D fragment: (row 16mt+g, cols 8nt+2t, +1) and (row 16mt+g+8, same cols)
+  float* red = reinterpret_cast<float*>(smem);  // [8][BM][XR + 1]
+#pragma unroll
+  for (int mt = 0; mt < MT; ++mt)
+#pragma unroll
+    for (int nt = 0; nt < NR; ++nt) {
+      float* r0 = red + (warp * BM + 16 * mt + gi) * (XR + 1) + 8 * nt + 2 * ti;
+      float* r1 = r0 + 8 * (XR + 1);
+      r0[0] = acc[mt][nt][0];
+      r0[1] = acc[mt][nt][1];
+      r1[0] = acc[mt][nt][2];
+      r1[1] = acc[mt][nt][3];
+    }
+  __syncthreads();
+  for (int e = threadIdx.x; e < BM * XR; e += 256) {
+    const int nn = e % BM, r = e / BM;
+    float v = 0.f;
+#pragma unroll
+    for (int wv = 0; wv < 8; ++wv) v += red[(wv * BM + nn) * (XR + 1) + r];
+    if (nn < w_rows && r < n_rows) y[(size_t)r * d_model + n0 + nn] = v;
+  }
+}
+
+template <int MT, int NR>
+cudaError_t launch_out_proj_stream(int nr, int d_model, int k_dim, const float* x, const void* w, float* y,
+                                   unsigned* err, cudaStream_t s) {
+  constexpr int smem = op_stages(MT, NR) * op_stage_bytes(MT, NR);
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(out_proj_stream_kernel<MT, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  const int grid = (d_model + 16 * MT - 1) / (16 * MT);
+  out_proj_stream_kernel<MT, NR><<<grid, 256, smem, s>>>(nr, d_model, k_dim, x,
+                                                          static_cast<const __nv_bfloat16*>(w), y, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
-                            int w_dtype, float* y, cudaStream_t s) {
+                            int w_dtype, float* y, unsigned* err, cudaStream_t s) {
   if (n_rows == 0 || d_model == 0) return cudaSuccess;
   const dim3 grid((d_model + 31) / 32);
   for (int r0 = 0; r0 < n_rows; r0 += 32) {
     const int nr = n_rows - r0 < 32 ? n_rows - r0 : 32;
     const float* xr = x + (size_t)r0 * k_dim;
     float* yr = y + (size_t)r0 * d_model;
+    if (w_dtype == KVQ_BF16) {
+      // 32-row W blocks when they alone give ~a CTA per SM, else 16-row blocks
+      const bool wide = (d_model + 31) / 32 >= 100;
+      cudaError_t e;
+      if (nr <= 8) e = wide ? launch_out_proj_stream<2, 1>(nr, d_model, k_dim, xr, w, yr, err, s)
+                            : launch_out_proj_stream<1, 1>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else if (nr <= 16) e = wide ? launch_out_proj_stream<2, 2>(nr, d_model, k_dim, xr, w, yr, err, s)
+                                  : launch_out_proj_stream<1, 2>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else e = wide ? launch_out_proj_stream<2, 4>(nr, d_model, k_dim, xr, w, yr, err, s)
+                    : launch_out_proj_stream<1, 4>(nr, d_model, k_dim, xr, w, yr, err, s);
+      if (e != cudaSuccess) return e;
+      continue;
+    }
 #define KVQ_OP(NRR)                                                                                  \
   if (w_dtype == KVQ_F32) out_proj_mma_kernel<KVQ_F32, NRR><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr); \
   else out_proj_mma_kernel<KVQ_BF16, NRR><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr)

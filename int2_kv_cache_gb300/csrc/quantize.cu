@@ -170,6 +170,131 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
   }
 }
 
+// locate() for one warp: the sequences are searched 32 at a time (one per lane)
+// instead of by bisection, so the lookup is a few independent loads deep.
+__device__ __forceinline__ bool locate_warp(int t, int n_seqs, const int32_t* cu_new, const int32_t* start_pos,
+                                            const int32_t* table, const PageGeom& g, unsigned* err,
+                                            long long* rec_index, int* slot, int head, int lane) {
+  int b = -1;
+  for (int b0 = 0; b0 < n_seqs && b < 0; b0 += 32) {
+    const int bb = b0 + lane;
+    const bool hit = bb < n_seqs && __ldg(cu_new + bb) <= t && t < __ldg(cu_new + bb + 1);
+    const unsigned m = __ballot_sync(0xffffffffu, hit);
+    if (m) b = b0 + __ffs(m) - 1;
+  }
+  if (b < 0) {
+    if (lane == 0) flag_error(err, ERR_SEQ_RANGE);
+    return false;
+  }
+  const long long pos = (long long)__ldg(start_pos + b) + (t - __ldg(cu_new + b));
+  const long long page = pos / g.page_tokens;
+  if (pos < 0 || page >= g.max_blocks) {
+    if (lane == 0) flag_error(err, ERR_POS_RANGE);
+    return false;
+  }
+  const int blk = __ldg(table + (size_t)b * g.max_blocks + page);
+  if (blk < 0 || blk >= g.num_blocks) {
+    if (lane == 0) flag_error(err, ERR_BLOCK_RANGE);
+    return false;
+  }
+  *rec_index = (long long)blk * g.n_kv_heads + head;
+  *slot = (int)(pos % g.page_tokens);
+  return true;
+}
+
+// Small appends (a decode step's one token per sequence): one CTA per (token,
+// head, role) so the double-float rotations are spread over the whole GPU.
+// Warps 0-3 each accumulate the terms of 32 input channels (rows of a dense R_h
+// read from global memory, L2-resident) while warp 4 finds the token's page
+// slot; the four double-float partial sums are added in a fixed order, and
+// warp 0 centres, quantizes and writes the group.
+// grid = (n_new, n_kv_heads, roles), block = 160.
+constexpr int APPEND_SMALL_MAX = 128;  // tokens per call below which this path is used
+
+__global__ void __launch_bounds__(160, 4) append_small_dense_kernel(
+    PageGeom g, int n_seqs, int dtype, const int32_t* __restrict__ cu_new, const int32_t* __restrict__ start_pos,
+    const int32_t* __restrict__ table, AppendRoles roles, uint8_t* __restrict__ pool, unsigned* err) {
+  __shared__ float2 part[4][D];  // (hi, lo) of each warp's partial x R
+  __shared__ long long s_rec;    // record index, or -1 when the token is skipped
+  __shared__ int s_slot;
+  const AppendRole ro = blockIdx.z ? roles.r[1] : roles.r[0];
+  const int t = blockIdx.x, h = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (warp == 4) {
+    long long rec;
+    int slot;
+    // flag each bad token once (role 0), skip it in both roles
+    const bool ok = locate_warp(t, n_seqs, cu_new, start_pos, table, g, blockIdx.z == 0 ? err : nullptr, &rec, &slot,
+                                h, lane);
+    if (lane == 0) {
+      s_rec = ok ? rec : -1;
+      s_slot = slot;
+    }
+    __syncthreads();
+    return;
+  }
+  const float4 v = load4(ro.src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
+  const float xin[4] = {v.x, v.y, v.z, v.w};
+  const float4* R4 = reinterpret_cast<const float4*>(ro.rot.dense + (size_t)h * D * D) + lane;
+  float sh[4][4], sl[4][4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) sh[u][i] = sl[u][i] = 0.f;
+  // the warp's 32 rows of R in two batches of 16 loads in flight
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    float4 rr[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) rr[j] = __ldg(R4 + (size_t)(32 * warp + 16 * half + j) * 32);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int m = 8 * warp + 4 * half + (j >> 2), u = j & 3;  // row 4m + u
+      const float xh = __shfl_sync(0xffffffffu, xin[u], m);    // channel 4m + u lives in lane m
+      const float r[4] = {rr[j].x, rr[j].y, rr[j].z, rr[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __fmul_rn(xh, r[i]);
+        const float pe = __fmaf_rn(xh, r[i], -p);
+        const DF q = two_sum(sh[u][i], p);
+        sh[u][i] = q.hi;
+        sl[u][i] = __fadd_rn(sl[u][i], __fadd_rn(q.lo, pe));
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const DF a = df_add(DF{sh[0][i], sl[0][i]}, DF{sh[1][i], sl[1][i]});
+    const DF b = df_add(DF{sh[2][i], sl[2][i]}, DF{sh[3][i], sl[3][i]});
+    const DF c = df_add(a, b);
+    part[warp][4 * lane + i] = make_float2(c.hi, c.lo);
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const long long rec = s_rec;
+  const int slot = s_slot;
+  if (rec < 0) return;
+  DF x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 p0 = part[0][4 * lane + i], p1 = part[1][4 * lane + i];
+    const float2 p2 = part[2][4 * lane + i], p3 = part[3][4 * lane + i];
+    x[i] = df_add(df_add(DF{p0.x, p0.y}, DF{p1.x, p1.y}), df_add(DF{p2.x, p2.y}, DF{p3.x, p3.y}));
+  }
+  if (ro.mu_rot) {
+    const float4 m = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
+    x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
+    x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+  }
+  QParams qp;
+  const unsigned byte = quantize_warp_df(x, ro.clip, qp);
+  uint8_t* recp = pool + (size_t)rec * g.record;
+  recp[ro.codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
+  if (lane == 0)
+    *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
+        (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+}
+
 cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* k,
                                    const void* v, int dtype, const int32_t* cu_new,
                                    const int32_t* start_pos, const int32_t* table, RotDev rot_k,
@@ -190,6 +315,27 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
   }
   // keys and values may use different rotation kinds: one launch per kind
   const bool kd = rot_k.kind == KVQ_ROT_DENSE, vd = rot_v.kind == KVQ_ROT_DENSE;
+  if (n_new <= APPEND_SMALL_MAX && kd && vd) {
+    append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 2), 160, 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
+                                                                             table, roles, pool, err);
+    return cudaGetLastError();
+  }
+  if (n_new <= APPEND_SMALL_MAX && (kd || vd)) {
+    // dense roles through the small-append kernel, the others through the warp kernel
+    for (int role = 0; role < 2; ++role) {
+      AppendRoles one;
+      one.r[0] = roles.r[role];
+      one.r[1] = roles.r[role];
+      if (role == 0 ? kd : vd)
+        append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 1), 160, 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
+                                                                                 table, one, pool, err);
+      else
+        append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
+      const cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   if (kd == vd) {
     const dim3 g2(grid.x, grid.y, 2);
     if (kd) append_kernel<true><<<g2, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
