@@ -47,7 +47,7 @@ namespace kvq {
 
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int DEC_WARPS = 4;
-constexpr int DEC_STAGES = 4;
+constexpr int DEC_STAGES = 3;  // stages of 64 tokens per warp
 constexpr int SM_COUNT = 152;  // GB300
 // Lazy softmax rescaling: the running sums keep their reference maximum until a
 // chunk's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
@@ -286,11 +286,14 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     const int32_t* __restrict__ table, const uint8_t* __restrict__ pool, DecWs ws,
     float* __restrict__ o_rot, unsigned* err) {
   constexpr int NT = n_tiles(G);
-  constexpr int PPC = 32 / P;       // pages per chunk
-  constexpr int REC = 72 * P;       // bytes per page record
-  constexpr int CHUNK = PPC * REC;  // 2304
-  constexpr int CPF = 32 / PPC;     // chunks per fill of the page cache
-  constexpr uint32_t ALL_PAGES = (1u << PPC) - 1u;
+  constexpr int PPC = 32 / P;              // pages per 32-token chunk
+  constexpr int REC = 72 * P;              // bytes per page record
+  constexpr int CHUNK = PPC * REC;         // 2304 bytes: one 32-token chunk
+  constexpr int PPS = 2 * PPC;             // pages per stage (64 tokens)
+  constexpr int STAGE = 2 * CHUNK;         // 4608 bytes
+  constexpr int CPF = 32 / PPS;            // stages per fill of the page cache
+  constexpr uint32_t ALL_PAGES = (1u << PPS) - 1u;
+  constexpr uint32_t CHUNK_PAGES = (1u << PPC) - 1u;
   constexpr unsigned FULLM = 0xffffffffu;
   using CL = ChunkLayout<P>;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -298,13 +301,15 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   const int Hkv = g.n_kv_heads;
   const int max_len = g.max_blocks * P;
 
-  __shared__ __align__(128) uint8_t stage[DEC_WARPS][DEC_STAGES][CHUNK];
+  extern __shared__ __align__(128) uint8_t dyn_smem[];  // [DEC_WARPS][DEC_STAGES][STAGE]
+  auto stage_ptr = [&](int w, int sidx) { return dyn_smem + (w * DEC_STAGES + sidx) * STAGE; };
   __shared__ __align__(8) uint64_t bars[DEC_WARPS][DEC_STAGES];
-  __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the staged chunk was copied
+  __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the staged entry was copied
   __shared__ int s_sum[DEC_WARPS];
   __shared__ int s_start[DEC_WARPS][2];  // first sequence of each warp's slice, chunks before it
 
-  auto n_chunks_of = [&](int len) { return (len <= 0 || len > max_len) ? 0 : (len + 31) >> 5; };
+  // list entries (64-token stages) of a sequence of `len` tokens
+  auto n_chunks_of = [&](int len) { return (len <= 0 || len > max_len) ? 0 : (len + 63) >> 6; };
 
   // ---- the batch's chunk list: sequence b holds H_kv * nb_b entries, unit (b, h)
   //      the nb_b entries from H_kv * prefix_b + h * nb_b on ----
@@ -377,17 +382,17 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   }
   ChunkWalker cw = iw;  // consume side
 
-  // Page cache: lane l holds the record index (block * H_kv + h) of page l % PPC
-  // of the warp's chunk i0 + l / PPC; -2: past the sequence, -1: bad block id.
+  // Page cache: lane l holds the record index (block * H_kv + h) of page l % PPS
+  // of the warp's entry i0 + l / PPS; -2: past the sequence, -1: bad block id.
   int rec = -2;
   int n_issued = 0;  // chunks whose copies were issued
   auto fill_cache = [&](int i0) {
     ChunkWalker w = iw;
-    const int i = i0 + lane / PPC;
+    const int i = i0 + lane / PPS;
     rec = -2;
     if (i < my_n) {
       walk_to(w, ga + i);
-      const int pg = (ga + i - w.S) * PPC + lane % PPC;
+      const int pg = (ga + i - w.S) * PPS + lane % PPS;
       if (pg < (w.len + P - 1) / P) {
         const int pid = __ldg(table + (size_t)w.b * g.max_blocks + pg);
         rec = (pid >= 0 && pid < g.num_blocks) ? pid * Hkv + w.h : -1;
@@ -401,11 +406,11 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     walk_to(iw, ga + i);
     if (i % CPF == 0) fill_cache(i);
     const int sidx = i % DEC_STAGES;
-    const bool mine = lane / PPC == i % CPF;
+    const bool mine = lane / PPS == i % CPF;
     const bool ok = mine && rec >= 0;
     const unsigned okm = __ballot_sync(FULLM, ok);
     const unsigned badm = __ballot_sync(FULLM, mine && rec == -1);
-    const uint32_t bits = (okm >> ((i % CPF) * PPC)) & ALL_PAGES;
+    const uint32_t bits = (okm >> ((i % CPF) * PPS)) & ALL_PAGES;
     uint64_t* bar = &bars[warp][sidx];
     if (lane == 0) {
       if (badm) flag_error(err, ERR_BLOCK_RANGE);
@@ -415,7 +420,7 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     __syncwarp();
     if (ok) {
       fence_proxy_async();
-      bulk_g2s(stage[warp][sidx] + (lane % PPC) * REC, pool + (size_t)rec * g.record, REC, bar);
+      bulk_g2s(stage_ptr(warp, sidx) + (lane % PPS) * REC, pool + (size_t)rec * g.record, REC, bar);
     }
   };
 
@@ -504,7 +509,7 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   const uint32_t sel = (gi & 1) ? 0x7632u : 0x5410u;  // pick remainder / high halves
   const int srcA = 8 * ti + (gi >> 1);                // lanes holding tokens 2t, 2t + 8 of head 4nt + g/2
   // ldmatrix row address of this lane inside a staged chunk (tile 0); tile 1 is 1,152 bytes on
-  const uint32_t vrow = smem_u32(stage[warp][0]) + CL::v(0, 8 * (lane >> 4) + (lane & 7)) + 16 * ((lane >> 3) & 1);
+  const uint32_t vrow = smem_u32(stage_ptr(warp, 0)) + CL::v(0, 8 * (lane >> 4) + (lane & 7)) + 16 * ((lane >> 3) & 1);
 
   // One 32-token chunk from a staged stage.  FULL: every token valid and copied.
   auto chunk = [&](auto full_tag, const uint8_t* st, uint32_t vaddr, int tok0, int len, int bits) {
@@ -654,12 +659,18 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
       cur_S = cw.S;
       cur_E = cw.E;
     }
-    const uint8_t* st = stage[warp][sidx];
-    const uint32_t vaddr = vrow + sidx * CHUNK;
     const int bits = sflag[warp][sidx];
-    const int tok0 = (ga + i - cw.S) * 32;
-    if (tok0 + 32 <= cw.len && bits == (int)ALL_PAGES) chunk(std::true_type{}, st, vaddr, tok0, cw.len, bits);
-    else chunk(std::false_type{}, st, vaddr, tok0, cw.len, bits);
+    const int tokS = (ga + i - cw.S) * 64;
+#pragma unroll 1
+    for (int sub = 0; sub < 2; ++sub) {  // the stage's two 32-token chunks
+      const int tok0 = tokS + 32 * sub;
+      if (tok0 >= cw.len) break;
+      const uint8_t* st = stage_ptr(warp, sidx) + sub * CHUNK;
+      const uint32_t vaddr = vrow + sidx * STAGE + sub * CHUNK;
+      const int cbits = (bits >> (sub * PPC)) & (int)CHUNK_PAGES;
+      if (tok0 + 32 <= cw.len && cbits == (int)CHUNK_PAGES) chunk(std::true_type{}, st, vaddr, tok0, cw.len, cbits);
+      else chunk(std::false_type{}, st, vaddr, tok0, cw.len, cbits);
+    }
     __syncwarp();
     if (i + DEC_STAGES < my_n) issue(i + DEC_STAGES);
   }
@@ -734,6 +745,19 @@ __global__ void __launch_bounds__(CB_WARPS * 32) decode_combine_kernel(int n_kv_
   }
 }
 
+// Shared-memory ring of the decode kernel: 4 warps x DEC_STAGES stages of 64 tokens.
+constexpr int DEC_SMEM = DEC_WARPS * DEC_STAGES * 2 * 1152 * 2;
+
+template <int G, int P>
+cudaError_t decode_smem_attr() {
+  static bool done = false;  // one flag per kernel instance
+  if (done) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(decode_split_kernel<G, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM);
+  if (e == cudaSuccess) done = true;
+  return e;
+}
+
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q, int q_dtype,
                           const int32_t* seq_lens, int max_seq_len, const int32_t* table, RotDev rot_k,
                           const uint8_t* pool, int n_ctas, void* ws_base, float* o_rot, unsigned* err,
@@ -763,15 +787,20 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_ctas);
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = DEC_SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-#define KVQ_DEC(GG, PP) \
-  e = cudaLaunchKernelEx(&cfg, decode_split_kernel<GG, PP>, g, n_seqs, n_q_heads, seq_lens, table, pool, ws, o_rot, err)
+#define KVQ_DEC(GG, PP)                                                                                    \
+  do {                                                                                                    \
+    e = decode_smem_attr<GG, PP>();                                                                       \
+    if (e == cudaSuccess)                                                                                 \
+      e = cudaLaunchKernelEx(&cfg, decode_split_kernel<GG, PP>, g, n_seqs, n_q_heads, seq_lens, table, pool, ws, \
+                             o_rot, err);                                                                  \
+  } while (0)
 #define KVQ_DEC_P(GG) \
   if (g.page_tokens == 16) KVQ_DEC(GG, 16); else KVQ_DEC(GG, 8)
   switch (gqa) {
@@ -788,6 +817,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   // the combine is a programmatic dependent of the decode kernel
   cfg.gridDim = dim3(n_seqs * g.n_kv_heads, gqa);
   cfg.blockDim = dim3(CB_WARPS * 32);
+  cfg.dynamicSmemBytes = 0;
 #define KVQ_CB(GG) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<GG>, g.n_kv_heads, n_q_heads, ws, o_rot)
   switch (gqa) {
     case 1: KVQ_CB(1); break;
