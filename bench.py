@@ -45,8 +45,10 @@ def parse():
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
     p.add_argument("--case", choices=["decode_step", "append_chunk", "calib"], default="decode_step")
-    p.add_argument("--seqs", type=int, default=16)
-    p.add_argument("--ctx", type=int, default=32768)
+    p.add_argument("--workload", choices=["gqa8b", "long4b", "serve14b"], default="gqa8b",
+                   help="decode-step shape: gqa8b (default, the headline), long4b (128K), serve14b (ragged)")
+    p.add_argument("--seqs", type=int, default=None, help="sequences (default: 16 gqa8b, 1 long4b, 64 serve14b)")
+    p.add_argument("--ctx", type=int, default=None, help="context (gqa8b default 32768, long4b 131072)")
     p.add_argument("--splits", type=int, default=0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
@@ -161,18 +163,41 @@ def gen_parallel(fn, n):
         return list(ex.map(fn, range(n)))
 
 
-class DecodeStep:
-    """The decode-step workload resident on one GPU."""
+def decode_workload(args):
+    """The decode case named by --workload (sizes from --seqs / --ctx when given)."""
+    from int2_kv_cache_gb300 import workloads as W
+    if args.workload == "long4b":
+        return W.long4b_128k(n_seqs=args.seqs or 1, ctx=args.ctx or 131072)
+    if args.workload == "serve14b":
+        return W.serve14b_ragged(n_seqs=args.seqs or 64)
+    return W.gqa8b_32k(n_seqs=args.seqs or 16, ctx=args.ctx or 32768)
 
-    def __init__(self, n_seqs: int, ctx: int, splits: int, device: str):
+
+def workload_text(c) -> str:
+    lens = np.asarray(c.seq_lens)
+    ctx = f"ctx {int(lens[0])}" if lens.min() == lens.max() else f"ragged ctx {int(lens.min())}..{int(lens.max())}"
+    rot = {"dense": "dense expm(A-A^T)", "signed_hadamard": "signed-Hadamard", "identity": "identity"}[c.rot_k.kind]
+    return (f"{c.name.split('_')[0]} decode step: B={len(lens)} x {ctx}, Hq {c.n_q_heads} / Hkv {c.n_kv_heads}, "
+            f"d 128, hidden {c.d_model}, {c.page_tokens}-token pages (shuffled), {rot} rotations, mu-centred keys, "
+            f"clip {float(c.clip_k):g}")
+
+
+class DecodeStep:
+    """The decode-step workload resident on one GPU: every sequence holds len - 1
+    cached tokens; a step appends its last token, decodes over len tokens and
+    projects through the folded W_O."""
+
+    def __init__(self, c, splits: int, device: str):
         import torch
         import int2_kv_cache_gb300 as kvq
-        from int2_kv_cache_gb300 import workloads as W
 
         self.torch, self.kvq, self.dev = torch, kvq, device
-        c = W.gqa8b_32k(n_seqs=n_seqs, ctx=ctx)
         self.case = c
-        self.B, self.L, self.hq, self.hkv, self.dm = n_seqs, ctx, c.n_q_heads, c.n_kv_heads, c.d_model
+        lens = np.asarray(c.seq_lens, dtype=np.int64)
+        n_seqs = len(lens)
+        self.lens_np = lens
+        self.B, self.L, self.hq, self.hkv, self.dm = n_seqs, int(lens.max()), c.n_q_heads, c.n_kv_heads, c.d_model
+        ctx = self.L
         bf = torch.bfloat16
         t = lambda x, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(device).to(dt)
         self.t = t
@@ -185,13 +210,13 @@ class DecodeStep:
         kvq.kvq_key_mean(t(c.calibration_keys(), bf), mu)
         self.mu_rot = torch.empty_like(mu)
         kvq.kvq_rotate_heads(mu.reshape(1, c.n_kv_heads, 128), self.rot_k, self.mu_rot.reshape(1, c.n_kv_heads, 128))
-        # paged cache: positions 0 .. L-2 are history; every step writes position L-1
+        # paged cache: positions 0 .. len-2 are history; every step writes position len-1
         self.pool = torch.zeros(kvq.kvq_pool_bytes(self.layout), dtype=torch.uint8, device=device)
-        hist = ctx - 1
         for b0 in range(0, n_seqs, 4):
             kvs = gen_parallel(lambda i: c.kv(b0 + i), min(4, n_seqs - b0))
             for i, (k, v) in enumerate(kvs):
                 b = b0 + i
+                hist = int(lens[b]) - 1
                 kvq.kvq_quantize_append(self.layout, t(k[:hist], bf), t(v[:hist], bf), t(np.array([0, hist]), torch.int32),
                                         t(np.array([0]), torch.int32), self.table[b:b + 1].contiguous(), self.rot_k,
                                         self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
@@ -209,13 +234,13 @@ class DecodeStep:
         self.k_new = self.host_k.to(device)
         self.v_new = self.host_v.to(device)
         self.cu_new = t(np.arange(n_seqs + 1), torch.int32)
-        self.start = t(np.full(n_seqs, hist), torch.int32)
-        self.lens = t(np.full(n_seqs, ctx), torch.int32)
+        self.start = t(lens - 1, torch.int32)
+        self.lens = t(lens, torch.int32)
         self.splits = splits
         ws = kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, splits)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         # thread blocks of the decode kernel (the library's choice when splits == 0)
-        self.n_ctas = splits or next(s for s in range(1, 1025)
+        self.n_ctas = splits or next(s for s in range(1, 8193)
                                      if kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, s) == ws)
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
         self.y = torch.empty(n_seqs, self.dm, device=device)
@@ -247,17 +272,18 @@ class DecodeStep:
         self.host_y.copy_(self.y, non_blocking=True)
 
     def decode_bytes(self) -> dict:
-        B, L, hq, hkv = self.B, self.L, self.hq, self.hkv
+        B, hq, hkv = self.B, self.hq, self.hkv
+        lens = self.lens_np
         g = hq // hkv
         units = B * hkv
         # one partial (acc[128], m, l per query head) per (warp slice, unit) pair:
         # at most 4 * n_ctas + units of them, written once and read once
-        pairs = min(4 * self.n_ctas + units, units * ((L + 31) // 32))
-        cache = B * L * hkv * 72
+        pairs = min(4 * self.n_ctas + units, int(hkv * ((lens + 63) // 64).sum()))
+        cache = int(lens.sum()) * hkv * 72
         return {
             "kv_cache": cache,
             "q": B * hq * 128 * 2,
-            "block_table": B * ((L + 15) // 16) * 4,
+            "block_table": int(((lens + self.case.page_tokens - 1) // self.case.page_tokens).sum()) * 4,
             "rotation": hkv * 128 * 128 * 4,
             "query_fragments_write_read": 2 * units * (((g + 3) // 4) * 16 * 32 * 4 + g * 16),
             "partials_write_read": 2 * pairs * g * 130 * 4,
@@ -275,7 +301,7 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    w = DecodeStep(args.seqs, args.ctx, args.splits, device)
+    w = DecodeStep(decode_workload(args), args.splits, device)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -341,8 +367,7 @@ def run_gpu(args):
         "dtype": "f32",
         "data": "synthetic (seeded; bf16 q/K/V/W_O, 2-bit cache)",
         "config": {
-            "workload": f"gqa8b decode step: B={w.B} x ctx {w.L}, Hq 32 / Hkv 8, d 128, hidden 4096, "
-                        "16-token pages (shuffled), dense expm(A-A^T) rotations, mu-centred keys, clip 1.0",
+            "workload": workload_text(w.case),
             "batch": w.B, "ctx": w.L, "n_q_heads": w.hq, "n_kv_heads": w.hkv, "d_model": w.dm,
             "decode_ctas": w.n_ctas, "parallelism": f"replicas x{world}",
             "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (w.pool.numel() / 1e6),
@@ -424,8 +449,7 @@ def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return
-    from int2_kv_cache_gb300 import workloads as W
-    case = W.gqa8b_32k(n_seqs=args.seqs, ctx=args.ctx)
+    case = decode_workload(args)
     st = OracleStep(case, 0)
     for _ in range(max(args.warmup, 3)):
         st.step()
@@ -434,13 +458,14 @@ def run_reference(args):
         st.step()
     el = time.perf_counter() - t0
     value = args.steps / el
-    sample = f"each step = one decode step (append, decode over {args.ctx} tokens, W_O) of 1 of {args.seqs} sequences"
+    sample = (f"each step = one decode step (append, decode over {int(case.seq_lens[0])} tokens, W_O) of sequence 0 "
+              f"of {case.n_seqs}")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": max(args.warmup, 3), "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"gqa8b decode step: B={args.seqs} x ctx {args.ctx}, Hq 32 / Hkv 8, d 128, hidden 4096",
-                   "batch": args.seqs, "ctx": args.ctx},
+        "config": {"workload": workload_text(case), "batch": case.n_seqs, "ctx": int(np.max(case.seq_lens)),
+                   "n_q_heads": case.n_q_heads, "n_kv_heads": case.n_kv_heads, "d_model": case.d_model},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cpu_cores(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

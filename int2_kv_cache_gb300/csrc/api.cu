@@ -215,7 +215,7 @@ kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int m
                                      int n_splits, size_t* bytes) {
   KVQ_CHECK(check_layout(layout, true));
   if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");
-  if (n_seqs < 0 || max_seq_len < 0 || n_splits < 0 || n_splits > 1024)
+  if (n_seqs < 0 || max_seq_len < 0 || n_splits < 0 || n_splits > 8192)
     return fail(KVQ_EINVAL, "bad n_seqs %d / max_seq_len %d / n_splits %d", n_seqs, max_seq_len, n_splits);
   KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
   const int gqa = layout->n_q_heads / layout->n_kv_heads;
@@ -233,7 +233,7 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
   if (!valid_dtype(q_dtype)) return fail(KVQ_EINVAL, "bad q dtype %d", (int)q_dtype);
   if (max_seq_len < 0 || (long long)max_seq_len > (long long)layout->max_blocks_per_seq * layout->page_tokens)
     return fail(KVQ_EINVAL, "max_seq_len %d outside [0, max_blocks_per_seq * page_tokens]", max_seq_len);
-  if (n_splits < 0 || n_splits > 1024) return fail(KVQ_EINVAL, "n_splits %d outside [0, 1024]", n_splits);
+  if (n_splits < 0 || n_splits > 8192) return fail(KVQ_EINVAL, "n_splits %d outside [0, 8192]", n_splits);
   KVQ_CHECK(check_rot(rot_k, "rot_k"));
   if (n_seqs == 0) return KVQ_OK;
   KVQ_PTR(q, "q");

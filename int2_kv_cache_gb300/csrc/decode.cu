@@ -120,6 +120,13 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
+// The same product with a zero accumulator input (d = A B).
+__device__ __forceinline__ void mma16816_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t d;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -527,8 +534,6 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
       const uint2 kr0 = *reinterpret_cast<const uint2*>(st + CL::k(u, gi) + 8 * ti);
       const uint2 kr1 = *reinterpret_cast<const uint2*>(st + CL::k(u, gi + 8) + 8 * ti);
       float d[NT][4];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) d[nt][0] = d[nt][1] = d[nt][2] = d[nt][3] = 0.f;
       const uint32_t s00 = kr0.x >> 10, s01 = kr0.y >> 10, s10 = kr1.x >> 10, s11 = kr1.y >> 10;
 #pragma unroll
       for (int s = 0; s < 8; ++s) {
@@ -538,7 +543,10 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
         const uint32_t a2 = (s <= 4 ? kr0.y : s01) & mask;  // row g,   channels 32t+16+s | 32t+24+s
         const uint32_t a3 = (s <= 4 ? kr1.y : s11) & mask;  // row g+8
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma16816(d[nt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+        for (int nt = 0; nt < NT; ++nt) {
+          if (s == 0) mma16816_zero(d[nt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+          else mma16816(d[nt], a0, a1, a2, a3, bq[nt][s][0], bq[nt][s][1]);
+        }
       }
       const float2 km0 = meta_pair(st + CL::km(u, gi));
       const float2 km1 = meta_pair(st + CL::km(u, gi + 8));
@@ -687,60 +695,69 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Combine: grid (U, G), 256 threads.  o_rot of query head j of unit u is the
-// log-sum-exp merge of the unit's partials (slots k + u, k0 <= k <= k1): warp w
-// folds slots k0 + w, k0 + w + 8, ... with a running maximum, then the eight
-// warp results are merged in warp order, so the result does not depend on timing.
+// Combine: grid (U, G), nw warps (1..32, from the average partials per unit).
+// o_rot of query head j of unit u is the log-sum-exp merge of the unit's
+// partials (slots k + u, k0 <= k <= k1): the block first takes the maximum M of
+// every slot's m, then warp w sums the slots w, w + nw, ... weighted by
+// 2^(m - M) (independent loads, many in flight), and the warp sums are added in
+// warp order, so the result does not depend on timing.
 // ---------------------------------------------------------------------------
-constexpr int CB_WARPS = 8;
+constexpr int CB_MAX_WARPS = 32;
 
 template <int G>
-__global__ void __launch_bounds__(CB_WARPS * 32) decode_combine_kernel(int n_kv_heads, int n_q_heads, DecWs ws,
-                                                                       float* __restrict__ o_rot) {
-  __shared__ float sm_m[CB_WARPS], sm_l[CB_WARPS];
-  __shared__ __align__(16) float sm_a[CB_WARPS][D];
+__global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n_kv_heads, int n_q_heads, DecWs ws,
+                                                                           float* __restrict__ o_rot) {
+  __shared__ float sm_m[CB_MAX_WARPS], sm_l[CB_MAX_WARPS];
+  __shared__ __align__(16) float sm_a[CB_MAX_WARPS][D];
   pdl_wait();  // the partials come from decode_split_kernel
   const int u = blockIdx.x, j = blockIdx.y;
+  const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int2 sp = __ldcg(ws.span + u);
   if (sp.x > sp.y) return;  // no cached tokens (o = 0 already) or an invalid length
-  float m = -INFINITY, l = 0.f;
+  const int ns = sp.y - sp.x + 1;
+  const size_t stride = (size_t)G * PART;  // floats between consecutive slots
+  const float* base = ws.part + ((size_t)(sp.x + u) * G + j) * PART;
+  float m = -INFINITY;
+  for (int t = threadIdx.x; t < ns; t += blockDim.x) m = fmaxf(m, __ldcg(base + t * stride + D));
+  m = warp_max(m);
+  if (nw > 1) {
+    if (lane == 0) sm_m[warp] = m;
+    __syncthreads();
+    m = -INFINITY;
+    for (int w = 0; w < nw; ++w) m = fmaxf(m, sm_m[w]);
+  }
+  const float M = m;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 2
-  for (int k = sp.x + warp; k <= sp.y; k += CB_WARPS) {
-    const float* pp = ws.part + ((size_t)(k + u) * G + j) * PART;
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + D));
-    const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + lane);
-    if (ml.x == -INFINITY) continue;
-    const float mn = fmaxf(m, ml.x);
-    const float so = exp2f(m - mn), sn = exp2f(ml.x - mn);
-    l = fmaf(l, so, ml.y * sn);
-    a.x = fmaf(a.x, so, x.x * sn); a.y = fmaf(a.y, so, x.y * sn);
-    a.z = fmaf(a.z, so, x.z * sn); a.w = fmaf(a.w, so, x.w * sn);
-    m = mn;
+  float l = 0.f;
+  if (M != -INFINITY) {
+#pragma unroll 4
+    for (int t = warp; t < ns; t += nw) {
+      const float* pp = base + t * stride;
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + D));
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + lane);
+      const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+      l = fmaf(e, ml.y, l);
+      a.x = fmaf(e, x.x, a.x); a.y = fmaf(e, x.y, a.y); a.z = fmaf(e, x.z, a.z); a.w = fmaf(e, x.w, a.w);
+    }
   }
-  if (lane == 0) {
-    sm_m[warp] = m;
-    sm_l[warp] = l;
+  const int b = u / n_kv_heads, h = u % n_kv_heads;
+  float4* dst = reinterpret_cast<float4*>(o_rot + ((size_t)b * n_q_heads + h * G + j) * D);
+  if (nw == 1) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    dst[lane] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+    return;
   }
+  if (lane == 0) sm_l[warp] = l;
   reinterpret_cast<float4*>(sm_a[warp])[lane] = a;
   __syncthreads();
   if (threadIdx.x < D) {
     const int c = threadIdx.x;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < CB_WARPS; ++w) M = fmaxf(M, sm_m[w]);
     float A = 0.f, L = 0.f;
-    if (M != -INFINITY) {
-#pragma unroll
-      for (int w = 0; w < CB_WARPS; ++w) {
-        if (sm_m[w] == -INFINITY) continue;
-        const float e = exp2f(sm_m[w] - M);
-        A = fmaf(e, sm_a[w][c], A);
-        L = fmaf(e, sm_l[w], L);
-      }
+    for (int w = 0; w < nw; ++w) {
+      A += sm_a[w][c];
+      L += sm_l[w];
     }
-    const int b = u / n_kv_heads, h = u % n_kv_heads;
     o_rot[((size_t)b * n_q_heads + h * G + j) * D + c] = L > 0.f ? A / L : 0.f;
   }
 }
@@ -815,8 +832,13 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   if (e != cudaSuccess) return e;
 
   // the combine is a programmatic dependent of the decode kernel
-  cfg.gridDim = dim3(n_seqs * g.n_kv_heads, gqa);
-  cfg.blockDim = dim3(CB_WARPS * 32);
+  // warps per (unit, head): ~8 partials each, 1 .. 32
+  const int units = n_seqs * g.n_kv_heads;
+  const int per_unit = (DEC_WARPS * n_ctas + units - 1) / units + 1;
+  int nw = 1;
+  while (nw < CB_MAX_WARPS && nw * 8 < per_unit) nw *= 2;
+  cfg.gridDim = dim3(units, gqa);
+  cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = 0;
 #define KVQ_CB(GG) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<GG>, g.n_kv_heads, n_q_heads, ws, o_rot)
   switch (gqa) {

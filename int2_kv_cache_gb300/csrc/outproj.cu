@@ -174,43 +174,45 @@ __global__ void __launch_bounds__(256) out_proj_mma_kernel(int n_rows, int d_mod
 // bf16 weights, the decode-size case: W streamed through shared memory.
 //
 // A CTA owns BM = 16 MT rows of W and a pass of up to 8 NR activation rows.
-// W (row slices of OP_BK columns) and the matching x columns are staged in a
+// W (row slices of BK columns) and the matching x columns are staged in a
 // ring of shared-memory stages by bulk copies (one row per lane, completed on
 // an mbarrier), so tens of kilobytes per SM are in flight; rows are padded by
 // 16 (W) and 32 (x) bytes so the ldmatrix reads of W and the 8-byte reads of
-// x are free of bank conflicts.  Warp w takes columns 32w .. 32w + 31 of every stage; x is
+// x are free of bank conflicts.  Warp w takes columns BK/8 w .. BK/8 (w + 1) - 1 of every stage; x is
 // split into bf16 high and remainder parts (two products into one fp32
 // accumulator); the eight warps are summed in a fixed order at the end.
-constexpr int OP_BK = 256;
 constexpr int OP_MAX_STAGES = 4;
 constexpr int OP_SMEM_TARGET = 110 * 1024;  // two CTAs per SM
 
-__host__ __device__ constexpr int op_stage_bytes(int mt, int nr) {
-  return 16 * mt * (OP_BK * 2 + 16) + 8 * nr * (OP_BK * 4 + 32);
+__host__ __device__ constexpr int op_stage_bytes(int mt, int nr, int bk) {
+  return 16 * mt * (bk * 2 + 16) + 8 * nr * (bk * 4 + 32);
 }
-__host__ __device__ constexpr int op_stages(int mt, int nr) {
-  return OP_SMEM_TARGET / op_stage_bytes(mt, nr) > OP_MAX_STAGES ? OP_MAX_STAGES
-         : OP_SMEM_TARGET / op_stage_bytes(mt, nr) < 2          ? 2
-                                                                  : OP_SMEM_TARGET / op_stage_bytes(mt, nr);
+__host__ __device__ constexpr int op_stages(int mt, int nr, int bk) {
+  return OP_SMEM_TARGET / op_stage_bytes(mt, nr, bk) > OP_MAX_STAGES ? OP_MAX_STAGES
+         : OP_SMEM_TARGET / op_stage_bytes(mt, nr, bk) < 2          ? 2
+                                                                      : OP_SMEM_TARGET / op_stage_bytes(mt, nr, bk);
 }
 
-template <int MT, int NR>
+// BK = 256 for up to 32 activation rows, 128 for 64 (so two CTAs still fit an SM).
+template <int MT, int NR, int BK>
 __global__ void __launch_bounds__(256) out_proj_stream_kernel(int n_rows, int d_model, int k_dim,
                                                               const float* __restrict__ x,
                                                               const __nv_bfloat16* __restrict__ w,
                                                               float* __restrict__ y, unsigned* err) {
   constexpr int BM = 16 * MT, XR = 8 * NR;
-  constexpr int WROW = OP_BK * 2 + 16;  // bytes per staged W row
-  constexpr int XROW = OP_BK * 4 + 32;  // bytes per staged x row
-  constexpr int STAGE = op_stage_bytes(MT, NR);
-  constexpr int S = op_stages(MT, NR);
+  constexpr int KS = BK / 128;        // 16-wide k-steps per warp per stage
+  constexpr int WROW = BK * 2 + 16;   // bytes per staged W row
+  constexpr int XROW = BK * 4 + 32;   // bytes per staged x row
+  constexpr int STAGE = op_stage_bytes(MT, NR, BK);
+  constexpr int S = op_stages(MT, NR, BK);
+  static_assert(BM <= 32 && XR <= 64, "row-to-thread mapping of the copies");
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full[OP_MAX_STAGES];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gi = lane >> 2, ti = lane & 3;
   const int n0 = blockIdx.x * BM;
   const int w_rows = min(BM, d_model - n0);
-  const int n_k = (k_dim + OP_BK - 1) / OP_BK;
+  const int n_k = (k_dim + BK - 1) / BK;
 
   // One arrival per row copy: every copying thread arms the barrier with its own
   // bytes, so the copies need no ordering among threads.
@@ -223,18 +225,18 @@ __global__ void __launch_bounds__(256) out_proj_stream_kernel(int n_rows, int d_
   // CTAs start at different column blocks, so at any moment they read different
   // slices of x (all of them share x).
   const int kc0 = blockIdx.x % n_k;
-  // The row this thread stages: W row `lane / 4 * 8 + warp` for lanes 0..3 of
-  // each warp (BM <= 32), x row `(lane - 4) * 8 + warp` for lanes 4..7 (<= 32
-  // rows), so the copies of a stage are spread over all eight warps.
+  // The row this thread stages: W row `lane * 8 + warp` for lanes 0..3 of each
+  // warp (BM <= 32), x row `(lane - 4) * 8 + warp` for lanes 4..11 (<= 64 rows),
+  // so the copies of a stage are spread over all eight warps.
   const int my_wr = lane < 4 ? lane * 8 + warp : -1;
-  const int my_xr = (lane >= 4 && lane < 8) ? (lane - 4) * 8 + warp : -1;
+  const int my_xr = (lane >= 4 && lane < 12) ? (lane - 4) * 8 + warp : -1;
   const bool copies_w = my_wr >= 0 && my_wr < w_rows;
   const bool copies_x = my_xr >= 0 && my_xr < n_rows;
   auto issue = [&](int kc) {
     if (!copies_w && !copies_x) return;
     const int st = kc % S;
-    const int k0 = ((kc + kc0) % n_k) * OP_BK;
-    const int kw = min(OP_BK, k_dim - k0);
+    const int k0 = ((kc + kc0) % n_k) * BK;
+    const int kw = min(BK, k_dim - k0);
     uint8_t* dst = smem + st * STAGE;
     fence_proxy_async();
     if (copies_w) {
@@ -264,13 +266,13 @@ __global__ void __launch_bounds__(256) out_proj_stream_kernel(int n_rows, int d_
       for (int k2 = kc; k2 < n_k && k2 < kc + S; ++k2) mbar_wait_bounded(&full[k2 % S], (k2 / S) & 1);
       return;
     }
-    const int kw = min(OP_BK, k_dim - ((kc + kc0) % n_k) * OP_BK);
-    if (32 * warp < kw) {
+    const int kw = min(BK, k_dim - ((kc + kc0) % n_k) * BK);
+    if (BK / 8 * warp < kw) {
       const uint8_t* sb = smem + st * STAGE;
       const uint32_t sa = smem_u32(sb) + a_off;
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {
-        const int kb = 32 * warp + 16 * ks;
+      for (int ks = 0; ks < KS; ++ks) {
+        const int kb = BK / 8 * warp + 16 * ks;
         uint32_t a[MT][4];
 #pragma unroll
         for (int mt = 0; mt < MT; ++mt) ldsm_x4(sa + 16 * mt * WROW + kb * 2, a[mt]);
@@ -317,20 +319,21 @@ __global__ void __launch_bounds__(256) out_proj_stream_kernel(int n_rows, int d_
   }
 }
 
-template <int MT, int NR>
+template <int MT, int NR, int BK>
 cudaError_t launch_out_proj_stream(int nr, int d_model, int k_dim, const float* x, const void* w, float* y,
                                    unsigned* err, cudaStream_t s) {
-  constexpr int smem = op_stages(MT, NR) * op_stage_bytes(MT, NR);
-  static bool attr_set = false;
+  constexpr int smem = op_stages(MT, NR, BK) * op_stage_bytes(MT, NR, BK);
+  static_assert(smem >= 8 * 16 * MT * (8 * NR + 1) * 4, "the final reduction reuses the stages");
+  static bool attr_set = false;  // one flag per kernel instance
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(out_proj_stream_kernel<MT, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(out_proj_stream_kernel<MT, NR, BK>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
   const int grid = (d_model + 16 * MT - 1) / (16 * MT);
-  out_proj_stream_kernel<MT, NR><<<grid, 256, smem, s>>>(nr, d_model, k_dim, x,
-                                                          static_cast<const __nv_bfloat16*>(w), y, err);
+  out_proj_stream_kernel<MT, NR, BK><<<grid, 256, smem, s>>>(nr, d_model, k_dim, x,
+                                                              static_cast<const __nv_bfloat16*>(w), y, err);
   return cudaGetLastError();
 }
 
@@ -338,20 +341,23 @@ cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, 
                             int w_dtype, float* y, unsigned* err, cudaStream_t s) {
   if (n_rows == 0 || d_model == 0) return cudaSuccess;
   const dim3 grid((d_model + 31) / 32);
-  for (int r0 = 0; r0 < n_rows; r0 += 32) {
-    const int nr = n_rows - r0 < 32 ? n_rows - r0 : 32;
+  const int pass_rows = 32;  // one pass per 32 activation rows (a 64-row pass measured slower)
+  for (int r0 = 0; r0 < n_rows; r0 += pass_rows) {
+    const int nr = n_rows - r0 < pass_rows ? n_rows - r0 : pass_rows;
     const float* xr = x + (size_t)r0 * k_dim;
     float* yr = y + (size_t)r0 * d_model;
     if (w_dtype == KVQ_BF16) {
       // 32-row W blocks when they alone give ~a CTA per SM, else 16-row blocks
       const bool wide = (d_model + 31) / 32 >= 100;
       cudaError_t e;
-      if (nr <= 8) e = wide ? launch_out_proj_stream<2, 1>(nr, d_model, k_dim, xr, w, yr, err, s)
-                            : launch_out_proj_stream<1, 1>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else if (nr <= 16) e = wide ? launch_out_proj_stream<2, 2>(nr, d_model, k_dim, xr, w, yr, err, s)
-                                  : launch_out_proj_stream<1, 2>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else e = wide ? launch_out_proj_stream<2, 4>(nr, d_model, k_dim, xr, w, yr, err, s)
-                    : launch_out_proj_stream<1, 4>(nr, d_model, k_dim, xr, w, yr, err, s);
+      if (nr <= 8) e = wide ? launch_out_proj_stream<2, 1, 256>(nr, d_model, k_dim, xr, w, yr, err, s)
+                            : launch_out_proj_stream<1, 1, 256>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else if (nr <= 16) e = wide ? launch_out_proj_stream<2, 2, 256>(nr, d_model, k_dim, xr, w, yr, err, s)
+                                  : launch_out_proj_stream<1, 2, 256>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else if (nr <= 32) e = wide ? launch_out_proj_stream<2, 4, 256>(nr, d_model, k_dim, xr, w, yr, err, s)
+                                  : launch_out_proj_stream<1, 4, 256>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else e = wide ? launch_out_proj_stream<2, 8, 128>(nr, d_model, k_dim, xr, w, yr, err, s)
+                    : launch_out_proj_stream<1, 8, 128>(nr, d_model, k_dim, xr, w, yr, err, s);
       if (e != cudaSuccess) return e;
       continue;
     }
