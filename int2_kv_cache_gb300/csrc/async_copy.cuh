@@ -65,4 +65,13 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                : "memory");
 }
 
+// Programmatic dependent launch: a grid launched with the programmatic
+// stream-serialization attribute may start before the preceding kernel has
+// finished; pdl_wait() blocks until that kernel has completed and its memory is
+// visible, pdl_launch_dependents() lets the next such grid start.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace kvq

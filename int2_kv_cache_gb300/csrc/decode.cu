@@ -174,11 +174,6 @@ __host__ __device__ constexpr int v_pe(int f) { return f == 0 ? 8 : (f <= 4 ? 2 
 __host__ __device__ constexpr bool v_swapped(int f) { return f == 0 || f >= 5; }
 
 
-__device__ __forceinline__ void pdl_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
-
 // ---------------------------------------------------------------------------
 // Query preparation (Eq. 22), one CTA per (KV head h, sequence b), 256 threads:
 // q'_j = q[b][h G + j] R_K,h * log2(e)/sqrt(128) for the G query heads of the
@@ -709,7 +704,8 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
                                                                            float* __restrict__ o_rot) {
   __shared__ float sm_m[CB_MAX_WARPS], sm_l[CB_MAX_WARPS];
   __shared__ __align__(16) float sm_a[CB_MAX_WARPS][D];
-  pdl_wait();  // the partials come from decode_split_kernel
+  pdl_wait();               // the partials come from decode_split_kernel
+  pdl_launch_dependents();  // a following projection may start streaming its weights
   const int u = blockIdx.x, j = blockIdx.y;
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
