@@ -308,17 +308,22 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   __shared__ __align__(8) uint64_t bars[DEC_WARPS][DEC_STAGES];
   __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the staged entry was copied
   __shared__ int s_sum[DEC_WARPS];
-  __shared__ int s_start[DEC_WARPS][2];  // first sequence of each warp's slice, chunks before it
+  __shared__ int s_start[DEC_WARPS][3];  // first sequence of each warp's slice, entries before it, its length
 
   // list entries (64-token stages) of a sequence of `len` tokens
   auto n_chunks_of = [&](int len) { return (len <= 0 || len > max_len) ? 0 : (len + 63) >> 6; };
 
   // ---- the batch's chunk list: sequence b holds H_kv * nb_b entries, unit (b, h)
   //      the nb_b entries from H_kv * prefix_b + h * nb_b on ----
+  // the lengths are kept in the (still unused) stage memory for the second pass
+  int* s_len = reinterpret_cast<int*>(dyn_smem);
+  const bool cached = n_seqs <= DEC_WARPS * DEC_STAGES * STAGE / (int)sizeof(int);
+  auto len_of = [&](int b) { return cached ? s_len[b] : __ldg(seq_lens + b); };
   int tot = 0;
   for (int b = threadIdx.x; b < n_seqs; b += 128) {
     const int len = __ldg(seq_lens + b);
     if ((len < 0 || len > max_len) && blockIdx.x == 0) flag_error(err, ERR_SEQ_RANGE);
+    if (cached) s_len[b] = len;
     tot += n_chunks_of(len);
   }
 #pragma unroll
@@ -336,7 +341,8 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   int base = 0;
   for (int b0 = 0; b0 < n_seqs; b0 += 128) {
     const int b = b0 + threadIdx.x;
-    const int n = b < n_seqs ? n_chunks_of(__ldg(seq_lens + b)) : 0;
+    const int len = b < n_seqs ? len_of(b) : 0;
+    const int n = n_chunks_of(len);
     int inc = n;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
@@ -354,6 +360,7 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
         if (gs < T && gs >= Hkv * excl && gs < Hkv * (excl + n)) {
           s_start[w][0] = b;
           s_start[w][1] = excl;
+          s_start[w][2] = len;
         }
       }
     }
@@ -375,7 +382,7 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   ChunkWalker iw;  // issue side
   if (my_n > 0) {
     iw.b = s_start[warp][0];
-    iw.len = __ldg(seq_lens + iw.b);
+    iw.len = s_start[warp][2];
     iw.nb = n_chunks_of(iw.len);
     const int sb = Hkv * s_start[warp][1];
     iw.h = (ga - sb) / iw.nb;
@@ -747,8 +754,7 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
   if (lane == 0) sm_l[warp] = l;
   reinterpret_cast<float4*>(sm_a[warp])[lane] = a;
   __syncthreads();
-  if (threadIdx.x < D) {
-    const int c = threadIdx.x;
+  for (int c = threadIdx.x; c < D; c += blockDim.x) {  // 64 or more threads
     float A = 0.f, L = 0.f;
     for (int w = 0; w < nw; ++w) {
       A += sm_a[w][c];

@@ -204,23 +204,25 @@ __device__ __forceinline__ bool locate_warp(int t, int n_seqs, const int32_t* cu
 
 // Small appends (a decode step's one token per sequence): one CTA per (token,
 // head, role) so the double-float rotations are spread over the whole GPU.
-// Warps 0-3 each accumulate the terms of 32 input channels (rows of a dense R_h
-// read from global memory, L2-resident) while warp 4 finds the token's page
-// slot; the four double-float partial sums are added in a fixed order, and
-// warp 0 centres, quantizes and writes the group.
-// grid = (n_new, n_kv_heads, roles), block = 160.
+// Warps 0-7 each accumulate the terms of 16 input channels (rows of a dense R_h
+// read from global memory, L2-resident, all 16 loads in flight at once) while
+// warp 8 finds the token's page slot; the eight double-float partial sums are
+// added in a fixed order, and warp 0 centres, quantizes and writes the group.
+// grid = (n_new, n_kv_heads, roles), block = 288.
 constexpr int APPEND_SMALL_MAX = 128;  // tokens per call below which this path is used
 
-__global__ void __launch_bounds__(160, 4) append_small_dense_kernel(
+constexpr int APPEND_ROT_WARPS = 8;
+
+__global__ void __launch_bounds__(32 * (APPEND_ROT_WARPS + 1), 2) append_small_dense_kernel(
     PageGeom g, int n_seqs, int dtype, const int32_t* __restrict__ cu_new, const int32_t* __restrict__ start_pos,
     const int32_t* __restrict__ table, AppendRoles roles, uint8_t* __restrict__ pool, unsigned* err) {
-  __shared__ float2 part[4][D];  // (hi, lo) of each warp's partial x R
+  __shared__ float2 part[APPEND_ROT_WARPS][D];  // (hi, lo) of each warp's partial x R
   __shared__ long long s_rec;    // record index, or -1 when the token is skipped
   __shared__ int s_slot;
   const AppendRole ro = blockIdx.z ? roles.r[1] : roles.r[0];
   const int t = blockIdx.x, h = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == 4) {
+  if (warp == APPEND_ROT_WARPS) {
     long long rec;
     int slot;
     // flag each bad token once (role 0), skip it in both roles
@@ -241,16 +243,15 @@ __global__ void __launch_bounds__(160, 4) append_small_dense_kernel(
   for (int u = 0; u < 4; ++u)
 #pragma unroll
     for (int i = 0; i < 4; ++i) sh[u][i] = sl[u][i] = 0.f;
-  // the warp's 32 rows of R in two batches of 16 loads in flight
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
+  // the warp's 16 rows of R, all loads in flight at once
+  {
     float4 rr[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) rr[j] = __ldg(R4 + (size_t)(32 * warp + 16 * half + j) * 32);
+    for (int j = 0; j < 16; ++j) rr[j] = __ldg(R4 + (size_t)(16 * warp + j) * 32);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-      const int m = 8 * warp + 4 * half + (j >> 2), u = j & 3;  // row 4m + u
-      const float xh = __shfl_sync(0xffffffffu, xin[u], m);    // channel 4m + u lives in lane m
+      const int m = 4 * warp + (j >> 2), u = j & 3;          // row 4m + u
+      const float xh = __shfl_sync(0xffffffffu, xin[u], m);  // channel 4m + u lives in lane m
       const float r[4] = {rr[j].x, rr[j].y, rr[j].z, rr[j].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
@@ -277,9 +278,10 @@ __global__ void __launch_bounds__(160, 4) append_small_dense_kernel(
   DF x[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float2 p0 = part[0][4 * lane + i], p1 = part[1][4 * lane + i];
-    const float2 p2 = part[2][4 * lane + i], p3 = part[3][4 * lane + i];
-    x[i] = df_add(df_add(DF{p0.x, p0.y}, DF{p1.x, p1.y}), df_add(DF{p2.x, p2.y}, DF{p3.x, p3.y}));
+    DF q[APPEND_ROT_WARPS];
+#pragma unroll
+    for (int w = 0; w < APPEND_ROT_WARPS; ++w) q[w] = DF{part[w][4 * lane + i].x, part[w][4 * lane + i].y};
+    x[i] = df_add(df_add(df_add(q[0], q[1]), df_add(q[2], q[3])), df_add(df_add(q[4], q[5]), df_add(q[6], q[7])));
   }
   if (ro.mu_rot) {
     const float4 m = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
@@ -316,7 +318,7 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
   // keys and values may use different rotation kinds: one launch per kind
   const bool kd = rot_k.kind == KVQ_ROT_DENSE, vd = rot_v.kind == KVQ_ROT_DENSE;
   if (n_new <= APPEND_SMALL_MAX && kd && vd) {
-    append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 2), 160, 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
+    append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 2), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
                                                                              table, roles, pool, err);
     return cudaGetLastError();
   }
@@ -327,7 +329,7 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
       one.r[0] = roles.r[role];
       one.r[1] = roles.r[role];
       if (role == 0 ? kd : vd)
-        append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 1), 160, 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
+        append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 1), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
                                                                                  table, one, pool, err);
       else
         append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
