@@ -9,6 +9,7 @@
 
 #include "async_copy.cuh"
 #include "quant_common.cuh"
+#include "tcgen05.cuh"
 
 namespace kvq {
 
@@ -43,10 +44,10 @@ cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, i
   return cudaGetLastError();
 }
 
-// y[r][n] = sum_k x[r][k] w[n][k]: a weight-streaming tensor-core GEMM.
+// y[r][n] = sum_k x[r][k] w[n][k]: weight-streaming tensor-core GEMMs.  With a
+// few activation rows (decode batches) the product is bound by reading W once.
 //
-// With a few activation rows (decode batches) the product is bound by reading W
-// once, so the kernel streams W through registers and computes the transposed
+// fp32 weights: the kernel streams W through registers and computes the transposed
 // product D[n][r] = W[n][:] . x[r][:] with mma.sync m16n8k16 bf16 -> fp32:
 // * A = a 16-row slice of W (row-major, K contiguous): each thread loads 16
 //   contiguous bytes of two rows per 32-wide K chunk; the K order inside a
@@ -174,37 +175,6 @@ __global__ void __launch_bounds__(256) out_proj_mma_kernel(int n_rows, int d_mod
   }
 }
 
-// bf16 weights, the decode-size case: W streamed once through shared memory by
-// the tensor-memory-access engine.
-//
-// A CTA owns BM = 16 MT rows of W and a pass of up to 8 NR activation rows, and
-// is warp-specialised: one producer warp stages each 256-column block of W
-// (four 2-D boxes of 64 columns x BM rows) and of x (eight boxes of 32 columns x
-// 8 NR rows) into a ring of OP_STAGES shared-memory stages with tensor copies
-// (cp.async.bulk.tensor, 128-byte swizzle, out-of-range rows and columns read as
-// zeros), and 16 consumer warps each take 16 columns of every stage and release
-// it on the stage's "empty" mbarrier - no block barrier in the loop.  The
-// swizzle makes the ldmatrix reads of W and the 8-byte reads of x free of bank
-// conflicts; x is split into bf16 high and remainder parts (two products into
-// one fp32 accumulator); CTAs start at different column blocks (they all share
-// x); the consumers' partial sums are added in a fixed order at the end.
-constexpr int OP_BK = 256;
-constexpr int OP_CW = 16;                   // consumer warps
-constexpr int OP_PW = 3;                    // producer warps, 4 tensor copies each per stage
-constexpr int OP_THREADS = 32 * (OP_CW + OP_PW);
-
-__host__ __device__ constexpr int op_stage_bytes(int mt, int nr) { return OP_BK * 2 * 16 * mt + OP_BK * 4 * 8 * nr; }
-// stages in flight: as many as fit two CTAs per SM (at least 2, at most 4)
-__host__ __device__ constexpr int op_stages(int mt, int nr) {
-  return (110 * 1024) / op_stage_bytes(mt, nr) >= 4 ? 4 : ((110 * 1024) / op_stage_bytes(mt, nr) >= 2 ? (110 * 1024) / op_stage_bytes(mt, nr) : 2);
-}
-__host__ __device__ constexpr int op_smem_bytes(int mt, int nr) {
-  // stages (1,024-byte aligned for the swizzle) or the final reduction, whichever is larger
-  return 1024 + (op_stages(mt, nr) * op_stage_bytes(mt, nr) > OP_CW * 16 * mt * (8 * nr + 1) * 4
-                     ? op_stages(mt, nr) * op_stage_bytes(mt, nr)
-                     : OP_CW * 16 * mt * (8 * nr + 1) * 4);
-}
-
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
@@ -213,335 +183,314 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-template <int MT, int NR>
-__global__ void __launch_bounds__(OP_THREADS) out_proj_tma_kernel(const __grid_constant__ CUtensorMap tw,
-                                                                  const __grid_constant__ CUtensorMap tx,
-                                                                  int n_rows, int d_model, int k_dim,
-                                                                  float* __restrict__ y, unsigned* err) {
-  constexpr int BM = 16 * MT, XR = 8 * NR;
-  constexpr int WBOX = 128 * BM;          // bytes of one W box (64 bf16 columns x BM rows)
-  constexpr int XBOX = 128 * XR;          // bytes of one x box (32 fp32 columns x XR rows)
-  constexpr int STAGE = op_stage_bytes(MT, NR);
-  constexpr int S = op_stages(MT, NR);
-  constexpr int MAX_S = 4;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[MAX_S], empty[MAX_S];
-  __shared__ int s_abort;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gi = lane >> 2, ti = lane & 3;
-  const int n0 = blockIdx.x * BM;
-  const int w_rows = min(BM, d_model - n0);
-  const int n_k = (k_dim + OP_BK - 1) / OP_BK;
-  const int kc0 = blockIdx.x % n_k;  // CTAs start at different column blocks
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], OP_PW);   // one arrival (with its bytes) per producer warp
-      mbar_init(&empty[i], OP_CW);  // one arrival per consumer warp
-    }
-    s_abort = 0;
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  if (warp >= OP_CW) {
-    // ---- producers: copies q = 4 p + lane (lanes 0-3 of producer p) of the stage's
-    //      12 boxes: W boxes 0-3, then x boxes 0-7 ----
-    const int q = 4 * (warp - OP_CW) + lane;
-    if (warp != OP_CW) pdl_wait();  // x may come from the preceding kernel; W is read before it ends
-    int issued = 0;
-    for (int kc = 0; kc < n_k; ++kc) {
-      const int st = kc % S;
-      if (kc >= S) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], ((kc / S) - 1) & 1));
-        if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
-          if (!ok && lane == 0) {
-            flag_error(err, ERR_TIMEOUT);
-            *reinterpret_cast<volatile int*>(&s_abort) = 1;
-          }
-          break;
-        }
-      }
-      const int k0 = ((kc + kc0) % n_k) * OP_BK;
-      uint8_t* dst = smem + st * STAGE;
-      if (lane == 0)
-        mbar_arrive_expect_tx(&full[st], (uint32_t)(warp == OP_CW ? 4 * WBOX : 4 * XBOX));
-      __syncwarp();
-      if (lane < 4) {
-        if (q < 4) tma_load_2d(dst + q * WBOX, &tw, k0 + 64 * q, n0, &full[st]);
-        else tma_load_2d(dst + 4 * WBOX + (q - 4) * XBOX, &tx, k0 + 32 * (q - 4), 0, &full[st]);
-      }
-      issued = kc + 1;
-    }
-    // before the CTA retires, wait (bounded) for every stage this warp filled
-    for (int kc = (issued > S ? issued - S : 0); kc < issued; ++kc) mbar_wait_bounded(&full[kc % S], (kc / S) & 1);
-  }
-
-  float acc[MT][NR][4];
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < NR; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-  if (warp < OP_CW) {
-    // ---- consumers: warp c takes columns 16c .. 16c + 15 of every stage ----
-    // W: box c / 4, 16-byte chunks 2 (c % 4) + (lane >> 4) of rows 16 mt + (lane & 15)
-    const int wbox = warp >> 2;
-    const int wr = (lane & 7) + 8 * ((lane >> 3) & 1);            // row within an m-tile (rows +16 mt keep r % 8)
-    const int wch = (2 * (warp & 3) + (lane >> 4)) ^ (wr & 7);    // swizzled chunk
-    // x: box c / 2, columns 16 (c % 2) + 2t (+ 8) of rows 8 nt + g
-    const int xbox = warp >> 1;
-    const int xc0 = 16 * (warp & 1) + 2 * ti;
-    const int xch0 = (xc0 >> 2) ^ gi, xch1 = ((xc0 + 8) >> 2) ^ gi;
-    const int xoff = (xc0 & 3) * 4;
-    for (int kc = 0; kc < n_k; ++kc) {
-      const int st = kc % S;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (kc / S) & 1));
-      if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
-        if (!ok && lane == 0) {
-          flag_error(err, ERR_TIMEOUT);
-          *reinterpret_cast<volatile int*>(&s_abort) = 1;
-        }
-        break;
-      }
-      const uint8_t* sb = smem + st * STAGE;
-      uint32_t a[MT][4];
-#pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-        ldsm_x4(smem_u32(sb + wbox * WBOX + (16 * mt + wr) * 128 + wch * 16), a[mt]);
-#pragma unroll
-      for (int nt = 0; nt < NR; ++nt) {
-        const uint8_t* xr = sb + 4 * WBOX + xbox * XBOX + (8 * nt + gi) * 128;
-        const float2 p0 = *reinterpret_cast<const float2*>(xr + xch0 * 16 + xoff);
-        const float2 p1 = *reinterpret_cast<const float2*>(xr + xch1 * 16 + xoff);
-        const float h0 = bf_rn(p0.x), h1 = bf_rn(p0.y), h2 = bf_rn(p1.x), h3 = bf_rn(p1.y);
-        const uint32_t bh0 = pack_bf2(h0, h1), bh1 = pack_bf2(h2, h3);
-        const uint32_t bl0 = pack_bf2(p0.x - h0, p0.y - h1), bl1 = pack_bf2(p1.x - h2, p1.y - h3);
-#pragma unroll
-        for (int mt = 0; mt < MT; ++mt) {
-          mma_bf16(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], bh0, bh1);
-          mma_bf16(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], bl0, bl1);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
-    }
-  }
-  __syncthreads();  // every stage consumed and every copy landed: the stages become the reduction buffer
-  pdl_wait();       // y may still be read by the preceding kernel
-  if (*reinterpret_cast<volatile int*>(&s_abort)) return;
-
-  // D fragment: (row 16mt+g, cols 8nt+2t, +1) and (row 16mt+g+8, same cols)
-  float* red = reinterpret_cast<float*>(smem);  // [OP_CW][BM][XR + 1]
-  if (warp < OP_CW) {
-#pragma unroll
-    for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NR; ++nt) {
-        float* r0 = red + (warp * BM + 16 * mt + gi) * (XR + 1) + 8 * nt + 2 * ti;
-        float* r1 = r0 + 8 * (XR + 1);
-        r0[0] = acc[mt][nt][0];
-        r0[1] = acc[mt][nt][1];
-        r1[0] = acc[mt][nt][2];
-        r1[1] = acc[mt][nt][3];
-      }
-  }
-  __syncthreads();
-  for (int e = threadIdx.x; e < BM * XR; e += OP_THREADS) {
-    const int nn = e % BM, r = e / BM;
-    float v = 0.f;
-#pragma unroll
-    for (int wv = 0; wv < OP_CW; ++wv) v += red[(wv * BM + nn) * (XR + 1) + r];
-    if (nn < w_rows && r < n_rows) y[(size_t)r * d_model + n0 + nn] = v;
-  }
-}
-
-// Decode-size projection (up to 16 activation rows), split over K in a cluster:
-// a cluster of OPC_SPLIT CTAs owns 128 rows of W, CTA r the r-th quarter of the
-// columns, so each CTA reads a quarter of x for 128 rows of W.  Stages are 64
-// columns wide - one 64 x 128 tensor box of W (16 KB) and two 32-column boxes of
-// x - and OPC_STAGES deep (~160 KB in flight per SM).  Consumer warp c takes
-// k-step c % 4 (16 columns) of the stage for row tiles 2 (c / 4) and 2 (c / 4) + 1;
-// the four k-step warps of a row group are summed in shared memory, then CTA 0
-// adds the four partial outputs through distributed shared memory in rank order.
-constexpr int OPC_SPLIT = 4;
-constexpr int OPC_BM = 128;
-constexpr int OPC_BK = 64;
-constexpr int OPC_STAGES = 8;
-
-__host__ __device__ constexpr int opc_stage_bytes(int nr) { return OPC_BK * 2 * OPC_BM + OPC_BK * 4 * 8 * nr; }
-__host__ __device__ constexpr int opc_red_bytes(int nr) { return 4 * OPC_BM * (8 * nr + 1) * 4; }
-__host__ __device__ constexpr int opc_smem_bytes(int nr) {  // stages, or reduction + receive buffers
-  return 1024 + (OPC_STAGES * opc_stage_bytes(nr) > opc_red_bytes(nr) + OPC_SPLIT * OPC_BM * 8 * nr * 4
-                     ? OPC_STAGES * opc_stage_bytes(nr)
-                     : opc_red_bytes(nr) + OPC_SPLIT * OPC_BM * 8 * nr * 4);
-}
-
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Store v at the same shared-memory offset as `local` in CTA `rank` of the cluster.
-__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t rank, float v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+// bf16 weights on the fifth-generation tensor cores (tcgen05), split over K in
+// a cluster.  D[n][c] = sum_k W[n][k] B[c][k] with M = 128 rows of W per CTA
+// and N = 2 NRP columns: B holds the pass's activation rows twice, as bf16
+// high parts (columns 0 .. NRP-1) and bf16 remainders (NRP .. 2 NRP-1), so
+// y[r][n] = D[n][r] + D[n][NRP + r] keeps ~16 bits of x against bf16 W.
+// K advances in 64-column stages through three shared-memory rings sized
+// independently - W (read from memory once), x (read by every row tile, from
+// L2) and the converted B tiles:
+// * warp 0 streams the 128 x 64 boxes of W into a ring of SW stages by tensor
+//   copies (128-byte swizzle, zero fill past the edges), from the start: W does
+//   not depend on the preceding kernel;
+// * warps 4-11 fetch x (fp32) with per-thread asynchronous copies into a ring of
+//   SX stages, once the preceding kernel (which writes x) has finished, split
+//   each stage into the bf16 B tile (128-byte swizzle) in a ring of SB stages
+//   and release it to the tensor core;
+// * one thread of warp 1 issues four 128 x N x 16 MMAs per stage into tensor
+//   memory, then commits them to the W stage's and the B stage's "free" barriers;
+// * warps 4-7 read the accumulator back (warp w: lanes 32 (w % 4) ..), and the
+//   cluster's K partials meet by distributed shared memory: rank j receives
+//   rows [j rpr, (j + 1) rpr) of every CTA's tile and adds them in rank order.
+// Every wait is bounded (error flag and early exit; the cluster barriers are
+// always reached); tensor memory is freed by the warp that took it.
+constexpr int OPT_BM = 128;
+constexpr int OPT_BK = 64;
+constexpr int OPT_THREADS = 384;
+constexpr int OPT_WBYTES = OPT_BM * 128;  // one W stage: 128 rows x 64 bf16
+
+__host__ __device__ constexpr int opt_xbytes(int nrp) { return 256 * nrp; }  // x stage: NRP rows x 64 fp32
+__host__ __device__ constexpr int opt_bbytes(int nrp) { return 256 * nrp; }  // B stage: 2 NRP rows x 64 bf16
+// x and B ring depths: the x copies (from L2) and the B round trip (convert,
+// MMA, commit) each take about a microsecond, W copies from memory longer
+__host__ __device__ constexpr int opt_sx(int nrp) { return nrp <= 16 ? 8 : (nrp <= 32 ? 6 : 4); }
+__host__ __device__ constexpr int opt_sb(int nrp) { return nrp <= 16 ? 8 : (nrp <= 32 ? 6 : 4); }
+// W ring depth: four 16 KB boxes in flight per SM measured fastest (deeper rings
+// of these 128-row boxes lost up to 40% on GB300)
+__host__ __device__ constexpr int opt_sw(int) { return 4; }
+__host__ __device__ constexpr int opt_smem_bytes(int nrp) {
+  return 1024 + opt_sw(nrp) * OPT_WBYTES + opt_sx(nrp) * opt_xbytes(nrp) + opt_sb(nrp) * opt_bbytes(nrp);
 }
 
-template <int NR>
-__global__ void __launch_bounds__(OP_THREADS) out_proj_cluster_kernel(const __grid_constant__ CUtensorMap tw,
-                                                                      const __grid_constant__ CUtensorMap tx,
-                                                                      int n_rows, int d_model, int k_dim,
-                                                                      float* __restrict__ y, unsigned* err) {
-  constexpr int XR = 8 * NR;
-  constexpr int WBOX = 128 * OPC_BM;  // 64 bf16 columns x 128 rows
-  constexpr int XBOX = 128 * XR;      // 32 fp32 columns x XR rows
-  constexpr int STAGE = opc_stage_bytes(NR);
-  constexpr int S = OPC_STAGES;
+// x -> (hi, lo) bf16 pairs of two values: hi = bf16(x) rounded to nearest even,
+// lo = bf16(x - hi); hi + lo keeps ~16 significant bits of x.
+__device__ __forceinline__ void split_bf2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_bf2(a, b);
+  lo = pack_bf2(a - __uint_as_float(hi << 16), b - __uint_as_float(hi & 0xffff0000u));
+}
+
+// 16-byte global -> shared copy through L2 (cp.async, completion by commit groups).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Shared-memory address of `local_base` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* local_base, uint32_t rank) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local_base)), "r"(rank));
+  return remote;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
+template <int NRP>
+__global__ void __launch_bounds__(OPT_THREADS, 1) out_proj_tc_kernel(const __grid_constant__ CUtensorMap tw,
+                                                                     const float* __restrict__ x, int n_rows,
+                                                                     int d_model, int k_dim, float* __restrict__ y,
+                                                                     unsigned* err) {
+  constexpr int N = 2 * NRP;
+  constexpr int SW = opt_sw(NRP), SX = opt_sx(NRP), SB = opt_sb(NRP);
+  constexpr int XS = opt_xbytes(NRP), BS = opt_bbytes(NRP);
+  constexpr uint32_t TCOLS = N < 32 ? 32 : N;
+  constexpr uint32_t IDESC = idesc_bf16_f32(OPT_BM, N);
+  constexpr unsigned FULLM = 0xffffffffu;
+  static_assert(N >= 16 && N <= 256 && N % 16 == 0, "tcgen05 M=128 tile needs 16 <= N <= 256, N % 16 == 0");
+  static_assert(XS % 1024 == 0 && BS % 1024 == 0, "ring stages stay 1,024-byte aligned (128-byte swizzle)");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  __shared__ __align__(8) uint64_t full[S], empty[S];
+  uint8_t* wring = smem;
+  uint8_t* xring = smem + SW * OPT_WBYTES;
+  uint8_t* bring = xring + SX * XS;
+  __shared__ __align__(8) uint64_t wfull[SW], wfree[SW], bfull[SB], bfree[SB];
+  __shared__ __align__(8) uint64_t adone;  // one phase: every MMA of the CTA has completed
+  __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gi = lane >> 2, ti = lane & 3;
-  uint32_t rank;
+  uint32_t rank, split;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(rank));
-  const int n0 = blockIdx.x * OPC_BM;
-  const int w_rows = min(OPC_BM, d_model - n0);
-  const int n_k_all = (k_dim + OPC_BK - 1) / OPC_BK;
-  const int per = (n_k_all + OPC_SPLIT - 1) / OPC_SPLIT;
-  const int kc_begin = min(n_k_all, (int)rank * per);
-  const int n_k = min(n_k_all, kc_begin + per) - kc_begin;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(split));
+  const int n0 = blockIdx.x * OPT_BM;
+  const int n_kb = (k_dim + OPT_BK - 1) / OPT_BK;
+  const int kb0 = (int)((long long)n_kb * rank / split);
+  const int n_k = (int)((long long)n_kb * (rank + 1) / split) - kb0;  // >= 1: split <= n_kb
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], OP_CW);
+    for (int i = 0; i < SW; ++i) {
+      mbar_init(&wfull[i], 1);  // the W producer's arrival (with the box's bytes)
+      mbar_init(&wfree[i], 1);  // the MMA commit
     }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&bfull[i], OPT_THREADS / 32 - 4);  // one arrival per converter warp
+      mbar_init(&bfree[i], 1);  // the MMA commit
+    }
+    mbar_init(&adone, 1);
     s_abort = 0;
     fence_mbar_init();
   }
+  if (warp == 1) {
+    tmem_alloc(&s_tmem, TCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  auto aborted = [&]() { return *reinterpret_cast<volatile int*>(&s_abort) != 0; };
+  auto give_up = [&]() {
+    flag_error(err, ERR_TIMEOUT);
+    *reinterpret_cast<volatile int*>(&s_abort) = 1;
+  };
+  // bounded, warp-uniform wait; false (and the CTA marked aborted) on a time-out
+  auto warp_wait = [&](uint64_t* bar, uint32_t parity) {
+    const bool ok = __all_sync(FULLM, mbar_wait_bounded(bar, parity));
+    if (!ok && lane == 0) give_up();
+    return ok && !aborted();
+  };
 
-  if (warp == OP_CW) {
-    // ---- producer: lane 0 the W box, lanes 1-2 the x boxes of a stage; the W
-    //      boxes of the first stages go out before the preceding kernel ends ----
+  if (warp == 0) {
+    // ---- W producer ----
     int issued = 0;
-    bool x_ready = false;
-    for (int kc = 0; kc < n_k; ++kc) {
-      const int st = kc % S;
-      if (kc >= S) {
-        const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&empty[st], ((kc / S) - 1) & 1));
-        if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
-          if (!ok && lane == 0) {
-            flag_error(err, ERR_TIMEOUT);
-            *reinterpret_cast<volatile int*>(&s_abort) = 1;
-          }
-          break;
-        }
-      }
-      const int k0 = (kc_begin + kc) * OPC_BK;
-      uint8_t* dst = smem + st * STAGE;
+    for (int kb = 0; kb < n_k; ++kb) {
+      const int st = kb % SW;
+      if (kb >= SW && !warp_wait(&wfree[st], ((kb / SW) - 1) & 1)) break;
       if (lane == 0) {
-        mbar_arrive_expect_tx(&full[st], (uint32_t)STAGE);
-        tma_load_2d(dst, &tw, k0, n0, &full[st]);
-      }
-      __syncwarp();  // the byte count is armed before the x copies of this stage
-      issued = kc + 1;
-      if (kc + 1 == min(n_k, S) || kc >= S) {  // the x boxes of every stage issued so far
-        if (!x_ready) {
-          pdl_wait();  // x comes from the preceding kernel
-          x_ready = true;
-        }
-        for (int k2 = (kc >= S ? kc : 0); k2 <= kc; ++k2) {
-          const int s2 = k2 % S;
-          if (lane >= 1 && lane < 3)
-            tma_load_2d(smem + s2 * STAGE + WBOX + (lane - 1) * XBOX, &tx, (kc_begin + k2) * OPC_BK + 32 * (lane - 1), 0,
-                        &full[s2]);
-        }
+        mbar_arrive_expect_tx(&wfull[st], OPT_WBYTES);
+        tma_load_2d(wring + st * OPT_WBYTES, &tw, (kb0 + kb) * OPT_BK, n0, &wfull[st]);
       }
       __syncwarp();
+      issued = kb + 1;
     }
-    if (!x_ready) pdl_wait();
-    for (int kc = (issued > S ? issued - S : 0); kc < issued; ++kc) mbar_wait_bounded(&full[kc % S], (kc / S) & 1);
+    // every copy has landed before the ring is reused or the CTA retires
+    for (int kb = (issued > SW ? issued - SW : 0); kb < issued; ++kb)
+      mbar_wait_bounded(&wfull[kb % SW], (kb / SW) & 1);
+  } else if (warp == 1) {
+    // ---- MMA issue ----
+    int last = -1;
+    for (int kb = 0; kb < n_k; ++kb) {
+      const int sw = kb % SW, sb = kb % SB;
+      if (!warp_wait(&wfull[sw], (kb / SW) & 1)) break;
+      if (!warp_wait(&bfull[sb], (kb / SB) & 1)) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint64_t ad = sw128_desc(wring + sw * OPT_WBYTES), bd = sw128_desc(bring + sb * BS);
+#pragma unroll
+        for (int kk = 0; kk < OPT_BK / 16; ++kk) tc_mma_bf16(tmem, ad + 2 * kk, bd + 2 * kk, IDESC, kb > 0 || kk > 0);
+        tc_commit(&wfree[sw]);
+        tc_commit(&bfree[sb]);
+      }
+      __syncwarp();
+      last = kb;
+    }
+    // the accumulator is complete (or the loop was abandoned) once every MMA
+    // issued has completed: no tensor-core work in flight past this point
+    if (lane == 0 && last >= 0) tc_commit(&adone);
+    __syncwarp();
+    if (last >= 0) mbar_wait_bounded(&adone, 0);
+  } else if (warp >= 4) {
+    // ---- x -> bf16 high / remainder B tile (warps 4-11) ----
+    // Thread ct owns items i = ct + 256 t (row i / 8, columns 8 (i % 8) .. + 7 of
+    // the stage): it copies their x into its own slots of the x ring with
+    // cp.async (SX - 1 stages ahead) and converts them, so x needs no barrier.
+    constexpr int CT = OPT_THREADS - 128;          // converter threads
+    constexpr int IT = (NRP * 8 + CT - 1) / CT;   // items per thread and stage
+    const int ct = threadIdx.x - 128;
+    pdl_wait();  // x comes from the preceding kernel
+    auto fetch = [&](int kb) {  // stage kb's items -> x ring slot kb % SX (one commit group)
+      if (kb < n_k) {
+        uint8_t* xs = xring + (kb % SX) * XS;
+        const int k0 = (kb0 + kb) * OPT_BK;
+#pragma unroll
+        for (int t = 0; t < IT; ++t) {
+          const int i = ct + CT * t;
+          const int r = i >> 3, col = k0 + 8 * (i & 7);
+          if (i < NRP * 8 && r < n_rows && col < k_dim) {
+            const float* src = x + (size_t)r * k_dim + col;
+            cp_async16(xs + i * 32, src);
+            cp_async16(xs + i * 32 + 16, src + 4);
+          }
+        }
+      }
+      cp_async_commit();
+    };
+    for (int kb = 0; kb < SX - 1; ++kb) fetch(kb);
+    for (int kb = 0; kb < n_k; ++kb) {
+      const int sb = kb % SB;
+      fetch(kb + SX - 1);  // into the slot converted in the previous iteration
+      cp_async_wait<SX - 1>();  // this thread's copies of stage kb have landed
+      if (kb >= SB && !warp_wait(&bfree[sb], ((kb / SB) - 1) & 1)) break;
+      const uint8_t* xs = xring + (kb % SX) * XS;
+      uint8_t* bs = bring + sb * BS;
+      const int k0 = (kb0 + kb) * OPT_BK;
+      // all of the thread's x first (independent loads), then the B stores
+      float4 xa[IT], xb[IT];
+#pragma unroll
+      for (int t = 0; t < IT; ++t) {
+        const int i = ct + CT * t;
+        xa[t] = xb[t] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (i < NRP * 8 && (i >> 3) < n_rows && k0 + 8 * (i & 7) < k_dim) {
+          xa[t] = *reinterpret_cast<const float4*>(xs + i * 32);
+          xb[t] = *reinterpret_cast<const float4*>(xs + i * 32 + 16);
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < IT; ++t) {
+        const int i = ct + CT * t;
+        if (i < NRP * 8) {
+          const int r = i >> 3, j = i & 7, sw = r & 7;  // row, 16-byte chunk (8 columns) of the B row
+          uint4 hi, lo;
+          split_bf2(xa[t].x, xa[t].y, hi.x, lo.x);
+          split_bf2(xa[t].z, xa[t].w, hi.y, lo.y);
+          split_bf2(xb[t].x, xb[t].y, hi.z, lo.z);
+          split_bf2(xb[t].z, xb[t].w, hi.w, lo.w);
+          *reinterpret_cast<uint4*>(bs + r * 128 + (j ^ sw) * 16) = hi;
+          *reinterpret_cast<uint4*>(bs + (NRP + r) * 128 + (j ^ sw) * 16) = lo;
+        }
+      }
+      fence_proxy_async();  // the tensor cores read B through the async proxy
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bfull[sb]);
+    }
+    cp_async_wait<0>();  // no copy in flight when the ring is reused
   }
 
-  const int ks = warp & 3, rg = warp >> 2;  // k-step of the stage, row group (tiles 2 rg, 2 rg + 1)
-  float acc[2][NR][4];
+  // ---- epilogue: accumulator rows -> registers (warps 4-7) ----
+  const int q4 = warp & 3;
+  const int m = 32 * q4 + lane;  // row of the W tile held by this thread
+  float v[NRP];
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
+  for (int i = 0; i < NRP; ++i) v[i] = 0.f;
+  if (warp >= 4 && warp < 8) {
+    bool ok = !aborted();
+    // a separate one-phase barrier: the stage barriers' parities cannot tell how
+    // many rounds behind the tensor core is
+    if (ok) ok = mbar_wait_bounded(&adone, 0);
+    ok = __all_sync(FULLM, ok);
+    if (!ok && lane == 0 && !aborted()) give_up();
+    tc_fence_after();
+    if (ok) {
+      const uint32_t trow = tmem + ((uint32_t)(32 * q4) << 16);
 #pragma unroll
-    for (int nt = 0; nt < NR; ++nt) acc[mt][nt][0] = acc[mt][nt][1] = acc[mt][nt][2] = acc[mt][nt][3] = 0.f;
-  if (warp < OP_CW) {
-    const int wr = (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int wch = (2 * ks + (lane >> 4)) ^ (wr & 7);
-    const int xc0 = 16 * (ks & 1) + 2 * ti;  // column within x box ks / 2
-    const int xch0 = (xc0 >> 2) ^ gi, xch1 = ((xc0 + 8) >> 2) ^ gi;
-    const int xoff = (xc0 & 3) * 4;
-    for (int kc = 0; kc < n_k; ++kc) {
-      const int st = kc % S;
-      const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[st], (kc / S) & 1));
-      if (!ok || *reinterpret_cast<volatile int*>(&s_abort)) {
-        if (!ok && lane == 0) {
-          flag_error(err, ERR_TIMEOUT);
-          *reinterpret_cast<volatile int*>(&s_abort) = 1;
-        }
-        break;
+      for (int c = 0; c < NRP; c += 8) {
+        float h[8], l[8];
+        tmem_ld8(trow + c, h);
+        tmem_ld8(trow + NRP + c, l);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[c + i] = h[i] + l[i];
       }
-      const uint8_t* sb = smem + st * STAGE;
-      uint32_t a[2][4];
-#pragma unroll
-      for (int mt = 0; mt < 2; ++mt) ldsm_x4(smem_u32(sb + (16 * (2 * rg + mt) + wr) * 128 + wch * 16), a[mt]);
-#pragma unroll
-      for (int nt = 0; nt < NR; ++nt) {
-        const uint8_t* xr = sb + WBOX + (ks >> 1) * XBOX + (8 * nt + gi) * 128;
-        const float2 p0 = *reinterpret_cast<const float2*>(xr + xch0 * 16 + xoff);
-        const float2 p1 = *reinterpret_cast<const float2*>(xr + xch1 * 16 + xoff);
-        const float h0 = bf_rn(p0.x), h1 = bf_rn(p0.y), h2 = bf_rn(p1.x), h3 = bf_rn(p1.y);
-        const uint32_t bh0 = pack_bf2(h0, h1), bh1 = pack_bf2(h2, h3);
-        const uint32_t bl0 = pack_bf2(p0.x - h0, p0.y - h1), bl1 = pack_bf2(p1.x - h2, p1.y - h3);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          mma_bf16(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], bh0, bh1);
-          mma_bf16(acc[mt][nt], a[mt][0], a[mt][1], a[mt][2], a[mt][3], bl0, bl1);
-        }
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[st]);
     }
   }
-  __syncthreads();  // every stage consumed and every copy landed
-  pdl_wait();       // y may still be read by the preceding kernel
-  const bool aborted = *reinterpret_cast<volatile int*>(&s_abort) != 0;
-  float* red = reinterpret_cast<float*>(smem);                       // [4 k-steps][128][XR + 1]
-  float* recv = reinterpret_cast<float*>(smem + opc_red_bytes(NR));  // [OPC_SPLIT][XR][128] (CTA 0)
-  if (warp < OP_CW) {
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < NR; ++nt) {
-        float* r0 = red + (ks * OPC_BM + 16 * (2 * rg + mt) + gi) * (XR + 1) + 8 * nt + 2 * ti;
-        float* r1 = r0 + 8 * (XR + 1);
-        r0[0] = acc[mt][nt][0];
-        r0[1] = acc[mt][nt][1];
-        r1[0] = acc[mt][nt][2];
-        r1[1] = acc[mt][nt][3];
-      }
-  }
+  tc_fence_before();
   __syncthreads();
-  // every CTA stores its partial into slot `rank` of CTA 0's receive buffer
-  for (int e = threadIdx.x; e < OPC_BM * XR; e += OP_THREADS) {
-    const int nn = e % OPC_BM, r = e / OPC_BM;
-    const float v = ((red[(0 * OPC_BM + nn) * (XR + 1) + r] + red[(1 * OPC_BM + nn) * (XR + 1) + r]) +
-                     red[(2 * OPC_BM + nn) * (XR + 1) + r]) + red[(3 * OPC_BM + nn) * (XR + 1) + r];
-    st_cluster_f32(recv + rank * OPC_BM * XR + e, 0, v);
-  }
-  cluster_sync_all();  // release / acquire: every partial has landed in CTA 0
-  if (rank == 0 && !aborted) {
-    for (int e = threadIdx.x; e < OPC_BM * XR; e += OP_THREADS) {
-      const int nn = e % OPC_BM, r = e / OPC_BM;
-      float v = recv[e];
+  cluster_sync_all();  // every CTA of the cluster is past its rings
+  // rank j receives rows [j rpr, (j + 1) rpr): recv[src rank][row - j rpr][r], rows NRP + 4 floats apart
+  constexpr int RS = NRP + 4;
+  const int rpr = (OPT_BM + (int)split - 1) / (int)split;
+  float* recv = reinterpret_cast<float*>(smem);
+  if (warp >= 4 && warp < 8) {
+    const int dst = m / rpr, mm = m - dst * rpr;
+    const uint32_t base = cluster_addr(recv, (uint32_t)dst) + (uint32_t)(((rank * rpr + mm) * RS) * 4);
 #pragma unroll
-      for (int q = 1; q < OPC_SPLIT; ++q) v += recv[q * OPC_BM * XR + e];
-      if (nn < w_rows && r < n_rows) y[(size_t)r * d_model + n0 + nn] = v;
+    for (int r = 0; r < NRP; r += 4) st_cluster_v4(base + (uint32_t)(r * 4), v[r], v[r + 1], v[r + 2], v[r + 3]);
+  }
+  cluster_sync_all();  // release / acquire: every partial has landed
+  pdl_wait();          // y may still be read by the preceding kernel
+  if (!aborted()) {
+    // thread: one row mm of this rank's slice and 4 activation rows per item
+    // (16-byte shared-memory reads, warp-coalesced stores of y)
+    const int j0 = (int)rank * rpr;
+    int rows = OPT_BM - j0 < rpr ? OPT_BM - j0 : rpr;
+    if (d_model - n0 - j0 < rows) rows = d_model - n0 - j0;
+    const int groups = (n_rows + 3) >> 2;
+    for (int e = threadIdx.x; e < rows * groups; e += OPT_THREADS) {
+      const int g = e / rows, mm = e - g * rows;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (uint32_t src = 0; src < split; ++src) {
+        const float4 t = *reinterpret_cast<const float4*>(recv + (src * rpr + mm) * RS + 4 * g);
+        acc.x += t.x;
+        acc.y += t.y;
+        acc.z += t.z;
+        acc.w += t.w;
+      }
+      float* yc = y + (size_t)(4 * g) * d_model + n0 + j0 + mm;
+      const float a4[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * g + i < n_rows) yc[(size_t)i * d_model] = a4[i];
     }
+  }
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TCOLS);
   }
 }
 
@@ -575,66 +524,52 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, 
          CUDA_SUCCESS;
 }
 
-template <int NR>
-cudaError_t launch_out_proj_cluster(int nr, int d_model, int k_dim, const float* x, const void* w, float* y,
-                                    unsigned* err, cudaStream_t s) {
-  constexpr int smem = opc_smem_bytes(NR);
+static int sm_count() {
+  static int n = 0;
+  if (n == 0) {
+    int dev = 0, c = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+      n = c;
+    if (n <= 0) n = 152;
+  }
+  return n;
+}
+
+template <int NRP>
+cudaError_t launch_out_proj_tc(int nr, int d_model, int k_dim, const float* x, const void* w, float* y, unsigned* err,
+                               cudaStream_t s) {
+  constexpr int smem = opt_smem_bytes(NRP);
   static bool attr_set = false;  // one flag per kernel instance
   if (!attr_set) {
     const cudaError_t e =
-        cudaFuncSetAttribute(out_proj_cluster_kernel<NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+        cudaFuncSetAttribute(out_proj_tc_kernel<NRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  CUtensorMap tw, tx;
-  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, 64, OPC_BM) ||
-      !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, nr, k_dim, 32, 8 * NR))
-    return cudaErrorNotSupported;
+  CUtensorMap tw;
+  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, OPT_BK, OPT_BM)) return cudaErrorNotSupported;
+  // K split (the cluster size): about one CTA per SM, at most 8, at most one per K stage
+  const int n_mt = (d_model + OPT_BM - 1) / OPT_BM;
+  const int n_kb = (k_dim + OPT_BK - 1) / OPT_BK;
+  int split = sm_count() / n_mt;
+  if (split > 8) split = 8;
+  if (split > n_kb) split = n_kb;
+  if (split < 1) split = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((d_model + OPC_BM - 1) / OPC_BM, OPC_SPLIT);
-  cfg.blockDim = dim3(OP_THREADS);
+  cfg.gridDim = dim3(n_mt, split);
+  cfg.blockDim = dim3(OPT_THREADS);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = OPC_SPLIT;
+  attr[0].val.clusterDim.y = split;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, out_proj_cluster_kernel<NR>, tw, tx, nr, d_model, k_dim, y, err);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
-}
-
-template <int MT, int NR>
-cudaError_t launch_out_proj_tma(int nr, int d_model, int k_dim, const float* x, const void* w, float* y,
-                                unsigned* err, cudaStream_t s) {
-  constexpr int smem = op_smem_bytes(MT, NR);
-  static bool attr_set = false;  // one flag per kernel instance
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(out_proj_tma_kernel<MT, NR>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  CUtensorMap tw, tx;
-  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, 64, 16 * MT) ||
-      !encode_2d(&tx, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, x, nr, k_dim, 32, 8 * NR))
-    return cudaErrorNotSupported;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((d_model + 16 * MT - 1) / (16 * MT));
-  cfg.blockDim = dim3(OP_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, out_proj_tma_kernel<MT, NR>, tw, tx, nr, d_model, k_dim, y, err);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, out_proj_tc_kernel<NRP>, tw, x, nr, d_model, k_dim, y, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
@@ -642,35 +577,29 @@ cudaError_t launch_out_proj_tma(int nr, int d_model, int k_dim, const float* x, 
 cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
                             int w_dtype, float* y, unsigned* err, cudaStream_t s) {
   if (n_rows == 0 || d_model == 0) return cudaSuccess;
+  if (w_dtype == KVQ_BF16) {
+    // tensor-core passes of up to 64 activation rows
+    for (int r0 = 0; r0 < n_rows; r0 += 64) {
+      const int nr = n_rows - r0 < 64 ? n_rows - r0 : 64;
+      const float* xr = x + (size_t)r0 * k_dim;
+      float* yr = y + (size_t)r0 * d_model;
+      cudaError_t e;
+      if (nr <= 8) e = launch_out_proj_tc<8>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else if (nr <= 16) e = launch_out_proj_tc<16>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else if (nr <= 32) e = launch_out_proj_tc<32>(nr, d_model, k_dim, xr, w, yr, err, s);
+      else e = launch_out_proj_tc<64>(nr, d_model, k_dim, xr, w, yr, err, s);
+      if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+  }
   const dim3 grid((d_model + 31) / 32);
-  const int pass_rows = 32;  // one pass per 32 activation rows (a 64-row pass measured slower)
-  for (int r0 = 0; r0 < n_rows; r0 += pass_rows) {
-    const int nr = n_rows - r0 < pass_rows ? n_rows - r0 : pass_rows;
+  for (int r0 = 0; r0 < n_rows; r0 += 32) {
+    const int nr = n_rows - r0 < 32 ? n_rows - r0 : 32;
     const float* xr = x + (size_t)r0 * k_dim;
     float* yr = y + (size_t)r0 * d_model;
-    if (w_dtype == KVQ_BF16) {
-      // 32-row W blocks when they alone give ~a CTA per SM, else 16-row blocks
-      const bool wide = (d_model + 31) / 32 >= 100;
-      cudaError_t e;
-      if (nr <= 16 && (d_model + OPC_BM - 1) / OPC_BM * OPC_SPLIT >= 100)
-        e = nr <= 8 ? launch_out_proj_cluster<1>(nr, d_model, k_dim, xr, w, yr, err, s)
-                    : launch_out_proj_cluster<2>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else if (nr <= 8) e = wide ? launch_out_proj_tma<2, 1>(nr, d_model, k_dim, xr, w, yr, err, s)
-                            : launch_out_proj_tma<1, 1>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else if (nr <= 16) e = wide ? launch_out_proj_tma<2, 2>(nr, d_model, k_dim, xr, w, yr, err, s)
-                                  : launch_out_proj_tma<1, 2>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else e = wide ? launch_out_proj_tma<2, 4>(nr, d_model, k_dim, xr, w, yr, err, s)
-                    : launch_out_proj_tma<1, 4>(nr, d_model, k_dim, xr, w, yr, err, s);
-      if (e != cudaSuccess) return e;
-      continue;
-    }
-#define KVQ_OP(NRR)                                                                                  \
-  if (w_dtype == KVQ_F32) out_proj_mma_kernel<KVQ_F32, NRR><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr); \
-  else out_proj_mma_kernel<KVQ_BF16, NRR><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr)
-    if (nr <= 8) { KVQ_OP(1); }
-    else if (nr <= 16) { KVQ_OP(2); }
-    else { KVQ_OP(4); }
-#undef KVQ_OP
+    if (nr <= 8) out_proj_mma_kernel<KVQ_F32, 1><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr);
+    else if (nr <= 16) out_proj_mma_kernel<KVQ_F32, 2><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr);
+    else out_proj_mma_kernel<KVQ_F32, 4><<<grid, 256, 0, s>>>(nr, d_model, k_dim, xr, w, yr);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

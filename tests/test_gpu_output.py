@@ -32,7 +32,7 @@ def test_fold_wo(rot, wdt, odt):
 @pytest.mark.parametrize("rows,dm,hq,wdt", [(1, 128, 1, "f32"), (16, 4096, 32, "bf16"), (5, 200, 3, "bf16"),
                                             (64, 640, 10, "f32"), (48, 520, 5, "bf16"), (64, 5120, 40, "bf16"),
                                             (100, 256, 2, "bf16"), (27, 3300, 3, "bf16"),
-                                            # split over K in CTA clusters (<= 16 rows, >= 25 blocks of 128 rows):
+                                            # cluster sizes (K split) 5 and 8, one and two 8-row groups:
                                             (8, 3328, 8, "bf16"), (11, 3300, 8, "bf16"), (9, 3300, 3, "bf16")])
 def test_out_proj(rows, dm, hq, wdt):
     import oracle
