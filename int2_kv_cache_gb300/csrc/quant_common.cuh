@@ -295,6 +295,95 @@ __device__ __forceinline__ float4 rotate_vec_warp(float4 v, const RotDev& rot, i
   return v;
 }
 
+// ---------------------------------------------------------------------------
+// Certified fp32 path.  The group is first decided from fp32 values d_i that
+// are known to lie within E of the exact x_i (E from an a-priori bound on the
+// fp32 rotation and subtraction errors).  A decision (the fp16 rounding of
+// scale or zero, a code) is taken only if no value in [d - E, d + E] could
+// change it; it then equals the decision on the exact x, which is what the
+// double-float path computes too.  Otherwise the caller falls back to the
+// double-float path for the whole group.  Ties always fall back.
+// ---------------------------------------------------------------------------
+
+// Powers of two for the error bounds (exact multiplies).
+constexpr float P2_M19 = 1.9073486328125e-06f;  // 2^-19
+constexpr float P2_M22 = 2.384185791015625e-07f;  // 2^-22 = 4 u
+
+// fp16 rounding of the exact value v* with |v* - v| <= err: true and h =
+// fp16_rn(v*) when every value in that interval rounds alike (finite).
+__device__ __forceinline__ bool half_rn_certain(float v, float err, __half& h) {
+  err = __fmaf_rn(fabsf(v), P2_M22, err);  // covers the rounding of v - err and v + err
+  const __half a = __float2half_rn(__fsub_rn(v, err)), b = __float2half_rn(__fadd_rn(v, err));
+  h = a;
+  return __half_as_ushort(a) == __half_as_ushort(b) && (__half_as_ushort(a) & 0x7c00u) != 0x7c00u;
+}
+
+// x R_head in fp32 for the identity and signed-Hadamard kinds (lane l holds
+// channels 4l..4l+3; the input values are exact floats and the signs +-1).
+// Returns B with |y_i - (x R)_i| <= B for every channel of the warp.
+__device__ __forceinline__ float rotate_f32_bounded(float y[4], const RotDev& rot, int head, int lane) {
+  if (rot.kind != KVQ_ROT_SIGNED_HADAMARD) return 0.f;  // identity: exact
+  const float4 s = __ldg(reinterpret_cast<const float4*>(rot.signs + (size_t)head * D) + lane);
+  y[0] *= s.x; y[1] *= s.y; y[2] *= s.z; y[3] *= s.w;
+  // every butterfly stage adds at most u * sum|x| to each output (the nodes an
+  // output depends on at one stage partition the inputs); 7 stages, then the
+  // scaling by fp32(1/sqrt(128)) (relative error < 0.2 u) and its rounding
+  const float l1 = warp_sum(fabsf(y[0]) + fabsf(y[1]) + fabsf(y[2]) + fabsf(y[3]));
+  float a0 = y[0] + y[1], a1 = y[0] - y[1], a2 = y[2] + y[3], a3 = y[2] - y[3];
+  y[0] = a0 + a2; y[2] = a0 - a2; y[1] = a1 + a3; y[3] = a1 - a3;
+#pragma unroll
+  for (int m = 1; m < 32; m <<= 1) {
+    const float sg = (lane & m) ? -1.f : 1.f;  // upper half: p - y, lower half: y + p
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float p = __shfl_xor_sync(0xffffffffu, y[i], m);
+      y[i] = __fmaf_rn(sg, y[i], p);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) y[i] = __fmul_rn(y[i], INV_SQRT_D);
+  // 8.2 u * l1 / sqrt(128) + u |y|, with |y| <= l1 / sqrt(128), and a factor 2 of margin
+  return l1 * INV_SQRT_D * P2_M19;
+}
+
+// Group decision from d (|d_i - x_i| <= E for every channel of the warp).
+// Returns false (warp-uniform) when some decision is not certain.
+__device__ __forceinline__ bool quantize_warp_certain(const float d[4], float E, float clip, QParams& p,
+                                                      unsigned& byte) {
+  const float mn = warp_min(fminf(fminf(d[0], d[1]), fminf(d[2], d[3])));
+  const float mx = warp_max(fmaxf(fmaxf(d[0], d[1]), fmaxf(d[2], d[3])));
+  // exact min / max lie within E of mn / mx
+  const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
+  const float elo = __fmaf_rn(clip, E, fabsf(lo) * P2_M22);
+  const float ehi = __fmaf_rn(clip, E, fabsf(hi) * P2_M22);
+  const float range = __fsub_rn(hi, lo);
+  const float third = __fdiv_rn(range, 3.0f);
+  const float eth = (elo + ehi + fabsf(range) * P2_M22) * 0.3334f + fabsf(third) * P2_M22;
+  __half s16, z16;
+  bool ok = half_rn_certain(third, eth, s16);
+  ok = half_rn_certain(lo, elo, z16) && ok;
+  p.s_bits = __half_as_ushort(s16);
+  p.z_bits = __half_as_ushort(z16);
+  p.s = __half2float(s16);
+  p.z = __half2float(z16);
+  p.t05 = 0.5f * p.s;
+  p.t15 = 1.5f * p.s;
+  p.t25 = 2.5f * p.s;
+  byte = 0u;
+  if (p.s > 0.f) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float dz = __fsub_rn(d[i], p.z);
+      const float eb = __fmaf_rn(fabsf(d[i]) + fabsf(dz), P2_M22, E);
+      ok = ok && fabsf(__fsub_rn(dz, p.t05)) > eb && fabsf(__fsub_rn(dz, p.t15)) > eb &&
+           fabsf(__fsub_rn(dz, p.t25)) > eb;
+      const unsigned c = (dz > p.t05 ? 1u : 0u) + (dz > p.t15 ? 1u : 0u) + (dz > p.t25 ? 1u : 0u);
+      byte |= c << (2 * i);
+    }
+  }
+  return __all_sync(0xffffffffu, ok);
+}
+
 // Quantize one warp-held group (4 double-float channels per lane): returns this
 // lane's packed byte (channels 4l..4l+3) and the group's fp16 meta.
 __device__ __forceinline__ unsigned quantize_warp_df(const DF x[4], float clip, QParams& qp) {

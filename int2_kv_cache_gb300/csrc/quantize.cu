@@ -142,31 +142,331 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int t0 = blockIdx.x * APPEND_TOK;
   const int t1 = min(n_new, t0 + APPEND_TOK);
+  // the tile's tokens are located once, one thread each (record index of head
+  // 0 of the token's page, or -1 to skip; slot in the page)
+  __shared__ long long s_rec[APPEND_TOK];
+  __shared__ int s_slot[APPEND_TOK];
+  if (threadIdx.x < APPEND_TOK) {
+    const int t = t0 + threadIdx.x;
+    long long rec = -1;
+    int slot = 0;
+    if (t < t1 && !locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, 0)) rec = -1;
+    s_rec[threadIdx.x] = rec;
+    s_slot[threadIdx.x] = slot;
+  }
   if (DENSE) {
     const float4* src = reinterpret_cast<const float4*>(ro.rot.dense + (size_t)h * D * D);
     for (int i = threadIdx.x; i < D * D / 4; i += 256) s_r4[i] = __ldg(src + i);
-    __syncthreads();
   }
+  __syncthreads();
   for (int t = t0 + warp; t < t1; t += 8) {
-    long long rec;
-    int slot;
-    if (!locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, h)) continue;
+    if (s_rec[t - t0] < 0) continue;
+    const long long rec = s_rec[t - t0] + h;
+    const int slot = s_slot[t - t0];
     const float4 v = load4(ro.src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
-    DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
-    if (DENSE) dense_rotate_df_smem(x, s_r4, lane);
-    else rotate_df_warp(x, ro.rot, h, lane);
-    if (ro.mu_rot) {
-      const float4 m = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
-      x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
-      x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
-    }
+    float4 m = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ro.mu_rot) m = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
     QParams qp;
-    const unsigned byte = quantize_warp_df(x, ro.clip, qp);
+    unsigned byte = 0u;
+    bool done = false;
+    if (!DENSE) {
+      // certified fp32 decision (identity and signed Hadamard); a group with an
+      // uncertain decision is redone below in double-float
+      float y[4] = {v.x, v.y, v.z, v.w};
+      float E = rotate_f32_bounded(y, ro.rot, h, lane);
+      if (ro.mu_rot) {
+        y[0] = __fsub_rn(y[0], m.x); y[1] = __fsub_rn(y[1], m.y);
+        y[2] = __fsub_rn(y[2], m.z); y[3] = __fsub_rn(y[3], m.w);
+        // the subtraction's rounding: u (|y| + |mu|), y bounded through E's l1 norm or |x|
+        E += (warp_max(fmaxf(fmaxf(fabsf(v.x) + fabsf(m.x), fabsf(v.y) + fabsf(m.y)),
+                             fmaxf(fabsf(v.z) + fabsf(m.z), fabsf(v.w) + fabsf(m.w)))) +
+              E * 524288.f) * P2_M22;
+      }
+      done = quantize_warp_certain(y, E, ro.clip, qp, byte);
+    }
+    if (!done) {
+      DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+      if (DENSE) dense_rotate_df_smem(x, s_r4, lane);
+      else rotate_df_warp(x, ro.rot, h, lane);
+      if (ro.mu_rot) {
+        x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
+        x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+      }
+      byte = quantize_warp_df(x, ro.clip, qp);
+    }
     uint8_t* recp = pool + (size_t)rec * g.record;
     recp[ro.codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
     if (lane == 0)
       *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
           (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Bulk cache write for the identity and signed-Hadamard rotations: certified
+// fp32 decisions (quantize_warp_certain's rules) with a double-float redo of
+// any group that is not certain.  A warp handles four groups at a time, 8
+// lanes x 16 channels each (lane j of a group owns channels 16j..16j+15 and so
+// 4 bytes of the packed codes); the Walsh-Hadamard transform runs its four low
+// stages in registers and its three high stages across the 8 lanes, and the
+// paired fp32 instructions of sm_100 (f32x2) do two channels each.  Tasks are
+// (token, head) in token-major order, so a warp's four groups are consecutive
+// input rows.  Per CTA: AF_TOK tokens, located once, and per head the sign
+// masks and the rotated key mean staged in shared memory.
+// grid = (ceil(n_new / AF_TOK), roles), block = AF_THREADS.
+// ---------------------------------------------------------------------------
+constexpr int AF_TOK = 32;
+constexpr int AF_THREADS = 256;
+constexpr int AF_MAX_HEADS = 192;  // shared-memory staging: 1,028 bytes per head
+
+__device__ __forceinline__ uint64_t f2pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2up(uint64_t p) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+__global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
+    PageGeom g, int n_seqs, int n_new, int dtype, const int32_t* __restrict__ cu_new,
+    const int32_t* __restrict__ start_pos, const int32_t* __restrict__ table, AppendRoles roles,
+    uint8_t* __restrict__ pool, unsigned* err) {
+  constexpr unsigned FULLM = 0xffffffffu;
+  const AppendRole ro = blockIdx.y ? roles.r[1] : roles.r[0];
+  const int H = g.n_kv_heads;
+  const int t0 = blockIdx.x * AF_TOK;
+  const int nt = min(AF_TOK, n_new - t0);
+  const bool had = ro.rot.kind == KVQ_ROT_SIGNED_HADAMARD;
+  const bool has_mu = ro.mu_rot != nullptr;
+  __shared__ long long s_rec[AF_TOK];
+  __shared__ int s_slot[AF_TOK];
+  extern __shared__ uint32_t s_dyn[];
+  uint32_t* s_msk = s_dyn;                                     // [H][8 lanes][16] sign-bit masks
+  float* s_mu = reinterpret_cast<float*>(s_dyn + H * 128);     // [H][128] rotated key mean (or 0)
+  float* s_mumax = s_mu + H * 128;                             // [H] max |mean|
+  if (threadIdx.x < AF_TOK) {
+    const int t = t0 + threadIdx.x;
+    long long rec = -1;
+    int slot = 0;
+    if (t < n_new && !locate(t, n_seqs, cu_new, start_pos, table, g, err, &rec, &slot, 0)) rec = -1;
+    s_rec[threadIdx.x] = rec;
+    s_slot[threadIdx.x] = slot;
+  }
+  // sign masks: fp32 input, word e of lane j = sign bit of channel 16j + e;
+  // bf16 input, word w (< 8) = sign bits 15 / 31 of channels 16j + 2w / + 1
+  for (int i = threadIdx.x; i < H * 128; i += AF_THREADS) {
+    const int h = i >> 7, c = i & 127, base = h * 128 + (c & ~15), e = c & 15;
+    uint32_t word = 0u;
+    if (had) {
+      if (dtype == KVQ_F32) {
+        word = __ldg(ro.rot.signs + base + e) < 0.f ? 0x80000000u : 0u;
+      } else if (e < 8) {
+        word = (__ldg(ro.rot.signs + base + 2 * e) < 0.f ? 0x00008000u : 0u) |
+               (__ldg(ro.rot.signs + base + 2 * e + 1) < 0.f ? 0x80000000u : 0u);
+      }
+    }
+    s_msk[i] = word;
+    s_mu[i] = has_mu ? __ldg(ro.mu_rot + i) : 0.f;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  for (int h = warp; h < H; h += AF_THREADS / 32) {
+    const float4 m = *reinterpret_cast<const float4*>(s_mu + h * 128 + 4 * lane);
+    const float mx = warp_max(fmaxf(fmaxf(fabsf(m.x), fabsf(m.y)), fmaxf(fabsf(m.z), fabsf(m.w))));
+    if (lane == 0) s_mumax[h] = mx;
+  }
+  __syncthreads();
+
+  const int gq = lane >> 3, j = lane & 7;
+  const float sg1 = (j & 1) ? -1.f : 1.f, sg2 = (j & 2) ? -1.f : 1.f, sg4 = (j & 4) ? -1.f : 1.f;
+  const uint64_t pinv = f2pk(INV_SQRT_D, INV_SQRT_D);
+  const int n_tasks = nt * H;
+  for (int base = warp * 4; base < n_tasks; base += AF_THREADS / 8) {
+    const int task = base + gq;
+    const bool valid = task < n_tasks;
+    const int tl = valid ? task / H : 0;
+    const int h = valid ? task - tl * H : 0;
+    const long long rec0 = valid ? s_rec[tl] : -1;
+    const bool live = rec0 >= 0;
+    const size_t row = ((size_t)(t0 + tl) * H + h) * D + 16 * j;
+    // ---- 16 channels, signs applied ----
+    uint64_t P[8];
+    float l1 = 0.f;
+    if (dtype == KVQ_F32) {
+      const uint4* mk = reinterpret_cast<const uint4*>(s_msk + (h * 8 + j) * 16);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (live) a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(ro.src) + row) + q);
+        const uint4 m = mk[q];
+        a.x = __uint_as_float(__float_as_uint(a.x) ^ m.x);
+        a.y = __uint_as_float(__float_as_uint(a.y) ^ m.y);
+        a.z = __uint_as_float(__float_as_uint(a.z) ^ m.z);
+        a.w = __uint_as_float(__float_as_uint(a.w) ^ m.w);
+        l1 += (fabsf(a.x) + fabsf(a.y)) + (fabsf(a.z) + fabsf(a.w));
+        P[2 * q] = f2pk(a.x, a.y);
+        P[2 * q + 1] = f2pk(a.z, a.w);
+      }
+    } else {
+      const uint4* mk = reinterpret_cast<const uint4*>(s_msk + (h * 8 + j) * 16);
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (live) w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ro.src) + row) + q);
+        const uint4 m = mk[q];
+        const uint32_t ww[4] = {w.x ^ m.x, w.y ^ m.y, w.z ^ m.z, w.w ^ m.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float a = __uint_as_float(ww[i] << 16), b = __uint_as_float(ww[i] & 0xffff0000u);
+          l1 += fabsf(a) + fabsf(b);
+          P[4 * q + i] = f2pk(a, b);
+        }
+      }
+    }
+    l1 += __shfl_xor_sync(FULLM, l1, 1);
+    l1 += __shfl_xor_sync(FULLM, l1, 2);
+    l1 += __shfl_xor_sync(FULLM, l1, 4);
+    // ---- rotation, with a bound E on |y - (x R)| for every channel of the group ----
+    float E = 0.f, ymax = l1;  // identity: exact, |y| <= l1
+    if (had) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {  // channel bit 0 (inside a pair)
+        const float2 v = f2up(P[i]);
+        P[i] = f2pk(__fadd_rn(v.x, v.y), __fsub_rn(v.x, v.y));
+      }
+#pragma unroll
+      for (int b = 1; b < 8; b <<= 1)  // channel bits 1-3 (between pairs)
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          if (!(i & b)) {
+            const uint64_t a = P[i], c = P[i | b];
+            P[i] = f2add(a, c);
+            P[i | b] = f2sub(a, c);
+          }
+      // channel bits 4-6 (lanes j ^ 1, 2, 4): lower half y + p, upper half p - y
+      const uint64_t s1 = f2pk(sg1, sg1), s2 = f2pk(sg2, sg2), s4 = f2pk(sg4, sg4);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P[i] = f2fma(s1, P[i], __shfl_xor_sync(FULLM, P[i], 1));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P[i] = f2fma(s2, P[i], __shfl_xor_sync(FULLM, P[i], 2));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P[i] = f2fma(s4, P[i], __shfl_xor_sync(FULLM, P[i], 4));
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P[i] = f2mul(P[i], pinv);
+      // each stage adds at most u * l1 to an output (the nodes it depends on at one
+      // stage partition the inputs): 7 u l1, the scaling by fp32(1/sqrt(128))
+      // (relative error < 0.2 u) and its rounding (u |y|, |y| <= l1 / sqrt(128));
+      // 2^-20 = 16 u leaves a factor ~2
+      ymax = l1 * INV_SQRT_D;
+      E = ymax * 9.5367431640625e-07f;  // 2^-20
+    }
+    if (has_mu) {
+      const uint64_t* mp = reinterpret_cast<const uint64_t*>(s_mu + h * 128 + 16 * j);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) P[i] = f2sub(P[i], mp[i]);
+      E = __fmaf_rn(ymax + s_mumax[h], 1.1920928955078125e-07f, E);  // rounding of y - mu: 2u (|y| + |mu|)
+    }
+    // ---- group decision (certified) ----
+    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float2 v = f2up(P[i]);
+      mn = fminf(mn, fminf(v.x, v.y));
+      mx = fmaxf(mx, fmaxf(v.x, v.y));
+    }
+    mn = fminf(mn, __shfl_xor_sync(FULLM, mn, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 1));
+    mn = fminf(mn, __shfl_xor_sync(FULLM, mn, 2));
+    mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 2));
+    mn = fminf(mn, __shfl_xor_sync(FULLM, mn, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 4));
+    const float clip = ro.clip;
+    const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
+    const float elo = __fmaf_rn(clip, E, fabsf(lo) * 1.1920928955078125e-07f);
+    const float ehi = __fmaf_rn(clip, E, fabsf(hi) * 1.1920928955078125e-07f);
+    const float range = __fsub_rn(hi, lo);
+    const float third = __fdiv_rn(range, 3.0f);
+    const float eth = (elo + ehi + fabsf(range) * 1.1920928955078125e-07f) * 0.33334f +
+                      fabsf(third) * 1.1920928955078125e-07f;
+    __half s16, z16;
+    bool ok = half_rn_certain(third, eth, s16);
+    ok = half_rn_certain(lo, elo, z16) && ok;
+    const float sc = __half2float(s16), zf = __half2float(z16);
+    uint32_t code32 = 0u;
+    if (sc > 0.f) {
+      const float inv = __frcp_rn(sc);
+      // |q* - c| <= E / s + 3 u |c| for c = fl(fl(d - z) / s) and q* = (x - z) / s
+      const float cmax = fmaxf(fabsf(mn - zf), fabsf(mx - zf)) * inv * 1.0001f;
+      const float lim = 0.5f - (E * inv * 1.0001f + cmax * 4.76837158203125e-07f);  // 4 u
+      const uint64_t pz = f2pk(zf, zf), pinv2 = f2pk(inv, inv), magic = f2pk(12582912.f, 12582912.f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float2 cf = f2up(f2mul(f2sub(P[i], pz), pinv2));
+        const float c0 = fminf(fmaxf(cf.x, 0.f), 3.f), c1 = fminf(fmaxf(cf.y, 0.f), 3.f);
+        const float r0 = rintf(c0), r1 = rintf(c1);
+        const float2 f = f2up(f2sub(f2pk(c0, c1), f2pk(r0, r1)));
+        ok = ok && fabsf(f.x) < lim && fabsf(f.y) < lim;
+        const float2 mg = f2up(f2add(f2pk(r0, r1), magic));  // r + 1.5 * 2^23: the integer in the low bits
+        code32 |= ((__float_as_uint(mg.x) & 3u) | ((__float_as_uint(mg.y) & 3u) << 2)) << (4 * i);
+      }
+    }
+    const unsigned bad = __ballot_sync(FULLM, live && !ok);
+    const int slot = valid ? s_slot[tl] : 0;
+    if (live && ((bad >> (8 * gq)) & 0xffu) == 0u) {
+      uint8_t* recp = pool + (size_t)(rec0 + h) * g.record;
+      *reinterpret_cast<uint32_t*>(recp + ro.codes_off + GROUP_BYTES * slot + 4 * j) = code32;
+      if (j == 0)
+        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
+            (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
+    }
+    // ---- groups with an uncertain decision: the whole warp, in double-float ----
+    unsigned todo = 0u;
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if ((bad >> (8 * q)) & 0xffu) todo |= 1u << q;
+    while (todo) {
+      const int q = __ffs(todo) - 1;
+      todo &= todo - 1;
+      const int tq = base + q, tlq = tq / H, hq = tq - tlq * H;
+      const float4 v = load4(ro.src, ((size_t)(t0 + tlq) * H + hq) * D + 4 * lane, dtype);
+      DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+      rotate_df_warp(x, ro.rot, hq, lane);
+      if (has_mu) {
+        const float4 m = *reinterpret_cast<const float4*>(s_mu + hq * 128 + 4 * lane);
+        x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
+        x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+      }
+      QParams qp;
+      const unsigned byte = quantize_warp_df(x, ro.clip, qp);
+      uint8_t* recp = pool + (size_t)(s_rec[tlq] + hq) * g.record;
+      recp[ro.codes_off + GROUP_BYTES * s_slot[tlq] + lane] = (uint8_t)byte;
+      if (lane == 0)
+        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * s_slot[tlq]) =
+            (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+    }
   }
 }
 
@@ -297,6 +597,28 @@ __global__ void __launch_bounds__(32 * (APPEND_ROT_WARPS + 1), 2) append_small_d
         (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
 }
 
+// Non-dense roles: the certified kernel (the warp-per-group kernel beyond AF_MAX_HEADS heads).
+static cudaError_t launch_append_nondense(const PageGeom& g, int n_seqs, int n_new, int dtype, const int32_t* cu_new,
+                                          const int32_t* start_pos, const int32_t* table, const AppendRoles& roles,
+                                          int n_roles, uint8_t* pool, unsigned* err, cudaStream_t s) {
+  if (g.n_kv_heads > AF_MAX_HEADS) {
+    const dim3 grid((n_new + APPEND_TOK - 1) / APPEND_TOK, g.n_kv_heads, n_roles);
+    append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
+    return cudaGetLastError();
+  }
+  const size_t smem = (size_t)g.n_kv_heads * 1028;
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(append_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               AF_MAX_HEADS * 1028);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  append_fast_kernel<<<dim3((n_new + AF_TOK - 1) / AF_TOK, n_roles), AF_THREADS, smem, s>>>(
+      g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, const void* k,
                                    const void* v, int dtype, const int32_t* cu_new,
                                    const int32_t* start_pos, const int32_t* table, RotDev rot_k,
@@ -317,42 +639,33 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
   }
   // keys and values may use different rotation kinds: one launch per kind
   const bool kd = rot_k.kind == KVQ_ROT_DENSE, vd = rot_v.kind == KVQ_ROT_DENSE;
+  if (!kd && !vd) return launch_append_nondense(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, 2, pool, err, s);
   if (n_new <= APPEND_SMALL_MAX && kd && vd) {
     append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 2), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
                                                                              table, roles, pool, err);
     return cudaGetLastError();
   }
-  if (n_new <= APPEND_SMALL_MAX && (kd || vd)) {
-    // dense roles through the small-append kernel, the others through the warp kernel
-    for (int role = 0; role < 2; ++role) {
-      AppendRoles one;
-      one.r[0] = roles.r[role];
-      one.r[1] = roles.r[role];
-      if (role == 0 ? kd : vd)
-        append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 1), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
-                                                                                 table, one, pool, err);
-      else
-        append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
-      const cudaError_t e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-  }
-  if (kd == vd) {
-    const dim3 g2(grid.x, grid.y, 2);
-    if (kd) append_kernel<true><<<g2, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
-    else append_kernel<false><<<g2, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
+  if (kd && vd) {
+    append_kernel<true><<<dim3(grid.x, grid.y, 2), 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table,
+                                                                     roles, pool, err);
     return cudaGetLastError();
   }
+  // one dense role and one other
   for (int role = 0; role < 2; ++role) {
     AppendRoles one;
     one.r[0] = roles.r[role];
     one.r[1] = roles.r[role];
-    if (role == 0 ? kd : vd)
-      append_kernel<true><<<grid, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
-    else
-      append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (role == 0 ? kd : vd) {
+      if (n_new <= APPEND_SMALL_MAX)
+        append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 1), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(
+            g, n_seqs, dtype, cu_new, start_pos, table, one, pool, err);
+      else
+        append_kernel<true><<<grid, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
+      e = cudaGetLastError();
+    } else {
+      e = launch_append_nondense(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, 1, pool, err, s);
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

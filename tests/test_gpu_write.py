@@ -103,3 +103,51 @@ def test_key_mean_and_rotate_heads_match_oracle():
         kvq.kvq_rotate_heads(gu.dev(x), kvq.DeviceRot.from_spec(spec), y, heads_per_rot=2)
         yr = oracle.cache.rotate_heads(x, r, heads_per_rot=2)
         assert gu.normwise_err(y.cpu().numpy(), yr) < 1e-6, rot
+
+
+def _tie_groups(rng, n_tok, n_heads):
+    """Groups whose exact values sit on, next to and away from the code
+    boundaries: min 0 and max 3 * step (so scale = step, zero = 0 exactly), the
+    rest at k * step, (k + 1/2) * step (exact ties), (k + 1/2) * step +- step *
+    2^-23 (inside the fp32 decision's error bound) and +- step * 2^-14 (outside)."""
+    x = np.empty((n_tok, n_heads, 128), np.float32)
+    for t in range(n_tok):
+        for h in range(n_heads):
+            step = np.float32(2.0 ** rng.integers(-6, 4))
+            k = rng.integers(0, 3, 128).astype(np.float64)
+            kind = rng.integers(0, 5, 128)
+            off = np.select([kind == 0, kind == 1, kind == 2, kind == 3],
+                            [0.0, 0.5, 0.5 + 2.0 ** -23 * rng.choice([-1, 1], 128),
+                             0.5 + 2.0 ** -14 * rng.choice([-1, 1], 128)], rng.uniform(0, 1, 128))
+            v = (k + off) * step
+            v[rng.integers(0, 64)] = 0.0
+            v[64 + rng.integers(0, 64)] = 3.0 * step
+            x[t, h] = np.clip(v, 0.0, 3.0 * step).astype(np.float32)
+    return x
+
+
+def test_exact_ties_and_near_ties_match_the_oracle():
+    """Codes on and next to the rounding midpoints (identity rotation, fp32 input,
+    no centring) equal the fp64 oracle's: the certified fp32 decision must hand
+    every uncertain group to the double-float path, which breaks ties to even."""
+    import oracle
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    rng = np.random.default_rng(2718)
+    n_tok, hkv, page = 160, 2, 16
+    k = _tie_groups(rng, n_tok, hkv)
+    v = _tie_groups(rng, n_tok, hkv)
+    nb = n_tok // page
+    lay = kvq.make_layout(page, hkv, hkv, nb, nb)
+    pool = torch.zeros(kvq.kvq_pool_bytes(lay), dtype=torch.uint8, device="cuda")
+    ident = kvq.DeviceRot("identity")
+    kvq.kvq_quantize_append(lay, gu.dev(k), gu.dev(v), gu.dev_i32([0, n_tok]), gu.dev_i32([0]),
+                            gu.dev_i32(np.arange(nb)[None, :]), ident, ident, None, 1.0, 1.0, pool)
+    kvq.kvq_device_check()
+    gpool = pool.cpu().numpy()
+    for which, x in (("k", k), ("v", v)):
+        codes, s, z = oracle.quant.quantize_groups(x.astype(np.float64), 1.0)
+        got_c, got_m = gu.seq_codes_meta(gpool, hkv, page, np.arange(nb), n_tok, which)
+        assert np.array_equal(got_m[..., 0], oracle.quant.fp16_bits(s)), which
+        assert np.array_equal(got_m[..., 1], oracle.quant.fp16_bits(z)), which
+        assert np.array_equal(got_c, codes), (which, int((got_c != codes).sum()))
