@@ -5,6 +5,8 @@
 // launch that rotates keys, subtracts the precomputed mu R, clips, quantizes,
 // packs and writes), appendix Eqs. 19-21 (key mean; (k - mu) R = k R - mu R),
 // Eq. 27 (values stored rotated), §3.1 Eq. 4 (the quantizer).
+#include <type_traits>
+
 #include "quant_common.cuh"
 
 namespace kvq {
@@ -218,6 +220,7 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
 constexpr int AF_TOK = 32;
 constexpr int AF_THREADS = 256;
 constexpr int AF_MAX_HEADS = 192;  // shared-memory staging: 1,028 bytes per head
+constexpr int AF_LPG = 8;          // lanes per group
 
 __device__ __forceinline__ uint64_t f2pk(float a, float b) {
   uint64_t r;
@@ -250,11 +253,19 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
   return r;
 }
 
+template <int LPG>  // lanes per group: 8 (16 channels each) or 4 (32)
 __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
     PageGeom g, int n_seqs, int n_new, int dtype, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ table, AppendRoles roles,
     uint8_t* __restrict__ pool, unsigned* err) {
   constexpr unsigned FULLM = 0xffffffffu;
+  constexpr int CPL = D / LPG;   // channels per lane
+  constexpr int NP = CPL / 2;    // channel pairs per lane
+  constexpr int GPW = 32 / LPG;  // groups (consecutive heads of one token) per warp
+  constexpr unsigned GMASK = (1u << LPG) - 1u;
+  using Codes = typename std::conditional<LPG == 8, uint32_t, uint64_t>::type;
+  constexpr int NQ = CPL / 4;    // 16-byte input words per lane (fp32; bf16 uses the first half)
+  constexpr float U1 = 6.5e-8f;  // 1.09 u: one rounding, with margin
   const AppendRole ro = blockIdx.y ? roles.r[1] : roles.r[0];
   const int H = g.n_kv_heads;
   const int t0 = blockIdx.x * AF_TOK;
@@ -264,9 +275,11 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
   __shared__ long long s_rec[AF_TOK];
   __shared__ int s_slot[AF_TOK];
   extern __shared__ uint32_t s_dyn[];
-  uint32_t* s_msk = s_dyn;                                     // [H][8 lanes][16] sign-bit masks
-  float* s_mu = reinterpret_cast<float*>(s_dyn + H * 128);     // [H][128] rotated key mean (or 0)
-  float* s_mumax = s_mu + H * 128;                             // [H] max |mean|
+  // per head: sign-bit masks (fp32 input: word c = channel c; bf16: word w = channels 2w, 2w + 1
+  // in bits 15 / 31), the rotated key mean (or 0), max |mean|
+  uint32_t* s_msk = s_dyn;                                  // [H][128]
+  float* s_mu = reinterpret_cast<float*>(s_dyn + H * 128);  // [H][128]
+  float* s_mumax = s_mu + H * 128;                          // [H]
   if (threadIdx.x < AF_TOK) {
     const int t = t0 + threadIdx.x;
     long long rec = -1;
@@ -275,18 +288,13 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
     s_rec[threadIdx.x] = rec;
     s_slot[threadIdx.x] = slot;
   }
-  // sign masks: fp32 input, word e of lane j = sign bit of channel 16j + e;
-  // bf16 input, word w (< 8) = sign bits 15 / 31 of channels 16j + 2w / + 1
   for (int i = threadIdx.x; i < H * 128; i += AF_THREADS) {
-    const int h = i >> 7, c = i & 127, base = h * 128 + (c & ~15), e = c & 15;
+    const int h = i >> 7, c = i & 127;
+    const float* sg = ro.rot.signs + (size_t)h * D;
     uint32_t word = 0u;
     if (had) {
-      if (dtype == KVQ_F32) {
-        word = __ldg(ro.rot.signs + base + e) < 0.f ? 0x80000000u : 0u;
-      } else if (e < 8) {
-        word = (__ldg(ro.rot.signs + base + 2 * e) < 0.f ? 0x00008000u : 0u) |
-               (__ldg(ro.rot.signs + base + 2 * e + 1) < 0.f ? 0x80000000u : 0u);
-      }
+      if (dtype == KVQ_F32) word = __ldg(sg + c) < 0.f ? 0x80000000u : 0u;
+      else if (c < 64) word = (__ldg(sg + 2 * c) < 0.f ? 0x00008000u : 0u) | (__ldg(sg + 2 * c + 1) < 0.f ? 0x80000000u : 0u);
     }
     s_msk[i] = word;
     s_mu[i] = has_mu ? __ldg(ro.mu_rot + i) : 0.f;
@@ -300,144 +308,157 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
   }
   __syncthreads();
 
-  const int gq = lane >> 3, j = lane & 7;
-  const float sg1 = (j & 1) ? -1.f : 1.f, sg2 = (j & 2) ? -1.f : 1.f, sg4 = (j & 4) ? -1.f : 1.f;
+  const int gq = lane / LPG, j = lane % LPG;
   const uint64_t pinv = f2pk(INV_SQRT_D, INV_SQRT_D);
-  const int n_tasks = nt * H;
-  for (int base = warp * 4; base < n_tasks; base += AF_THREADS / 8) {
-    const int task = base + gq;
-    const bool valid = task < n_tasks;
-    const int tl = valid ? task / H : 0;
-    const int h = valid ? task - tl * H : 0;
-    const long long rec0 = valid ? s_rec[tl] : -1;
-    const bool live = rec0 >= 0;
-    const size_t row = ((size_t)(t0 + tl) * H + h) * D + 16 * j;
-    // ---- 16 channels, signs applied ----
-    uint64_t P[8];
+  const uint64_t pmagic = f2pk(12582912.f, 12582912.f);  // 1.5 * 2^23: adding it rounds to an integer
+  const int n_hb = (H + GPW - 1) / GPW;
+  // a warp iteration: token tl, heads GPW hb .. GPW hb + GPW - 1 (warp w: tokens w, w + 8, ...)
+  auto fetch = [&](int tlk, int hbk, uint4 (&raw)[NQ]) {
+    const int hk = GPW * hbk + gq;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) raw[q] = make_uint4(0u, 0u, 0u, 0u);
+    if (tlk < nt && hk < H && s_rec[tlk] >= 0) {
+      const size_t rw = ((size_t)(t0 + tlk) * H + hk) * D + CPL * j;
+      if (dtype == KVQ_F32) {
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) raw[q] = __ldg(reinterpret_cast<const uint4*>(static_cast<const float*>(ro.src) + rw) + q);
+      } else {
+#pragma unroll
+        for (int q = 0; q < NQ / 2; ++q)
+          raw[q] = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ro.src) + rw) + q);
+      }
+    }
+  };
+  uint4 nxt[NQ];
+  int tl = warp, hb = 0;
+  fetch(tl, hb, nxt);
+  while (tl < nt) {
+    uint4 cur[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) cur[q] = nxt[q];
+    const int tln = hb + 1 < n_hb ? tl : tl + AF_THREADS / 32, hbn = hb + 1 < n_hb ? hb + 1 : 0;
+    if (tln < nt) fetch(tln, hbn, nxt);
+    const int h = GPW * hb + gq;
+    const long long rec0 = s_rec[tl];
+    const bool live = h < H && rec0 >= 0;
+    const int hs = h < H ? h : 0;  // a valid head for the shared-memory tables
+    // ---- 16 channels with signs, channel bit 0 butterflies done while unpacking ----
+    uint64_t P[NP];
     float l1 = 0.f;
     if (dtype == KVQ_F32) {
-      const uint4* mk = reinterpret_cast<const uint4*>(s_msk + (h * 8 + j) * 16);
+      const uint4* mk = reinterpret_cast<const uint4*>(s_msk + hs * 128 + CPL * j);
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (live) a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(ro.src) + row) + q);
+      for (int q = 0; q < NQ; ++q) {
         const uint4 m = mk[q];
-        a.x = __uint_as_float(__float_as_uint(a.x) ^ m.x);
-        a.y = __uint_as_float(__float_as_uint(a.y) ^ m.y);
-        a.z = __uint_as_float(__float_as_uint(a.z) ^ m.z);
-        a.w = __uint_as_float(__float_as_uint(a.w) ^ m.w);
-        l1 += (fabsf(a.x) + fabsf(a.y)) + (fabsf(a.z) + fabsf(a.w));
-        P[2 * q] = f2pk(a.x, a.y);
-        P[2 * q + 1] = f2pk(a.z, a.w);
+        const float ax = __uint_as_float(cur[q].x ^ m.x), ay = __uint_as_float(cur[q].y ^ m.y);
+        const float az = __uint_as_float(cur[q].z ^ m.z), aw = __uint_as_float(cur[q].w ^ m.w);
+        l1 += (fabsf(ax) + fabsf(ay)) + (fabsf(az) + fabsf(aw));
+        if (had) {
+          P[2 * q] = f2pk(__fadd_rn(ax, ay), __fsub_rn(ax, ay));
+          P[2 * q + 1] = f2pk(__fadd_rn(az, aw), __fsub_rn(az, aw));
+        } else {
+          P[2 * q] = f2pk(ax, ay);
+          P[2 * q + 1] = f2pk(az, aw);
+        }
       }
     } else {
-      const uint4* mk = reinterpret_cast<const uint4*>(s_msk + (h * 8 + j) * 16);
+      const uint4* mk = reinterpret_cast<const uint4*>(s_msk + hs * 128 + (CPL / 2) * j);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (live) w = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(ro.src) + row) + q);
+      for (int q = 0; q < NQ / 2; ++q) {
         const uint4 m = mk[q];
-        const uint32_t ww[4] = {w.x ^ m.x, w.y ^ m.y, w.z ^ m.z, w.w ^ m.w};
+        const uint32_t ww[4] = {cur[q].x ^ m.x, cur[q].y ^ m.y, cur[q].z ^ m.z, cur[q].w ^ m.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float a = __uint_as_float(ww[i] << 16), b = __uint_as_float(ww[i] & 0xffff0000u);
           l1 += fabsf(a) + fabsf(b);
-          P[4 * q + i] = f2pk(a, b);
+          P[4 * q + i] = had ? f2pk(__fadd_rn(a, b), __fsub_rn(a, b)) : f2pk(a, b);
         }
       }
     }
-    l1 += __shfl_xor_sync(FULLM, l1, 1);
-    l1 += __shfl_xor_sync(FULLM, l1, 2);
-    l1 += __shfl_xor_sync(FULLM, l1, 4);
+#pragma unroll
+    for (int m = 1; m < LPG; m <<= 1) l1 += __shfl_xor_sync(FULLM, l1, m);
     // ---- rotation, with a bound E on |y - (x R)| for every channel of the group ----
     float E = 0.f, ymax = l1;  // identity: exact, |y| <= l1
     if (had) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {  // channel bit 0 (inside a pair)
-        const float2 v = f2up(P[i]);
-        P[i] = f2pk(__fadd_rn(v.x, v.y), __fsub_rn(v.x, v.y));
-      }
+      for (int b = 1; b < NP; b <<= 1)  // channel bits 1-3 (between pairs)
 #pragma unroll
-      for (int b = 1; b < 8; b <<= 1)  // channel bits 1-3 (between pairs)
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
+        for (int i = 0; i < NP; ++i)
           if (!(i & b)) {
             const uint64_t a = P[i], c = P[i | b];
             P[i] = f2add(a, c);
             P[i | b] = f2sub(a, c);
           }
       // channel bits 4-6 (lanes j ^ 1, 2, 4): lower half y + p, upper half p - y
-      const uint64_t s1 = f2pk(sg1, sg1), s2 = f2pk(sg2, sg2), s4 = f2pk(sg4, sg4);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) P[i] = f2fma(s1, P[i], __shfl_xor_sync(FULLM, P[i], 1));
+      for (int m = 1; m < LPG; m <<= 1) {
+        const float sgn = (j & m) ? -1.f : 1.f;
+        const uint64_t sp = f2pk(sgn, sgn);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) P[i] = f2fma(s2, P[i], __shfl_xor_sync(FULLM, P[i], 2));
+        for (int i = 0; i < NP; ++i) P[i] = f2fma(sp, P[i], __shfl_xor_sync(FULLM, P[i], m));
+      }
 #pragma unroll
-      for (int i = 0; i < 8; ++i) P[i] = f2fma(s4, P[i], __shfl_xor_sync(FULLM, P[i], 4));
-#pragma unroll
-      for (int i = 0; i < 8; ++i) P[i] = f2mul(P[i], pinv);
-      // each stage adds at most u * l1 to an output (the nodes it depends on at one
-      // stage partition the inputs): 7 u l1, the scaling by fp32(1/sqrt(128))
-      // (relative error < 0.2 u) and its rounding (u |y|, |y| <= l1 / sqrt(128));
-      // 2^-20 = 16 u leaves a factor ~2
+      for (int i = 0; i < NP; ++i) P[i] = f2mul(P[i], pinv);
+      // each stage adds at most u * l1 to an output (the nodes an output depends on
+      // at one stage partition the inputs): 7 u l1; the scaling by fp32(1/sqrt(128))
+      // (relative error < 0.2 u) and its rounding (u |y|, |y| <= l1 / sqrt(128)): 8.2 u
       ymax = l1 * INV_SQRT_D;
-      E = ymax * 9.5367431640625e-07f;  // 2^-20
+      E = ymax * 5.1e-7f;  // 8.56 u
     }
     if (has_mu) {
-      const uint64_t* mp = reinterpret_cast<const uint64_t*>(s_mu + h * 128 + 16 * j);
+      const uint64_t* mp = reinterpret_cast<const uint64_t*>(s_mu + hs * 128 + CPL * j);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) P[i] = f2sub(P[i], mp[i]);
-      E = __fmaf_rn(ymax + s_mumax[h], 1.1920928955078125e-07f, E);  // rounding of y - mu: 2u (|y| + |mu|)
+      for (int i = 0; i < NP; ++i) P[i] = f2sub(P[i], mp[i]);
+      E = __fmaf_rn(ymax + s_mumax[hs], U1, E);  // rounding of y - mu
     }
     // ---- group decision (certified) ----
     float mn = INFINITY, mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < NP; ++i) {
       const float2 v = f2up(P[i]);
       mn = fminf(mn, fminf(v.x, v.y));
       mx = fmaxf(mx, fmaxf(v.x, v.y));
     }
-    mn = fminf(mn, __shfl_xor_sync(FULLM, mn, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 1));
-    mn = fminf(mn, __shfl_xor_sync(FULLM, mn, 2));
-    mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 2));
-    mn = fminf(mn, __shfl_xor_sync(FULLM, mn, 4));
-    mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 4));
+#pragma unroll
+    for (int m = 1; m < LPG; m <<= 1) {
+      mn = fminf(mn, __shfl_xor_sync(FULLM, mn, m));
+      mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, m));
+    }
     const float clip = ro.clip;
     const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
-    const float elo = __fmaf_rn(clip, E, fabsf(lo) * 1.1920928955078125e-07f);
-    const float ehi = __fmaf_rn(clip, E, fabsf(hi) * 1.1920928955078125e-07f);
+    const float elo = __fmaf_rn(clip, E, fabsf(lo) * U1);
+    const float ehi = __fmaf_rn(clip, E, fabsf(hi) * U1);
     const float range = __fsub_rn(hi, lo);
     const float third = __fdiv_rn(range, 3.0f);
-    const float eth = (elo + ehi + fabsf(range) * 1.1920928955078125e-07f) * 0.33334f +
-                      fabsf(third) * 1.1920928955078125e-07f;
+    const float eth = (elo + ehi + fabsf(range) * U1) * 0.33334f + fabsf(third) * U1;
     __half s16, z16;
     bool ok = half_rn_certain(third, eth, s16);
     ok = half_rn_certain(lo, elo, z16) && ok;
     const float sc = __half2float(s16), zf = __half2float(z16);
-    uint32_t code32 = 0u;
+    Codes codes = 0u;
     if (sc > 0.f) {
       const float inv = __frcp_rn(sc);
-      // |q* - c| <= E / s + 3 u |c| for c = fl(fl(d - z) / s) and q* = (x - z) / s
+      // |q* - c| <= E / s + 3 u |c| for c = fl(fl(d - z) / s) and q* = (x - z) / s;
+      // a code is certain when the clamped c is further than that from a half-integer
       const float cmax = fmaxf(fabsf(mn - zf), fabsf(mx - zf)) * inv * 1.0001f;
-      const float lim = 0.5f - (E * inv * 1.0001f + cmax * 4.76837158203125e-07f);  // 4 u
-      const uint64_t pz = f2pk(zf, zf), pinv2 = f2pk(inv, inv), magic = f2pk(12582912.f, 12582912.f);
+      const float lim = 0.5f - (E * inv * 1.0001f + cmax * 2.1e-7f);  // 3.5 u
+      const uint64_t pz = f2pk(zf, zf), pinv2 = f2pk(inv, inv);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
+      for (int i = 0; i < NP; ++i) {
         const float2 cf = f2up(f2mul(f2sub(P[i], pz), pinv2));
-        const float c0 = fminf(fmaxf(cf.x, 0.f), 3.f), c1 = fminf(fmaxf(cf.y, 0.f), 3.f);
-        const float r0 = rintf(c0), r1 = rintf(c1);
-        const float2 f = f2up(f2sub(f2pk(c0, c1), f2pk(r0, r1)));
+        const uint64_t cc = f2pk(fminf(fmaxf(cf.x, 0.f), 3.f), fminf(fmaxf(cf.y, 0.f), 3.f));
+        const uint64_t mg = f2add(cc, pmagic);                   // integer r in the low mantissa bits
+        const float2 f = f2up(f2sub(cc, f2sub(mg, pmagic)));     // c - r, exact
         ok = ok && fabsf(f.x) < lim && fabsf(f.y) < lim;
-        const float2 mg = f2up(f2add(f2pk(r0, r1), magic));  // r + 1.5 * 2^23: the integer in the low bits
-        code32 |= ((__float_as_uint(mg.x) & 3u) | ((__float_as_uint(mg.y) & 3u) << 2)) << (4 * i);
+        const float2 mgs = f2up(mg);
+        codes |= (Codes)((__float_as_uint(mgs.x) & 3u) | ((__float_as_uint(mgs.y) & 3u) << 2)) << (4 * i);
       }
     }
     const unsigned bad = __ballot_sync(FULLM, live && !ok);
-    const int slot = valid ? s_slot[tl] : 0;
-    if (live && ((bad >> (8 * gq)) & 0xffu) == 0u) {
+    const int slot = s_slot[tl];
+    if (live && ((bad >> (LPG * gq)) & GMASK) == 0u) {
       uint8_t* recp = pool + (size_t)(rec0 + h) * g.record;
-      *reinterpret_cast<uint32_t*>(recp + ro.codes_off + GROUP_BYTES * slot + 4 * j) = code32;
+      *reinterpret_cast<Codes*>(recp + ro.codes_off + GROUP_BYTES * slot + (CPL / 4) * j) = codes;
       if (j == 0)
         *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
             (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
@@ -445,13 +466,13 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
     // ---- groups with an uncertain decision: the whole warp, in double-float ----
     unsigned todo = 0u;
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
-      if ((bad >> (8 * q)) & 0xffu) todo |= 1u << q;
+    for (int q = 0; q < GPW; ++q)
+      if ((bad >> (LPG * q)) & GMASK) todo |= 1u << q;
     while (todo) {
       const int q = __ffs(todo) - 1;
       todo &= todo - 1;
-      const int tq = base + q, tlq = tq / H, hq = tq - tlq * H;
-      const float4 v = load4(ro.src, ((size_t)(t0 + tlq) * H + hq) * D + 4 * lane, dtype);
+      const int hq = GPW * hb + q;
+      const float4 v = load4(ro.src, ((size_t)(t0 + tl) * H + hq) * D + 4 * lane, dtype);
       DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
       rotate_df_warp(x, ro.rot, hq, lane);
       if (has_mu) {
@@ -461,12 +482,14 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
       }
       QParams qp;
       const unsigned byte = quantize_warp_df(x, ro.clip, qp);
-      uint8_t* recp = pool + (size_t)(s_rec[tlq] + hq) * g.record;
-      recp[ro.codes_off + GROUP_BYTES * s_slot[tlq] + lane] = (uint8_t)byte;
+      uint8_t* recp = pool + (size_t)(rec0 + hq) * g.record;
+      recp[ro.codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
       if (lane == 0)
-        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * s_slot[tlq]) =
+        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
             (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
     }
+    tl = tln;
+    hb = hbn;
   }
 }
 
@@ -609,12 +632,12 @@ static cudaError_t launch_append_nondense(const PageGeom& g, int n_seqs, int n_n
   const size_t smem = (size_t)g.n_kv_heads * 1028;
   static bool attr_set = false;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(append_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const cudaError_t e = cudaFuncSetAttribute(append_fast_kernel<AF_LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                AF_MAX_HEADS * 1028);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  append_fast_kernel<<<dim3((n_new + AF_TOK - 1) / AF_TOK, n_roles), AF_THREADS, smem, s>>>(
+  append_fast_kernel<AF_LPG><<<dim3((n_new + AF_TOK - 1) / AF_TOK, n_roles), AF_THREADS, smem, s>>>(
       g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
   return cudaGetLastError();
 }
