@@ -195,8 +195,7 @@ __device__ __forceinline__ void cluster_sync_all() {
 // independently - W (read from memory once), x (read by every row tile, from
 // L2) and the converted B tiles:
 // * warp 0 streams the 128 x 64 boxes of W into a ring of SW stages by tensor
-//   copies (128-byte swizzle, zero fill past the edges), from the start: W does
-//   not depend on the preceding kernel;
+//   copies (128-byte swizzle, zero fill past the edges);
 // * warps 4-11 fetch x (fp32) with per-thread asynchronous copies into a ring of
 //   SX stages, once the preceding kernel (which writes x) has finished, split
 //   each stage into the bf16 B tile (128-byte swizzle) in a ring of SB stages
@@ -319,6 +318,8 @@ __global__ void __launch_bounds__(OPT_THREADS, 1) out_proj_tc_kernel(const __gri
 
   if (warp == 0) {
     // ---- W producer ----
+    // W too may come from the preceding kernel (a fold right before the projection)
+    pdl_wait();
     int issued = 0;
     for (int kb = 0; kb < n_k; ++kb) {
       const int st = kb % SW;

@@ -493,131 +493,169 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
   }
 }
 
-// locate() for one warp: the sequences are searched 32 at a time (one per lane)
-// instead of by bisection, so the lookup is a few independent loads deep.
-__device__ __forceinline__ bool locate_warp(int t, int n_seqs, const int32_t* cu_new, const int32_t* start_pos,
-                                            const int32_t* table, const PageGeom& g, unsigned* err,
-                                            long long* rec_index, int* slot, int head, int lane) {
-  int b = -1;
-  for (int b0 = 0; b0 < n_seqs && b < 0; b0 += 32) {
-    const int bb = b0 + lane;
-    const bool hit = bb < n_seqs && __ldg(cu_new + bb) <= t && t < __ldg(cu_new + bb + 1);
-    const unsigned m = __ballot_sync(0xffffffffu, hit);
-    if (m) b = b0 + __ffs(m) - 1;
-  }
-  if (b < 0) {
-    if (lane == 0) flag_error(err, ERR_SEQ_RANGE);
-    return false;
-  }
-  const long long pos = (long long)__ldg(start_pos + b) + (t - __ldg(cu_new + b));
-  const long long page = pos / g.page_tokens;
-  if (pos < 0 || page >= g.max_blocks) {
-    if (lane == 0) flag_error(err, ERR_POS_RANGE);
-    return false;
-  }
-  const int blk = __ldg(table + (size_t)b * g.max_blocks + page);
-  if (blk < 0 || blk >= g.num_blocks) {
-    if (lane == 0) flag_error(err, ERR_BLOCK_RANGE);
-    return false;
-  }
-  *rec_index = (long long)blk * g.n_kv_heads + head;
-  *slot = (int)(pos % g.page_tokens);
-  return true;
-}
+constexpr int APPEND_SMALL_MAX = 128;  // tokens per call below which the step kernel is used
 
-// Small appends (a decode step's one token per sequence): one CTA per (token,
-// head, role) so the double-float rotations are spread over the whole GPU.
-// Warps 0-7 each accumulate the terms of 16 input channels (rows of a dense R_h
-// read from global memory, L2-resident, all 16 loads in flight at once) while
-// warp 8 finds the token's page slot; the eight double-float partial sums are
-// added in a fixed order, and warp 0 centres, quantizes and writes the group.
-// grid = (n_new, n_kv_heads, roles), block = 288.
-constexpr int APPEND_SMALL_MAX = 128;  // tokens per call below which this path is used
+// ---------------------------------------------------------------------------
+// Cache write with a dense R for a few tokens (a decode step): one CTA per
+// (tb <= ADS_TB tokens, head, role), 8 warps.  Warp w keeps rows 16w..16w+15 of R_h in
+// registers and forms, for every token of the CTA, its partial x R and the
+// partial sum of |x_c| |R_ci| (the error bound's scale).  Warp t then adds the
+// 8 partials of token t in a fixed tree and decides the group with certified
+// fp32 (quantize_warp_certain): a 16-term FMA chain and a 3-level sum are off
+// by at most 19.1 u sum_c |x_c R_ci|.  Uncertain groups are redone by all 8
+// warps in double-float from the same register-held rows.
+// grid = (ceil(n_new / tb), n_kv_heads, roles), block = 256, tb chosen for ~2 CTAs per SM.
+// ---------------------------------------------------------------------------
+constexpr int ADS_TB = 8;
 
-constexpr int APPEND_ROT_WARPS = 8;
-
-__global__ void __launch_bounds__(32 * (APPEND_ROT_WARPS + 1), 2) append_small_dense_kernel(
-    PageGeom g, int n_seqs, int dtype, const int32_t* __restrict__ cu_new, const int32_t* __restrict__ start_pos,
-    const int32_t* __restrict__ table, AppendRoles roles, uint8_t* __restrict__ pool, unsigned* err) {
-  __shared__ float2 part[APPEND_ROT_WARPS][D];  // (hi, lo) of each warp's partial x R
-  __shared__ long long s_rec;    // record index, or -1 when the token is skipped
-  __shared__ int s_slot;
+__global__ void __launch_bounds__(256) append_dense_step_kernel(
+    PageGeom g, int n_seqs, int n_new, int tb, int dtype, const int32_t* __restrict__ cu_new,
+    const int32_t* __restrict__ start_pos, const int32_t* __restrict__ table, AppendRoles roles,
+    uint8_t* __restrict__ pool, unsigned* err) {
+  __shared__ __align__(16) float s_x[ADS_TB][D];          // the tokens' input rows
+  __shared__ __align__(16) float4 s_val[ADS_TB][8][32];   // partial x R (lane l: outputs 4l..4l+3)
+  __shared__ float s_abs[ADS_TB][8];                      // max over the warp's outputs of its partial sum |x| |R|
+  __shared__ long long s_rec[ADS_TB];
+  __shared__ int s_slot[ADS_TB], s_redo[ADS_TB];
   const AppendRole ro = blockIdx.z ? roles.r[1] : roles.r[0];
-  const int t = blockIdx.x, h = blockIdx.y;
+  const int h = blockIdx.y, t0 = blockIdx.x * tb;
+  const int nt = min(tb, n_new - t0);
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (warp == APPEND_ROT_WARPS) {
-    long long rec;
-    int slot;
-    // flag each bad token once (role 0), skip it in both roles
-    const bool ok = locate_warp(t, n_seqs, cu_new, start_pos, table, g, blockIdx.z == 0 ? err : nullptr, &rec, &slot,
-                                h, lane);
-    if (lane == 0) {
-      s_rec = ok ? rec : -1;
-      s_slot = slot;
-    }
-    __syncthreads();
-    return;
-  }
-  const float4 v = load4(ro.src, ((size_t)t * g.n_kv_heads + h) * D + 4 * lane, dtype);
-  const float xin[4] = {v.x, v.y, v.z, v.w};
+  // rows 16 warp .. 16 warp + 15 of R_h, lane l: columns 4l .. 4l + 3 (issued first: the
+  // token lookups and input loads below overlap them)
   const float4* R4 = reinterpret_cast<const float4*>(ro.rot.dense + (size_t)h * D * D) + lane;
-  float sh[4][4], sl[4][4];
+  float4 rr[16];
 #pragma unroll
-  for (int u = 0; u < 4; ++u)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) sh[u][i] = sl[u][i] = 0.f;
-  // the warp's 16 rows of R, all loads in flight at once
-  {
-    float4 rr[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) rr[j] = __ldg(R4 + (size_t)(16 * warp + j) * 32);
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int m = 4 * warp + (j >> 2), u = j & 3;          // row 4m + u
-      const float xh = __shfl_sync(0xffffffffu, xin[u], m);  // channel 4m + u lives in lane m
-      const float r[4] = {rr[j].x, rr[j].y, rr[j].z, rr[j].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float p = __fmul_rn(xh, r[i]);
-        const float pe = __fmaf_rn(xh, r[i], -p);
-        const DF q = two_sum(sh[u][i], p);
-        sh[u][i] = q.hi;
-        sl[u][i] = __fadd_rn(sl[u][i], __fadd_rn(q.lo, pe));
-      }
-    }
+  for (int r = 0; r < 16; ++r) rr[r] = __ldg(R4 + (size_t)(16 * warp + r) * 32);
+  for (int i = warp; i < ADS_TB; i += 8) {
+    const float4 v = i < nt ? load4(ro.src, ((size_t)(t0 + i) * g.n_kv_heads + h) * D + 4 * lane, dtype)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(s_x[i])[lane] = v;
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const DF a = df_add(DF{sh[0][i], sl[0][i]}, DF{sh[1][i], sl[1][i]});
-    const DF b = df_add(DF{sh[2][i], sl[2][i]}, DF{sh[3][i], sl[3][i]});
-    const DF c = df_add(a, b);
-    part[warp][4 * lane + i] = make_float2(c.hi, c.lo);
+  if (warp == 7 && lane < ADS_TB) {
+    const int t = t0 + lane;
+    long long rec = -1;
+    int slot = 0;
+    // each bad token is flagged once (role 0) and skipped in both roles
+    if (lane < nt && !locate(t, n_seqs, cu_new, start_pos, table, g, blockIdx.z == 0 ? err : nullptr, &rec, &slot, h))
+      rec = -1;
+    s_rec[lane] = rec;
+    s_slot[lane] = slot;
+    s_redo[lane] = 0;
   }
   __syncthreads();
-  if (warp != 0) return;
-  const long long rec = s_rec;
-  const int slot = s_slot;
-  if (rec < 0) return;
-  DF x[4];
+  for (int tk = 0; tk < nt; ++tk) {
+    float a[4] = {0.f, 0.f, 0.f, 0.f}, b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    DF q[APPEND_ROT_WARPS];
+    for (int r = 0; r < 16; ++r) {
+      const float xc = s_x[tk][16 * warp + r], ax = fabsf(xc);
+      a[0] = __fmaf_rn(xc, rr[r].x, a[0]); a[1] = __fmaf_rn(xc, rr[r].y, a[1]);
+      a[2] = __fmaf_rn(xc, rr[r].z, a[2]); a[3] = __fmaf_rn(xc, rr[r].w, a[3]);
+      b[0] = __fmaf_rn(ax, fabsf(rr[r].x), b[0]); b[1] = __fmaf_rn(ax, fabsf(rr[r].y), b[1]);
+      b[2] = __fmaf_rn(ax, fabsf(rr[r].z), b[2]); b[3] = __fmaf_rn(ax, fabsf(rr[r].w), b[3]);
+    }
+    s_val[tk][warp][lane] = make_float4(a[0], a[1], a[2], a[3]);
+    const float bm = warp_max(fmaxf(fmaxf(b[0], b[1]), fmaxf(b[2], b[3])));
+    if (lane == 0) s_abs[tk][warp] = bm;
+  }
+  __syncthreads();
+  float4 mu = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (ro.mu_rot) mu = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
+  if (warp < nt && s_rec[warp] >= 0) {
+    const int tk = warp;
+    float y[4];
 #pragma unroll
-    for (int w = 0; w < APPEND_ROT_WARPS; ++w) q[w] = DF{part[w][4 * lane + i].x, part[w][4 * lane + i].y};
-    x[i] = df_add(df_add(df_add(q[0], q[1]), df_add(q[2], q[3])), df_add(df_add(q[4], q[5]), df_add(q[6], q[7])));
+    for (int i = 0; i < 4; ++i) {
+      float v[8];
+#pragma unroll
+      for (int w = 0; w < 8; ++w) {
+        const float4 p = s_val[tk][w][lane];
+        v[w] = i == 0 ? p.x : i == 1 ? p.y : i == 2 ? p.z : p.w;
+      }
+      y[i] = ((v[0] + v[1]) + (v[2] + v[3])) + ((v[4] + v[5]) + (v[6] + v[7]));
+    }
+    // sum over warps of each warp's largest partial sum |x R| bounds every output's
+    // sum_c |x_c R_ci|; 16-term chains and a 3-level sum are off by at most 19.1 u of
+    // it, and the computed bound is itself low by at most 20 u: 20 u * 1.0001 covers both
+    const float bound = ((s_abs[tk][0] + s_abs[tk][1]) + (s_abs[tk][2] + s_abs[tk][3])) +
+                        ((s_abs[tk][4] + s_abs[tk][5]) + (s_abs[tk][6] + s_abs[tk][7]));
+    float E = bound * 1.1921e-06f;  // 20 u
+    if (ro.mu_rot) {
+      y[0] = __fsub_rn(y[0], mu.x); y[1] = __fsub_rn(y[1], mu.y);
+      y[2] = __fsub_rn(y[2], mu.z); y[3] = __fsub_rn(y[3], mu.w);
+      E += warp_max(fmaxf(fmaxf(fabsf(y[0]) + fabsf(mu.x), fabsf(y[1]) + fabsf(mu.y)),
+                          fmaxf(fabsf(y[2]) + fabsf(mu.z), fabsf(y[3]) + fabsf(mu.w))) + E) *
+           1.1921e-07f;  // rounding of y - mu (2 u)
+    }
+    QParams qp;
+    unsigned byte = 0u;
+    if (quantize_warp_certain(y, E, ro.clip, qp, byte)) {
+      uint8_t* recp = pool + (size_t)s_rec[tk] * g.record;
+      recp[ro.codes_off + GROUP_BYTES * s_slot[tk] + lane] = (uint8_t)byte;
+      if (lane == 0)
+        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * s_slot[tk]) =
+            (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+    } else if (lane == 0) {
+      s_redo[tk] = 1;
+    }
   }
-  if (ro.mu_rot) {
-    const float4 m = __ldg(reinterpret_cast<const float4*>(ro.mu_rot + (size_t)h * D) + lane);
-    x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
-    x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+  __syncthreads();
+  // ---- double-float redo of the uncertain groups, all warps ----
+  float2* part = reinterpret_cast<float2*>(&s_val[0][0][0]);  // [8 warps][128] (hi, lo)
+  for (int tk = 0; tk < nt; ++tk) {
+    if (!s_redo[tk]) continue;  // uniform: shared flag after a barrier
+    float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      const float xc = s_x[tk][16 * warp + r];
+      const float rv[4] = {rr[r].x, rr[r].y, rr[r].z, rr[r].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float p = __fmul_rn(xc, rv[i]);
+        const float pe = __fmaf_rn(xc, rv[i], -p);
+        const DF q = two_sum(sh[i], p);
+        sh[i] = q.hi;
+        sl[i] = __fadd_rn(sl[i], __fadd_rn(q.lo, pe));
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const DF c = df_norm(sh[i], sl[i]);
+      part[warp * D + 4 * lane + i] = make_float2(c.hi, c.lo);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      DF x[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        DF q[8];
+#pragma unroll
+        for (int w = 0; w < 8; ++w) q[w] = DF{part[w * D + 4 * lane + i].x, part[w * D + 4 * lane + i].y};
+        x[i] = df_add(df_add(df_add(q[0], q[1]), df_add(q[2], q[3])), df_add(df_add(q[4], q[5]), df_add(q[6], q[7])));
+      }
+      if (ro.mu_rot) {
+        x[0] = df_add_f(x[0], -mu.x); x[1] = df_add_f(x[1], -mu.y);
+        x[2] = df_add_f(x[2], -mu.z); x[3] = df_add_f(x[3], -mu.w);
+      }
+      QParams qp;
+      const unsigned byte = quantize_warp_df(x, ro.clip, qp);
+      uint8_t* recp = pool + (size_t)s_rec[tk] * g.record;
+      recp[ro.codes_off + GROUP_BYTES * s_slot[tk] + lane] = (uint8_t)byte;
+      if (lane == 0)
+        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * s_slot[tk]) =
+            (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+    }
+    __syncthreads();
   }
-  QParams qp;
-  const unsigned byte = quantize_warp_df(x, ro.clip, qp);
-  uint8_t* recp = pool + (size_t)rec * g.record;
-  recp[ro.codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
-  if (lane == 0)
-    *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
-        (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+}
+
+// Tokens per CTA of append_dense_step_kernel: about 300 CTAs (two per SM), at most ADS_TB.
+static int dense_step_tokens(int n_new, int n_heads, int n_roles) {
+  const long long groups = (long long)n_new * n_heads * n_roles;
+  long long tb = (groups + 299) / 300;
+  if (tb < 1) tb = 1;
+  if (tb > ADS_TB) tb = ADS_TB;
+  return (int)tb;
 }
 
 // Non-dense roles: the certified kernel (the warp-per-group kernel beyond AF_MAX_HEADS heads).
@@ -664,8 +702,9 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
   const bool kd = rot_k.kind == KVQ_ROT_DENSE, vd = rot_v.kind == KVQ_ROT_DENSE;
   if (!kd && !vd) return launch_append_nondense(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, 2, pool, err, s);
   if (n_new <= APPEND_SMALL_MAX && kd && vd) {
-    append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 2), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(g, n_seqs, dtype, cu_new, start_pos,
-                                                                             table, roles, pool, err);
+    const int tb = dense_step_tokens(n_new, g.n_kv_heads, 2);
+    append_dense_step_kernel<<<dim3((n_new + tb - 1) / tb, g.n_kv_heads, 2), 256, 0, s>>>(
+        g, n_seqs, n_new, tb, dtype, cu_new, start_pos, table, roles, pool, err);
     return cudaGetLastError();
   }
   if (kd && vd) {
@@ -681,8 +720,11 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
     cudaError_t e;
     if (role == 0 ? kd : vd) {
       if (n_new <= APPEND_SMALL_MAX)
-        append_small_dense_kernel<<<dim3(n_new, g.n_kv_heads, 1), 32 * (APPEND_ROT_WARPS + 1), 0, s>>>(
-            g, n_seqs, dtype, cu_new, start_pos, table, one, pool, err);
+        append_dense_step_kernel<<<dim3((n_new + dense_step_tokens(n_new, g.n_kv_heads, 1) - 1) /
+                                            dense_step_tokens(n_new, g.n_kv_heads, 1),
+                                        g.n_kv_heads, 1),
+                                   256, 0, s>>>(g, n_seqs, n_new, dense_step_tokens(n_new, g.n_kv_heads, 1), dtype,
+                                                cu_new, start_pos, table, one, pool, err);
       else
         append_kernel<true><<<grid, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
       e = cudaGetLastError();

@@ -15,7 +15,7 @@ CASES = [
     ("dense", "f32", 8, [33, 250], (0.96, 0.92)),
     ("dense", "bf16", 16, [511, 2, 64], (1.0, 1.0)),
     ("identity", "bf16", 8, [7, 8, 9], (0.8, 0.8)),
-    # at most 128 new tokens per call: the small-append path (one CTA per group)
+    # at most 128 new tokens per call with dense R: the decode-step kernel (certified fp32, double-float redo)
     ("dense", "bf16", 16, [1, 37, 60], (0.95, 0.9)),
     ("dense", "f32", 8, [5, 3, 9], (1.0, 0.85)),
 ]
@@ -45,8 +45,8 @@ def test_quantize_append_matches_oracle(rot, dtype, page, lengths, clips):
 
 @pytest.mark.parametrize("rot,chunks", [("signed_hadamard", 3), ("dense", 3), ("dense", 8)])
 def test_chunked_append_equals_single_append(rot, chunks):
-    # chunks=8 puts <= 128 tokens in each call: the small-append path against the
-    # shared-R path of the single call (double-float either way: equal codes)
+    # chunks=8 puts <= 128 tokens in each call: the decode-step kernel (certified fp32 with a
+    # double-float redo) against the double-float shared-R kernel of the single call: equal codes
     case = W.decode_case(12, [300, 45, 160], 8, 4, 128, rot, "bf16", page_tokens=16, clip_k=0.9, n_cal=128)
     g = gu.GpuCase(case)
     a = g.new_pool()
