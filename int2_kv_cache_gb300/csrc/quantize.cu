@@ -211,7 +211,9 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
 // lanes x 16 channels each (lane j of a group owns channels 16j..16j+15 and so
 // 4 bytes of the packed codes); the Walsh-Hadamard transform runs its four low
 // stages in registers and its three high stages across the 8 lanes, and the
-// paired fp32 instructions of sm_100 (f32x2) do two channels each.  Tasks are
+// paired fp32 instructions of sm_100 (f32x2) do two channels each.  Groups with
+// an uncertain decision are listed in shared memory and redone at the end of
+// the CTA, one warp each, in double-float.  Tasks are
 // (token, head) in token-major order, so a warp's four groups are consecutive
 // input rows.  Per CTA: AF_TOK tokens, located once, and per head the sign
 // masks and the rotated key mean staged in shared memory.
@@ -219,7 +221,7 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
 // ---------------------------------------------------------------------------
 constexpr int AF_TOK = 32;
 constexpr int AF_THREADS = 256;
-constexpr int AF_MAX_HEADS = 192;  // shared-memory staging: 1,028 bytes per head
+constexpr int AF_MAX_HEADS = 192;  // shared-memory staging: 1,156 bytes per head
 constexpr int AF_LPG = 8;          // lanes per group
 
 __device__ __forceinline__ uint64_t f2pk(float a, float b) {
@@ -254,7 +256,7 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
 }
 
 template <int LPG>  // lanes per group: 8 (16 channels each) or 4 (32)
-__global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
+__global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
     PageGeom g, int n_seqs, int n_new, int dtype, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ table, AppendRoles roles,
     uint8_t* __restrict__ pool, unsigned* err) {
@@ -274,12 +276,14 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
   const bool has_mu = ro.mu_rot != nullptr;
   __shared__ long long s_rec[AF_TOK];
   __shared__ int s_slot[AF_TOK];
+  __shared__ int s_nredo;
   extern __shared__ uint32_t s_dyn[];
   // per head: sign-bit masks (fp32 input: word c = channel c; bf16: word w = channels 2w, 2w + 1
-  // in bits 15 / 31), the rotated key mean (or 0), max |mean|
+  // in bits 15 / 31), the rotated key mean (or 0), max |mean|; then the groups to redo
   uint32_t* s_msk = s_dyn;                                  // [H][128]
   float* s_mu = reinterpret_cast<float*>(s_dyn + H * 128);  // [H][128]
   float* s_mumax = s_mu + H * 128;                          // [H]
+  int* s_redo = reinterpret_cast<int*>(s_mumax + H);        // [AF_TOK * H]: token << 8 | head
   if (threadIdx.x < AF_TOK) {
     const int t = t0 + threadIdx.x;
     long long rec = -1;
@@ -288,6 +292,7 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
     s_rec[threadIdx.x] = rec;
     s_slot[threadIdx.x] = slot;
   }
+  if (threadIdx.x == 0) s_nredo = 0;
   for (int i = threadIdx.x; i < H * 128; i += AF_THREADS) {
     const int h = i >> 7, c = i & 127;
     const float* sg = ro.rot.signs + (size_t)h * D;
@@ -463,33 +468,30 @@ __global__ void __launch_bounds__(AF_THREADS) append_fast_kernel(
         *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
             (uint32_t)__half_as_ushort(s16) | ((uint32_t)__half_as_ushort(z16) << 16);
     }
-    // ---- groups with an uncertain decision: the whole warp, in double-float ----
-    unsigned todo = 0u;
-#pragma unroll
-    for (int q = 0; q < GPW; ++q)
-      if ((bad >> (LPG * q)) & GMASK) todo |= 1u << q;
-    while (todo) {
-      const int q = __ffs(todo) - 1;
-      todo &= todo - 1;
-      const int hq = GPW * hb + q;
-      const float4 v = load4(ro.src, ((size_t)(t0 + tl) * H + hq) * D + 4 * lane, dtype);
-      DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
-      rotate_df_warp(x, ro.rot, hq, lane);
-      if (has_mu) {
-        const float4 m = *reinterpret_cast<const float4*>(s_mu + hq * 128 + 4 * lane);
-        x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
-        x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
-      }
-      QParams qp;
-      const unsigned byte = quantize_warp_df(x, ro.clip, qp);
-      uint8_t* recp = pool + (size_t)(rec0 + hq) * g.record;
-      recp[ro.codes_off + GROUP_BYTES * slot + lane] = (uint8_t)byte;
-      if (lane == 0)
-        *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * slot) =
-            (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
-    }
+    // groups with an uncertain decision are listed and redone after the loop
+    if (live && j == 0 && ((bad >> (LPG * gq)) & GMASK) != 0u) s_redo[atomicAdd(&s_nredo, 1)] = (tl << 8) | h;
     tl = tln;
     hb = hbn;
+  }
+  // ---- the listed groups: one warp each, in double-float ----
+  __syncthreads();
+  for (int i = warp; i < s_nredo; i += AF_THREADS / 32) {
+    const int tlq = s_redo[i] >> 8, hq = s_redo[i] & 0xff;
+    const float4 v = load4(ro.src, ((size_t)(t0 + tlq) * H + hq) * D + 4 * lane, dtype);
+    DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+    rotate_df_warp(x, ro.rot, hq, lane);
+    if (has_mu) {
+      const float4 m = *reinterpret_cast<const float4*>(s_mu + hq * 128 + 4 * lane);
+      x[0] = df_add_f(x[0], -m.x); x[1] = df_add_f(x[1], -m.y);
+      x[2] = df_add_f(x[2], -m.z); x[3] = df_add_f(x[3], -m.w);
+    }
+    QParams qp;
+    const unsigned byte = quantize_warp_df(x, ro.clip, qp);
+    uint8_t* recp = pool + (size_t)(s_rec[tlq] + hq) * g.record;
+    recp[ro.codes_off + GROUP_BYTES * s_slot[tlq] + lane] = (uint8_t)byte;
+    if (lane == 0)
+      *reinterpret_cast<uint32_t*>(recp + ro.meta_off + META_BYTES * s_slot[tlq]) =
+          (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
   }
 }
 
@@ -667,11 +669,11 @@ static cudaError_t launch_append_nondense(const PageGeom& g, int n_seqs, int n_n
     append_kernel<false><<<grid, 256, 0, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
     return cudaGetLastError();
   }
-  const size_t smem = (size_t)g.n_kv_heads * 1028;
+  const size_t smem = (size_t)g.n_kv_heads * (1028 + 4 * AF_TOK);
   static bool attr_set = false;
   if (!attr_set) {
     const cudaError_t e = cudaFuncSetAttribute(append_fast_kernel<AF_LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               AF_MAX_HEADS * 1028);
+                                               AF_MAX_HEADS * (1028 + 4 * AF_TOK));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
