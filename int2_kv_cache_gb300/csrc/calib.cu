@@ -17,8 +17,11 @@ namespace kvq {
 
 
 struct CalibWs {
-  float *qf, *qr, *kf, *vf, *xk_hi, *xk_lo, *xv_hi, *xv_lo, *kq, *vq, *o_rot, *o_ref, *o_un, *gram;
+  float *qf, *qr, *kf, *vf, *xk_hi, *xk_lo, *xv_hi, *xv_lo, *kq, *vq, *o_rot, *o_ref, *o_un, *gram, *part;
+  double* gpart;  // [n_groups][(gd / 32)^2] quadratic-form partials
 };
+
+constexpr int CA_SPLIT_MAX = 8;  // key splits of the calibration attention
 
 static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -28,17 +31,20 @@ static CalibWs carve(void* ws, int n_tok, int n_qpos, int n_kv_heads, int gqa, i
   const size_t qn = (size_t)n_qpos * hq * D, kn = (size_t)n_tok * n_kv_heads * D;
   const size_t gd = joint ? hq * D : (size_t)gqa * D;
   const size_t gn = (joint ? 1 : (size_t)n_kv_heads) * gd * gd;
-  const size_t sizes[14] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn};
+  const size_t pn = (size_t)CA_SPLIT_MAX * n_qpos * hq * (D + 4);  // attention partials
+  const size_t gpn = 2 * (joint ? 1 : (size_t)n_kv_heads) * (gd / 32) * (gd / 32);  // doubles, as float pairs
+  const size_t sizes[16] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn, pn, gpn};
   char* p = static_cast<char*>(ws);
-  float* ptrs[14];
+  float* ptrs[16];
   size_t off = 0;
-  for (int i = 0; i < 14; ++i) {
+  for (int i = 0; i < 16; ++i) {
     ptrs[i] = reinterpret_cast<float*>(p + off);
     off += align_up(sizes[i] * sizeof(float));
   }
   if (total) *total = off;
-  return CalibWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6],
-                 ptrs[7], ptrs[8], ptrs[9], ptrs[10], ptrs[11], ptrs[12], ptrs[13]};
+  return CalibWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6], ptrs[7],
+                 ptrs[8], ptrs[9], ptrs[10], ptrs[11], ptrs[12], ptrs[13], ptrs[14],
+                 reinterpret_cast<double*>(ptrs[15])};
 }
 
 size_t calib_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint) {
@@ -57,52 +63,263 @@ __global__ void to_f32_kernel(size_t n, int n_heads, const void* __restrict__ sr
   dst[i] = v;
 }
 
-// Causal attention of the queries at positions n_tok - n_qpos + i against fp32
-// keys/values: one block per (query position, query head).
-__global__ void __launch_bounds__(128) causal_attn_kernel(int n_tok, int n_qpos, int n_kv_heads,
-                                                          int gqa, const float* __restrict__ q,
-                                                          const float* __restrict__ k,
-                                                          const float* __restrict__ v,
-                                                          float* __restrict__ o) {
-  extern __shared__ float sc[];  // [n_tok]
-  __shared__ __align__(16) float qs[D];
-  __shared__ float red[4];
-  const int qi = blockIdx.x, j = blockIdx.y, hq = n_kv_heads * gqa, h = j / gqa;
-  const int t = n_tok - n_qpos + qi;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  qs[tid] = q[((size_t)qi * hq + j) * D + tid] * INV_SQRT_D;
-  __syncthreads();
-  float mloc = -INFINITY;
-  for (int s = tid; s <= t; s += 128) {
-    const float4* kr = reinterpret_cast<const float4*>(k + ((size_t)s * n_kv_heads + h) * D);
-    float a = 0.f;
-#pragma unroll 8
-    for (int c4 = 0; c4 < 32; ++c4) {
-      const float4 kk = __ldg(kr + c4);
-      const float4 qq = reinterpret_cast<const float4*>(qs)[c4];
-      a = fmaf(qq.x, kk.x, a); a = fmaf(qq.y, kk.y, a); a = fmaf(qq.z, kk.z, a); a = fmaf(qq.w, kk.w, a);
+// Causal attention, tiled: a CTA takes the G query heads of KV head h at 64 / G
+// query positions (64 rows) and a range of keys (one of `split` ranges), and
+// streams the keys and values through shared memory 64 tokens at a time
+// (cp.async, double-buffered), with an online softmax per row in fp32.
+// S = Q K^T: thread (ty, tx) owns rows 4ty..4ty+3 x tokens 4tx..4tx+3; O += P V:
+// rows 4ty..4ty+3 x channels 8tx..8tx+7.  With split > 1 each CTA writes the
+// row partials (m, l, unnormalised acc) for calib_attn_combine_kernel.
+// grid = (n_kv_heads, ceil(n_qpos / (64 / G)), split), block = 256.
+constexpr int CA_ROWS = 64, CA_KT = 64, CA_KS = D + 4;  // K rows padded: conflict-free column reads
+constexpr int CA_SMEM = (CA_ROWS * D + 2 * CA_KT * CA_KS + 2 * CA_KT * D + CA_ROWS * (CA_KT + 4) + 3 * CA_ROWS) * 4;
+
+__device__ __forceinline__ void ca_cp16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"((uint32_t)__cvta_generic_to_shared(dst)), "l"(src)
+               : "memory");
+}
+
+template <int G>
+__global__ void __launch_bounds__(256, 1) calib_attn_tiled_kernel(int n_tok, int n_qpos, int n_kv_heads, int split,
+                                                                  const float* __restrict__ q,
+                                                                  const float* __restrict__ k,
+                                                                  const float* __restrict__ v, float* __restrict__ o,
+                                                                  float* __restrict__ part) {
+  constexpr int QB = CA_ROWS / G;  // query positions per CTA
+  extern __shared__ __align__(16) float ca_smem[];
+  float* sq = ca_smem;                          // [64][128] queries / sqrt(128)
+  float* sk = sq + CA_ROWS * D;                 // [2][64][132]
+  float* sv = sk + 2 * CA_KT * CA_KS;           // [2][64][128]
+  float* sp = sv + 2 * CA_KT * D;               // [64][68] probabilities
+  float* sm = sp + CA_ROWS * (CA_KT + 4);       // [64] running max
+  float* sl = sm + CA_ROWS;                     // [64] running sum
+  float* ss = sl + CA_ROWS;                     // [64] rescale of this tile
+  const int h = blockIdx.x, qb0 = blockIdx.y * QB, sidx = blockIdx.z;
+  const int hq = n_kv_heads * G;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  // rows r = G * (position - qb0) + head offset
+  for (int i = tid; i < CA_ROWS * D / 4; i += 256) {
+    const int r = i / (D / 4), c4 = i % (D / 4);
+    const int qi = qb0 + r / G, j = h * G + r % G;
+    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (qi < n_qpos) x = reinterpret_cast<const float4*>(q + ((size_t)qi * hq + j) * D)[c4];
+    x.x *= INV_SQRT_D; x.y *= INV_SQRT_D; x.z *= INV_SQRT_D; x.w *= INV_SQRT_D;
+    reinterpret_cast<float4*>(sq + r * D)[c4] = x;
+  }
+  if (tid < CA_ROWS) {
+    sm[tid] = -INFINITY;
+    sl[tid] = 0.f;
+  }
+  // the keys of this split, limited by the last (causal) position of the CTA's rows
+  const int last_q = min(n_qpos, qb0 + QB) - 1;
+  const int t_max = n_tok - n_qpos + last_q;  // inclusive
+  const int n_tiles_all = (n_tok + CA_KT - 1) / CA_KT;
+  const int per = (n_tiles_all + split - 1) / split;
+  const int tile0 = sidx * per;
+  const int tile1 = min(min(n_tiles_all, tile0 + per), t_max / CA_KT + 1);
+  auto load_tile = [&](int tile, int buf) {
+    const int s0 = tile * CA_KT;
+    for (int i = tid; i < CA_KT * D / 4; i += 256) {
+      const int r = i / (D / 4), c4 = i % (D / 4);
+      const int s = min(s0 + r, n_tok - 1);  // rows past the end are masked below
+      ca_cp16(sk + (buf * CA_KT + r) * CA_KS + 4 * c4, k + ((size_t)s * n_kv_heads + h) * D + 4 * c4);
+      ca_cp16(sv + (buf * CA_KT + r) * D + 4 * c4, v + ((size_t)s * n_kv_heads + h) * D + 4 * c4);
     }
-    sc[s] = a;
-    mloc = fmaxf(mloc, a);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  float acc[4][8];
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+  if (tile0 < tile1) load_tile(tile0, 0);
+  __syncthreads();
+  for (int tile = tile0; tile < tile1; ++tile) {
+    const int buf = (tile - tile0) & 1;
+    if (tile + 1 < tile1) {
+      load_tile(tile + 1, buf ^ 1);
+      asm volatile("cp.async.wait_group 1;" ::: "memory");
+    } else {
+      asm volatile("cp.async.wait_group 0;" ::: "memory");
+    }
+    __syncthreads();
+    // ---- scores ----
+    const float* kb = sk + buf * CA_KT * CA_KS;
+    float sc[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) sc[a][b] = 0.f;
+#pragma unroll 4
+    for (int c4 = 0; c4 < D / 4; ++c4) {
+      float4 qa[4], kk[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) qa[a] = reinterpret_cast<const float4*>(sq + (4 * ty + a) * D)[c4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) kk[b] = reinterpret_cast<const float4*>(kb + (4 * tx + b) * CA_KS)[c4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          sc[a][b] = fmaf(qa[a].x, kk[b].x, sc[a][b]);
+          sc[a][b] = fmaf(qa[a].y, kk[b].y, sc[a][b]);
+          sc[a][b] = fmaf(qa[a].z, kk[b].z, sc[a][b]);
+          sc[a][b] = fmaf(qa[a].w, kk[b].w, sc[a][b]);
+        }
+    }
+    // ---- causal mask, online softmax (16 threads per row group) ----
+    const int s0 = tile * CA_KT;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const int r = 4 * ty + a;
+      const int qi = qb0 + r / G;
+      const int tpos = n_tok - n_qpos + qi;  // keys s <= tpos
+      float mx = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int s = s0 + 4 * tx + b;
+        if (s > tpos || s >= n_tok || qi >= n_qpos) sc[a][b] = -INFINITY;
+        mx = fmaxf(mx, sc[a][b]);
+      }
+#pragma unroll
+      for (int m = 1; m < 16; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+      const float mold = sm[r];
+      const float mnew = fmaxf(mold, mx);
+      float psum = 0.f;
+      float4 pv;
+      float pr[4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        pr[b] = mnew == -INFINITY ? 0.f : __expf(sc[a][b] - mnew);
+        psum += pr[b];
+      }
+      pv = make_float4(pr[0], pr[1], pr[2], pr[3]);
+      reinterpret_cast<float4*>(sp + r * (CA_KT + 4))[tx] = pv;
+#pragma unroll
+      for (int m = 1; m < 16; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
+      __syncwarp();
+      if (tx == 0) {
+        const float scale = mold == -INFINITY ? 0.f : __expf(mold - mnew);
+        ss[r] = scale;
+        sl[r] = sl[r] * scale + psum;
+        sm[r] = mnew;
+      }
+    }
+    __syncthreads();
+    // ---- O = O * scale + P V ----
+    const float* vb = sv + buf * CA_KT * D;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const float f = ss[4 * ty + a];
+#pragma unroll
+      for (int b = 0; b < 8; ++b) acc[a][b] *= f;
+    }
+#pragma unroll 4
+    for (int s4 = 0; s4 < CA_KT / 4; ++s4) {
+      float4 pa[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) pa[a] = reinterpret_cast<const float4*>(sp + (4 * ty + a) * (CA_KT + 4))[s4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const float4 v0 = reinterpret_cast<const float4*>(vb + (4 * s4 + u) * D)[2 * tx];
+        const float4 v1 = reinterpret_cast<const float4*>(vb + (4 * s4 + u) * D)[2 * tx + 1];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float p = u == 0 ? pa[a].x : u == 1 ? pa[a].y : u == 2 ? pa[a].z : pa[a].w;
+          acc[a][0] = fmaf(p, v0.x, acc[a][0]); acc[a][1] = fmaf(p, v0.y, acc[a][1]);
+          acc[a][2] = fmaf(p, v0.z, acc[a][2]); acc[a][3] = fmaf(p, v0.w, acc[a][3]);
+          acc[a][4] = fmaf(p, v1.x, acc[a][4]); acc[a][5] = fmaf(p, v1.y, acc[a][5]);
+          acc[a][6] = fmaf(p, v1.z, acc[a][6]); acc[a][7] = fmaf(p, v1.w, acc[a][7]);
+        }
+      }
+    }
+    __syncthreads();  // the buffer and P are reused by the next tile
   }
-  mloc = warp_max(mloc);
-  if (lane == 0) red[warp] = mloc;
-  __syncthreads();
-  const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-  __syncthreads();
-  float sloc = 0.f;
-  for (int s = tid; s <= t; s += 128) {
-    const float e = __expf(sc[s] - M);
-    sc[s] = e;
-    sloc += e;
+  // ---- output: normalised rows (one split) or row partials ----
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const int r = 4 * ty + a;
+    const int qi = qb0 + r / G, j = h * G + r % G;
+    if (qi >= n_qpos) continue;
+    const size_t row = (size_t)qi * hq + j;
+    if (split == 1) {
+      const float inv = sl[r] > 0.f ? 1.f / sl[r] : 0.f;
+      float4* dst = reinterpret_cast<float4*>(o + row * D) + 2 * tx;
+      dst[0] = make_float4(acc[a][0] * inv, acc[a][1] * inv, acc[a][2] * inv, acc[a][3] * inv);
+      dst[1] = make_float4(acc[a][4] * inv, acc[a][5] * inv, acc[a][6] * inv, acc[a][7] * inv);
+    } else {
+      float* pp = part + ((size_t)sidx * n_qpos * hq + row) * (D + 4);
+      float4* dst = reinterpret_cast<float4*>(pp) + 2 * tx;
+      dst[0] = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+      dst[1] = make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
+      if (tx == 0) {
+        pp[D] = sm[r];
+        pp[D + 1] = sl[r];
+      }
+    }
   }
-  sloc = warp_sum(sloc);
-  if (lane == 0) red[warp] = sloc;
-  __syncthreads();
-  const float L = red[0] + red[1] + red[2] + red[3];
-  float acc = 0.f;
-  for (int s = 0; s <= t; ++s) acc = fmaf(sc[s], v[((size_t)s * n_kv_heads + h) * D + tid], acc);
-  o[((size_t)qi * hq + j) * D + tid] = acc / L;
+}
+
+// Log-sum-exp merge of the split partials of calib_attn_tiled_kernel, in split
+// order.  One warp per (query position, query head); lane l: channels 4l..4l+3.
+__global__ void calib_attn_combine_kernel(int n_rows, int split, const float* __restrict__ part,
+                                          float* __restrict__ o) {
+  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (row >= n_rows) return;
+  float M = -INFINITY;
+  for (int s = 0; s < split; ++s) M = fmaxf(M, part[((size_t)s * n_rows + row) * (D + 4) + D]);
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L = 0.f;
+  if (M != -INFINITY) {
+    for (int s = 0; s < split; ++s) {
+      const float* pp = part + ((size_t)s * n_rows + row) * (D + 4);
+      const float m = pp[D];
+      if (m == -INFINITY) continue;
+      const float e = __expf(m - M);
+      const float4 x = reinterpret_cast<const float4*>(pp)[lane];
+      L = fmaf(e, pp[D + 1], L);
+      a.x = fmaf(e, x.x, a.x); a.y = fmaf(e, x.y, a.y); a.z = fmaf(e, x.z, a.z); a.w = fmaf(e, x.w, a.w);
+    }
+  }
+  const float inv = L > 0.f ? 1.f / L : 0.f;
+  reinterpret_cast<float4*>(o + (size_t)row * D)[lane] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
+}
+
+template <int G>
+static cudaError_t launch_calib_attn_g(int n_tok, int n_qpos, int n_kv_heads, const float* q, const float* k,
+                                       const float* v, float* o, float* part, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    const cudaError_t e =
+        cudaFuncSetAttribute(calib_attn_tiled_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, CA_SMEM);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  constexpr int QB = CA_ROWS / G;
+  const int nqb = (n_qpos + QB - 1) / QB;
+  const int n_tiles = (n_tok + CA_KT - 1) / CA_KT;
+  int split = 152 / (n_kv_heads * nqb);  // about one CTA per SM
+  if (split > CA_SPLIT_MAX) split = CA_SPLIT_MAX;
+  if (split > n_tiles) split = n_tiles;
+  if (split < 1) split = 1;
+  calib_attn_tiled_kernel<G><<<dim3(n_kv_heads, nqb, split), 256, CA_SMEM, s>>>(n_tok, n_qpos, n_kv_heads, split, q, k,
+                                                                                 v, o, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || split == 1) return e;
+  const int rows = n_qpos * n_kv_heads * G;
+  calib_attn_combine_kernel<<<(rows + 7) / 8, 256, 0, s>>>(rows, split, part, o);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_calib_attn(int n_tok, int n_qpos, int n_kv_heads, int gqa, const float* q, const float* k,
+                                     const float* v, float* o, float* part, cudaStream_t s) {
+  switch (gqa) {
+    case 1: return launch_calib_attn_g<1>(n_tok, n_qpos, n_kv_heads, q, k, v, o, part, s);
+    case 2: return launch_calib_attn_g<2>(n_tok, n_qpos, n_kv_heads, q, k, v, o, part, s);
+    case 4: return launch_calib_attn_g<4>(n_tok, n_qpos, n_kv_heads, q, k, v, o, part, s);
+    case 8: return launch_calib_attn_g<8>(n_tok, n_qpos, n_kv_heads, q, k, v, o, part, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 // Gram matrices G_g = W_g^T W_g for head groups g of gd = cols columns each.
@@ -136,34 +353,73 @@ __global__ void __launch_bounds__(256) gram_kernel(int d_model, int total_cols, 
     gram[((size_t)grp * gd + a0 + ty + 8 * r) * gd + b0 + tx] = acc[r];
 }
 
-// out[slot] += sum over (position, group) of du G du^T with du = (a - b) (or a when b == NULL).
-// grid = (n_qpos, n_groups), block = 256.
-__global__ void __launch_bounds__(256) gram_form_kernel(int n_qpos, int n_groups, int gd,
-                                                        const float* __restrict__ a,
-                                                        const float* __restrict__ b,
-                                                        const float* __restrict__ gram,
-                                                        double* __restrict__ out) {
-  extern __shared__ float du[];  // [gd]
-  __shared__ float red[8];
-  const int qi = blockIdx.x, grp = blockIdx.y, tid = threadIdx.x;
-  const size_t base = ((size_t)qi * n_groups + grp) * gd;
-  for (int i = tid; i < gd; i += 256) du[i] = b ? a[base + i] - b[base + i] : a[base + i];
-  __syncthreads();
-  const float* G = gram + (size_t)grp * gd * gd;
-  float part = 0.f;
-  for (int c = tid; c < gd; c += 256) {
-    float wsum = 0.f;
-    for (int r = 0; r < gd; ++r) wsum = fmaf(G[(size_t)r * gd + c], du[r], wsum);
-    part = fmaf(wsum, du[c], part);
+// sum over positions p of du_p G du_p^T (du = a - b, or a when b == NULL) as
+// trace(G M) with M = sum_p du_p^T du_p: block (ri, ci, group) forms the 32 x 32
+// tile of M over all positions and adds G o M over the tile in double ->
+// part[group][ri * nt + ci]; gram_reduce_kernel adds the tiles in a fixed order.
+// grid = (gd / 32, gd / 32, n_groups), block = 256.
+__global__ void __launch_bounds__(256) gram_trace_kernel(int n_qpos, int n_groups, int gd,
+                                                         const float* __restrict__ a,
+                                                         const float* __restrict__ b,
+                                                         const float* __restrict__ gram,
+                                                         double* __restrict__ part) {
+  __shared__ float sr[64][33], sc[64][33];  // du of 64 positions at the tile's rows / columns
+  __shared__ double sred[8];
+  const int ci = blockIdx.x, ri = blockIdx.y, grp = blockIdx.z, tid = threadIdx.x;
+  const int tx = tid & 31, ty = tid >> 5;  // column tx, rows ty + 8 i
+  const int r0 = 32 * ri, c0 = 32 * ci;
+  float m[4] = {0.f, 0.f, 0.f, 0.f};
+  for (int p0 = 0; p0 < n_qpos; p0 += 64) {
+    for (int i = tid; i < 64 * 32; i += 256) {
+      const int pp = i >> 5, k = i & 31, qi = p0 + pp;
+      float xr = 0.f, xc = 0.f;
+      if (qi < n_qpos) {
+        const size_t base = ((size_t)qi * n_groups + grp) * gd;
+        xr = b ? a[base + r0 + k] - b[base + r0 + k] : a[base + r0 + k];
+        xc = b ? a[base + c0 + k] - b[base + c0 + k] : a[base + c0 + k];
+      }
+      sr[pp][k] = xr;
+      sc[pp][k] = xc;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int pp = 0; pp < 64; ++pp) {
+      const float xc = sc[pp][tx];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) m[i] = fmaf(sr[pp][ty + 8 * i], xc, m[i]);
+    }
+    __syncthreads();
   }
-  part = warp_sum(part);
-  if ((tid & 31) == 0) red[tid >> 5] = part;
+  double acc = 0.0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    acc += (double)m[i] * (double)gram[((size_t)grp * gd + r0 + ty + 8 * i) * gd + c0 + tx];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (tx == 0) sred[ty] = acc;
   __syncthreads();
   if (tid == 0) {
-    double s = 0.0;
-    for (int i = 0; i < 8; ++i) s += (double)red[i];
-    atomicAdd(out + grp, s);
+    double t = 0.0;
+    for (int i = 0; i < 8; ++i) t += sred[i];
+    part[((size_t)grp * gridDim.y + ri) * gridDim.x + ci] = t;
   }
+}
+
+// out[g] = sum of part[g][:] (n_tiles values): 256 strided partial sums, then a
+// fixed tree (deterministic).  One block per group.
+__global__ void __launch_bounds__(256) gram_reduce_kernel(int n_tiles, const double* __restrict__ part,
+                                                          double* __restrict__ out) {
+  __shared__ double sh[256];
+  const int g = blockIdx.x, tid = threadIdx.x;
+  double t = 0.0;
+  for (int i = tid; i < n_tiles; i += 256) t += part[(size_t)g * n_tiles + i];
+  sh[tid] = t;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (tid < w) sh[tid] += sh[tid + w];
+    __syncthreads();
+  }
+  if (tid == 0) out[g] = sh[0];
 }
 
 // out[slot] += sum over (position, group) of ||du W_g^T||^2 computed directly
@@ -231,11 +487,8 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
   to_f32_kernel<<<blocks(kn), 256, 0, s>>>(kn, n_kv_heads, k, dtype, nullptr, w.kf);
   to_f32_kernel<<<blocks(kn), 256, 0, s>>>(kn, n_kv_heads, v, dtype, nullptr, w.vf);
   KVQ_TRY(cudaSuccess);
-  const size_t attn_smem = (size_t)n_tok * sizeof(float);
   // reference readout with unquantized, unrotated, uncentred keys and values
-  causal_attn_kernel<<<dim3(n_qpos, hq), 128, attn_smem, s>>>(n_tok, n_qpos, n_kv_heads, gqa, w.qf,
-                                                              w.kf, w.vf, w.o_ref);
-  KVQ_TRY(cudaSuccess);
+  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qf, w.kf, w.vf, w.o_ref, w.part, s));
   // ||du W^T||^2: directly when d_model <= gd, else through the group's Gram matrix
   const bool direct = d_model <= gd;
   if (!direct)
@@ -249,8 +502,10 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
     if (direct)
       proj_err_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, d_model, a, b, w_o,
                                                                      w_dtype, dst);
-    else
-      gram_form_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, a, b, w.gram, dst);
+    else {
+      gram_trace_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(n_qpos, n_groups, gd, a, b, w.gram, w.gpart);
+      gram_reduce_kernel<<<n_groups, 256, 0, s>>>((gd / 32) * (gd / 32), w.gpart, dst);
+    }
   };
   out_err(w.o_ref, nullptr, ref);
   KVQ_TRY(cudaSuccess);
@@ -263,9 +518,7 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
     for (int c = 0; c < n_clip; ++c) {
       KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clips[c], w.kq, s));
       KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clips[c], w.vq, s));
-      causal_attn_kernel<<<dim3(n_qpos, hq), 128, attn_smem, s>>>(n_tok, n_qpos, n_kv_heads, gqa,
-                                                                  w.qr, w.kq, w.vq, w.o_rot);
-      KVQ_TRY(cudaSuccess);
+      KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qr, w.kq, w.vq, w.o_rot, w.part, s));
       KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.o_rot, r, w.o_un, true, s));
       double* slot = nmse + (size_t)(i * n_clip + c) * n_groups;
       out_err(w.o_un, w.o_ref, slot);

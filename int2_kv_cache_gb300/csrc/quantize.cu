@@ -42,10 +42,73 @@ __global__ void rotate_heads_kernel(int n_rows, int n_heads, int hpr, const floa
   reinterpret_cast<float4*>(y + (size_t)warp * D)[lane] = v;
 }
 
+// Dense R, batched: one CTA per (rotation head rh, block of 32 of its n_rows x
+// hpr vectors) stages R_rh (or its transpose) in shared memory once; thread t
+// forms output channels 4 (t % 32) .. + 3 of vectors t / 32 + 8 i (i < 4).
+constexpr int RH_VB = 32;
+__global__ void __launch_bounds__(256) rotate_heads_dense_kernel(int n_rows, int n_heads, int hpr, const float* x,
+                                                                 const float* __restrict__ dense, float* y,
+                                                                 bool transpose) {
+  extern __shared__ float rh_smem[];
+  float* sR = rh_smem;            // [128][128]: row c = the weights of input channel c
+  float* sx = rh_smem + D * D;    // [RH_VB][128]
+  const int rh = blockIdx.y, vb0 = blockIdx.x * RH_VB, tid = threadIdx.x;
+  const int n_vec = n_rows * hpr;
+  const float* R = dense + (size_t)rh * D * D;
+  for (int i = tid; i < D * D; i += 256) {
+    const int r = i >> 7, c = i & 127;
+    sR[i] = transpose ? __ldg(R + (size_t)c * D + r) : __ldg(R + i);
+  }
+  auto vec_index = [&](int vv) {  // vector vv of this rotation head -> row in x
+    const int row = vv / hpr, jj = rh * hpr + vv % hpr;
+    return (size_t)row * n_heads + jj;
+  };
+  for (int i = tid; i < RH_VB * D / 4; i += 256) {
+    const int vv = vb0 + i / (D / 4), c4 = i % (D / 4);
+    const float4 v = vv < n_vec ? reinterpret_cast<const float4*>(x + vec_index(vv) * D)[c4]
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+    reinterpret_cast<float4*>(sx + (i / (D / 4)) * D)[c4] = v;
+  }
+  __syncthreads();
+  const int lane = tid & 31, vw = tid >> 5;
+  float4 acc[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+  for (int c = 0; c < D; ++c) {
+    const float4 r = reinterpret_cast<const float4*>(sR + c * D)[lane];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float xc = sx[(vw + 8 * i) * D + c];
+      acc[i].x = fmaf(xc, r.x, acc[i].x); acc[i].y = fmaf(xc, r.y, acc[i].y);
+      acc[i].z = fmaf(xc, r.z, acc[i].z); acc[i].w = fmaf(xc, r.w, acc[i].w);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int vv = vb0 + vw + 8 * i;
+    if (vv < n_vec) reinterpret_cast<float4*>(y + vec_index(vv) * D)[lane] = acc[i];
+  }
+}
+
 cudaError_t launch_rotate_heads(int n_rows, int n_heads, int heads_per_rot, const float* x,
                                 RotDev rot, float* y, bool transpose, cudaStream_t s) {
   long long warps = (long long)n_rows * n_heads;
   if (warps == 0) return cudaSuccess;
+  if (rot.kind == KVQ_ROT_DENSE && x != y) {
+    constexpr int smem = (D * D + RH_VB * D) * (int)sizeof(float);
+    static bool attr = false;
+    if (!attr) {
+      const cudaError_t e = cudaFuncSetAttribute(rotate_heads_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (e != cudaSuccess) return e;
+      attr = true;
+    }
+    const int n_rot = n_heads / heads_per_rot;
+    const int n_vec = n_rows * heads_per_rot;
+    rotate_heads_dense_kernel<<<dim3((n_vec + RH_VB - 1) / RH_VB, n_rot), 256, smem, s>>>(
+        n_rows, n_heads, heads_per_rot, x, rot.dense, y, transpose);
+    return cudaGetLastError();
+  }
   int blocks = (int)((warps * 32 + 255) / 256);
   rotate_heads_kernel<<<blocks, 256, 0, s>>>(n_rows, n_heads, heads_per_rot, x, rot, y, transpose);
   return cudaGetLastError();
