@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
   const uint64_t pinv = f2pk(INV_SQRT_D, INV_SQRT_D);
   const uint64_t pmagic = f2pk(12582912.f, 12582912.f);  // 1.5 * 2^23: adding it rounds to an integer
   const int n_hb = (H + GPW - 1) / GPW;
-  // a warp iteration: token tl, heads GPW hb .. GPW hb + GPW - 1 (warp w: tokens w, w + 8, ...)
+  // a warp iteration: token tl, heads GPW hb .. GPW hb + GPW - 1
   auto fetch = [&](int tlk, int hbk, uint4 (&raw)[NQ]) {
     const int hk = GPW * hbk + gq;
 #pragma unroll
@@ -397,15 +397,26 @@ __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
       }
     }
   };
+  // warp w takes the (token, head block) pairs w, w + 8, ... (a one-token append still
+  // spreads its head blocks over the warps)
+  constexpr int NWARP = AF_THREADS / 32;
+  const int n_pairs = nt * n_hb;
+  const int q8 = NWARP / n_hb, r8 = NWARP - q8 * n_hb;  // the pair step in (token, head block)
   uint4 nxt[NQ];
-  int tl = warp, hb = 0;
-  fetch(tl, hb, nxt);
-  while (tl < nt) {
+  int pi = warp;
+  int tl = pi / n_hb, hb = pi - tl * n_hb;
+  if (pi < n_pairs) fetch(tl, hb, nxt);
+  while (pi < n_pairs) {
     uint4 cur[NQ];
 #pragma unroll
     for (int q = 0; q < NQ; ++q) cur[q] = nxt[q];
-    const int tln = hb + 1 < n_hb ? tl : tl + AF_THREADS / 32, hbn = hb + 1 < n_hb ? hb + 1 : 0;
-    if (tln < nt) fetch(tln, hbn, nxt);
+    const int pin = pi + NWARP;
+    int tln = tl + q8, hbn = hb + r8;
+    if (hbn >= n_hb) {
+      hbn -= n_hb;
+      ++tln;
+    }
+    if (pin < n_pairs) fetch(tln, hbn, nxt);
     const int h = GPW * hb + gq;
     const long long rec0 = s_rec[tl];
     const bool live = h < H && rec0 >= 0;
@@ -533,6 +544,7 @@ __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
     }
     // groups with an uncertain decision are listed and redone after the loop
     if (live && j == 0 && ((bad >> (LPG * gq)) & GMASK) != 0u) s_redo[atomicAdd(&s_nredo, 1)] = (tl << 8) | h;
+    pi = pin;
     tl = tln;
     hb = hbn;
   }
