@@ -44,7 +44,8 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    p.add_argument("--case", choices=["decode_step", "append_chunk", "calib"], default="decode_step")
+    p.add_argument("--case", choices=["decode_step", "append_chunk", "append_chunk_dense", "calib"],
+                   default="decode_step")
     p.add_argument("--workload", choices=["gqa8b", "long4b", "serve14b"], default="gqa8b",
                    help="decode-step shape: gqa8b (default, the headline), long4b (128K), serve14b (ragged)")
     p.add_argument("--seqs", type=int, default=None, help="sequences (default: 16 gqa8b, 1 long4b, 64 serve14b)")
@@ -484,13 +485,15 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 
 def run_append_chunk(args):
-    """4,096-token prefill append per sequence (4B-class layer, signed Hadamard, clip 0.9)."""
+    """4,096-token prefill append per sequence: 4 sequences of the 4B-class layer (signed
+    Hadamard, clip 0.9), or with --case append_chunk_dense of the 8B-class layer (dense R)."""
     import torch
     import int2_kv_cache_gb300 as kvq
     from int2_kv_cache_gb300 import workloads as W
     device = "cuda:0"
     n_seq = 4
-    c = W.long4b_128k(n_seqs=n_seq, ctx=4096)
+    dense = args.case == "append_chunk_dense"
+    c = W.gqa8b_32k(n_seqs=n_seq, ctx=4096) if dense else W.long4b_128k(n_seqs=n_seq, ctx=4096)
     t = lambda x, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(device).to(dt)
     lay = kvq.make_layout(16, 8, 32, c.num_blocks, c.block_table.shape[1])
     pool = torch.zeros(kvq.kvq_pool_bytes(lay), dtype=torch.uint8, device=device)
@@ -518,7 +521,7 @@ def run_append_chunk(args):
     ms = e0.elapsed_time(e1) / args.steps
     bytes_ = n_seq * 4096 * 8 * (2 * 256 + 72) + 8 * 128 * 4 * 2
     peak, kind = peaks()
-    print(json.dumps({"case": "append_chunk", "ms": ms, "tokens": n_seq * 4096, "bytes": bytes_,
+    print(json.dumps({"case": args.case, "ms": ms, "tokens": n_seq * 4096, "bytes": bytes_,
                       "gbs": bytes_ / ms / 1e6, "frac": bytes_ / ms / 1e6 / peak, "peak_kind": kind}), flush=True)
 
 
@@ -560,7 +563,7 @@ def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
-    elif args.case == "append_chunk":
+    elif args.case in ("append_chunk", "append_chunk_dense"):
         run_append_chunk(args)
     elif args.case == "calib":
         run_calib(args)

@@ -219,11 +219,23 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
     s_rec[threadIdx.x] = rec;
     s_slot[threadIdx.x] = slot;
   }
+  __shared__ float s_cn[4];  // dense: largest column norm of R_h (from 4 partial maxima)
   if (DENSE) {
     const float4* src = reinterpret_cast<const float4*>(ro.rot.dense + (size_t)h * D * D);
     for (int i = threadIdx.x; i < D * D / 4; i += 256) s_r4[i] = __ldg(src + i);
+    __syncthreads();
+    // column norms, for the Cauchy-Schwarz bound of the fp32 products below
+    if (threadIdx.x < D) {
+      const float* sr = reinterpret_cast<const float*>(s_r4);
+      float ss = 0.f;
+      for (int r = 0; r < D; ++r) ss = fmaf(sr[r * D + threadIdx.x], sr[r * D + threadIdx.x], ss);
+      const float cn = warp_max(sqrtf(ss));
+      if (lane == 0) s_cn[warp] = cn;
+    }
   }
   __syncthreads();
+  // largest column norm, with margin for its own rounding
+  const float cn_max = DENSE ? fmaxf(fmaxf(s_cn[0], s_cn[1]), fmaxf(s_cn[2], s_cn[3])) * 1.0001f : 0.f;
   for (int t = t0 + warp; t < t1; t += 8) {
     if (s_rec[t - t0] < 0) continue;
     const long long rec = s_rec[t - t0] + h;
@@ -246,6 +258,40 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
         E += (warp_max(fmaxf(fmaxf(fabsf(v.x) + fabsf(m.x), fabsf(v.y) + fabsf(m.y)),
                              fmaxf(fabsf(v.z) + fabsf(m.z), fabsf(v.w) + fabsf(m.w)))) +
               E * 524288.f) * P2_M22;
+      }
+      done = quantize_warp_certain(y, E, ro.clip, qp, byte);
+    } else {
+      // certified fp32 with a dense R: four FMA chains of 32 terms (channel 4m + u in
+      // chain u) and a 2-level sum are off by at most 34.1 u sum_c |x_c R_ci|
+      // <= 34.1 u ||x|| ||R_:,i|| (Cauchy-Schwarz): charged 36 u ||x|| max_i ||R_:,i||
+      const float xin[4] = {v.x, v.y, v.z, v.w};
+      float sh[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) sh[u][i] = 0.f;
+#pragma unroll 2
+      for (int mm = 0; mm < 32; ++mm) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float xh = __shfl_sync(0xffffffffu, xin[u], mm);  // channel 4mm + u lives in lane mm
+          const float4 r4 = s_r4[(4 * mm + u) * 32 + lane];
+          sh[u][0] = __fmaf_rn(xh, r4.x, sh[u][0]); sh[u][1] = __fmaf_rn(xh, r4.y, sh[u][1]);
+          sh[u][2] = __fmaf_rn(xh, r4.z, sh[u][2]); sh[u][3] = __fmaf_rn(xh, r4.w, sh[u][3]);
+        }
+      }
+      float y[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) y[i] = (sh[0][i] + sh[1][i]) + (sh[2][i] + sh[3][i]);
+      const float nrm = sqrtf(warp_sum(v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w)) * 1.0001f;
+      float E = nrm * cn_max * 2.1458e-06f;  // 36 u
+      if (ro.mu_rot) {
+        y[0] = __fsub_rn(y[0], m.x); y[1] = __fsub_rn(y[1], m.y);
+        y[2] = __fsub_rn(y[2], m.z); y[3] = __fsub_rn(y[3], m.w);
+        // the subtraction's rounding: 2 u (|y| + |mu|)
+        E += warp_max(fmaxf(fmaxf(fabsf(y[0]) + fabsf(m.x), fabsf(y[1]) + fabsf(m.y)),
+                            fmaxf(fabsf(y[2]) + fabsf(m.z), fabsf(y[3]) + fabsf(m.w))) + E) *
+             1.1921e-07f;
       }
       done = quantize_warp_certain(y, E, ro.clip, qp, byte);
     }
