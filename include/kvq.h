@@ -212,7 +212,10 @@ kvq_status kvq_fold_wo(int d_model, int n_q_heads, int n_kv_heads, const void* w
 /* Output projection (OptR Eqs. 3, 7, 31): y[r] = sum_k x[r][k] w[n][k] for n < d_model,
  * i.e. y = x W^T with x = o_rot viewed as [n_rows][n_q_heads*128] and W = the folded W_O.
  *   x: float [n_rows][k_dim]; w: [d_model][k_dim] of w_dtype; y: float [n_rows][d_model].
- * k_dim must be a multiple of 32 (it is n_q_heads * 128); otherwise KVQ_EUNSUPPORTED. */
+ * k_dim must be a multiple of 32 (it is n_q_heads * 128); otherwise KVQ_EUNSUPPORTED.
+ * Tensor-core products with fp32 accumulation: x enters as a bf16 high part plus a bf16
+ * remainder (about 16 significant bits), an fp32 w as two bf16 parts likewise; partial sums
+ * over K are added in a fixed order, so the result does not depend on timing. */
 kvq_status kvq_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
                         kvq_dtype w_dtype, float* y, kvq_stream stream);
 

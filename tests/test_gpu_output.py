@@ -62,3 +62,19 @@ def test_folded_projection_of_rotated_readout_equals_unrotated():
     y = torch.empty(3, dm, device="cuda")
     kvq.kvq_out_proj(gu.dev(o_rot).reshape(3, -1), wf, y)
     assert gu.normwise_err(y.cpu().numpy(), oracle.output.out_proj(o, w)) < 1e-4
+
+
+@pytest.mark.parametrize("rows,dm,k", [(70, 300, 96), (1, 129, 32), (64, 1000, 160), (65, 256, 4096)])
+def test_out_proj_ragged_k_and_passes(rows, dm, k):
+    """K not a multiple of the 64-column stage (the last stage reads zeros past the edge),
+    d_model not a multiple of the 128-row tile, and row counts around the 64-row pass."""
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    rng = np.random.default_rng(rows * 7 + k)
+    w = (rng.standard_normal((dm, k)) / np.sqrt(k)).astype(np.float32)
+    w = torch.from_numpy(w).to(torch.bfloat16).float().numpy()  # bf16-exact weights
+    x = rng.standard_normal((rows, k)).astype(np.float32)
+    y = torch.empty(rows, dm, device="cuda")
+    kvq.kvq_out_proj(gu.dev(x), gu.dev(w, "bf16"), y)
+    ref = x.astype(np.float64) @ w.astype(np.float64).T
+    assert gu.normwise_err(y.cpu().numpy(), ref) <= gu.OUT_TOL
