@@ -215,9 +215,12 @@ constexpr int OPT_WBYTES = OPT_BM * 128;  // one W stage: 128 rows x 64 bf16
 __host__ __device__ constexpr int opt_xbytes(int nrp) { return 256 * nrp; }  // x stage: NRP rows x 64 fp32
 __host__ __device__ constexpr int opt_bbytes(int nrp) { return 256 * nrp; }  // B stage: 2 NRP rows x 64 bf16
 // x and B ring depths: the x copies (from L2) and the B round trip (convert,
-// MMA, commit) each take about a microsecond, W copies from memory longer
-__host__ __device__ constexpr int opt_sx(int nrp) { return nrp <= 16 ? 8 : (nrp <= 32 ? 6 : 4); }
-__host__ __device__ constexpr int opt_sb(int nrp) { return nrp <= 16 ? 8 : (nrp <= 32 ? 6 : 4); }
+// MMA, commit) each take about a microsecond.  Up to 16 activation rows two CTAs
+// share an SM (97 KB of rings each, <= 84 registers), with twice the K split:
+// 16 x 4096 x 4096 measured 11.6 us against 13.7 us with one CTA per SM.
+__host__ __device__ constexpr int opt_ctas_per_sm(int nrp) { return nrp <= 16 ? 2 : 1; }
+__host__ __device__ constexpr int opt_sx(int nrp) { return nrp <= 16 ? 4 : (nrp <= 32 ? 6 : 4); }
+__host__ __device__ constexpr int opt_sb(int nrp) { return nrp <= 16 ? 4 : (nrp <= 32 ? 6 : 4); }
 // W ring depth: four 16 KB boxes in flight per SM measured fastest (deeper rings
 // of these 128-row boxes lost up to 40% on GB300)
 __host__ __device__ constexpr int opt_sw(int) { return 4; }
@@ -254,7 +257,7 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
 }
 
 template <int NRP>
-__global__ void __launch_bounds__(OPT_THREADS, 1) out_proj_tc_kernel(const __grid_constant__ CUtensorMap tw,
+__global__ void __launch_bounds__(OPT_THREADS, opt_ctas_per_sm(NRP)) out_proj_tc_kernel(const __grid_constant__ CUtensorMap tw,
                                                                      const float* __restrict__ x, int n_rows,
                                                                      int d_model, int k_dim, float* __restrict__ y,
                                                                      unsigned* err) {
@@ -549,10 +552,10 @@ cudaError_t launch_out_proj_tc(int nr, int d_model, int k_dim, const float* x, c
   }
   CUtensorMap tw;
   if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, OPT_BK, OPT_BM)) return cudaErrorNotSupported;
-  // K split (the cluster size): about one CTA per SM, at most 8, at most one per K stage
+  // K split (the cluster size): about opt_ctas_per_sm CTAs per SM, at most 8, at most one per K stage
   const int n_mt = (d_model + OPT_BM - 1) / OPT_BM;
   const int n_kb = (k_dim + OPT_BK - 1) / OPT_BK;
-  int split = sm_count() / n_mt;
+  int split = opt_ctas_per_sm(NRP) * sm_count() / n_mt;
   if (split > 8) split = 8;
   if (split > n_kb) split = n_kb;
   if (split < 1) split = 1;
