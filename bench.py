@@ -139,8 +139,9 @@ class Clocks:
 
 
 def traffic_record(kernel_file: str, key: str):
-    """Per-launch DRAM traffic from a committed ncu summary, valid only while the
-    kernel source is unchanged (the summary stores the source's sha256)."""
+    """Per-launch DRAM traffic from a committed ncu summary, valid only for the
+    workload named in the key and while the kernel source is unchanged (the
+    summary stores the source's sha256); None otherwise."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     src = os.path.join(ROOT, "int2_kv_cache_gb300", "csrc", kernel_file)
     try:
@@ -360,7 +361,7 @@ def run_gpu(args):
     by = w.decode_bytes()
     alg = sum(by.values())
     achieved = alg / (t_dec * 1e-3) / 1e9
-    traffic = traffic_record("decode.cu", "decode_step")
+    traffic = traffic_record("decode.cu", "decode_step_" + args.workload)
     line = {
         "metric": METRIC,
         "value": world * w.B / (ms_step * 1e-3),
