@@ -6,8 +6,8 @@ Test infrastructure only (see the package header).
 details and Table A (64 sink tokens and 256 recent tokens kept in BF16), §4.1
 and the appendix paragraphs "OptR Algorithm" and "Key-mean estimation and
 application" (window tokens skip INT2 quantization, their keys keep the same
-centring, their values stay unchanged in BF16), Eqs. 24, 26, 27 and 29-30 (the
-value that the folded V projection emits is v' = v R_V).
+centring, their values stay unchanged in BF16), Eqs. 24, 26 and 27 (the readout
+in the rotated-V basis is o' = o R_V).
 
 Readings (the pages leave these open):
 
@@ -20,9 +20,10 @@ Readings (the pages leave these open):
   rounded once to bf16.  mu is the unrotated key mean (Eq. 19); no mu, no
   centring.  Its logit uses the unrotated query: q . k~ / sqrt(d), which equals
   (q R_K) . ((k - mu) R_K) / sqrt(d) up to the bf16 rounding (Eq. 24).
-* Window value = bf16_rne(v R_V): the exact rotated value (what the folded V
-  projection of Eqs. 29-30 emits) rounded once to bf16, so the readout stays in
-  the rotated-V basis of Eq. 27 like the INT2 values.
+* Window value = bf16_rne(v): the value as given, unchanged (for bf16 inputs an
+  exact copy).  The INT2 values are stored rotated (v R_V) and the readout is
+  kept in the rotated-V basis (Eq. 27), so the window part of the readout is
+  rotated once: o' = sum_INT2 p v^_R + (sum_window p v~) R_V.
 * Storage, per (sequence, KV head): (S + R) / 8 records of 4,096 bytes, one
   record per 8 consecutive slots: the 8 keys, then the 8 values, each a row of
   128 bf16.  Position p lives in slot p (p < S) or S + (p mod R); slot s in
@@ -45,7 +46,6 @@ from __future__ import annotations
 import numpy as np
 
 from .attention import rotate_queries, softmax
-from .cache import rotate_heads
 
 D = 128
 RECORD_TOKENS = 8
@@ -122,12 +122,12 @@ def window_key(k, mu=None) -> np.ndarray:
     return bf16_rne(k32.astype(np.float64))
 
 
-def window_value(v, r_v) -> np.ndarray:
-    """bf16_rne(v R_V) for v [..., H, 128], the product in float64."""
-    return bf16_rne(rotate_heads(v, r_v))
+def window_value(v) -> np.ndarray:
+    """bf16_rne(v) for v [..., H, 128]: the value unchanged, in bf16."""
+    return bf16_rne(np.asarray(v, np.float64))
 
 
-def write_window(region: np.ndarray, k, v, start_pos: int, sink: int, recent: int, mu, r_v) -> None:
+def write_window(region: np.ndarray, k, v, start_pos: int, sink: int, recent: int, mu) -> None:
     """Append tokens k, v [T, H, 128] of one sequence at positions start_pos..;
     region: uint8 [H, region_bytes(sink, recent)], written in place."""
     check_window(sink, recent)
@@ -135,7 +135,7 @@ def write_window(region: np.ndarray, k, v, start_pos: int, sink: int, recent: in
     n, h = k.shape[0], k.shape[1]
     new_len = start_pos + n
     kw = bf16_bits(window_key(k, mu))
-    vw = bf16_bits(window_value(v, r_v))
+    vw = bf16_bits(window_value(v))
     ch = np.arange(D)
     for t in range(n):
         p = start_pos + t
@@ -167,14 +167,15 @@ def read_window(region: np.ndarray, length: int, sink: int, recent: int):
     return pos, keys, vals
 
 
-def decode_attention_windowed(q, k_hat, v_hat, win_pos, win_k, win_v, r_k, gqa: int, length: int,
+def decode_attention_windowed(q, k_hat, v_hat, win_pos, win_k, win_v, r_k, r_v, gqa: int, length: int,
                               sink: int, recent: int) -> np.ndarray:
     """One query per head over a sequence of `length` with BF16 windows.
 
     q [H_q, 128]; k_hat, v_hat [>= length, H_kv, 128]: the dequantized INT2
     cache in the rotated basis (only the INT2 positions are read);
-    win_pos, win_k, win_v: ``read_window`` output (keys centred and unrotated,
-    values rotated).  Returns o' [H_q, 128] in the rotated-V basis.
+    win_pos, win_k, win_v: ``read_window`` output (keys centred, values as
+    given; neither rotated).  Returns o' [H_q, 128] in the rotated-V basis:
+    the INT2 values are already rotated, the window values are rotated here.
     """
     q = np.asarray(q, np.float64)
     qr = rotate_queries(q, r_k, gqa)
@@ -185,5 +186,6 @@ def decode_attention_windowed(q, k_hat, v_hat, win_pos, win_k, win_v, r_k, gqa: 
         h = j // gqa
         a = np.concatenate([k_hat[ipos, h, :] @ qr[j], win_k[:, h, :] @ q[j]]) / np.sqrt(D)
         p = softmax(a)
-        out[j] = p @ np.concatenate([v_hat[ipos, h, :], win_v[:, h, :]])
+        n = len(ipos)
+        out[j] = p[:n] @ v_hat[ipos, h, :] + (p[n:] @ win_v[:, h, :]) @ r_v[h]
     return out

@@ -59,20 +59,18 @@ def test_ring_contents_after_chunked_appends():
     k = g.standard_normal((total, h, D)).astype(np.float32).astype(np.float64) * 3
     v = g.standard_normal((total, h, D)).astype(np.float32).astype(np.float64)
     mu = g.standard_normal((h, D)).astype(np.float32).astype(np.float64)
-    r_v = np.stack([rotations.expm_skew(g.normal(0, 0.05, (D, D))) for _ in range(h)])
     region = np.zeros((h, window.region_bytes(sink, recent)), np.uint8)
     pos = 0
     for n in (1, 70, 1, 1, 90, 3, 200, 1, 33):
-        window.write_window(region, k[pos:pos + n], v[pos:pos + n], pos, sink, recent, mu, r_v)
+        window.write_window(region, k[pos:pos + n], v[pos:pos + n], pos, sink, recent, mu)
         pos += n
         wp, wk, wv = window.read_window(region, pos, sink, recent)
         assert np.array_equal(wp, window.window_positions(pos, sink, recent))
-        # the key: one fp32 subtraction rounded to bf16; the value: exact v R_V rounded to bf16
+        # the key: one fp32 subtraction rounded to bf16; the value: v rounded to bf16
         kk = torch.from_numpy((k[wp].astype(np.float32) - mu.astype(np.float32)[None])).to(torch.bfloat16)
         assert np.array_equal(wk, kk.to(torch.float64).numpy())
-        vv = np.einsum("thc,hcd->thd", v[wp], r_v)
-        assert np.array_equal(wv, window.bf16_rne(vv))
-        assert np.abs(wv - vv).max() <= 2 ** -8 * np.abs(vv).max()
+        vv = torch.from_numpy(v[wp].astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+        assert np.array_equal(wv, vv)
 
 
 def _grid_group(g, n):
@@ -88,7 +86,7 @@ def _grid_group(g, n):
 @pytest.mark.parametrize("sink,recent,length", [(0, 0, 150), (64, 40, 150), (64, 256, 150), (0, 16, 37),
                                                 (128, 8, 500)])
 def test_windowed_readout_equals_plain_attention_on_lossless_inputs(sink, recent, length):
-    """Window tokens: k - mu and v R_V exact in bf16; INT2 tokens: (k - mu) R_K and
+    """Window tokens: k - mu and v exact in bf16; INT2 tokens: (k - mu) R_K and
     v R_V on the INT2 grid.  Both stores are then lossless, and the windowed
     readout, rotated back, must equal attention on the raw k, v (Eqs. 1-2, 24, 27)."""
     g = np.random.default_rng(sink + recent + length)
@@ -104,7 +102,8 @@ def test_windowed_readout_equals_plain_attention_on_lossless_inputs(sink, recent
                   _grid_group(g, length * hkv).reshape(length, hkv, D))
     # window keys: k - mu = xk (unrotated); INT2 keys: (k - mu) R_K = xk
     k = np.where(win[:, None, None], xk, np.einsum("thd,hcd->thc", xk, r_k)) + mu[None]
-    v = np.einsum("thd,hcd->thc", xv, r_v)  # v R_V = xv
+    # window values: v = xv (stored as is); INT2 values: v R_V = xv
+    v = np.where(win[:, None, None], xv, np.einsum("thd,hcd->thc", xv, r_v))
     q = g.standard_normal((hkv * gqa, D))
 
     enc = cache.encode_tokens(k, v, r_k, r_v, mu, 1.0, 1.0)
@@ -116,9 +115,9 @@ def test_windowed_readout_equals_plain_attention_on_lossless_inputs(sink, recent
 
     region = np.zeros((hkv, max(window.region_bytes(sink, recent), 1)), np.uint8)
     if sink + recent:
-        window.write_window(region, k, v, 0, sink, recent, mu, r_v)
+        window.write_window(region, k, v, 0, sink, recent, mu)
     wp, wk, wv = window.read_window(region, length, sink, recent)
-    got = window.decode_attention_windowed(q, k_hat, v_hat, wp, wk, wv, r_k, gqa, length, sink, recent)
+    got = window.decode_attention_windowed(q, k_hat, v_hat, wp, wk, wv, r_k, r_v, gqa, length, sink, recent)
     ref = attention.reference_attention(q, k, v, gqa)
     back = np.einsum("jd,jcd->jc", got, r_v[np.arange(hkv * gqa) // gqa])  # o' R_V^T
     assert np.abs(back - ref).max() < 1e-11 * max(1.0, np.abs(ref).max())
@@ -133,25 +132,27 @@ def test_empty_windows_equal_plain_decode():
     q = g.standard_normal((hkv * gqa, D))
     wp = np.zeros(0, np.int64)
     got = window.decode_attention_windowed(q, k_hat, v_hat, wp, np.zeros((0, hkv, D)), np.zeros((0, hkv, D)),
-                                           r_k, gqa, length, 0, 0)
+                                           r_k, r_k, gqa, length, 0, 0)
     assert np.array_equal(got, attention.decode_attention(q, k_hat, v_hat, r_k, gqa)) or \
         np.abs(got - attention.decode_attention(q, k_hat, v_hat, r_k, gqa)).max() < 1e-14
 
 
 def test_windowed_readout_matches_brute_force_loops():
     """Pure-Python loops over a tiny mixed sequence: INT2 positions meet q' = q R_K,
-    window positions meet the unrotated q; one softmax over all of them."""
+    window positions meet the unrotated q; one softmax over all of them; window
+    values enter the rotated-V readout as v R_V."""
     import math
     g = np.random.default_rng(4)
     length, sink, recent, hkv, gqa = 11, 0, 8, 1, 2
     r_k = rotations.expm_skew(g.normal(0, 0.3, (D, D)))[None]
+    r_v = rotations.expm_skew(g.normal(0, 0.3, (D, D)))[None]
     q = g.standard_normal((gqa, D))
     k_hat = g.standard_normal((length, hkv, D))
     v_hat = g.standard_normal((length, hkv, D))
     wp = window.window_positions(length, sink, recent)
     wk = g.standard_normal((len(wp), hkv, D))
     wv = g.standard_normal((len(wp), hkv, D))
-    got = window.decode_attention_windowed(q, k_hat, v_hat, wp, wk, wv, r_k, gqa, length, sink, recent)
+    got = window.decode_attention_windowed(q, k_hat, v_hat, wp, wk, wv, r_k, r_v, gqa, length, sink, recent)
     for j in range(gqa):
         qj = q[j].tolist()
         qr = [sum(qj[c] * r_k[0][c][d] for c in range(D)) for d in range(D)]
@@ -160,7 +161,7 @@ def test_windowed_readout_matches_brute_force_loops():
             if p in wp.tolist():
                 i = wp.tolist().index(p)
                 logits.append(sum(qj[d] * wk[i][0][d] for d in range(D)) / math.sqrt(D))
-                vals.append(wv[i][0])
+                vals.append([sum(wv[i][0][c] * r_v[0][c][d] for c in range(D)) for d in range(D)])
             else:
                 logits.append(sum(qr[d] * k_hat[p][0][d] for d in range(D)) / math.sqrt(D))
                 vals.append(v_hat[p][0])
