@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--seqs", type=int, default=None, help="sequences (default: 16 gqa8b, 1 long4b, 64 serve14b)")
     p.add_argument("--ctx", type=int, default=None, help="context (gqa8b default 32768, long4b 131072)")
     p.add_argument("--splits", type=int, default=0)
+    p.add_argument("--window", default=None, metavar="SINK,RECENT",
+                   help="decode step with BF16 sink / recent windows, e.g. 64,256 (default: all tokens INT2)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     return p.parse_args()
@@ -189,7 +191,7 @@ class DecodeStep:
     cached tokens; a step appends its last token, decodes over len tokens and
     projects through the folded W_O."""
 
-    def __init__(self, c, splits: int, device: str):
+    def __init__(self, c, splits: int, device: str, window=None):
         import torch
         import int2_kv_cache_gb300 as kvq
 
@@ -222,6 +224,25 @@ class DecodeStep:
                 kvq.kvq_quantize_append(self.layout, t(k[:hist], bf), t(v[:hist], bf), t(np.array([0, hist]), torch.int32),
                                         t(np.array([0]), torch.int32), self.table[b:b + 1].contiguous(), self.rot_k,
                                         self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
+        # BF16 sink / recent windows: the window copies of the history
+        self.win = None
+        self.mu = mu
+        if window is not None:
+            s_w, r_w = window
+            self.win = kvq.Window(s_w, r_w, torch.zeros(kvq.Window.buffer_bytes(n_seqs, c.n_kv_heads, s_w, r_w),
+                                                        dtype=torch.uint8, device=device))
+            for b0 in range(0, n_seqs, 4):
+                kvs = gen_parallel(lambda i: c.kv(b0 + i), min(4, n_seqs - b0))
+                for i, (k, v) in enumerate(kvs):
+                    b = b0 + i
+                    hist = int(lens[b]) - 1
+                    # only the tokens that end up in a window are needed: the sink and the last r_w
+                    for lo, hi in ((0, min(s_w, hist)), (max(s_w, hist - r_w), hist)):
+                        if hi <= lo:
+                            continue
+                        kvq.kvq_window_append(self.layout, t(k[lo:hi], bf), t(v[lo:hi], bf),
+                                              t(np.array([0, hi - lo]), torch.int32), t(np.array([lo]), torch.int32),
+                                              mu, self.win_row(b))
         torch.cuda.synchronize()
         kvq.kvq_device_check()
         # folded W_O (Eqs. 29-31), bf16
@@ -239,15 +260,22 @@ class DecodeStep:
         self.start = t(lens - 1, torch.int32)
         self.lens = t(lens, torch.int32)
         self.splits = splits
-        ws = kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, splits)
+        ws = kvq.kvq_decode_workspace_size_win(self.layout, n_seqs, ctx, self.win, splits)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
         # thread blocks of the decode kernel (the library's choice when splits == 0)
         self.n_ctas = splits or next(s for s in range(1, 8193)
-                                     if kvq.kvq_decode_workspace_size(self.layout, n_seqs, ctx, s) == ws)
+                                     if kvq.kvq_decode_workspace_size_win(self.layout, n_seqs, ctx, self.win, s) == ws)
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
         self.y = torch.empty(n_seqs, self.dm, device=device)
         self.host_y = torch.empty(n_seqs, self.dm).pin_memory()
-        self.launches_per_step = 1 + 3 + 1  # append (K and V), query prep + decode + combine, W_O
+        # append (K and V) [+ window copies], query prep + decode + combine, W_O
+        self.launches_per_step = 1 + (1 if self.win else 0) + 3 + 1
+
+    def win_row(self, b):
+        """A window struct over sequence b's rows only (for appending one sequence at a time)."""
+        w = self.win
+        per = self.kvq.Window.buffer_bytes(1, self.case.n_kv_heads, w.sink_tokens, w.recent_tokens)
+        return self.kvq.Window(w.sink_tokens, w.recent_tokens, w.buf[b * per:(b + 1) * per])
 
     def step(self, ev=None):
         kvq = self.kvq
@@ -256,10 +284,16 @@ class DecodeStep:
             ev[0].record()
         kvq.kvq_quantize_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.table, self.rot_k,
                                 self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
+        if self.win is not None:
+            kvq.kvq_window_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.mu, self.win)
         if ev is not None:
             ev[1].record()
-        kvq.kvq_decode_attention(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.pool, self.ws,
-                                 self.o, n_splits=self.splits)
+        if self.win is None:
+            kvq.kvq_decode_attention(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.pool,
+                                     self.ws, self.o, n_splits=self.splits)
+        else:
+            kvq.kvq_decode_attention_win(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.rot_v,
+                                         self.pool, self.win, self.ws, self.o, n_splits=self.splits)
         if ev is not None:
             ev[2].record()
         kvq.kvq_out_proj(self.o.reshape(self.B, -1), self.w_fold, self.y)
@@ -278,6 +312,24 @@ class DecodeStep:
         lens = self.lens_np
         g = hq // hkv
         units = B * hkv
+        frag = ((g + 3) // 4) * 16 * 32 * 4
+        if self.win is not None:
+            # INT2 positions [S, L - R) read at 72 bytes, window positions at 512 (bf16 key + value)
+            s_w, r_w = self.win.sink_tokens, self.win.recent_tokens
+            n_win = np.minimum(lens, s_w) + np.maximum(0, lens - np.maximum(s_w, lens - r_w))
+            n_int2 = lens - n_win
+            pairs = min(4 * self.n_ctas + units, int(hkv * ((n_int2 + 63) // 64).sum()))
+            pairs_w = min(4 * self.n_ctas + units, int(hkv * ((n_win + 7) // 8 + 1).sum()))
+            return {
+                "kv_cache": int(n_int2.sum()) * hkv * 72,
+                "bf16_windows": int(n_win.sum()) * hkv * 512,
+                "q": B * hq * 128 * 2,
+                "block_table": int(((n_int2 + self.case.page_tokens - 1) // self.case.page_tokens).sum()) * 4,
+                "rotation": hkv * 128 * 128 * 4,
+                "query_fragments_write_read": 2 * units * (2 * frag + g * 16),
+                "partials_write_read": 2 * (pairs + pairs_w) * g * 130 * 4,
+                "o_rot": B * hq * 128 * 4,
+            }
         # one partial (acc[128], m, l per query head) per (warp slice, unit) pair:
         # at most 4 * n_ctas + units of them, written once and read once
         pairs = min(4 * self.n_ctas + units, int(hkv * ((lens + 63) // 64).sum()))
@@ -303,7 +355,8 @@ def run_gpu(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl")
-    w = DecodeStep(decode_workload(args), args.splits, device)
+    window = tuple(int(x) for x in args.window.split(",")) if args.window else None
+    w = DecodeStep(decode_workload(args), args.splits, device, window)
     stream = torch.cuda.current_stream()
 
     def barrier():
@@ -361,7 +414,7 @@ def run_gpu(args):
     by = w.decode_bytes()
     alg = sum(by.values())
     achieved = alg / (t_dec * 1e-3) / 1e9
-    traffic = traffic_record("decode.cu", "decode_step_" + args.workload)
+    traffic = traffic_record("decode.cu", "decode_step_" + args.workload) if window is None else None
     line = {
         "metric": METRIC,
         "value": world * w.B / (ms_step * 1e-3),
@@ -379,6 +432,8 @@ def run_gpu(args):
             "workload": workload_text(w.case),
             "batch": w.B, "ctx": w.L, "n_q_heads": w.hq, "n_kv_heads": w.hkv, "d_model": w.dm,
             "decode_ctas": w.n_ctas, "parallelism": f"replicas x{world}",
+            "bf16_windows": (f"sink {window[0]} + recent {window[1]} tokens per sequence in BF16"
+                             if window else "none (every token INT2)"),
             "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (w.pool.numel() / 1e6),
         },
         "kernel_ms": {"quantize_append": t_app, "decode_attention": t_dec, "out_proj": t_out},

@@ -96,6 +96,31 @@ typedef struct {
   int max_blocks_per_seq;  /* row stride of block_table */
 } kvq_layout;
 
+/* BF16 sink and recent windows ("Output-Aware Rotation for INT2 KV-Cache
+ * Quantization", §5 implementation details and Table A: 64 sink and 256 recent
+ * tokens stay in BF16; appendix "OptR Algorithm" and "Key-mean estimation and
+ * application": window tokens skip INT2, their keys keep the centring, their
+ * values stay unchanged in BF16).
+ * At length L, position p < L is a window token iff p < sink_tokens or
+ * p >= L - recent_tokens; the windowed decode reads it from `buf` and every
+ * other position from the INT2 pages (which still hold every token).
+ *   window key   = bf16_rn(fp32(k - mu))   centred, not rotated (mu NULL: k)
+ *   window value = bf16_rn(v)              unchanged (a copy for bf16 inputs)
+ * Neither is rotated: the windowed decode rotates the window part of its
+ * readout by R_V once, so that the output stays in the rotated-V basis (Eq. 27).
+ * buf: uint8 [n_seqs][n_kv_heads][(sink + recent) / 8][4096], caller-owned,
+ * 16-byte aligned.  Record i of a (sequence, KV head) holds slots 8i .. 8i + 7:
+ * 8 key rows, then 8 value rows, each 128 bf16 (256 bytes); position p uses
+ * slot p (p < sink) or sink + p % recent; inside row r = slot % 8 the 16-byte
+ * chunk c (channels 8c .. 8c + 7) is stored at chunk position c ^ r.
+ * sink_tokens: a multiple of 64; recent_tokens: a multiple of 8;
+ * sink_tokens + recent_tokens <= 65536.  Both 0: no windows. */
+typedef struct {
+  int sink_tokens;
+  int recent_tokens;
+  uint8_t* buf;
+} kvq_window;
+
 /* Size in bytes of the pool described by `layout`. */
 size_t kvq_pool_bytes(const kvq_layout* layout);
 
@@ -175,6 +200,45 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
                                 const int32_t* block_table, kvq_rot rot_k, const uint8_t* pool,
                                 int n_splits, void* workspace, size_t workspace_bytes,
                                 float* o_rot, kvq_stream stream);
+
+/* Window copies of appended tokens (see kvq_window).  For every new token of
+ * sequence b at position p = start_pos[b] + (t - cu_new[b]) that is a window
+ * token at the sequence's new length (p < sink, or p >= start_pos[b] + n_new_b -
+ * recent), and every KV head h, writes bf16_rn(fp32(k - mu_k[h])) and
+ * bf16_rn(v) into its slot.  Call it beside kvq_quantize_append with the same
+ * tokens.
+ *   k, v, dtype, cu_new, start_pos: as in kvq_quantize_append
+ *   mu_k:  float [n_kv_heads][128], the UNROTATED key mean, or NULL
+ *   win:   host struct; buf rows are indexed by the sequence index b */
+kvq_status kvq_window_append(const kvq_layout* layout, int n_seqs, int n_new_total, const void* k,
+                             const void* v, kvq_dtype dtype, const int32_t* cu_new,
+                             const int32_t* start_pos, const float* mu_k, const kvq_window* win,
+                             kvq_stream stream);
+
+/* Workspace bytes of kvq_decode_attention_win: kvq_decode_workspace_size plus,
+ * with windows, a second set of partials, the windows' query fragments and spans. */
+kvq_status kvq_decode_workspace_size_win(const kvq_layout* layout, int n_seqs, int max_seq_len,
+                                         int n_splits, const kvq_window* win, size_t* bytes);
+
+/* Decode attention over INT2 pages and BF16 windows together (OptR Eqs. 1-2,
+ * 5, 22, 24, 26, 27 with the windows of kvq_window): one softmax over
+ *   a_s = q'_j . (zero_s + scale_s * codeK_s) / sqrt(128)   INT2 positions (q' = q R_K)
+ *   a_s = q_j . key~_s / sqrt(128)                          window positions (unrotated q)
+ *   o_rot[b][j] = sum_INT2 p_s (zero_s + scale_s * codeV_s) + (sum_window p_s value~_s) R_V,h
+ * (rotated-V basis; the window values are stored unrotated, so their part of
+ * the readout is rotated once, in fp32, per sequence and query head).
+ * The INT2 positions of the batch are split across the warps of the grid as in
+ * kvq_decode_attention, the 8-token window records in a second equal split;
+ * each split yields its own partials and the combine merges both in a fixed
+ * order (deterministic).  win NULL, or both window sizes 0, is
+ * kvq_decode_attention (rot_v unused).  Arguments otherwise as
+ * kvq_decode_attention; the workspace must hold kvq_decode_workspace_size_win bytes. */
+kvq_status kvq_decode_attention_win(const kvq_layout* layout, int n_seqs, const void* q,
+                                    kvq_dtype q_dtype, const int32_t* seq_lens, int max_seq_len,
+                                    const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v,
+                                    const uint8_t* pool, const kvq_window* win, int n_splits,
+                                    void* workspace, size_t workspace_bytes, float* o_rot,
+                                    kvq_stream stream);
 
 /* The same decode attention for callers that cannot allocate device memory
  * (the paper has no counterpart; this is a deployment convenience).

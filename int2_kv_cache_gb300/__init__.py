@@ -37,6 +37,10 @@ class KvqRot(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("signs", ctypes.c_void_p), ("dense", ctypes.c_void_p)]
 
 
+class KvqWindow(ctypes.Structure):
+    _fields_ = [("sink_tokens", ctypes.c_int), ("recent_tokens", ctypes.c_int), ("buf", ctypes.c_void_p)]
+
+
 _lib = None
 
 
@@ -49,6 +53,7 @@ def lib() -> ctypes.CDLL:
         L = ctypes.CDLL(LIB_PATH)
         vp, i, f, st, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
         lp = ctypes.POINTER(KvqLayout)
+        wp = ctypes.POINTER(KvqWindow)
         sigs = {
             "kvq_last_error": ([], ctypes.c_char_p),
             "kvq_pool_bytes": ([lp], sz),
@@ -59,6 +64,9 @@ def lib() -> ctypes.CDLL:
             "kvq_decode_workspace_size": ([lp, i, i, i, ctypes.POINTER(sz)], st),
             "kvq_decode_attention": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, sz, vp, vp], st),
             "kvq_decode_attention_noalloc": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, vp], st),
+            "kvq_window_append": ([lp, i, i, vp, vp, i, vp, vp, vp, wp, vp], st),
+            "kvq_decode_workspace_size_win": ([lp, i, i, i, wp, ctypes.POINTER(sz)], st),
+            "kvq_decode_attention_win": ([lp, i, vp, i, vp, i, vp, KvqRot, KvqRot, vp, wp, i, vp, sz, vp, vp], st),
             "kvq_fold_wo": ([i, i, i, vp, i, KvqRot, vp, i, vp], st),
             "kvq_out_proj": ([i, i, i, vp, vp, i, vp, vp], st),
             "kvq_calib_workspace_size": ([i, i, i, i, i, ctypes.POINTER(sz)], st),
@@ -75,7 +83,8 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mean", "kvq_rotate_heads",
             "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention",
-            "kvq_decode_attention_noalloc", "kvq_fold_wo",
+            "kvq_decode_attention_noalloc", "kvq_window_append", "kvq_decode_workspace_size_win",
+            "kvq_decode_attention_win", "kvq_fold_wo",
             "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse")
 
 
@@ -189,6 +198,53 @@ def kvq_decode_attention_noalloc(layout: KvqLayout, q, seq_lens, max_seq_len: in
     _check(lib().kvq_decode_attention_noalloc(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _dtype_code(q),
                                               _ptr(seq_lens), max_seq_len, _ptr(block_table), rot_k.c, _ptr(pool),
                                               n_splits, _ptr(o_rot), _stream(stream)))
+
+
+class Window:
+    """BF16 sink / recent window sizes and the caller's record buffer (see kvq_window)."""
+
+    def __init__(self, sink_tokens: int, recent_tokens: int, buf=None):
+        self.sink_tokens = sink_tokens
+        self.recent_tokens = recent_tokens
+        self.buf = buf
+
+    @staticmethod
+    def buffer_bytes(n_seqs: int, n_kv_heads: int, sink_tokens: int, recent_tokens: int) -> int:
+        return n_seqs * n_kv_heads * (sink_tokens + recent_tokens) * 512
+
+    @property
+    def c(self) -> KvqWindow:
+        return KvqWindow(self.sink_tokens, self.recent_tokens, _ptr(self.buf))
+
+
+def _win_ref(win):
+    return None if win is None else ctypes.byref(win.c)
+
+
+def kvq_window_append(layout: KvqLayout, k, v, cu_new, start_pos, mu_k, win: Window, stream=None) -> None:
+    _check(lib().kvq_window_append(ctypes.byref(layout), start_pos.shape[0], k.shape[0], _ptr(_contig(k, "k")),
+                                   _ptr(_contig(v, "v")), _dtype_code(k), _ptr(cu_new), _ptr(start_pos),
+                                   _ptr(mu_k), _win_ref(win), _stream(stream)))
+
+
+def kvq_decode_workspace_size_win(layout: KvqLayout, n_seqs: int, max_seq_len: int, win: Window | None,
+                                  n_splits: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().kvq_decode_workspace_size_win(ctypes.byref(layout), n_seqs, max_seq_len, n_splits, _win_ref(win),
+                                               ctypes.byref(out)))
+    return int(out.value)
+
+
+def kvq_decode_attention_win(layout: KvqLayout, q, seq_lens, max_seq_len: int, block_table, rot_k: DeviceRot,
+                             rot_v: DeviceRot, pool, win: Window | None, workspace, o_rot, n_splits: int = 0,
+                             stream=None) -> None:
+    n_seqs = q.shape[0]
+    _check(lib().kvq_decode_attention_win(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _dtype_code(q),
+                                          _ptr(seq_lens), max_seq_len, _ptr(block_table), rot_k.c, rot_v.c,
+                                          _ptr(pool),
+                                          _win_ref(win), n_splits, _ptr(workspace),
+                                          workspace.numel() * workspace.element_size(), _ptr(o_rot),
+                                          _stream(stream)))
 
 
 def kvq_fold_wo(w_o, n_q_heads: int, n_kv_heads: int, rot_v: DeviceRot, w_folded, stream=None) -> None:

@@ -91,6 +91,21 @@ kvq_status check_rot(const kvq_rot& r, const char* name) {
   }
 }
 
+// Window sizes (kvq_window); *out = no windows for NULL or two zero sizes.
+kvq_status check_window(const kvq_window* w, kvq::WinGeom* out) {
+  *out = kvq::WinGeom{0, 0, nullptr};
+  if (!w || (w->sink_tokens == 0 && w->recent_tokens == 0)) return KVQ_OK;
+  if (w->sink_tokens < 0 || w->sink_tokens % 64 != 0)
+    return fail(KVQ_EINVAL, "window sink_tokens %d is not a non-negative multiple of 64", w->sink_tokens);
+  if (w->recent_tokens < 0 || w->recent_tokens % 8 != 0)
+    return fail(KVQ_EINVAL, "window recent_tokens %d is not a non-negative multiple of 8", w->recent_tokens);
+  if (w->sink_tokens + w->recent_tokens > 65536)
+    return fail(KVQ_EUNSUPPORTED, "window of %d tokens > 65536", w->sink_tokens + w->recent_tokens);
+  if (!w->buf || !aligned16(w->buf)) return fail(KVQ_EINVAL, "window buf is NULL or not 16-byte aligned");
+  *out = kvq::WinGeom{w->sink_tokens, w->recent_tokens, w->buf};
+  return KVQ_OK;
+}
+
 kvq::PageGeom geom(const kvq_layout* L) {
   return kvq::PageGeom{L->page_tokens, L->n_kv_heads, L->num_blocks, L->max_blocks_per_seq,
                        72 * L->page_tokens};
@@ -199,6 +214,28 @@ kvq_status kvq_quantize_append(const kvq_layout* layout, int n_seqs, int n_new_t
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_quantize_append");
 }
 
+kvq_status kvq_window_append(const kvq_layout* layout, int n_seqs, int n_new_total, const void* k,
+                             const void* v, kvq_dtype dtype, const int32_t* cu_new, const int32_t* start_pos,
+                             const float* mu_k, const kvq_window* win, kvq_stream stream) {
+  KVQ_CHECK(check_layout(layout, false));
+  if (n_seqs < 1 || n_seqs > 65535) return fail(KVQ_EINVAL, "n_seqs %d outside [1, 65535]", n_seqs);
+  if (n_new_total < 0) return fail(KVQ_EINVAL, "n_new_total %d < 0", n_new_total);
+  if (!valid_dtype(dtype)) return fail(KVQ_EINVAL, "bad dtype %d", (int)dtype);
+  kvq::WinGeom wg;
+  KVQ_CHECK(check_window(win, &wg));
+  if (n_new_total == 0 || wg.sink + wg.recent == 0) return KVQ_OK;
+  KVQ_PTR(k, "k");
+  KVQ_PTR(v, "v");
+  KVQ_IDX(cu_new, "cu_new");
+  KVQ_IDX(start_pos, "start_pos");
+  if (mu_k && !aligned16(mu_k)) return fail(KVQ_EINVAL, "mu_k is not 16-byte aligned");
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
+  cudaError_t e = kvq::launch_window_append(layout->n_kv_heads, n_seqs, n_new_total, k, v, dtype, cu_new, start_pos,
+                                            mu_k, wg, err, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_window_append");
+}
+
 // Index ranges the decode kernels keep in 32-bit integers.
 static kvq_status check_decode_size(const kvq_layout* layout, int n_seqs, int max_seq_len) {
   if (n_seqs > 65535) return fail(KVQ_EUNSUPPORTED, "n_seqs %d > 65535", n_seqs);
@@ -213,14 +250,21 @@ static kvq_status check_decode_size(const kvq_layout* layout, int n_seqs, int ma
 
 kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int max_seq_len,
                                      int n_splits, size_t* bytes) {
+  return kvq_decode_workspace_size_win(layout, n_seqs, max_seq_len, n_splits, nullptr, bytes);
+}
+
+kvq_status kvq_decode_workspace_size_win(const kvq_layout* layout, int n_seqs, int max_seq_len, int n_splits,
+                                         const kvq_window* win, size_t* bytes) {
   KVQ_CHECK(check_layout(layout, true));
+  kvq::WinGeom wg;
+  KVQ_CHECK(check_window(win, &wg));
   if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");
   if (n_seqs < 0 || max_seq_len < 0 || n_splits < 0 || n_splits > 8192)
     return fail(KVQ_EINVAL, "bad n_seqs %d / max_seq_len %d / n_splits %d", n_seqs, max_seq_len, n_splits);
   KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
   const int gqa = layout->n_q_heads / layout->n_kv_heads;
   const int s = n_splits ? n_splits : kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, gqa, max_seq_len);
-  *bytes = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s);
+  *bytes = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s, wg.sink + wg.recent > 0);
   return KVQ_OK;
 }
 
@@ -228,7 +272,20 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
                                 const int32_t* seq_lens, int max_seq_len, const int32_t* block_table,
                                 kvq_rot rot_k, const uint8_t* pool, int n_splits, void* workspace,
                                 size_t workspace_bytes, float* o_rot, kvq_stream stream) {
+  const kvq_rot identity = {KVQ_ROT_IDENTITY, nullptr, nullptr};
+  return kvq_decode_attention_win(layout, n_seqs, q, q_dtype, seq_lens, max_seq_len, block_table, rot_k, identity,
+                                  pool, nullptr, n_splits, workspace, workspace_bytes, o_rot, stream);
+}
+
+kvq_status kvq_decode_attention_win(const kvq_layout* layout, int n_seqs, const void* q, kvq_dtype q_dtype,
+                                    const int32_t* seq_lens, int max_seq_len, const int32_t* block_table,
+                                    kvq_rot rot_k, kvq_rot rot_v, const uint8_t* pool, const kvq_window* win,
+                                    int n_splits, void* workspace, size_t workspace_bytes, float* o_rot,
+                                    kvq_stream stream) {
   KVQ_CHECK(check_layout(layout, true));
+  kvq::WinGeom wg;
+  KVQ_CHECK(check_window(win, &wg));
+  KVQ_CHECK(check_rot(rot_v, "rot_v"));
   if (n_seqs < 0) return fail(KVQ_EINVAL, "n_seqs %d < 0", n_seqs);
   if (!valid_dtype(q_dtype)) return fail(KVQ_EINVAL, "bad q dtype %d", (int)q_dtype);
   if (max_seq_len < 0 || (long long)max_seq_len > (long long)layout->max_blocks_per_seq * layout->page_tokens)
@@ -245,14 +302,14 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
   KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
   const int gqa = layout->n_q_heads / layout->n_kv_heads;
   const int s = n_splits ? n_splits : kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, gqa, max_seq_len);
-  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s);
+  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s, wg.sink + wg.recent > 0);
   if (workspace_bytes < need)
     return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
   unsigned* err = nullptr;
   KVQ_CHECK(device_error_word(&err));
   cudaError_t e = kvq::launch_decode(geom(layout), layout->n_q_heads, n_seqs, q, q_dtype, seq_lens,
                                      max_seq_len, block_table, kvq::to_dev(rot_k), pool, s, workspace,
-                                     o_rot, err, stream);
+                                     o_rot, err, stream, wg, kvq::to_dev(rot_v));
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_attention");
 }
 

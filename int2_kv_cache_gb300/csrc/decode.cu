@@ -68,37 +68,53 @@ __host__ __device__ constexpr int n_tiles(int gqa) { return (gqa + 3) / 4; }
 //   qfrag  [U][16 * NT][32] u32: query B fragments, lane-major
 //   qconst [U][gqa][4] fp32: dscale, sum(q')/dscale, TAU/dscale, 0
 //   span   [U] int2: the warp slices (k0, k1) that meet the unit, (1, 0) if none
+// and, with BF16 windows, the same for the window-record list:
+//   partw  [n_slots][gqa][132] fp32, wqfrag [U][16 * NT][32] u32 (bf16 pairs), spanw [U] int2
 // with U = n_seqs * n_kv_heads units (sequence b, KV head h) -> u = b * n_kv_heads + h.
 struct DecWs {
   float* part;
   uint32_t* qfrag;
   float* qconst;
   int2* span;
+  float* partw;       // nullptr without windows
+  uint32_t* wqfrag;
+  int2* spanw;
 };
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 __host__ __device__ inline size_t decode_ws_layout(void* base, int n_seqs, int n_kv_heads, int gqa, int n_ctas,
-                                                   DecWs* out) {
+                                                   bool windows, DecWs* out) {
   const size_t units = (size_t)n_seqs * n_kv_heads;
   const size_t slots = (size_t)DEC_WARPS * n_ctas + units;
+  const size_t frag_bytes = units * 16 * n_tiles(gqa) * 32 * sizeof(uint32_t);
   const size_t o_part = 0;
   const size_t o_frag = align256(o_part + slots * gqa * PART * sizeof(float));
-  const size_t o_const = align256(o_frag + units * 16 * n_tiles(gqa) * 32 * sizeof(uint32_t));
+  const size_t o_const = align256(o_frag + frag_bytes);
   const size_t o_span = align256(o_const + units * gqa * 4 * sizeof(float));
-  const size_t total = align256(o_span + units * sizeof(int2));
+  const size_t o_partw = align256(o_span + units * sizeof(int2));
+  size_t total = o_partw;
+  size_t o_wfrag = 0, o_spanw = 0;
+  if (windows) {
+    o_wfrag = align256(o_partw + slots * gqa * PART * sizeof(float));
+    o_spanw = align256(o_wfrag + frag_bytes);
+    total = align256(o_spanw + units * sizeof(int2));
+  }
   if (out) {
     char* p = static_cast<char*>(base);
     out->part = reinterpret_cast<float*>(p + o_part);
     out->qfrag = reinterpret_cast<uint32_t*>(p + o_frag);
     out->qconst = reinterpret_cast<float*>(p + o_const);
     out->span = reinterpret_cast<int2*>(p + o_span);
+    out->partw = windows ? reinterpret_cast<float*>(p + o_partw) : nullptr;
+    out->wqfrag = windows ? reinterpret_cast<uint32_t*>(p + o_wfrag) : nullptr;
+    out->spanw = windows ? reinterpret_cast<int2*>(p + o_spanw) : nullptr;
   }
   return total;
 }
 
-size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas) {
-  return decode_ws_layout(nullptr, n_seqs, n_kv_heads, gqa, n_ctas, nullptr);
+size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas, bool windows) {
+  return decode_ws_layout(nullptr, n_seqs, n_kv_heads, gqa, n_ctas, windows, nullptr);
 }
 
 // Default grid: a full single wave (4 or 3 CTAs per SM), but no more warps than
@@ -124,6 +140,19 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
 __device__ __forceinline__ void mma16816_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                               uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
+}
+// bf16 operands (the BF16 window records)
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma16816_bf16_zero(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                   uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.f));
 }
@@ -267,6 +296,31 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
     }
     fr[wv] = pack_half2(v0, v1);
   }
+  if (ws.wqfrag) {
+    // window B fragments: the UNROTATED q_j * log2(e)/sqrt(128) (window keys are
+    // not rotated, Eq. 24), as bf16 high part (column g even) and bf16 remainder
+    // (g odd) at channels 16 s + 2t + 8 r and 16 s + 2t + 8 r + 1
+    uint32_t* wf = ws.wqfrag + (size_t)u * NT * 16 * 32;
+    for (int wv = tid; wv < NT * 16 * 32; wv += QP_THREADS) {
+      const int w = wv >> 5, L = wv & 31;
+      const int nt = w >> 4, s = (w & 15) >> 1, r = w & 1;
+      const int gi = L >> 2, ti = L & 3;
+      const int j = 4 * nt + (gi >> 1);
+      uint32_t word = 0u;
+      if (j < G) {
+        const size_t e0 = ((size_t)b * n_q_heads + h * G + j) * D + 16 * s + 2 * ti + 8 * r;
+        const float x0 = load1(q, e0, q_dtype) * sc, x1 = load1(q, e0 + 1, q_dtype) * sc;
+        __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
+        if (gi & 1) {
+          h0 = __float2bfloat16_rn(x0 - __bfloat162float(h0));
+          h1 = __float2bfloat16_rn(x1 - __bfloat162float(h1));
+        }
+        word = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+      }
+      wf[wv] = word;
+    }
+    if (tid == 0) ws.spanw[u] = make_int2(1, 0);
+  }
   if (tid == 0) ws.span[u] = make_int2(1, 0);
   if (__ldg(seq_lens + b) == 0)  // no cached tokens: the softmax is over nothing, o = 0
     for (int i = tid; i < G * D; i += QP_THREADS) o_rot[((size_t)b * n_q_heads + h * G) * D + i] = 0.f;
@@ -282,12 +336,13 @@ struct ChunkWalker {
 // The decode kernel.  grid = n_ctas, block = 128 (4 independent warps).
 // G = query heads per KV head; NT = n-tiles of 8 columns (2 columns per head).
 // ---------------------------------------------------------------------------
-template <int G, int P>
+template <int G, int P, bool WIN>
 __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     PageGeom g, int n_seqs, int n_q_heads, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ table, const uint8_t* __restrict__ pool, DecWs ws,
-    float* __restrict__ o_rot, unsigned* err) {
+    float* __restrict__ o_rot, unsigned* err, WinGeom win) {
   constexpr int NT = n_tiles(G);
+  constexpr int NST = DEC_STAGES;
   constexpr int PPC = 32 / P;              // pages per 32-token chunk
   constexpr int REC = 72 * P;              // bytes per page record
   constexpr int CHUNK = PPC * REC;         // 2304 bytes: one 32-token chunk
@@ -302,16 +357,31 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   const int gi = lane >> 2, ti = lane & 3;  // MMA group id, thread id in group
   const int Hkv = g.n_kv_heads;
   const int max_len = g.max_blocks * P;
+  // BF16 windows: positions [0, S_w) and [len - R_w, len) are read from the window records
+  const int S_w = WIN ? win.sink : 0, R_w = WIN ? win.recent : 0;
+  const int n_wrec = (S_w + R_w) / WIN_REC_TOKENS;  // records per (sequence, KV head)
 
   extern __shared__ __align__(128) uint8_t dyn_smem[];  // [DEC_WARPS][DEC_STAGES][STAGE]
   auto stage_ptr = [&](int w, int sidx) { return dyn_smem + (w * DEC_STAGES + sidx) * STAGE; };
   __shared__ __align__(8) uint64_t bars[DEC_WARPS][DEC_STAGES];
   __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the staged entry was copied
-  __shared__ int s_sum[DEC_WARPS];
-  __shared__ int s_start[DEC_WARPS][3];  // first sequence of each warp's slice, entries before it, its length
+  __shared__ int s_sum[DEC_WARPS], s_sumw[DEC_WARPS];
+  __shared__ int s_start[DEC_WARPS][3];   // first sequence of each warp's slice, entries before it, its length
+  __shared__ int s_startw[DEC_WARPS][3];  // the same for the window-record list
 
-  // list entries (64-token stages) of a sequence of `len` tokens
-  auto n_chunks_of = [&](int len) { return (len <= 0 || len > max_len) ? 0 : (len + 63) >> 6; };
+  // list entries (64-token stages) of a sequence of `len` tokens: INT2 positions [S_w, len - R_w)
+  auto n_chunks_of = [&](int len) {
+    if (len <= 0 || len > max_len) return 0;
+    const int e = len - R_w;
+    return e > S_w ? (e - S_w + 63) >> 6 : 0;
+  };
+  // window records of a sequence of `len` tokens: the sink [0, min(S_w, len)) in records
+  // of 8 positions, then the recent part [max(S_w, len - R_w), len) by 8-aligned groups
+  auto n_wrec_of = [&](int len) {
+    if (!WIN || len <= 0 || len > max_len) return 0;
+    const int a = max(S_w, len - R_w);
+    return ((min(S_w, len) + 7) >> 3) + (a < len ? ((len + 7) >> 3) - (a >> 3) : 0);
+  };
 
   // ---- the batch's chunk list: sequence b holds H_kv * nb_b entries, unit (b, h)
   //      the nb_b entries from H_kv * prefix_b + h * nb_b on ----
@@ -319,16 +389,23 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   int* s_len = reinterpret_cast<int*>(dyn_smem);
   const bool cached = n_seqs <= DEC_WARPS * DEC_STAGES * STAGE / (int)sizeof(int);
   auto len_of = [&](int b) { return cached ? s_len[b] : __ldg(seq_lens + b); };
-  int tot = 0;
+  int tot = 0, totw = 0;
   for (int b = threadIdx.x; b < n_seqs; b += 128) {
     const int len = __ldg(seq_lens + b);
     if ((len < 0 || len > max_len) && blockIdx.x == 0) flag_error(err, ERR_SEQ_RANGE);
     if (cached) s_len[b] = len;
     tot += n_chunks_of(len);
+    if (WIN) totw += n_wrec_of(len);
   }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(FULLM, tot, o);
-  if (lane == 0) s_sum[warp] = tot;
+  for (int o = 16; o > 0; o >>= 1) {
+    tot += __shfl_xor_sync(FULLM, tot, o);
+    if (WIN) totw += __shfl_xor_sync(FULLM, totw, o);
+  }
+  if (lane == 0) {
+    s_sum[warp] = tot;
+    s_sumw[warp] = totw;
+  }
   __syncthreads();
   const int T = Hkv * (s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3]);
   const int n_warps = gridDim.x * DEC_WARPS;
@@ -336,60 +413,76 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   const int gw = blockIdx.x * DEC_WARPS + warp;
   const int ga = min(T, gw * Ww);
   const int my_n = min(T, ga + Ww) - ga;
+  // the window records are split the same way, in a list of their own
+  const int Tw = WIN ? Hkv * (s_sumw[0] + s_sumw[1] + s_sumw[2] + s_sumw[3]) : 0;
+  const int Wwn = (Tw + n_warps - 1) / n_warps;
+  const int gaw = min(Tw, gw * Wwn);
+  const int my_nw = min(Tw, gaw + Wwn) - gaw;
+  const int F = my_n + my_nw;  // stage fills of this warp
   __syncthreads();
-  // exclusive prefix of chunk counts, tile by tile: the sequence holding each slice's first entry
-  int base = 0;
-  for (int b0 = 0; b0 < n_seqs; b0 += 128) {
-    const int b = b0 + threadIdx.x;
-    const int len = b < n_seqs ? len_of(b) : 0;
-    const int n = n_chunks_of(len);
-    int inc = n;
+  // exclusive prefix of per-sequence counts, tile by tile: the sequence holding
+  // the first entry of each warp slice of a list (W entries per slice, Ttot in all)
+  auto find_starts = [&](auto count, int W, int Ttot, int (*st)[3]) {
+    int base = 0;
+    for (int b0 = 0; b0 < n_seqs; b0 += 128) {
+      const int b = b0 + threadIdx.x;
+      const int len = b < n_seqs ? len_of(b) : 0;
+      const int n = count(len);
+      int inc = n;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(FULLM, inc, o);
-      if (lane >= o) inc += y;
-    }
-    if (lane == 31) s_sum[warp] = inc;
-    __syncthreads();
-    int before = base;
-    for (int w = 0; w < warp; ++w) before += s_sum[w];
-    const int excl = before + inc - n;
-    if (n > 0) {
-      for (int w = 0; w < DEC_WARPS; ++w) {
-        const int gs = (blockIdx.x * DEC_WARPS + w) * Ww;
-        if (gs < T && gs >= Hkv * excl && gs < Hkv * (excl + n)) {
-          s_start[w][0] = b;
-          s_start[w][1] = excl;
-          s_start[w][2] = len;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(FULLM, inc, o);
+        if (lane >= o) inc += y;
+      }
+      if (lane == 31) s_sum[warp] = inc;
+      __syncthreads();
+      int before = base;
+      for (int w = 0; w < warp; ++w) before += s_sum[w];
+      const int excl = before + inc - n;
+      if (n > 0) {
+        for (int w = 0; w < DEC_WARPS; ++w) {
+          const int gs = (blockIdx.x * DEC_WARPS + w) * W;
+          if (gs < Ttot && gs >= Hkv * excl && gs < Hkv * (excl + n)) {
+            st[w][0] = b;
+            st[w][1] = excl;
+            st[w][2] = len;
+          }
         }
       }
+      base += s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
+      __syncthreads();
     }
-    base += s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
-    __syncthreads();
-  }
-  auto walk_to = [&](ChunkWalker& w, int gq) {
+  };
+  find_starts(n_chunks_of, Ww, T, s_start);
+  if (WIN) find_starts(n_wrec_of, Wwn, Tw, s_startw);
+  // advance a walker to list entry gq (entries per sequence from `count`)
+  auto walk_gen = [&](ChunkWalker& w, int gq, auto count) {
     while (gq >= w.E) {
       if (++w.h == Hkv) {
         w.h = 0;
         ++w.b;
         w.len = __ldg(seq_lens + w.b);
-        w.nb = n_chunks_of(w.len);
+        w.nb = count(w.len);
       }
       w.S = w.E;
       w.E = w.S + w.nb;
     }
   };
-  ChunkWalker iw;  // issue side
-  if (my_n > 0) {
-    iw.b = s_start[warp][0];
-    iw.len = s_start[warp][2];
-    iw.nb = n_chunks_of(iw.len);
-    const int sb = Hkv * s_start[warp][1];
-    iw.h = (ga - sb) / iw.nb;
-    iw.S = sb + iw.h * iw.nb;
-    iw.E = iw.S + iw.nb;
-  }
-  ChunkWalker cw = iw;  // consume side
+  auto walk_to = [&](ChunkWalker& w, int gq) { walk_gen(w, gq, n_chunks_of); };
+  auto walk_w = [&](ChunkWalker& w, int gq) { walk_gen(w, gq, n_wrec_of); };
+  auto init_walker = [&](ChunkWalker& w, const int* st, int g0, auto count) {
+    w.b = st[0];
+    w.len = st[2];
+    w.nb = count(w.len);
+    const int sb = Hkv * st[1];
+    w.h = (g0 - sb) / w.nb;
+    w.S = sb + w.h * w.nb;
+    w.E = w.S + w.nb;
+  };
+  ChunkWalker iw, iww;  // issue side: INT2 list, window list
+  if (my_n > 0) init_walker(iw, s_start[warp], ga, n_chunks_of);
+  if (WIN && my_nw > 0) init_walker(iww, s_startw[warp], gaw, n_wrec_of);
+  ChunkWalker cw = iw, cww = iww;  // consume side
 
   // Page cache: lane l holds the record index (block * H_kv + h) of page l % PPS
   // of the warp's entry i0 + l / PPS; -2: past the sequence, -1: bad block id.
@@ -401,20 +494,18 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     rec = -2;
     if (i < my_n) {
       walk_to(w, ga + i);
-      const int pg = (ga + i - w.S) * PPS + lane % PPS;
-      if (pg < (w.len + P - 1) / P) {
+      const int pg = S_w / P + (ga + i - w.S) * PPS + lane % PPS;
+      if (pg < (w.len - R_w + P - 1) / P) {
         const int pid = __ldg(table + (size_t)w.b * g.max_blocks + pg);
         rec = (pid >= 0 && pid < g.num_blocks) ? pid * Hkv + w.h : -1;
       }
     }
   };
-  // Stage the warp's i-th chunk: lane 0 arms the stage's mbarrier with the byte
-  // count, then each lane owning a valid page copies it.  Whole warp.
-  auto issue = [&](int i) {
-    n_issued = i + 1;
+  // Stage the warp's i-th list entry in stage sidx: lane 0 arms the stage's
+  // mbarrier with the byte count, then each lane owning a valid page copies it.
+  auto issue_int2 = [&](int i, int sidx) {
     walk_to(iw, ga + i);
     if (i % CPF == 0) fill_cache(i);
-    const int sidx = i % DEC_STAGES;
     const bool mine = lane / PPS == i % CPF;
     const bool ok = mine && rec >= 0;
     const unsigned okm = __ballot_sync(FULLM, ok);
@@ -432,18 +523,48 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
       bulk_g2s(stage_ptr(warp, sidx) + (lane % PPS) * REC, pool + (size_t)rec * g.record, REC, bar);
     }
   };
-
-  if (my_n > 0) {
+  // Window record j of the warp's slice (one 4,096-byte copy by lane 0).
+  // Local record r of a unit: sink record r (r < ns), else the recent group of
+  // positions starting at (a & ~7) + 8 (r - ns), a = max(S_w, len - R_w).
+  auto wrec_first_pos = [&](const ChunkWalker& w, int r) {
+    const int ns = (min(S_w, w.len) + 7) >> 3;
+    return r < ns ? 8 * r : (max(S_w, w.len - R_w) & ~7) + 8 * (r - ns);
+  };
+  auto issue_win = [&](int j, int sidx) {
+    walk_w(iww, gaw + j);
+    const int p0 = wrec_first_pos(iww, gaw + j - iww.S);
+    const int slot = p0 < S_w ? p0 : S_w + (R_w ? p0 % R_w : 0);
+    uint64_t* bar = &bars[warp][sidx];
     if (lane == 0) {
-      for (int s = 0; s < DEC_STAGES; ++s) mbar_init(&bars[warp][s], 1);
+      mbar_arrive_expect_tx(bar, WIN_REC_BYTES);
+      fence_proxy_async();
+      bulk_g2s(stage_ptr(warp, sidx),
+               win.buf + (((size_t)iww.b * Hkv + iww.h) * n_wrec + slot / WIN_REC_TOKENS) * WIN_REC_BYTES,
+               WIN_REC_BYTES, bar);
+    }
+    __syncwarp();
+  };
+  // Fill f of the warp's stage ring: even warps take their window records first,
+  // odd warps last, so that window (bandwidth) and INT2 (instruction) phases overlap.
+  const bool win_first = WIN && (gw & 1) == 0;
+  auto issue = [&](int f) {
+    n_issued = f + 1;
+    const int sidx = f % NST;
+    if (WIN && (win_first ? f < my_nw : f >= my_n)) issue_win(win_first ? f : f - my_n, sidx);
+    else issue_int2(win_first ? f - my_nw : f, sidx);
+  };
+
+  if (F > 0) {
+    if (lane == 0) {
+      for (int s = 0; s < NST; ++s) mbar_init(&bars[warp][s], 1);
       fence_mbar_init();
     }
     __syncwarp();
-    for (int i = 0; i < DEC_STAGES && i < my_n; ++i) issue(i);
+    for (int f = 0; f < NST && f < F; ++f) issue(f);
   }
   pdl_wait();               // the query fragments and spans come from qprep_kernel
   pdl_launch_dependents();  // the combine kernel may be scheduled as blocks retire
-  if (my_n <= 0) return;    // no block-level synchronisation follows
+  if (F <= 0) return;       // no block-level synchronisation follows
 
   // ---- per-segment state (one segment = the warp's entries of one unit) ----
   uint32_t bq[NT][8][2];  // B fragments of q'.c, k-slice s (see qprep_kernel)
@@ -647,53 +768,254 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     }
   };
 
-  bool aborted = false;
-  int consumed = 0;
-  for (int i = 0; i < my_n; ++i) {
-    const int sidx = i % DEC_STAGES;
-    bool ok = false;
-    for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][sidx], (i / DEC_STAGES) & 1);
-    ok = __all_sync(FULLM, ok);
-    if (!ok) {
-      if (lane == 0) flag_error(err, ERR_TIMEOUT);
-      aborted = true;
-      break;
-    }
-    consumed = i + 1;
-    walk_to(cw, ga + i);
-    const int u = cw.b * Hkv + cw.h;
-    if (u != cur_u) {
-      if (cur_u >= 0) finish_segment();
-      start_segment(u);
-      cur_u = u;
-      cur_S = cw.S;
-      cur_E = cw.E;
-    }
-    const int bits = sflag[warp][sidx];
-    const int tokS = (ga + i - cw.S) * 64;
+  if constexpr (!WIN) {
+    // without windows the fills are the list entries: the plain loop
+    bool aborted = false;
+    int consumed = 0;
+    for (int i = 0; i < my_n; ++i) {
+      const int sidx = i % NST;
+      bool ok = false;
+      for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][sidx], (i / NST) & 1);
+      ok = __all_sync(FULLM, ok);
+      if (!ok) {
+        if (lane == 0) flag_error(err, ERR_TIMEOUT);
+        aborted = true;
+        break;
+      }
+      consumed = i + 1;
+      walk_to(cw, ga + i);
+      const int u = cw.b * Hkv + cw.h;
+      if (u != cur_u) {
+        if (cur_u >= 0) finish_segment();
+        start_segment(u);
+        cur_u = u;
+        cur_S = cw.S;
+        cur_E = cw.E;
+      }
+      const int bits = sflag[warp][sidx];
+      const int tokS = (ga + i - cw.S) * 64;
 #pragma unroll 1
-    for (int sub = 0; sub < 2; ++sub) {  // the stage's two 32-token chunks
-      const int tok0 = tokS + 32 * sub;
-      if (tok0 >= cw.len) break;
-      const uint8_t* st = stage_ptr(warp, sidx) + sub * CHUNK;
-      const uint32_t vaddr = vrow + sidx * STAGE + sub * CHUNK;
-      const int cbits = (bits >> (sub * PPC)) & (int)CHUNK_PAGES;
-      if (tok0 + 32 <= cw.len && cbits == (int)CHUNK_PAGES) chunk(std::true_type{}, st, vaddr, tok0, cw.len, cbits);
-      else chunk(std::false_type{}, st, vaddr, tok0, cw.len, cbits);
+      for (int sub = 0; sub < 2; ++sub) {  // the stage's two 32-token chunks
+        const int tok0 = tokS + 32 * sub;
+        if (tok0 >= cw.len) break;
+        const uint8_t* st = stage_ptr(warp, sidx) + sub * CHUNK;
+        const uint32_t vaddr = vrow + sidx * STAGE + sub * CHUNK;
+        const int cbits = (bits >> (sub * PPC)) & (int)CHUNK_PAGES;
+        if (tok0 + 32 <= cw.len && cbits == (int)CHUNK_PAGES) chunk(std::true_type{}, st, vaddr, tok0, cw.len, cbits);
+        else chunk(std::false_type{}, st, vaddr, tok0, cw.len, cbits);
+      }
+      __syncwarp();
+      if (i + NST < my_n) issue(i + NST);
     }
-    __syncwarp();
-    if (i + DEC_STAGES < my_n) issue(i + DEC_STAGES);
-  }
-  if (aborted) {
+    if (aborted) {
+      // wait (bounded) for the copies still in flight before the stages go away;
+      // the open segment is dropped (its unit's output is not written, the error flag is set)
+      for (int i = consumed; i < n_issued; ++i) {
+        bool ok = false;
+        for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][i % NST], (i / NST) & 1);
+      }
+      return;
+    }
+    if (cur_u >= 0) finish_segment();
+    return;
+  } else {
+  int consumed = 0;  // fills consumed
+  // Bounded wait for fill f; false (error flag set) if its copies never completed.
+  auto wait_fill = [&](int f) {
+    bool ok = false;
+    for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][f % NST], (f / NST) & 1);
+    ok = __all_sync(FULLM, ok);
+    if (!ok && lane == 0) flag_error(err, ERR_TIMEOUT);
+    return ok;
+  };
+
+  // ---- INT2 phase: the warp's list entries, fills f0 .. f0 + my_n - 1 ----
+  auto run_int2 = [&](int f0) {
+    for (int i = 0; i < my_n; ++i) {
+      const int f = f0 + i;
+      const int sidx = f % NST;
+      if (!wait_fill(f)) return false;
+      consumed = f + 1;
+      walk_to(cw, ga + i);
+      const int u = cw.b * Hkv + cw.h;
+      if (u != cur_u) {
+        if (cur_u >= 0) finish_segment();
+        start_segment(u);
+        cur_u = u;
+        cur_S = cw.S;
+        cur_E = cw.E;
+      }
+      const int bits = sflag[warp][sidx];
+      const int e = cw.len - R_w;  // INT2 positions end here (the recent window follows)
+      const int tokS = S_w + (ga + i - cw.S) * 64;
+#pragma unroll 1
+      for (int sub = 0; sub < 2; ++sub) {  // the stage's two 32-token chunks
+        const int tok0 = tokS + 32 * sub;
+        if (tok0 >= e) break;
+        const uint8_t* st = stage_ptr(warp, sidx) + sub * CHUNK;
+        const uint32_t vaddr = vrow + sidx * STAGE + sub * CHUNK;
+        const int cbits = (bits >> (sub * PPC)) & (int)CHUNK_PAGES;
+        if (tok0 + 32 <= e && cbits == (int)CHUNK_PAGES) chunk(std::true_type{}, st, vaddr, tok0, e, cbits);
+        else chunk(std::false_type{}, st, vaddr, tok0, e, cbits);
+      }
+      __syncwarp();
+      if (f + NST < F) issue(f + NST);
+    }
+    if (cur_u >= 0) finish_segment();
+    return true;
+  };
+
+  // ---- window phase: 8-token BF16 records, fills f0 .. f0 + my_nw - 1 ----
+  // Keys (centred, not rotated) meet the unrotated query; values are already in
+  // the rotated basis.  Scores: A = the 8 key rows (rows 8-15 of the tile are
+  // zero), B = the query fragments (bf16 high part and remainder per head);
+  // values: A = the value rows transposed (ldmatrix .trans), k = the 8 tokens.
+  // Rows are stored with the 16-byte chunk c of row r at c ^ r, so the 8 rows of
+  // one ldmatrix come from 8 different bank groups.
+  auto run_win = [&](int f0) {
+    if constexpr (WIN) {
+      uint32_t bw[NT][8][2];
+      float wm[NT], wthr[NT], wl[NT];
+      float wacc[NT][8][4];
+      int wu = -1, wS = 0, wE = 0;
+      auto wstart = [&](int u) {
+        const uint32_t* fr = ws.wqfrag + (size_t)u * NT * 16 * 32 + lane;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int s = 0; s < 8; ++s) {
+            bw[nt][s][0] = __ldg(fr + (nt * 16 + 2 * s) * 32);
+            bw[nt][s][1] = __ldg(fr + (nt * 16 + 2 * s + 1) * 32);
+          }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          wm[nt] = -INFINITY;
+          wthr[nt] = -INFINITY;
+          wl[nt] = 0.f;
+#pragma unroll
+          for (int mt = 0; mt < 8; ++mt) wacc[nt][mt][0] = wacc[nt][mt][1] = wacc[nt][mt][2] = wacc[nt][mt][3] = 0.f;
+        }
+      };
+      auto wfinish = [&]() {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) wl[nt] += __shfl_xor_sync(FULLM, wl[nt], o);
+        float* pp = ws.partw + (size_t)(gw + wu) * G * PART;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int j = 4 * nt + ti;
+          if (j < G) {
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {  // channel rows 16 mt + g and 16 mt + 8 + g; high part + remainder
+              pp[j * PART + 16 * mt + gi] = wacc[nt][mt][0] + wacc[nt][mt][1];
+              pp[j * PART + 16 * mt + 8 + gi] = wacc[nt][mt][2] + wacc[nt][mt][3];
+            }
+            if (gi == 0) {
+              pp[j * PART + D] = wm[nt];
+              pp[j * PART + D + 1] = wl[nt];
+            }
+          }
+        }
+        if (lane == 0 && gw == wS / Wwn) ws.spanw[wu] = make_int2(gw, (wE - 1) / Wwn);
+      };
+      const uint32_t krow = (uint32_t)(lane & 7) * 256u;
+      for (int j = 0; j < my_nw; ++j) {
+        const int f = f0 + j;
+        const int sidx = f % NST;
+        if (!wait_fill(f)) return false;
+        consumed = f + 1;
+        walk_w(cww, gaw + j);
+        const int u = cww.b * Hkv + cww.h;
+        if (u != wu) {
+          if (wu >= 0) wfinish();
+          wstart(u);
+          wu = u;
+          wS = cww.S;
+          wE = cww.E;
+        }
+        // rows holding window positions: p0 + r inside the sink [0, min(S_w, len)) or the recent part [a, len)
+        const int p0 = wrec_first_pos(cww, gaw + j - cww.S);
+        const int lo = p0 < S_w ? 0 : max(S_w, cww.len - R_w);
+        const int hi = p0 < S_w ? min(S_w, cww.len) : cww.len;
+        const int first = max(lo - p0, 0), last = min(hi - p0, 8);
+        const unsigned vmask = (0xffu >> (8 - last)) & (0xffu << first) & 0xffu;
+        const uint32_t sbase = smem_u32(stage_ptr(warp, sidx)) + krow;
+        float d[NT][4];
+#pragma unroll
+        for (int sp = 0; sp < 4; ++sp) {  // k-slices 2 sp and 2 sp + 1 (channels 32 sp .. 32 sp + 31)
+          uint32_t kr[4];
+          ldsm_x4(sbase + ((uint32_t)((4 * sp + (lane >> 3)) ^ (lane & 7)) << 4), kr);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            if (sp == 0) mma16816_bf16_zero(d[nt], kr[0], 0u, kr[1], 0u, bw[nt][0][0], bw[nt][0][1]);
+            else mma16816_bf16(d[nt], kr[0], 0u, kr[1], 0u, bw[nt][2 * sp][0], bw[nt][2 * sp][1]);
+            mma16816_bf16(d[nt], kr[2], 0u, kr[3], 0u, bw[nt][2 * sp + 1][0], bw[nt][2 * sp + 1][1]);
+          }
+        }
+        const bool tv = (vmask >> gi) & 1u;  // this lane's row (token gi) holds a window position
+        uint32_t bpw[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const float sc = tv ? d[nt][0] + d[nt][1] : -INFINITY;  // log2 units (q carries log2(e)/sqrt(128))
+          if (__any_sync(FULLM, sc > wthr[nt])) {
+            float mx = fmaxf(sc, __shfl_xor_sync(FULLM, sc, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(FULLM, mx, 16));
+            const bool need = mx > wthr[nt];
+            const float alpha = need ? ex2(wm[nt] - mx) : 1.f;
+            if (need) {
+              wm[nt] = mx;
+              wthr[nt] = mx + TAU;
+            }
+            wl[nt] *= alpha;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+              wacc[nt][mt][0] *= alpha; wacc[nt][mt][1] *= alpha; wacc[nt][mt][2] *= alpha; wacc[nt][mt][3] *= alpha;
+            }
+          }
+          const float pw = ex2(sc - wm[nt]);
+          wl[nt] += pw;
+          const __nv_bfloat16 ph = __float2bfloat16_rn(pw);
+          const __nv_bfloat16 pr = __float2bfloat16_rn(pw - __bfloat162float(ph));
+          const uint32_t pk = (uint32_t)__bfloat16_as_ushort(ph) | ((uint32_t)__bfloat16_as_ushort(pr) << 16);
+          // B fragment: tokens 2t, 2t + 1 of column g (head 4 nt + g/2, high part or remainder)
+          bpw[nt] = prmt(__shfl_sync(FULLM, pk, srcA), __shfl_sync(FULLM, pk, srcA + 4), sel);
+        }
+        // rows outside the window may hold stale or unwritten data: zero them (their weight is 0 already)
+        const uint32_t tmask = vmask == 0xffu ? 0xffffffffu
+                                              : ((((vmask >> (2 * ti)) & 1u) ? 0x0000ffffu : 0u) |
+                                                 (((vmask >> (2 * ti + 1)) & 1u) ? 0xffff0000u : 0u));
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {  // channel tiles 2 qq and 2 qq + 1
+          uint32_t vr[4];
+          ldsm_x4_trans(sbase + 2048u + ((uint32_t)((4 * qq + (lane >> 3)) ^ (lane & 7)) << 4), vr);
+#pragma unroll
+          for (int x = 0; x < 4; ++x) vr[x] &= tmask;
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma16816_bf16(wacc[nt][2 * qq], vr[0], vr[1], 0u, 0u, bpw[nt], 0u);
+            mma16816_bf16(wacc[nt][2 * qq + 1], vr[2], vr[3], 0u, 0u, bpw[nt], 0u);
+          }
+        }
+        __syncwarp();
+        if (f + NST < F) issue(f + NST);
+      }
+      if (wu >= 0) wfinish();
+    }
+    return true;
+  };
+
+  const bool ok = win_first ? (run_win(0) && run_int2(my_nw)) : (run_int2(0) && run_win(my_n));
+  if (!ok) {
     // wait (bounded) for the copies still in flight before the stages go away;
     // the open segment is dropped (its unit's output is not written, the error flag is set)
-    for (int i = consumed; i < n_issued; ++i) {
-      bool ok = false;
-      for (int it = 0; it < WAIT_LIMIT && !ok; ++it) ok = mbar_try_wait(&bars[warp][i % DEC_STAGES], (i / DEC_STAGES) & 1);
+    for (int f = consumed; f < n_issued; ++f) {
+      bool done = false;
+      for (int it = 0; it < WAIT_LIMIT && !done; ++it) done = mbar_try_wait(&bars[warp][f % NST], (f / NST) & 1);
     }
-    return;
   }
-  if (cur_u >= 0) finish_segment();
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -764,15 +1086,147 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
   }
 }
 
+// ---------------------------------------------------------------------------
+// Combine with BF16 windows: one CTA (8 warps) per unit.  Warp w merges the
+// slots w, w + 8, ... of the unit -- its INT2 partials, then its window
+// partials -- for all G query heads in one online pass (running maximum m_j,
+// rescaled sums; several slots' loads in flight), into l_j, A_j (INT2, already
+// in the rotated-V basis) and W_j (window values, unrotated).  The warp states
+// are then merged in warp order (deterministic), and W_j is rotated once by
+// R_V,h (Eq. 27): the FWHT for the signed Hadamard, and for a dense R each
+// warp multiplies 16 rows of R, the row blocks again added in warp order.
+//   o_rot = (A + W R_V) / l
+// ---------------------------------------------------------------------------
+constexpr int CBW_WARPS = 8;
+
+template <int G>
+__global__ void __launch_bounds__(CBW_WARPS * 32) decode_combine_win_kernel(int n_kv_heads, int n_q_heads, DecWs ws,
+                                                                           RotDev rot_v, float* __restrict__ o_rot) {
+  __shared__ __align__(16) float sA[G][D];
+  __shared__ __align__(16) float sW[G][D];
+  __shared__ __align__(16) float sY[G][D];
+  __shared__ float sL[G], sM[G];
+  pdl_wait();               // the partials come from decode_split_kernel
+  pdl_launch_dependents();  // a following projection may start streaming its weights
+  const int u = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int b = u / n_kv_heads, h = u % n_kv_heads;
+  const int2 sp = __ldcg(ws.span + u), spw = __ldcg(ws.spanw + u);
+  const int ni = max(0, sp.y - sp.x + 1), nwin = max(0, spw.y - spw.x + 1);
+  const int ns = ni + nwin;
+  if (ns == 0) return;  // no cached tokens (o = 0 already) or an invalid length
+  const size_t stride = (size_t)G * PART;
+  const float* base = ws.part + (size_t)(sp.x + u) * G * PART;
+  const float* basew = nwin ? ws.partw + (size_t)(spw.x + u) * G * PART : base;
+
+  float m[G], l[G];
+  float4 a[G], wv[G];
+#pragma unroll
+  for (int j = 0; j < G; ++j) {
+    m[j] = -INFINITY;
+    l[j] = 0.f;
+    a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+    wv[j] = a[j];
+  }
+#pragma unroll 4
+  for (int t = warp; t < ns; t += CBW_WARPS) {
+    const bool win = t >= ni;
+    const float* pp = win ? basew + (t - ni) * stride : base + t * stride;
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + j * PART + D));
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(pp + j * PART) + lane);
+      const float mn = fmaxf(m[j], ml.x);
+      const float so = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);  // rescale of the running sums
+      const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mn);
+      const float ea = win ? 0.f : e, ew = win ? e : 0.f;
+      m[j] = mn;
+      l[j] = fmaf(e, ml.y, l[j] * so);
+      a[j].x = fmaf(ea, x.x, a[j].x * so); a[j].y = fmaf(ea, x.y, a[j].y * so);
+      a[j].z = fmaf(ea, x.z, a[j].z * so); a[j].w = fmaf(ea, x.w, a[j].w * so);
+      wv[j].x = fmaf(ew, x.x, wv[j].x * so); wv[j].y = fmaf(ew, x.y, wv[j].y * so);
+      wv[j].z = fmaf(ew, x.z, wv[j].z * so); wv[j].w = fmaf(ew, x.w, wv[j].w * so);
+    }
+  }
+  // warp states merged in warp order, rescaled to the running maximum
+  for (int w = 0; w < CBW_WARPS; ++w) {
+    if (warp == w) {
+#pragma unroll
+      for (int j = 0; j < G; ++j) {
+        const float m0 = w ? sM[j] : -INFINITY;
+        const float mn = fmaxf(m0, m[j]);
+        const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn);
+        const float s1 = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);
+        float4 A = w ? reinterpret_cast<float4*>(sA[j])[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        float4 W = w ? reinterpret_cast<float4*>(sW[j])[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        A.x = fmaf(s1, a[j].x, A.x * s0); A.y = fmaf(s1, a[j].y, A.y * s0);
+        A.z = fmaf(s1, a[j].z, A.z * s0); A.w = fmaf(s1, a[j].w, A.w * s0);
+        W.x = fmaf(s1, wv[j].x, W.x * s0); W.y = fmaf(s1, wv[j].y, W.y * s0);
+        W.z = fmaf(s1, wv[j].z, W.z * s0); W.w = fmaf(s1, wv[j].w, W.w * s0);
+        reinterpret_cast<float4*>(sA[j])[lane] = A;
+        reinterpret_cast<float4*>(sW[j])[lane] = W;
+        __syncwarp();
+        if (lane == 0) {
+          sL[j] = fmaf(s1, l[j], (w ? sL[j] : 0.f) * s0);
+          sM[j] = mn;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  // rotate the window sums: y_j = W_j R_V,h
+  if (rot_v.kind == KVQ_ROT_DENSE) {
+    // warp w: rows 16 w .. 16 w + 15 of R (input channels), lane: output channels 4 lane .. 4 lane + 3
+    const float4* R = reinterpret_cast<const float4*>(rot_v.dense + (size_t)h * D * D) + lane;
+    float4 r[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) r[c] = __ldg(R + (size_t)(16 * warp + c) * (D / 4));
+    float4 y[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) {
+      y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float x = sW[j][16 * warp + c];
+        y[j].x = fmaf(x, r[c].x, y[j].x); y[j].y = fmaf(x, r[c].y, y[j].y);
+        y[j].z = fmaf(x, r[c].z, y[j].z); y[j].w = fmaf(x, r[c].w, y[j].w);
+      }
+    }
+    for (int w = 0; w < CBW_WARPS; ++w) {  // row blocks added in warp order
+      if (warp == w) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) {
+          float4 s4 = w ? reinterpret_cast<float4*>(sY[j])[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+          s4.x += y[j].x; s4.y += y[j].y; s4.z += y[j].z; s4.w += y[j].w;
+          reinterpret_cast<float4*>(sY[j])[lane] = s4;
+        }
+      }
+      __syncthreads();
+    }
+  } else {
+    for (int j = warp; j < G; j += CBW_WARPS) {
+      float4 x = reinterpret_cast<const float4*>(sW[j])[lane];
+      if (rot_v.kind == KVQ_ROT_SIGNED_HADAMARD) x = rotate_vec_warp(x, rot_v, h, lane, false);
+      reinterpret_cast<float4*>(sY[j])[lane] = x;
+    }
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < G * D; i += CBW_WARPS * 32) {
+    const int j = i / D, c = i % D;
+    const float L = sL[j];
+    o_rot[((size_t)b * n_q_heads + h * G + j) * D + c] = L > 0.f ? (sA[j][c] + sY[j][c]) / L : 0.f;
+  }
+}
+
 // Shared-memory ring of the decode kernel: 4 warps x DEC_STAGES stages of 64 tokens.
 constexpr int DEC_SMEM = DEC_WARPS * DEC_STAGES * 2 * 1152 * 2;
 
-template <int G, int P>
+template <int G, int P, bool WIN>
 cudaError_t decode_smem_attr() {
   static bool done = false;  // one flag per kernel instance
   if (done) return cudaSuccess;
   const cudaError_t e =
-      cudaFuncSetAttribute(decode_split_kernel<G, P>, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM);
+      cudaFuncSetAttribute(decode_split_kernel<G, P, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM);
   if (e == cudaSuccess) done = true;
   return e;
 }
@@ -780,12 +1234,13 @@ cudaError_t decode_smem_attr() {
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q, int q_dtype,
                           const int32_t* seq_lens, int max_seq_len, const int32_t* table, RotDev rot_k,
                           const uint8_t* pool, int n_ctas, void* ws_base, float* o_rot, unsigned* err,
-                          cudaStream_t s) {
+                          cudaStream_t s, WinGeom win, RotDev rot_v) {
   (void)max_seq_len;
   if (n_seqs == 0) return cudaSuccess;
   const int gqa = n_q_heads / g.n_kv_heads;
+  const bool windows = win.sink + win.recent > 0;
   DecWs ws;
-  decode_ws_layout(ws_base, n_seqs, g.n_kv_heads, gqa, n_ctas, &ws);
+  decode_ws_layout(ws_base, n_seqs, g.n_kv_heads, gqa, n_ctas, windows, &ws);
   const dim3 qg(g.n_kv_heads, n_seqs);
   const bool dense = rot_k.kind == KVQ_ROT_DENSE;
 #define KVQ_QPREP(GG)                                                                                     \
@@ -813,15 +1268,17 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-#define KVQ_DEC(GG, PP)                                                                                    \
+#define KVQ_DEC_W(GG, PP, WW)                                                                              \
   do {                                                                                                    \
-    e = decode_smem_attr<GG, PP>();                                                                       \
+    e = decode_smem_attr<GG, PP, WW>();                                                                   \
     if (e == cudaSuccess)                                                                                 \
-      e = cudaLaunchKernelEx(&cfg, decode_split_kernel<GG, PP>, g, n_seqs, n_q_heads, seq_lens, table, pool, ws, \
-                             o_rot, err);                                                                  \
+      e = cudaLaunchKernelEx(&cfg, decode_split_kernel<GG, PP, WW>, g, n_seqs, n_q_heads, seq_lens, table, pool, \
+                             ws, o_rot, err, win);                                                         \
   } while (0)
+#define KVQ_DEC(GG, PP) \
+  if (windows) KVQ_DEC_W(GG, PP, true); else KVQ_DEC_W(GG, PP, false)
 #define KVQ_DEC_P(GG) \
-  if (g.page_tokens == 16) KVQ_DEC(GG, 16); else KVQ_DEC(GG, 8)
+  if (g.page_tokens == 16) { KVQ_DEC(GG, 16); } else { KVQ_DEC(GG, 8); }
   switch (gqa) {
     case 1: KVQ_DEC_P(1); break;
     case 2: KVQ_DEC_P(2); break;
@@ -831,6 +1288,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   }
 #undef KVQ_DEC_P
 #undef KVQ_DEC
+#undef KVQ_DEC_W
   if (e != cudaSuccess) return e;
 
   // the combine is a programmatic dependent of the decode kernel
@@ -839,10 +1297,12 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   const int per_unit = (DEC_WARPS * n_ctas + units - 1) / units + 1;
   int nw = 1;
   while (nw < CB_MAX_WARPS && nw * 8 < per_unit) nw *= 2;
-  cfg.gridDim = dim3(units, gqa);
-  cfg.blockDim = dim3(nw * 32);
+  cfg.gridDim = windows ? dim3(units) : dim3(units, gqa);
+  cfg.blockDim = dim3(windows ? CBW_WARPS * 32 : nw * 32);
   cfg.dynamicSmemBytes = 0;
-#define KVQ_CB(GG) e = cudaLaunchKernelEx(&cfg, decode_combine_kernel<GG>, g.n_kv_heads, n_q_heads, ws, o_rot)
+#define KVQ_CB(GG)                                                                                          \
+  e = windows ? cudaLaunchKernelEx(&cfg, decode_combine_win_kernel<GG>, g.n_kv_heads, n_q_heads, ws, rot_v, o_rot) \
+              : cudaLaunchKernelEx(&cfg, decode_combine_kernel<GG>, g.n_kv_heads, n_q_heads, ws, o_rot)
   switch (gqa) {
     case 1: KVQ_CB(1); break;
     case 2: KVQ_CB(2); break;

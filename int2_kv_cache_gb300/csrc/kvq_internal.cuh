@@ -30,6 +30,14 @@ struct RotDev {
 
 inline RotDev to_dev(const kvq_rot& r) { return RotDev{r.kind, r.signs, r.dense}; }
 
+// BF16 windows (see kvq_window): sizes in tokens and the record buffer.
+struct WinGeom {
+  int sink, recent;
+  uint8_t* buf;
+};
+constexpr int WIN_REC_TOKENS = 8;
+constexpr int WIN_REC_BYTES = 4096;  // 8 key rows + 8 value rows of 128 bf16
+
 struct PageGeom {
   int page_tokens;
   int n_kv_heads;
@@ -84,13 +92,19 @@ cudaError_t launch_rotate_df(int n_rows, int n_heads, const void* src, int dtype
 cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x_lo, float clip,
                                  float* out, cudaStream_t s);
 
-// decode.cu
+// window.cu
+cudaError_t launch_window_append(int n_kv_heads, int n_seqs, int n_new, const void* k, const void* v,
+                                 int dtype, const int32_t* cu_new, const int32_t* start_pos,
+                                 const float* mu_k, WinGeom win, unsigned* err, cudaStream_t s);
+
+// decode.cu (win.sink = win.recent = 0: no windows)
 int decode_auto_ctas(int n_seqs, int n_kv_heads, int gqa, int max_seq_len);
-size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas);
+size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas, bool windows = false);
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q,
                           int q_dtype, const int32_t* seq_lens, int max_seq_len,
                           const int32_t* table, RotDev rot_k, const uint8_t* pool, int n_ctas,
-                          void* ws, float* o_rot, unsigned* err, cudaStream_t s);
+                          void* ws, float* o_rot, unsigned* err, cudaStream_t s,
+                          WinGeom win = WinGeom{0, 0, nullptr}, RotDev rot_v = RotDev{0, nullptr, nullptr});
 
 // outproj.cu
 cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, int w_dtype,

@@ -167,3 +167,47 @@ def test_calib_rejects_bad_arguments(kvq):
     out = ctypes.c_size_t(0)
     assert lib.kvq_calib_workspace_size(64, 65, 2, 2, 0, ctypes.byref(out)) == kvq.KVQ_EINVAL
     assert lib.kvq_calib_workspace_size(64, 4, 2, 2, 0, ctypes.byref(out)) == kvq.KVQ_OK and out.value > 0
+
+
+def test_window_arguments_are_checked(kvq):
+    lib = kvq.lib()
+    lay = _layout(kvq)
+    ident = kvq.KvqRot(0, None, None)
+    fake = 0x10000
+
+    def append(win, n_new=4):
+        return lib.kvq_window_append(ctypes.byref(lay), 1, n_new, fake, fake, 0, fake, fake, None,
+                                     ctypes.byref(win), None)
+
+    assert append(kvq.KvqWindow(32, 8, fake)) == kvq.KVQ_EINVAL and b"sink" in lib.kvq_last_error()
+    assert append(kvq.KvqWindow(64, 12, fake)) == kvq.KVQ_EINVAL and b"recent" in lib.kvq_last_error()
+    assert append(kvq.KvqWindow(64, 8, None)) == kvq.KVQ_EINVAL and b"buf" in lib.kvq_last_error()
+    assert append(kvq.KvqWindow(64, 8, fake + 8)) == kvq.KVQ_EINVAL
+    assert append(kvq.KvqWindow(65536, 8, fake)) == kvq.KVQ_EUNSUPPORTED
+    # no windows, or nothing to append: OK without touching a pointer
+    assert append(kvq.KvqWindow(0, 0, None)) == kvq.KVQ_OK
+    assert append(kvq.KvqWindow(64, 8, fake), n_new=0) == kvq.KVQ_OK
+
+
+def test_windowed_workspace_adds_a_second_partial_set(kvq):
+    lay = _layout(kvq, max_blocks_per_seq=4096)
+    a = lambda x: (x + 255) // 256 * 256
+    n_seqs, ctas = 16, 5
+    plain = kvq.kvq_decode_workspace_size(lay, n_seqs, 160, ctas)
+    assert kvq.kvq_decode_workspace_size_win(lay, n_seqs, 160, None, ctas) == plain
+    assert kvq.kvq_decode_workspace_size_win(lay, n_seqs, 160, kvq.Window(0, 0), ctas) == plain
+    u = n_seqs * 8
+    win = kvq.Window(64, 256, None)
+    win.buf = None
+    # a window struct with sizes needs a buffer even for the size query
+    with pytest.raises(kvq.KvqError):
+        kvq.kvq_decode_workspace_size_win(lay, n_seqs, 160, win, ctas)
+
+    class _Buf:  # an aligned address standing in for a device buffer (never dereferenced)
+        def data_ptr(self):
+            return 0x10000
+
+    win.buf = _Buf()
+    got = kvq.kvq_decode_workspace_size_win(lay, n_seqs, 160, win, ctas)
+    extra = a((4 * ctas + u) * 4 * 132 * 4) + a(u * 16 * 1 * 32 * 4) + a(u * 8)
+    assert got == plain + extra
