@@ -51,6 +51,9 @@ def parse():
     p.add_argument("--seqs", type=int, default=None, help="sequences (default: 16 gqa8b, 1 long4b, 64 serve14b)")
     p.add_argument("--ctx", type=int, default=None, help="context (gqa8b default 32768, long4b 131072)")
     p.add_argument("--splits", type=int, default=0)
+    p.add_argument("--page", type=int, choices=[8, 16], default=None, help="tokens per page (default 16)")
+    p.add_argument("--clips", default=None, metavar="K,V",
+                   help="clip ratios of keys and values, e.g. 0.96,0.92 (Table A); default per workload")
     p.add_argument("--window", default=None, metavar="SINK,RECENT",
                    help="decode step with BF16 sink / recent windows, e.g. 64,256 (default: all tokens INT2)")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -170,20 +173,27 @@ def gen_parallel(fn, n):
 def decode_workload(args):
     """The decode case named by --workload (sizes from --seqs / --ctx when given)."""
     from int2_kv_cache_gb300 import workloads as W
+    kw = {}
+    if args.page:
+        kw["page_tokens"] = args.page
+    if args.clips:
+        kw["clip_k"], kw["clip_v"] = (float(x) for x in args.clips.split(","))
     if args.workload == "long4b":
-        return W.long4b_128k(n_seqs=args.seqs or 1, ctx=args.ctx or 131072)
+        return W.long4b_128k(n_seqs=args.seqs or 1, ctx=args.ctx or 131072, **kw)
     if args.workload == "serve14b":
-        return W.serve14b_ragged(n_seqs=args.seqs or 64)
-    return W.gqa8b_32k(n_seqs=args.seqs or 16, ctx=args.ctx or 32768)
+        return W.serve14b_ragged(n_seqs=args.seqs or 64, **kw)
+    return W.gqa8b_32k(n_seqs=args.seqs or 16, ctx=args.ctx or 32768, **kw)
 
 
 def workload_text(c) -> str:
     lens = np.asarray(c.seq_lens)
     ctx = f"ctx {int(lens[0])}" if lens.min() == lens.max() else f"ragged ctx {int(lens.min())}..{int(lens.max())}"
     rot = {"dense": "dense expm(A-A^T)", "signed_hadamard": "signed-Hadamard", "identity": "identity"}[c.rot_k.kind]
+    clip = (f"clip {float(c.clip_k):g}" if c.clip_k == c.clip_v else
+            f"clips K {float(c.clip_k):g} / V {float(c.clip_v):g}")
     return (f"{c.name.split('_')[0]} decode step: B={len(lens)} x {ctx}, Hq {c.n_q_heads} / Hkv {c.n_kv_heads}, "
             f"d 128, hidden {c.d_model}, {c.page_tokens}-token pages (shuffled), {rot} rotations, mu-centred keys, "
-            f"clip {float(c.clip_k):g}")
+            f"{clip}")
 
 
 class DecodeStep:

@@ -277,29 +277,32 @@ def tiny_single_head(seed: int = 1) -> DecodeCase:
     return c
 
 
-def gqa8b_32k(seed: int = 3, n_seqs: int = 16, ctx: int = 32768) -> DecodeCase:
+def gqa8b_32k(seed: int = 3, n_seqs: int = 16, ctx: int = 32768, page_tokens: int = 16, clip_k: float = 1.0,
+              clip_v: float = 1.0) -> DecodeCase:
     """8B-class GQA decode layer: H_q 32, H_kv 8, d_model 4096, bf16, 16 x 32K,
     16-token pages with a shuffled table, dense expm(A - A^T) rotations."""
-    return decode_case(seed, [ctx] * n_seqs, 32, 8, 4096, "dense", "bf16",
-                       name=f"gqa8b_B{n_seqs}_ctx{ctx}")
+    return decode_case(seed, [ctx] * n_seqs, 32, 8, 4096, "dense", "bf16", page_tokens=page_tokens,
+                       clip_k=clip_k, clip_v=clip_v, name=f"gqa8b_B{n_seqs}_ctx{ctx}")
 
 
-def long4b_128k(seed: int = 4, n_seqs: int = 1, ctx: int = 131072) -> DecodeCase:
+def long4b_128k(seed: int = 4, n_seqs: int = 1, ctx: int = 131072, page_tokens: int = 16, clip_k: float = 0.9,
+                clip_v: float = 0.9) -> DecodeCase:
     """4B-class long-context layer: H_q 32, H_kv 8, d_model 2560, bf16, 128K context,
     signed-Hadamard R per head, clip 0.9 (plus a 4,096-token prefill append)."""
-    c = decode_case(seed, [ctx] * n_seqs, 32, 8, 2560, "signed_hadamard", "bf16",
-                    clip_k=0.9, clip_v=0.9, name=f"long4b_B{n_seqs}_ctx{ctx}")
+    c = decode_case(seed, [ctx] * n_seqs, 32, 8, 2560, "signed_hadamard", "bf16", page_tokens=page_tokens,
+                    clip_k=clip_k, clip_v=clip_v, name=f"long4b_B{n_seqs}_ctx{ctx}")
     c.extra["chunk"] = 4096
     return c
 
 
-def serve14b_ragged(seed: int = 5, n_seqs: int = 64) -> DecodeCase:
+def serve14b_ragged(seed: int = 5, n_seqs: int = 64, page_tokens: int = 16, clip_k: float = 1.0,
+                    clip_v: float = 1.0) -> DecodeCase:
     """14B-class serving layer: H_q 40, H_kv 10, d_model 5120, bf16, 64 ragged
     contexts uniform in [1024, 8192], dense per-head R."""
     g = _rng(seed, _TAG_LENS)
     lens = g.integers(1024, 8192 + 1, size=n_seqs)
-    return decode_case(seed, lens, 40, 10, 5120, "dense", "bf16", n_cal=2560,
-                       name=f"serve14b_B{n_seqs}_ragged")
+    return decode_case(seed, lens, 40, 10, 5120, "dense", "bf16", page_tokens=page_tokens, clip_k=clip_k,
+                       clip_v=clip_v, n_cal=2560, name=f"serve14b_B{n_seqs}_ragged")
 
 
 @dataclass
