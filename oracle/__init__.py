@@ -23,6 +23,8 @@ numpy, with no blocking, fusion or reordering beyond what the definitions state:
   NMSE, the exact key/value error decomposition (Eq. 8), summary statistics.
 * ``calib``      -- the candidate-rotation x clip-ratio sweep scored by post-W_O
   NMSE with argmin selection ("Output-aware INT2 KV-cache rotation evaluation").
+* ``report``     -- the per-head output-error report (Figure 5: RMS error as a
+  percentage of plain INT2; the Eq. 8 key/value split).
 * ``window``     -- BF16 sink and recent windows beside the INT2 cache (§5
   implementation details, Table A; appendix "OptR Algorithm"): membership, the
   window record layout, bf16 rounding, the windowed decode readout.
@@ -32,4 +34,4 @@ forms, library routines, brute force on tiny inputs or constants printed on the
 pages; the page-1 NMSE values (52.35 / 1.96) are the one quantity left
 "parity unpinned" (their generator and data recipe are not published).
 """
-from . import rotations, quant, cache, attention, output, calib, window  # noqa: F401
+from . import rotations, quant, cache, attention, output, calib, window, report  # noqa: F401
