@@ -44,7 +44,7 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    p.add_argument("--case", choices=["decode_step", "append_chunk", "append_chunk_dense", "calib"],
+    p.add_argument("--case", choices=["decode_step", "append_chunk", "append_chunk_dense", "calib", "report"],
                    default="decode_step")
     p.add_argument("--workload", choices=["gqa8b", "long4b", "serve14b"], default="gqa8b",
                    help="decode-step shape: gqa8b (default, the headline), long4b (128K), serve14b (ragged)")
@@ -625,12 +625,51 @@ def run_calib(args):
                       "clips": len(cc.clips), "heads": cc.n_kv_heads}), flush=True)
 
 
+def run_report(args):
+    """Per-head output-error report on the 14B-class calibration trace: the first two
+    dense candidates as R_K and R_V, key centring, Table A's clips 0.96 / 0.92."""
+    import torch
+    import int2_kv_cache_gb300 as kvq
+    from int2_kv_cache_gb300 import workloads as W
+    device = "cuda:0"
+    cc = W.serve14b_calibration(n_cand=2)
+    t = lambda x, dt=torch.float32: torch.from_numpy(np.ascontiguousarray(x)).to(device).to(dt)
+    bf = torch.bfloat16
+    mu = torch.empty(cc.n_kv_heads, 128, device=device)
+    kvq.kvq_key_mean(t(cc.k, bf), mu)
+    ws = torch.empty(kvq.kvq_report_workspace_size(cc.n_tok, cc.n_qpos, cc.n_kv_heads, cc.gqa),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty(5, cc.n_kv_heads, dtype=torch.float64, device=device)
+    rk, rv = (kvq.DeviceRot.from_spec(x, device) for x in cc.cands[:2])
+    q, k, v, w = t(cc.q, bf), t(cc.k, bf), t(cc.v, bf), t(cc.w_o, bf)
+
+    def step():
+        kvq.kvq_head_error_report(q, k, v, w, rk, rv, mu, 0.96, 0.92, out, ws)
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    n = max(1, min(args.steps, 5))
+    for _ in range(n):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    o = out.cpu().numpy()
+    print(json.dumps({"case": "report", "ms": e0.elapsed_time(e1) / n, "heads": cc.n_kv_heads, "n_tok": cc.n_tok,
+                      "n_qpos": cc.n_qpos, "rms_pct_of_naive": [round(float(x), 2) for x in 100 * np.sqrt(o[0] / o[3])],
+                      "key_share": [round(float(x), 3) for x in o[1] / (o[1] + o[2])]}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
     elif args.case in ("append_chunk", "append_chunk_dense"):
         run_append_chunk(args)
+    elif args.case == "report":
+        run_report(args)
     elif args.case == "calib":
         run_calib(args)
     else:

@@ -313,6 +313,34 @@ kvq_status kvq_calib_nmse(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_
                           double* nmse, double* ref, void* workspace, size_t workspace_bytes,
                           kvq_stream stream);
 
+/* Workspace bytes for kvq_head_error_report. */
+kvq_status kvq_report_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int gqa, size_t* bytes);
+
+/* Per-head output-error report ("Output-Aware Rotation for INT2 KV-Cache
+ * Quantization", Figure 5 and the appendix "Output-space error"; the key/value
+ * split of Eq. 8).  For the queries at the last n_qpos positions of an n_tok-token
+ * trace (causal, s <= t) and every query head j, with KV head h = j / gqa,
+ *   Delta y_{t,j} = (p~^T V~ - p^T V) W_O,j^T
+ * where p uses the raw keys, p~ the candidate's effective keys (centred by mu,
+ * rotated by R_K, INT2 with clip_k, met by q R_K), V~ = Q_2(V R_V; clip_v) R_V^T.
+ * out (device, double [5][n_kv_heads]) receives per KV head h, summed over the
+ * positions and the query heads of h:
+ *   [0] E       = sum ||Delta y||^2
+ *   [1] E_key   = sum ||(p~ - p)^T V W_O,j^T||^2        (key-induced term of Eq. 8)
+ *   [2] E_val   = sum ||p~^T (V~ - V) W_O,j^T||^2       (value-induced term)
+ *   [3] E_naive = E of plain per-group INT2: identity rotations, no centring, same clips
+ *   [4] Y       = sum ||p^T V W_O,j^T||^2
+ * The RMS error as a percentage of plain INT2 is 100 sqrt(E / E_naive).
+ * Shapes and limits as kvq_calib_nmse: q [n_qpos][n_kv_heads*gqa][128],
+ * k, v [n_tok][n_kv_heads][128] (dtype), w_o [d_model][n_kv_heads*gqa*128] (w_dtype,
+ * unfolded), mu float [n_kv_heads][128] (unrotated) or NULL, n_tok <= 12288.
+ * Sums are in a fixed order except for d_model <= 128 (double atomics). */
+kvq_status kvq_head_error_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model,
+                                 const void* q, const void* k, const void* v, kvq_dtype dtype,
+                                 const void* w_o, kvq_dtype w_dtype, kvq_rot rot_k, kvq_rot rot_v,
+                                 const float* mu, float clip_k, float clip_v, double* out,
+                                 void* workspace, size_t workspace_bytes, kvq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,9 @@ def lib() -> ctypes.CDLL:
             "kvq_fold_wo": ([i, i, i, vp, i, KvqRot, vp, i, vp], st),
             "kvq_out_proj": ([i, i, i, vp, vp, i, vp, vp], st),
             "kvq_calib_workspace_size": ([i, i, i, i, i, ctypes.POINTER(sz)], st),
+            "kvq_report_workspace_size": ([i, i, i, i, ctypes.POINTER(sz)], st),
+            "kvq_head_error_report": ([i, i, i, i, i, vp, vp, vp, i, vp, i, KvqRot, KvqRot, vp, f, f, vp, vp, sz,
+                                       vp], st),
             "kvq_calib_nmse": ([i, i, i, i, i, vp, vp, vp, i, vp, i, i, ctypes.POINTER(KvqRot), i,
                                 ctypes.POINTER(ctypes.c_float), vp, i, vp, vp, vp, sz, vp], st),
         }
@@ -85,7 +88,8 @@ EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mea
             "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention",
             "kvq_decode_attention_noalloc", "kvq_window_append", "kvq_decode_workspace_size_win",
             "kvq_decode_attention_win", "kvq_fold_wo",
-            "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse")
+            "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse", "kvq_report_workspace_size",
+            "kvq_head_error_report")
 
 
 def _check(status: int) -> None:
@@ -278,3 +282,21 @@ def kvq_calib_nmse(q, k, v, w_o, cands, clips, mu, joint: bool, nmse, ref, works
                                 len(cands), rot_arr, len(clips), clip_arr, _ptr(mu), int(joint), _ptr(nmse),
                                 _ptr(ref), _ptr(workspace), workspace.numel() * workspace.element_size(),
                                 _stream(stream)))
+
+
+def kvq_report_workspace_size(n_tok: int, n_qpos: int, n_kv_heads: int, gqa: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().kvq_report_workspace_size(n_tok, n_qpos, n_kv_heads, gqa, ctypes.byref(out)))
+    return int(out.value)
+
+
+def kvq_head_error_report(q, k, v, w_o, rot_k: DeviceRot, rot_v: DeviceRot, mu, clip_k: float, clip_v: float, out,
+                          workspace, stream=None) -> None:
+    """out: float64 [5, H_kv] (E, E_key, E_val, E_naive, Y per KV head; see include/kvq.h)."""
+    n_qpos, hq, _ = q.shape
+    n_tok, hkv, _ = k.shape
+    _check(lib().kvq_head_error_report(n_tok, n_qpos, hkv, hq // hkv, w_o.shape[0], _ptr(_contig(q, "q")),
+                                       _ptr(_contig(k, "k")), _ptr(_contig(v, "v")), _dtype_code(k),
+                                       _ptr(_contig(w_o, "w_o")), _dtype_code(w_o), rot_k.c, rot_v.c, _ptr(mu),
+                                       float(clip_k), float(clip_v), _ptr(out), _ptr(workspace),
+                                       workspace.numel() * workspace.element_size(), _stream(stream)))

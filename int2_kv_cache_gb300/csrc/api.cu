@@ -389,4 +389,42 @@ kvq_status kvq_calib_nmse(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_calib_nmse");
 }
 
+kvq_status kvq_report_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int gqa, size_t* bytes) {
+  if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");
+  if (n_tok < 1 || n_qpos < 1 || n_qpos > n_tok || n_kv_heads < 1 || gqa < 1)
+    return fail(KVQ_EINVAL, "bad shape n_tok %d n_qpos %d n_kv_heads %d gqa %d", n_tok, n_qpos, n_kv_heads, gqa);
+  *bytes = kvq::report_workspace_bytes(n_tok, n_qpos, n_kv_heads, gqa);
+  return KVQ_OK;
+}
+
+kvq_status kvq_head_error_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model, const void* q,
+                                 const void* k, const void* v, kvq_dtype dtype, const void* w_o, kvq_dtype w_dtype,
+                                 kvq_rot rot_k, kvq_rot rot_v, const float* mu, float clip_k, float clip_v,
+                                 double* out, void* workspace, size_t workspace_bytes, kvq_stream stream) {
+  if (n_tok < 1 || n_qpos < 1 || n_qpos > n_tok || n_kv_heads < 1 || d_model < 1)
+    return fail(KVQ_EINVAL, "bad shape n_tok %d n_qpos %d n_kv_heads %d d_model %d", n_tok, n_qpos, n_kv_heads,
+                d_model);
+  if (gqa != 1 && gqa != 2 && gqa != 4 && gqa != 8)
+    return fail(KVQ_EUNSUPPORTED, "query heads per KV head %d: supported 1, 2, 4, 8", gqa);
+  if (n_tok > 12288) return fail(KVQ_EUNSUPPORTED, "n_tok %d > 12288 calibration tokens", n_tok);
+  if (!valid_dtype(dtype) || !valid_dtype(w_dtype)) return fail(KVQ_EINVAL, "bad dtype");
+  if (!valid_clip(clip_k) || !valid_clip(clip_v))
+    return fail(KVQ_EINVAL, "clip ratios must lie in (0, 1] (got %g, %g)", clip_k, clip_v);
+  KVQ_CHECK(check_rot(rot_k, "rot_k"));
+  KVQ_CHECK(check_rot(rot_v, "rot_v"));
+  KVQ_PTR(q, "q");
+  KVQ_PTR(k, "k");
+  KVQ_PTR(v, "v");
+  KVQ_PTR(w_o, "w_o");
+  KVQ_PTR(out, "out");
+  KVQ_PTR(workspace, "workspace");
+  if (mu && !aligned16(mu)) return fail(KVQ_EINVAL, "mu is not 16-byte aligned");
+  const size_t need = kvq::report_workspace_bytes(n_tok, n_qpos, n_kv_heads, gqa);
+  if (workspace_bytes < need) return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  cudaError_t e = kvq::launch_head_report(n_tok, n_qpos, n_kv_heads, gqa, d_model, q, k, v, dtype, w_o, w_dtype,
+                                          kvq::to_dev(rot_k), kvq::to_dev(rot_v), mu, clip_k, clip_v, out,
+                                          workspace, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_head_error_report");
+}
+
 }  // extern "C"

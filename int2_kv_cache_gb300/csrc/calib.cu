@@ -19,37 +19,49 @@ namespace kvq {
 struct CalibWs {
   float *qf, *qr, *kf, *vf, *xk_hi, *xk_lo, *xv_hi, *xv_lo, *kq, *vq, *o_rot, *o_ref, *o_un, *gram, *part;
   double* gpart;  // [n_groups][(gd / 32)^2] quadratic-form partials
+  double* qsum;   // [5][H_q] per-query-head sums of the error report
 };
 
 constexpr int CA_SPLIT_MAX = 8;  // key splits of the calibration attention
 
 static size_t align_up(size_t x) { return (x + 255) & ~size_t(255); }
 
-static CalibWs carve(void* ws, int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint,
+// Scored groups: n_groups column blocks of gd channels of the attention output
+// (joint: one of H_q 128; per KV head: H_kv of G 128; per query head: H_q of 128).
+static CalibWs carve(void* ws, int n_tok, int n_qpos, int n_kv_heads, int gqa, int n_groups, int gd,
                      size_t* total) {
   const size_t hq = (size_t)n_kv_heads * gqa;
   const size_t qn = (size_t)n_qpos * hq * D, kn = (size_t)n_tok * n_kv_heads * D;
-  const size_t gd = joint ? hq * D : (size_t)gqa * D;
-  const size_t gn = (joint ? 1 : (size_t)n_kv_heads) * gd * gd;
+  const size_t gn = (size_t)n_groups * gd * gd;
   const size_t pn = (size_t)CA_SPLIT_MAX * n_qpos * hq * (D + 4);  // attention partials
-  const size_t gpn = 2 * (joint ? 1 : (size_t)n_kv_heads) * (gd / 32) * (gd / 32);  // doubles, as float pairs
-  const size_t sizes[16] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn, pn, gpn};
+  const size_t gpn = 2 * (size_t)n_groups * (gd / 32) * (gd / 32);  // doubles, as float pairs
+  const size_t sizes[17] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn, pn, gpn, 2 * 5 * hq};
   char* p = static_cast<char*>(ws);
-  float* ptrs[16];
+  float* ptrs[17];
   size_t off = 0;
-  for (int i = 0; i < 16; ++i) {
+  for (int i = 0; i < 17; ++i) {
     ptrs[i] = reinterpret_cast<float*>(p + off);
     off += align_up(sizes[i] * sizeof(float));
   }
   if (total) *total = off;
   return CalibWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6], ptrs[7],
                  ptrs[8], ptrs[9], ptrs[10], ptrs[11], ptrs[12], ptrs[13], ptrs[14],
-                 reinterpret_cast<double*>(ptrs[15])};
+                 reinterpret_cast<double*>(ptrs[15]), reinterpret_cast<double*>(ptrs[16])};
 }
+
+static int calib_groups(int n_kv_heads, int joint) { return joint ? 1 : n_kv_heads; }
+static int calib_gd(int n_kv_heads, int gqa, int joint) { return (joint ? n_kv_heads * gqa : gqa) * D; }
 
 size_t calib_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint) {
   size_t total = 0;
-  carve(nullptr, n_tok, n_qpos, n_kv_heads, gqa, joint, &total);
+  carve(nullptr, n_tok, n_qpos, n_kv_heads, gqa, calib_groups(n_kv_heads, joint), calib_gd(n_kv_heads, gqa, joint),
+        &total);
+  return total;
+}
+
+size_t report_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa) {
+  size_t total = 0;
+  carve(nullptr, n_tok, n_qpos, n_kv_heads, gqa, n_kv_heads * gqa, D, &total);
   return total;
 }
 
@@ -477,9 +489,9 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
                          const float* clips, const float* mu, int joint, double* nmse,
                          double* ref, void* ws, cudaStream_t s) {
   const int hq = n_kv_heads * gqa;
-  const int n_groups = joint ? 1 : n_kv_heads;
-  const int gd = joint ? hq * D : gqa * D;
-  CalibWs w = carve(ws, n_tok, n_qpos, n_kv_heads, gqa, joint, nullptr);
+  const int n_groups = calib_groups(n_kv_heads, joint);
+  const int gd = calib_gd(n_kv_heads, gqa, joint);
+  CalibWs w = carve(ws, n_tok, n_qpos, n_kv_heads, gqa, n_groups, gd, nullptr);
   const size_t qn = (size_t)n_qpos * hq * D, kn = (size_t)n_tok * n_kv_heads * D;
   auto blocks = [](size_t n) { return (unsigned)((n + 255) / 256); };
 
@@ -526,6 +538,89 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
     }
   }
   divide_kernel<<<(n_out + 255) / 256, 256, 0, s>>>(nmse, ref, n_out, n_groups);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Per-head output-error report ("Output-Aware Rotation for INT2 KV-Cache
+// Quantization", Figure 5 and the appendix "Output-space error"; Eq. 8).  Every
+// query head j is scored on its own: ||Delta y_{t,j}||^2 = ||du W_O,j^T||^2 with
+// du over the 128 channels of head j (groups of one query head).  Four causal
+// attention passes over the trace:
+//   reference  o   = softmax(q k) v                       raw keys and values
+//   candidate  o~  = softmax(qR_K Q(kR_K)) Q(vR_V) R_V^T  (keys centred by mu)
+//   keys only  o^K = softmax(qR_K Q(kR_K)) v              p~ with the exact values
+//   plain INT2 o^N = softmax(q Q(k)) Q(v)                 identity, no centring
+// give E = |o~ - o|, E_key = |o^K - o| (Eq. 8's (p~ - p) V term), E_val =
+// |o~ - o^K| (its p~ (V~ - V) term), E_naive = |o^N - o| and Y = |o| (each the
+// sum over positions of the squared post-W_O norms), summed per KV head.
+// ---------------------------------------------------------------------------
+__global__ void group_sum_kernel(int n_rows, int n_groups, int per, const double* __restrict__ in,
+                                 double* __restrict__ out) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_rows * n_groups) return;
+  const int r = i / n_groups, g = i % n_groups;
+  double t = 0.0;
+  for (int j = 0; j < per; ++j) t += in[(size_t)r * n_groups * per + g * per + j];  // fixed order
+  out[i] = t;
+}
+
+cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model, const void* q,
+                               const void* k, const void* v, int dtype, const void* w_o, int w_dtype, RotDev rot_k,
+                               RotDev rot_v, const float* mu, float clip_k, float clip_v, double* out, void* ws,
+                               cudaStream_t s) {
+  const int hq = n_kv_heads * gqa;
+  const int n_groups = hq, gd = D;
+  CalibWs w = carve(ws, n_tok, n_qpos, n_kv_heads, gqa, n_groups, gd, nullptr);
+  const size_t qn = (size_t)n_qpos * hq * D, kn = (size_t)n_tok * n_kv_heads * D;
+  auto blocks = [](size_t n) { return (unsigned)((n + 255) / 256); };
+  const RotDev ident{KVQ_ROT_IDENTITY, nullptr, nullptr};
+
+  to_f32_kernel<<<blocks(qn), 256, 0, s>>>(qn, hq, q, dtype, nullptr, w.qf);
+  to_f32_kernel<<<blocks(kn), 256, 0, s>>>(kn, n_kv_heads, k, dtype, nullptr, w.kf);
+  to_f32_kernel<<<blocks(kn), 256, 0, s>>>(kn, n_kv_heads, v, dtype, nullptr, w.vf);
+  zero_f64_kernel<<<1, 256, 0, s>>>(w.qsum, 5 * hq);
+  KVQ_TRY(cudaSuccess);
+  const bool direct = d_model <= gd;
+  if (!direct) gram_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype, w.gram);
+  auto out_err = [&](const float* a, const float* b, double* dst) {
+    if (direct)
+      proj_err_kernel<<<dim3(n_qpos, n_groups), 256, (size_t)gd * sizeof(float), s>>>(n_qpos, n_groups, gd, d_model,
+                                                                                   a, b, w_o, w_dtype, dst);
+    else {
+      gram_trace_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(n_qpos, n_groups, gd, a, b, w.gram, w.gpart);
+      gram_reduce_kernel<<<n_groups, 256, 0, s>>>((gd / 32) * (gd / 32), w.gpart, dst);
+    }
+  };
+  double* e_tot = w.qsum;
+  double* e_key = w.qsum + hq;
+  double* e_val = w.qsum + 2 * hq;
+  double* e_naive = w.qsum + 3 * hq;
+  double* y_ref = w.qsum + 4 * hq;
+  // reference
+  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qf, w.kf, w.vf, w.o_ref, w.part, s));
+  out_err(w.o_ref, nullptr, y_ref);
+  // candidate: keys centred and rotated by R_K, values rotated by R_V, both INT2
+  KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, k, dtype, mu, rot_k, w.xk_hi, w.xk_lo, s));
+  KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, v, dtype, nullptr, rot_v, w.xv_hi, w.xv_lo, s));
+  KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.qf, rot_k, w.qr, false, s));
+  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clip_k, w.kq, s));
+  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clip_v, w.vq, s));
+  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qr, w.kq, w.vq, w.o_rot, w.part, s));
+  KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.o_rot, rot_v, w.o_un, true, s));  // o~ (unrotated)
+  out_err(w.o_un, w.o_ref, e_tot);
+  // keys only: the candidate's weights p~ with the exact values (unrotated basis)
+  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qr, w.kq, w.vf, w.o_rot, w.part, s));
+  out_err(w.o_rot, w.o_ref, e_key);
+  out_err(w.o_un, w.o_rot, e_val);
+  // plain per-group INT2: identity rotations, no centring, the same clips
+  KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, k, dtype, nullptr, ident, w.xk_hi, w.xk_lo, s));
+  KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, v, dtype, nullptr, ident, w.xv_hi, w.xv_lo, s));
+  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clip_k, w.kq, s));
+  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clip_v, w.vq, s));
+  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qf, w.kq, w.vq, w.o_rot, w.part, s));
+  out_err(w.o_rot, w.o_ref, e_naive);
+  group_sum_kernel<<<blocks(5 * n_kv_heads), 256, 0, s>>>(5, n_kv_heads, gqa, w.qsum, out);
   return cudaGetLastError();
 }
 
