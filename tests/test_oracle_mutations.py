@@ -8,11 +8,13 @@ wrong side would not slip through.
 import numpy as np
 import pytest
 
-from oracle import quant, attention, output, rotations
+from oracle import quant, attention, output, rotations, window, report
 import test_oracle_quant as tq
 import test_oracle_attention as ta
 import test_oracle_output as to
 import test_oracle_rotations as tr
+import test_oracle_window as tw
+import test_oracle_report as trep
 
 
 def _floor_quantize(x, clip):
@@ -55,6 +57,28 @@ def _output_side_signs(signs):
     return rotations.sylvester_hadamard(len(s)) * s[None, :] / np.sqrt(len(s))
 
 
+def _unrotated_window_readout(q, k_hat, v_hat, win_pos, win_k, win_v, r_k, r_v, gqa, length, sink, recent):
+    eye = np.broadcast_to(np.eye(128), np.shape(r_v))
+    return _ORIG_WINDOWED(q, k_hat, v_hat, win_pos, win_k, win_v, r_k, eye, gqa, length, sink, recent)
+
+
+def _uncentred_window_key(k, mu=None):
+    return _ORIG_WINDOW_KEY(k, None)
+
+
+def _recent_edge_off_by_one(length, sink, recent):
+    p = np.arange(length)
+    return p[(p < sink) | (p > length - recent)]
+
+
+def _value_term_with_exact_weights(p, p_tilde, v, v_tilde, w_j):
+    dy, dk, _ = output.error_decomposition(p, p_tilde, v, v_tilde, w_j)
+    return dy, dk, (np.asarray(p) @ (np.asarray(v_tilde) - np.asarray(v))) @ np.asarray(w_j).T
+
+
+_ORIG_WINDOWED = window.decode_attention_windowed
+_ORIG_WINDOW_KEY = window.window_key
+
 MUTATIONS = [
     ("floor instead of round", quant, "quantize_groups", _floor_quantize,
      lambda: tq.test_codes_equal_nearest_level_brute_force(1.0)),
@@ -68,6 +92,14 @@ MUTATIONS = [
      to.test_folded_wo_reproduces_unrotated_output),
     ("signs on the output side", rotations, "signed_hadamard", _output_side_signs,
      tr.test_signed_hadamard_orthogonal_and_equals_fwht_of_signed_input),
+    ("window values not rotated into the readout basis", window, "decode_attention_windowed",
+     _unrotated_window_readout, lambda: tw.test_windowed_readout_equals_plain_attention_on_lossless_inputs(64, 40, 150)),
+    ("window keys not centred", window, "window_key", _uncentred_window_key,
+     lambda: tw.test_windowed_readout_equals_plain_attention_on_lossless_inputs(64, 40, 150)),
+    ("recent window edge off by one", window, "window_positions", _recent_edge_off_by_one,
+     tw.test_membership_matches_brute_force),
+    ("Eq. 8 value term with the exact weights", report, "error_decomposition", _value_term_with_exact_weights,
+     trep.test_matches_pure_python_loops),
 ]
 
 
