@@ -27,6 +27,12 @@
 // The second and third kernels are programmatic dependent launches: the batch
 // scan and the first page copies overlap the query rotation, and the combine
 // blocks are scheduled as decode blocks retire.
+// With BF16 sink / recent windows (decode_split_kernel<..., true>), positions
+// [0, S) and [L - R, L) of a sequence are read from 8-token bf16 records instead
+// of the pages: the records form a second list split evenly over the warps,
+// staged through the same ring; their keys (centred, not rotated) meet the
+// unrotated query, their values (unrotated) are summed apart, and
+// decode_combine_win_kernel rotates that sum by R_V once per unit (Eq. 27).
 // Inside a warp, q'.c and sum_t (p_t s_t) c_t are tensor-core products
 // (mma.sync m16n8k16, fp16 inputs, fp32 accumulation).  A 2-bit field masked in
 // place inside a 16-bit word is the fp16 value c * 2^(p-24) (a subnormal, p =
