@@ -835,42 +835,6 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     return ok;
   };
 
-  // ---- INT2 phase: the warp's list entries, fills f0 .. f0 + my_n - 1 ----
-  auto run_int2 = [&](int f0) {
-    for (int i = 0; i < my_n; ++i) {
-      const int f = f0 + i;
-      const int sidx = f % NST;
-      if (!wait_fill(f)) return false;
-      consumed = f + 1;
-      walk_to(cw, ga + i);
-      const int u = cw.b * Hkv + cw.h;
-      if (u != cur_u) {
-        if (cur_u >= 0) finish_segment();
-        start_segment(u);
-        cur_u = u;
-        cur_S = cw.S;
-        cur_E = cw.E;
-      }
-      const int bits = sflag[warp][sidx];
-      const int e = cw.len - R_w;  // INT2 positions end here (the recent window follows)
-      const int tokS = S_w + (ga + i - cw.S) * 64;
-#pragma unroll 1
-      for (int sub = 0; sub < 2; ++sub) {  // the stage's two 32-token chunks
-        const int tok0 = tokS + 32 * sub;
-        if (tok0 >= e) break;
-        const uint8_t* st = stage_ptr(warp, sidx) + sub * CHUNK;
-        const uint32_t vaddr = vrow + sidx * STAGE + sub * CHUNK;
-        const int cbits = (bits >> (sub * PPC)) & (int)CHUNK_PAGES;
-        if (tok0 + 32 <= e && cbits == (int)CHUNK_PAGES) chunk(std::true_type{}, st, vaddr, tok0, e, cbits);
-        else chunk(std::false_type{}, st, vaddr, tok0, e, cbits);
-      }
-      __syncwarp();
-      if (f + NST < F) issue(f + NST);
-    }
-    if (cur_u >= 0) finish_segment();
-    return true;
-  };
-
   // ---- window phase: 8-token BF16 records, fills f0 .. f0 + my_nw - 1 ----
   // Keys (centred, not rotated) meet the unrotated query; values are already in
   // the rotated basis.  Scores: A = the 8 key rows (rows 8-15 of the tile are
@@ -1012,7 +976,51 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     return true;
   };
 
-  const bool ok = win_first ? (run_win(0) && run_int2(my_nw)) : (run_int2(0) && run_win(my_n));
+  bool ok = true;
+  if (win_first) ok = run_win(0);
+  if (ok) {
+    // ---- INT2 phase: the warp's list entries, fills f0 .. f0 + my_n - 1 (the plain loop) ----
+    const int f0 = win_first ? my_nw : 0;
+    for (int i = 0; i < my_n; ++i) {
+      const int f = f0 + i;
+      const int sidx = f % NST;
+      bool got = false;
+      for (int it = 0; it < WAIT_LIMIT && !got; ++it) got = mbar_try_wait(&bars[warp][sidx], (f / NST) & 1);
+      got = __all_sync(FULLM, got);
+      if (!got) {
+        if (lane == 0) flag_error(err, ERR_TIMEOUT);
+        ok = false;
+        break;
+      }
+      consumed = f + 1;
+      walk_to(cw, ga + i);
+      const int u = cw.b * Hkv + cw.h;
+      if (u != cur_u) {
+        if (cur_u >= 0) finish_segment();
+        start_segment(u);
+        cur_u = u;
+        cur_S = cw.S;
+        cur_E = cw.E;
+      }
+      const int bits = sflag[warp][sidx];
+      const int e = cw.len - R_w;  // INT2 positions end here (the recent window follows)
+      const int tokS = S_w + (ga + i - cw.S) * 64;
+#pragma unroll 1
+      for (int sub = 0; sub < 2; ++sub) {  // the stage's two 32-token chunks
+        const int tok0 = tokS + 32 * sub;
+        if (tok0 >= e) break;
+        const uint8_t* st = stage_ptr(warp, sidx) + sub * CHUNK;
+        const uint32_t vaddr = vrow + sidx * STAGE + sub * CHUNK;
+        const int cbits = (bits >> (sub * PPC)) & (int)CHUNK_PAGES;
+        if (tok0 + 32 <= e && cbits == (int)CHUNK_PAGES) chunk(std::true_type{}, st, vaddr, tok0, e, cbits);
+        else chunk(std::false_type{}, st, vaddr, tok0, e, cbits);
+      }
+      __syncwarp();
+      if (f + NST < F) issue(f + NST);
+    }
+    if (ok && cur_u >= 0) finish_segment();
+  }
+  if (ok && !win_first) ok = run_win(my_n);
   if (!ok) {
     // wait (bounded) for the copies still in flight before the stages go away;
     // the open segment is dropped (its unit's output is not written, the error flag is set)
