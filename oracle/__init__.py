@@ -23,6 +23,9 @@ numpy, with no blocking, fusion or reordering beyond what the definitions state:
   NMSE, the exact key/value error decomposition (Eq. 8), summary statistics.
 * ``calib``      -- the candidate-rotation x clip-ratio sweep scored by post-W_O
   NMSE with argmin selection ("Output-aware INT2 KV-cache rotation evaluation").
+* ``optr``       -- Algorithm 1 on one KV head: the key and value losses (Eqs.
+  12-16), straight-through gradients (Eq. 18) through R = R^0 exp(A - A^T)
+  (Eq. 11), Adam, selection every 20 steps.
 * ``report``     -- the per-head output-error report (Figure 5: RMS error as a
   percentage of plain INT2; the Eq. 8 key/value split).
 * ``window``     -- BF16 sink and recent windows beside the INT2 cache (§5
@@ -34,4 +37,4 @@ forms, library routines, brute force on tiny inputs or constants printed on the
 pages; the page-1 NMSE values (52.35 / 1.96) are the one quantity left
 "parity unpinned" (their generator and data recipe are not published).
 """
-from . import rotations, quant, cache, attention, output, calib, window, report  # noqa: F401
+from . import rotations, quant, cache, attention, output, calib, window, report, optr  # noqa: F401
