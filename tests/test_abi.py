@@ -211,3 +211,25 @@ def test_windowed_workspace_adds_a_second_partial_set(kvq):
     got = kvq.kvq_decode_workspace_size_win(lay, n_seqs, 160, win, ctas)
     extra = a((4 * ctas + u) * 4 * 132 * 4) + a(u * 16 * 1 * 32 * 4) + a(u * 8)
     assert got == plain + extra
+
+
+def test_report_arguments_are_checked(kvq):
+    lib = kvq.lib()
+    fake = 0x10000
+    ident = kvq.KvqRot(0, None, None)
+    out = ctypes.c_size_t(0)
+    assert lib.kvq_report_workspace_size(64, 65, 2, 2, ctypes.byref(out)) == kvq.KVQ_EINVAL
+    assert lib.kvq_report_workspace_size(64, 4, 2, 2, ctypes.byref(out)) == kvq.KVQ_OK and out.value > 0
+    # more positions than tokens, an unsupported head group, a bad clip, a misaligned mu
+    args = lambda **kw: dict(dict(n_tok=64, n_qpos=4, hkv=2, gqa=2, d_model=128, clip_k=1.0, clip_v=1.0, mu=None), **kw)
+
+    def call(a):
+        return lib.kvq_head_error_report(a["n_tok"], a["n_qpos"], a["hkv"], a["gqa"], a["d_model"], fake, fake, fake,
+                                         0, fake, 0, ident, ident, a["mu"], a["clip_k"], a["clip_v"], fake, fake,
+                                         1 << 30, None)
+
+    assert call(args(n_qpos=65)) == kvq.KVQ_EINVAL
+    assert call(args(gqa=3)) == kvq.KVQ_EUNSUPPORTED
+    assert call(args(clip_v=0.0)) == kvq.KVQ_EINVAL and b"clip" in lib.kvq_last_error()
+    assert call(args(mu=fake + 4)) == kvq.KVQ_EINVAL and b"mu" in lib.kvq_last_error()
+    assert call(args(n_tok=20000, n_qpos=4)) == kvq.KVQ_EUNSUPPORTED
