@@ -32,7 +32,7 @@
 // of the pages: the records form a second list split evenly over the warps,
 // staged through the same ring; their keys (centred, not rotated) meet the
 // unrotated query, their values (unrotated) are summed apart, and
-// decode_combine_win_kernel rotates that sum by R_V once per unit (Eq. 27).
+// decode_combine_win_kernel rotates that sum by R_V once per (unit, query head) (Eq. 27).
 // Inside a warp, q'.c and sum_t (p_t s_t) c_t are tensor-core products
 // (mma.sync m16n8k16, fp16 inputs, fp32 accumulation).  A 2-bit field masked in
 // place inside a 16-bit word is the fp16 value c * 2^(p-24) (a subnormal, p =
@@ -1101,14 +1101,14 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
 }
 
 // ---------------------------------------------------------------------------
-// Combine with BF16 windows: one CTA (8 warps) per unit.  Warp w merges the
-// slots w, w + 8, ... of the unit -- its INT2 partials, then its window
-// partials -- for all G query heads in one online pass (running maximum m_j,
-// rescaled sums; several slots' loads in flight), into l_j, A_j (INT2, already
-// in the rotated-V basis) and W_j (window values, unrotated).  The warp states
-// are then merged in warp order (deterministic), and W_j is rotated once by
-// R_V,h (Eq. 27): the FWHT for the signed Hadamard, and for a dense R each
-// warp multiplies 16 rows of R, the row blocks again added in warp order.
+// Combine with BF16 windows: one CTA (8 warps) per (unit, query head j).  Warp w
+// merges the slots w, w + 8, ... of the unit -- its INT2 partials, then its
+// window partials -- in one online pass (running maximum, rescaled sums, several
+// slots' loads in flight) into l, A (INT2, already in the rotated-V basis) and W
+// (window values, unrotated); the warp states are merged in warp order
+// (deterministic).  W is then rotated by R_V,h (Eq. 27): the FWHT for the signed
+// Hadamard, and for a dense R each warp multiplies 16 rows of R, the row blocks
+// added in warp order.
 //   o_rot = (A + W R_V) / l
 // ---------------------------------------------------------------------------
 constexpr int CBW_WARPS = 8;
@@ -1116,13 +1116,13 @@ constexpr int CBW_WARPS = 8;
 template <int G>
 __global__ void __launch_bounds__(CBW_WARPS * 32) decode_combine_win_kernel(int n_kv_heads, int n_q_heads, DecWs ws,
                                                                            RotDev rot_v, float* __restrict__ o_rot) {
-  __shared__ __align__(16) float sA[G][D];
-  __shared__ __align__(16) float sW[G][D];
-  __shared__ __align__(16) float sY[G][D];
-  __shared__ float sL[G], sM[G];
+  __shared__ __align__(16) float sA[D];
+  __shared__ __align__(16) float sW[D];
+  __shared__ __align__(16) float sY[D];
+  __shared__ float sL, sM;
   pdl_wait();               // the partials come from decode_split_kernel
   pdl_launch_dependents();  // a following projection may start streaming its weights
-  const int u = blockIdx.x;
+  const int u = blockIdx.x, j = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = u / n_kv_heads, h = u % n_kv_heads;
   const int2 sp = __ldcg(ws.span + u), spw = __ldcg(ws.spanw + u);
@@ -1130,105 +1130,81 @@ __global__ void __launch_bounds__(CBW_WARPS * 32) decode_combine_win_kernel(int 
   const int ns = ni + nwin;
   if (ns == 0) return;  // no cached tokens (o = 0 already) or an invalid length
   const size_t stride = (size_t)G * PART;
-  const float* base = ws.part + (size_t)(sp.x + u) * G * PART;
-  const float* basew = nwin ? ws.partw + (size_t)(spw.x + u) * G * PART : base;
+  const float* base = ws.part + ((size_t)(sp.x + u) * G + j) * PART;
+  const float* basew = nwin ? ws.partw + ((size_t)(spw.x + u) * G + j) * PART : base;
 
-  float m[G], l[G];
-  float4 a[G], wv[G];
-#pragma unroll
-  for (int j = 0; j < G; ++j) {
-    m[j] = -INFINITY;
-    l[j] = 0.f;
-    a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-    wv[j] = a[j];
-  }
+  float m = -INFINITY, l = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f), w = a;
 #pragma unroll 4
   for (int t = warp; t < ns; t += CBW_WARPS) {
     const bool win = t >= ni;
     const float* pp = win ? basew + (t - ni) * stride : base + t * stride;
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + j * PART + D));
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(pp + j * PART) + lane);
-      const float mn = fmaxf(m[j], ml.x);
-      const float so = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);  // rescale of the running sums
-      const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mn);
-      const float ea = win ? 0.f : e, ew = win ? e : 0.f;
-      m[j] = mn;
-      l[j] = fmaf(e, ml.y, l[j] * so);
-      a[j].x = fmaf(ea, x.x, a[j].x * so); a[j].y = fmaf(ea, x.y, a[j].y * so);
-      a[j].z = fmaf(ea, x.z, a[j].z * so); a[j].w = fmaf(ea, x.w, a[j].w * so);
-      wv[j].x = fmaf(ew, x.x, wv[j].x * so); wv[j].y = fmaf(ew, x.y, wv[j].y * so);
-      wv[j].z = fmaf(ew, x.z, wv[j].z * so); wv[j].w = fmaf(ew, x.w, wv[j].w * so);
-    }
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + D));
+    const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + lane);
+    const float mn = fmaxf(m, ml.x);
+    const float so = m == -INFINITY ? 0.f : exp2f(m - mn);  // rescale of the running sums
+    const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - mn);
+    const float ea = win ? 0.f : e, ew = win ? e : 0.f;
+    m = mn;
+    l = fmaf(e, ml.y, l * so);
+    a.x = fmaf(ea, x.x, a.x * so); a.y = fmaf(ea, x.y, a.y * so);
+    a.z = fmaf(ea, x.z, a.z * so); a.w = fmaf(ea, x.w, a.w * so);
+    w.x = fmaf(ew, x.x, w.x * so); w.y = fmaf(ew, x.y, w.y * so);
+    w.z = fmaf(ew, x.z, w.z * so); w.w = fmaf(ew, x.w, w.w * so);
   }
   // warp states merged in warp order, rescaled to the running maximum
-  for (int w = 0; w < CBW_WARPS; ++w) {
-    if (warp == w) {
-#pragma unroll
-      for (int j = 0; j < G; ++j) {
-        const float m0 = w ? sM[j] : -INFINITY;
-        const float mn = fmaxf(m0, m[j]);
-        const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn);
-        const float s1 = m[j] == -INFINITY ? 0.f : exp2f(m[j] - mn);
-        float4 A = w ? reinterpret_cast<float4*>(sA[j])[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-        float4 W = w ? reinterpret_cast<float4*>(sW[j])[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-        A.x = fmaf(s1, a[j].x, A.x * s0); A.y = fmaf(s1, a[j].y, A.y * s0);
-        A.z = fmaf(s1, a[j].z, A.z * s0); A.w = fmaf(s1, a[j].w, A.w * s0);
-        W.x = fmaf(s1, wv[j].x, W.x * s0); W.y = fmaf(s1, wv[j].y, W.y * s0);
-        W.z = fmaf(s1, wv[j].z, W.z * s0); W.w = fmaf(s1, wv[j].w, W.w * s0);
-        reinterpret_cast<float4*>(sA[j])[lane] = A;
-        reinterpret_cast<float4*>(sW[j])[lane] = W;
-        __syncwarp();
-        if (lane == 0) {
-          sL[j] = fmaf(s1, l[j], (w ? sL[j] : 0.f) * s0);
-          sM[j] = mn;
-        }
+  for (int wv = 0; wv < CBW_WARPS; ++wv) {
+    if (warp == wv) {
+      const float m0 = wv ? sM : -INFINITY;
+      const float mn = fmaxf(m0, m);
+      const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - mn);
+      const float s1 = m == -INFINITY ? 0.f : exp2f(m - mn);
+      float4 A = wv ? reinterpret_cast<float4*>(sA)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      float4 W = wv ? reinterpret_cast<float4*>(sW)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+      A.x = fmaf(s1, a.x, A.x * s0); A.y = fmaf(s1, a.y, A.y * s0);
+      A.z = fmaf(s1, a.z, A.z * s0); A.w = fmaf(s1, a.w, A.w * s0);
+      W.x = fmaf(s1, w.x, W.x * s0); W.y = fmaf(s1, w.y, W.y * s0);
+      W.z = fmaf(s1, w.z, W.z * s0); W.w = fmaf(s1, w.w, W.w * s0);
+      reinterpret_cast<float4*>(sA)[lane] = A;
+      reinterpret_cast<float4*>(sW)[lane] = W;
+      __syncwarp();
+      if (lane == 0) {
+        sL = fmaf(s1, l, (wv ? sL : 0.f) * s0);
+        sM = mn;
       }
     }
     __syncthreads();
   }
-  // rotate the window sums: y_j = W_j R_V,h
+  // rotate the window sum: y = W R_V,h
   if (rot_v.kind == KVQ_ROT_DENSE) {
     // warp w: rows 16 w .. 16 w + 15 of R (input channels), lane: output channels 4 lane .. 4 lane + 3
     const float4* R = reinterpret_cast<const float4*>(rot_v.dense + (size_t)h * D * D) + lane;
-    float4 r[16];
+    float4 y = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int c = 0; c < 16; ++c) r[c] = __ldg(R + (size_t)(16 * warp + c) * (D / 4));
-    float4 y[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) {
-      y[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const float x = sW[j][16 * warp + c];
-        y[j].x = fmaf(x, r[c].x, y[j].x); y[j].y = fmaf(x, r[c].y, y[j].y);
-        y[j].z = fmaf(x, r[c].z, y[j].z); y[j].w = fmaf(x, r[c].w, y[j].w);
-      }
+    for (int c = 0; c < 16; ++c) {
+      const float4 r = __ldg(R + (size_t)(16 * warp + c) * (D / 4));
+      const float x = sW[16 * warp + c];
+      y.x = fmaf(x, r.x, y.x); y.y = fmaf(x, r.y, y.y); y.z = fmaf(x, r.z, y.z); y.w = fmaf(x, r.w, y.w);
     }
-    for (int w = 0; w < CBW_WARPS; ++w) {  // row blocks added in warp order
-      if (warp == w) {
-#pragma unroll
-        for (int j = 0; j < G; ++j) {
-          float4 s4 = w ? reinterpret_cast<float4*>(sY[j])[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
-          s4.x += y[j].x; s4.y += y[j].y; s4.z += y[j].z; s4.w += y[j].w;
-          reinterpret_cast<float4*>(sY[j])[lane] = s4;
-        }
+    for (int wv = 0; wv < CBW_WARPS; ++wv) {  // row blocks added in warp order
+      if (warp == wv) {
+        float4 s4 = wv ? reinterpret_cast<float4*>(sY)[lane] : make_float4(0.f, 0.f, 0.f, 0.f);
+        s4.x += y.x; s4.y += y.y; s4.z += y.z; s4.w += y.w;
+        reinterpret_cast<float4*>(sY)[lane] = s4;
       }
       __syncthreads();
     }
   } else {
-    for (int j = warp; j < G; j += CBW_WARPS) {
-      float4 x = reinterpret_cast<const float4*>(sW[j])[lane];
+    if (warp == 0) {
+      float4 x = reinterpret_cast<const float4*>(sW)[lane];
       if (rot_v.kind == KVQ_ROT_SIGNED_HADAMARD) x = rotate_vec_warp(x, rot_v, h, lane, false);
-      reinterpret_cast<float4*>(sY[j])[lane] = x;
+      reinterpret_cast<float4*>(sY)[lane] = x;
     }
     __syncthreads();
   }
-  for (int i = threadIdx.x; i < G * D; i += CBW_WARPS * 32) {
-    const int j = i / D, c = i % D;
-    const float L = sL[j];
-    o_rot[((size_t)b * n_q_heads + h * G + j) * D + c] = L > 0.f ? (sA[j][c] + sY[j][c]) / L : 0.f;
+  if (threadIdx.x < D) {
+    const int c = threadIdx.x;
+    o_rot[((size_t)b * n_q_heads + h * G + j) * D + c] = sL > 0.f ? (sA[c] + sY[c]) / sL : 0.f;
   }
 }
 
@@ -1311,7 +1287,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   const int per_unit = (DEC_WARPS * n_ctas + units - 1) / units + 1;
   int nw = 1;
   while (nw < CB_MAX_WARPS && nw * 8 < per_unit) nw *= 2;
-  cfg.gridDim = windows ? dim3(units) : dim3(units, gqa);
+  cfg.gridDim = dim3(units, gqa);
   cfg.blockDim = dim3(windows ? CBW_WARPS * 32 : nw * 32);
   cfg.dynamicSmemBytes = 0;
 #define KVQ_CB(GG)                                                                                          \
