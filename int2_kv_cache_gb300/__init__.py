@@ -7,6 +7,30 @@ built, importing the binding functions raises.
 
 Functions carry the C names (``kvq_quantize_append``, ``kvq_decode_attention``,
 ``kvq_out_proj``, ``kvq_calib_nmse`` and helpers) and take torch tensors.
+
+A decode step, end to end (shapes as in ``include/kvq.h``)::
+
+    import torch, int2_kv_cache_gb300 as kvq
+    from int2_kv_cache_gb300 import _build
+    _build.build()                                   # nvcc, sm_103a, in-tree libkvq.so
+    lay = kvq.make_layout(page_tokens=16, n_kv_heads=8, n_q_heads=32, num_blocks=nb, max_blocks_per_seq=mb)
+    pool = torch.zeros(kvq.kvq_pool_bytes(lay), dtype=torch.uint8, device="cuda")
+    rk = kvq.DeviceRot("dense", dense=r_k)           # [H_kv, 128, 128] fp32; or "signed_hadamard" / "identity"
+    rv = kvq.DeviceRot("dense", dense=r_v)
+    kvq.kvq_key_mean(k_calib, mu)                    # Eq. 19; then mu R_K (Eq. 20):
+    kvq.kvq_rotate_heads(mu[None], rk, mu_rot[None])
+    kvq.kvq_quantize_append(lay, k, v, cu_new, start_pos, table, rk, rv, mu_rot, 0.96, 0.92, pool)
+    ws = torch.empty(kvq.kvq_decode_workspace_size(lay, n_seqs, max_len), dtype=torch.uint8, device="cuda")
+    kvq.kvq_decode_attention(lay, q, seq_lens, max_len, table, rk, pool, ws, o_rot)
+    kvq.kvq_fold_wo(w_o, 32, 8, rv, w_fold)          # once: W_O R_V (Eqs. 29-31)
+    kvq.kvq_out_proj(o_rot.reshape(n_seqs, -1), w_fold, y)
+
+With BF16 sink / recent windows, add ``win = kvq.Window(64, 256, buf)`` (``buf`` of
+``kvq.Window.buffer_bytes(n_seqs, 8, 64, 256)`` bytes), call ``kvq_window_append(lay,
+k, v, cu_new, start_pos, mu, win)`` beside the append, and decode with
+``kvq_decode_attention_win(lay, q, seq_lens, max_len, table, rk, rv, pool, win, ws, o_rot)``
+(workspace from ``kvq_decode_workspace_size_win``).  Candidate selection:
+``kvq_calib_nmse``; per-head error report: ``kvq_head_error_report``.
 """
 from __future__ import annotations
 
