@@ -57,7 +57,7 @@ def test_chunked_append_equals_single_append(rot, chunks):
 
 
 def test_identity_rotation_equals_plain_int2_on_gpu():
-    # the benchmark spec pin: the identity rotation is plain INT2 (Eq. 4 with R = I); uncentred, clip 1
+    # pin: the identity rotation is plain INT2 (Eq. 4 with R = I); uncentred, clip 1
     case = W.decode_case(13, [100], 1, 1, 128, "identity", "f32", n_off=0)
     g = gu.GpuCase(case, mu_mode="none")
     pool = g.new_pool()
