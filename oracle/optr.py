@@ -143,7 +143,7 @@ def value_loss(a, r0, p_hat, v, w_o, clip: float, grad: bool = True, qfun=quant_
 
 
 def selected_key_weights(r_k, q, k, mu, clip: float):
-    """p^K_t of the selected key rotation (Algorithm 1, line 15), tagged with the query head."""
+    """p^K_t of the selected key rotation (Algorithm 1: the key path the value phase uses), tagged with the query head."""
     n_qpos, g, _ = q.shape
     n_tok = k.shape[0]
     x = k - (mu if mu is not None else 0.0)
