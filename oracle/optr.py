@@ -26,9 +26,14 @@ Readings (the pages leave these open):
 * Gradients of exp(S) use the Frechet derivative (SciPy's expm_frechet):
   dL/dS = Dexp(S^T)[dL/dE], then dL/dA = dL/dS - (dL/dS)^T.
 
-Pinned by tests/test_oracle_optr.py: the analytic gradients against central
-finite differences with a smooth stand-in for the quantizer (so the whole chain
--- softmax, KL, e_K / e_V, rotations, the exponential's Frechet derivative -- is
+Pinned by tests/test_oracle_optr.py: closed-form values of both losses on
+two-token heads worked by hand (KL against uniform = log 2 minus the binary
+entropy, with scipy.stats.entropy as a second evaluator; the output term's
+lambda_K (1/2 - p_0)^2 gamma^2 / d_model; the value loss c^2 / d_model for a
+constant shift; the mean over query heads), the KL term against
+torch.nn.functional.kl_div, the analytic gradients against central finite
+differences with a smooth stand-in for the quantizer (so the whole chain --
+softmax, KL, e_K / e_V, rotations, the exponential's Frechet derivative -- is
 differentiable), the straight-through mask, zero losses on lossless inputs,
 orthogonality of the iterates, loss decrease under Algorithm 1.
 """
@@ -58,6 +63,18 @@ def quant_ste(z: np.ndarray, clip: float):
     hi = clip * z.max(axis=-1, keepdims=True)
     mask = ((z >= lo) & (z <= hi)).astype(np.float64)
     return zq, mask
+
+
+def kl_term(p: np.ndarray, pk: np.ndarray):
+    """Eq. 14's D_KL(p_t || p_t^K) = sum_s p_s log(p_s / p^K_s) (the exact attention
+    distribution first) and its gradient with respect to the logits a^K of
+    p^K = softmax(a^K): p^K - p."""
+    return float(np.sum(p * (np.log(p) - np.log(pk)))), pk - p
+
+
+def output_error_term(e: np.ndarray, d_model: int):
+    """The post-W_O error term of Eqs. 14 and 16, ||e||_2^2 / d_model, and its gradient 2 e / d_model."""
+    return float(e @ e) / d_model, (2.0 / d_model) * e
 
 
 def _positions(n_tok: int, n_qpos: int):
@@ -90,13 +107,14 @@ def key_loss(a, r0, q, k, v, w_o, mu, clip: float, lam: float = 1.0, grad: bool 
             a_k = k_eff[: t + 1] @ qq / np.sqrt(D)
             p = softmax(a_ref)
             pk = softmax(a_k)
-            kl = float(np.sum(p * (np.log(p) - np.log(pk))))
+            kl, dkl = kl_term(p, pk)
             vw = v[: t + 1] @ w_j.T  # [t+1, d_model]: v_s W_j^T
             e = (pk - p) @ vw
-            loss += (kl + lam * float(e @ e) / dm) / n
+            err, derr = output_error_term(e, dm)
+            loss += (kl + lam * err) / n
             if grad:
-                dpk = (2.0 * lam / dm) * (vw @ e)  # d(lam ||e||^2 / dm) / dp^K_s
-                da = pk * (dpk - pk @ dpk) + (pk - p)  # softmax backward, plus dKL/da^K = p^K - p
+                dpk = lam * (vw @ derr)  # d(lam ||e||^2 / dm) / dp^K_s
+                da = pk * (dpk - pk @ dpk) + dkl  # softmax backward, plus dKL/da^K
                 g_keff[: t + 1] += np.outer(da / n, qq) / np.sqrt(D)
     if not grad:
         return loss, None
@@ -129,9 +147,10 @@ def value_loss(a, r0, p_hat, v, w_o, clip: float, grad: bool = True, qfun=quant_
         w_j = w_o[:, j * D:(j + 1) * D]
         m = len(pk)
         e = (pk @ dv[:m]) @ w_j.T
-        loss += float(e @ e) / dm / n
+        err, derr = output_error_term(e, dm)
+        loss += err / n
         if grad:
-            g_veff[:m] += np.outer(pk, (2.0 / dm / n) * (e @ w_j))
+            g_veff[:m] += np.outer(pk, (derr / n) @ w_j)
     if not grad:
         return loss, None
     d_r = g_veff.T @ zq

@@ -8,13 +8,14 @@ wrong side would not slip through.
 import numpy as np
 import pytest
 
-from oracle import quant, attention, output, rotations, window, report
+from oracle import quant, attention, output, rotations, window, report, optr
 import test_oracle_quant as tq
 import test_oracle_attention as ta
 import test_oracle_output as to
 import test_oracle_rotations as tr
 import test_oracle_window as tw
 import test_oracle_report as trep
+import test_oracle_optr as topt
 
 
 def _floor_quantize(x, clip):
@@ -76,6 +77,21 @@ def _value_term_with_exact_weights(p, p_tilde, v, v_tilde, w_j):
     return dy, dk, (np.asarray(p) @ (np.asarray(v_tilde) - np.asarray(v))) @ np.asarray(w_j).T
 
 
+def _reversed_kl(p, pk):
+    """KL(p^K || p) with its own (matching) gradient in the logits of p^K."""
+    r = np.log(pk) - np.log(p)
+    kl = float(np.sum(pk * r))
+    return kl, pk * (r - kl)
+
+
+def _error_over_head_dim(e, d_model):
+    return float(e @ e) / 128, (2.0 / 128) * e
+
+
+def _error_unnormalised(e, d_model):
+    return float(e @ e), 2.0 * e
+
+
 _ORIG_WINDOWED = window.decode_attention_windowed
 _ORIG_WINDOW_KEY = window.window_key
 
@@ -100,6 +116,12 @@ MUTATIONS = [
      tw.test_membership_matches_brute_force),
     ("Eq. 8 value term with the exact weights", report, "error_decomposition", _value_term_with_exact_weights,
      trep.test_matches_pure_python_loops),
+    ("reversed KL in the key loss", optr, "kl_term", _reversed_kl,
+     lambda: topt.test_key_loss_kl_term_closed_form(1.0)),
+    ("output error over the head dimension", optr, "output_error_term", _error_over_head_dim,
+     lambda: topt.test_key_loss_output_term_closed_form(1.0, 4)),
+    ("output error without 1/d_model (value loss)", optr, "output_error_term", _error_unnormalised,
+     lambda: topt.test_value_loss_closed_form(0.5, 4)),
 ]
 
 

@@ -126,3 +126,124 @@ def test_selection_never_returns_worse_than_the_base_rotation_on_held_out_data()
     base_v = optr.value_loss(zero, r0, p_sel, vh, w, 0.92, grad=False)[0]
     sel_v = optr.value_loss(zero, r_v, p_sel, vh, w, 0.92, grad=False)[0]
     assert sel_v <= base_v * (1 + 1e-12)
+
+
+# ---------------------------------------------------------------------------
+# Closed-form values of the two losses ("Output-Aware Rotation for INT2 KV-Cache
+# Quantization", §4.3 Eqs. 12-14 and §4.4 Eqs. 15-16), on heads small enough to
+# work by hand.  Two cached tokens, one query at position 1, the query along
+# channel 0 and the second key along channel 0 scaled so the exact logits are
+# (0, beta); a quantizer stand-in that stores every key as zero makes p^K uniform.
+# ---------------------------------------------------------------------------
+def _zero_keys(z, clip):
+    return np.zeros_like(z), np.ones_like(z)
+
+
+def _two_token_head(beta, gamma, g=1, d_model=4):
+    q = np.zeros((1, g, D))
+    q[0, :, 0] = 1.0
+    k = np.zeros((2, D))
+    k[1, 0] = beta * np.sqrt(D)
+    v = np.zeros((2, D))
+    v[0, 0] = gamma
+    w = np.zeros((d_model, g * D))
+    for j in range(g):  # every query head reads the first d_model channels
+        w[:, j * D:j * D + d_model] = np.eye(d_model)
+    return q, k, v, w
+
+
+def _p_exact(beta):
+    p1 = 1.0 / (1.0 + np.exp(-beta))
+    return np.array([1.0 - p1, p1])
+
+
+@pytest.mark.parametrize("beta", [1.0, -2.5, 4.0])
+def test_key_loss_kl_term_closed_form(beta):
+    """Values kept equal (v = 0), so e_K = 0 and L_K = D_KL(p || uniform) = log 2 - H(p),
+    H the binary entropy of the exact distribution (the direction of Eq. 14: the exact
+    distribution p first).  scipy.stats.entropy(p, q) evaluates the same divergence."""
+    from scipy.stats import entropy
+    q, k, v, w = _two_token_head(beta, 0.0)
+    loss, _ = optr.key_loss(np.zeros((D, D)), np.eye(D), q, k, v, w, None, 1.0, lam=1.0, grad=False,
+                            qfun=_zero_keys)
+    p = _p_exact(beta)
+    h = -(p[0] * np.log(p[0]) + p[1] * np.log(p[1]))
+    assert abs(loss - (np.log(2.0) - h)) < 1e-14
+    assert abs(loss - entropy(p, [0.5, 0.5])) < 1e-14
+
+
+@pytest.mark.parametrize("lam,d_model", [(1.0, 4), (0.7, 4), (2.0, 16)])
+def test_key_loss_output_term_closed_form(lam, d_model):
+    """v_0 - v_1 = gamma e_0 and W_O,j = [I | 0]: e_K = (1/2 - p_0) gamma e_0, so
+    L_K = D_KL(p || uniform) + lambda_K (1/2 - p_0)^2 gamma^2 / d_model (Eq. 14's
+    normalisation by the model width, not by the head dimension)."""
+    from scipy.stats import entropy
+    beta, gamma = 1.5, 3.0
+    q, k, v, w = _two_token_head(beta, gamma, d_model=d_model)
+    loss, _ = optr.key_loss(np.zeros((D, D)), np.eye(D), q, k, v, w, None, 1.0, lam=lam, grad=False,
+                            qfun=_zero_keys)
+    p = _p_exact(beta)
+    expect = entropy(p, [0.5, 0.5]) + lam * (0.5 - p[0]) ** 2 * gamma ** 2 / d_model
+    assert abs(loss - expect) < 1e-13 * max(1.0, expect)
+
+
+def test_key_loss_is_a_mean_over_query_heads_and_positions():
+    """Eq. 14's expectation over (t, j): two query heads that see the same query and
+    the same W_O columns give the one-head loss, not twice it."""
+    beta, gamma = 0.8, 2.0
+    args = dict(lam=1.0, grad=False, qfun=_zero_keys)
+    q1, k, v, w1 = _two_token_head(beta, gamma, g=1)
+    q2, _, _, w2 = _two_token_head(beta, gamma, g=2)
+    l1, _ = optr.key_loss(np.zeros((D, D)), np.eye(D), q1, k, v, w1, None, 1.0, **args)
+    l2, _ = optr.key_loss(np.zeros((D, D)), np.eye(D), q2, k, v, w2, None, 1.0, **args)
+    assert abs(l1 - l2) < 1e-15
+
+
+def test_key_loss_kl_matches_torch_kl_div():
+    """With the output term off (lambda_K = 0) and the identity rotation, L_K is the mean
+    over (t, j) of KL(p || p^K); torch.nn.functional.kl_div(log p^K, p) evaluates
+    exactly that divergence (its target is the first argument of KL)."""
+    torch = pytest.importorskip("torch")
+    from scipy.special import softmax as sp_softmax
+    gen = np.random.default_rng(11)
+    n_tok, n_qpos, g = 9, 3, 2
+    q = gen.standard_normal((n_qpos, g, D))
+    k = gen.standard_normal((n_tok, D)) * 2.0
+    v = gen.standard_normal((n_tok, D))
+    w = gen.standard_normal((6, g * D))
+    mu = k.mean(axis=0)
+    loss, _ = optr.key_loss(np.zeros((D, D)), np.eye(D), q, k, v, w, mu, 1.0, lam=0.0, grad=False, qfun=_smooth)
+    k_eff = _smooth(k - mu, 1.0)[0]
+    kls = []
+    for i in range(n_qpos):
+        t = n_tok - n_qpos + i
+        for j in range(g):
+            p = sp_softmax(k[: t + 1] @ q[i, j] / np.sqrt(D))
+            pk = sp_softmax(k_eff[: t + 1] @ q[i, j] / np.sqrt(D))
+            kls.append(float(torch.nn.functional.kl_div(torch.tensor(np.log(pk)), torch.tensor(p),
+                                                        reduction="sum")))
+    assert abs(loss - np.mean(kls)) < 1e-13
+
+
+@pytest.mark.parametrize("c,d_model", [(0.5, 4), (1.25, 8)])
+def test_value_loss_closed_form(c, d_model):
+    """A quantizer stand-in that shifts channel 0 of every value by c gives v~ - v = c e_0
+    for every token, so e_V = c e_0 W_O,j^T = c e_0 whatever the weights p^K (they sum to
+    one), and L_V = c^2 / d_model (Eq. 16)."""
+    def shift0(z, clip):
+        out = z.copy()
+        out[:, 0] += c
+        return out, np.ones_like(z)
+    gen = np.random.default_rng(12)
+    n_tok, g = 7, 2
+    v = gen.standard_normal((n_tok, D))
+    w = np.zeros((d_model, g * D))
+    for j in range(g):
+        w[:, j * D:j * D + d_model] = np.eye(d_model)
+    p_hat = []
+    for t in (4, 5, 6):
+        for j in range(g):
+            x = gen.random(t + 1)
+            p_hat.append((j, x / x.sum()))
+    loss, _ = optr.value_loss(np.zeros((D, D)), np.eye(D), p_hat, v, w, 1.0, grad=False, qfun=shift0)
+    assert abs(loss - c * c / d_model) < 1e-14
