@@ -256,6 +256,8 @@ kvq_status kvq_decode_attention_win(const kvq_layout* layout, int n_seqs, const 
  *     message naming both sizes.
  *   - The first call on each device looks up the buffer's device address; make
  *     that first call, with the device current, before any stream capture.
+ *     `stream` must belong to the current device, and the looked-up address
+ *     does not survive a cudaDeviceReset of that device.
  *   - All calls share the buffer: calls that overlap on the GPU (other streams,
  *     other host threads) race and must be serialised by the caller.  Each call
  *     writes every byte of scratch it reads, so nothing needs clearing. */

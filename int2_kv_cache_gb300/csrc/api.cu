@@ -134,6 +134,22 @@ kvq::PageGeom geom(const kvq_layout* L) {
 
 kvq_status kvq::set_error(kvq_status st, const char* msg) { return fail(st, "%s", msg); }
 
+int kvq::device_sm_count() {
+  static std::atomic<int> cache[64];  // per device ordinal, 0 = not yet looked up
+  int dev = 0, c = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    (void)cudaGetLastError();  // leave no error behind for the caller's launch checks
+    return 152;
+  }
+  if (dev >= 0 && dev < 64 && (c = cache[dev].load(std::memory_order_relaxed)) > 0) return c;
+  if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0) {
+    (void)cudaGetLastError();
+    return 152;
+  }
+  if (dev >= 0 && dev < 64) cache[dev].store(c, std::memory_order_relaxed);
+  return c;
+}
+
 extern "C" {
 
 const char* kvq_last_error(void) { return g_last_error.c_str(); }

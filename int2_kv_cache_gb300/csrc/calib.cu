@@ -300,13 +300,9 @@ __global__ void calib_attn_combine_kernel(int n_rows, int split, const float* __
 template <int G>
 static cudaError_t launch_calib_attn_g(int n_tok, int n_qpos, int n_kv_heads, const float* q, const float* k,
                                        const float* v, float* o, float* part, cudaStream_t s) {
-  static bool attr = false;
-  if (!attr) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(calib_attn_tiled_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, CA_SMEM);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};  // per device
+  const cudaError_t ea = smem_limit_once(attr, calib_attn_tiled_kernel<G>, CA_SMEM);
+  if (ea != cudaSuccess) return ea;
   constexpr int QB = CA_ROWS / G;
   const int nqb = (n_qpos + QB - 1) / QB;
   const int n_tiles = (n_tok + CA_KT - 1) / CA_KT;

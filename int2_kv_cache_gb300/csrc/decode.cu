@@ -54,7 +54,6 @@ namespace kvq {
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr int DEC_WARPS = 4;
 constexpr int DEC_STAGES = 3;  // stages of 64 tokens per warp
-constexpr int SM_COUNT = 152;  // GB300
 // Lazy softmax rescaling: the running sums keep their reference maximum until a
 // chunk's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
 constexpr float TAU = 6.f;
@@ -128,7 +127,7 @@ size_t decode_workspace_bytes(int n_seqs, int n_kv_heads, int gqa, int n_ctas, b
 int decode_auto_ctas(int n_seqs, int n_kv_heads, int gqa, int max_seq_len) {
   const long long chunks = (long long)n_seqs * n_kv_heads * ((max_seq_len + 31) / 32);
   const long long by_work = (chunks + 4 * DEC_WARPS - 1) / (4 * DEC_WARPS);
-  long long n = (long long)SM_COUNT * ctas_per_sm(gqa);
+  long long n = (long long)device_sm_count() * ctas_per_sm(gqa);
   if (n > by_work) n = by_work;
   return n < 1 ? 1 : (int)n;
 }
@@ -1213,12 +1212,8 @@ constexpr int DEC_SMEM = DEC_WARPS * DEC_STAGES * 2 * 1152 * 2;
 
 template <int G, int P, bool WIN>
 cudaError_t decode_smem_attr() {
-  static bool done = false;  // one flag per kernel instance
-  if (done) return cudaSuccess;
-  const cudaError_t e =
-      cudaFuncSetAttribute(decode_split_kernel<G, P, WIN>, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM);
-  if (e == cudaSuccess) done = true;
-  return e;
+  static std::atomic<unsigned long long> done{0};  // one set of per-device flags per kernel instance
+  return smem_limit_once(done, decode_split_kernel<G, P, WIN>, DEC_SMEM);
 }
 
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q, int q_dtype,

@@ -12,7 +12,9 @@
 // The buffer is a file-scope __device__ array of NOALLOC_SCRATCH_BYTES, so every
 // GPU that loads the library holds it until the process exits.  Its device
 // address is looked up once per device, on the first call made while that
-// device is current; make that first call before any stream capture.  All calls
+// device is current; make that first call before any stream capture.  The
+// stream passed in must belong to the current device, and the cached address
+// does not survive a cudaDeviceReset of that device.  All calls
 // share the one buffer: calls whose executions overlap on the GPU (different
 // streams, or different host threads) race on it and must be serialised by the
 // caller.  Every call writes all of the scratch it reads, so nothing has to be
@@ -42,14 +44,28 @@ extern "C" kvq_status kvq_decode_attention_noalloc(const kvq_layout* layout, int
   kvq_status st = kvq_decode_workspace_size(layout, n_seqs, max_seq_len, n_splits, &need);
   if (st != KVQ_OK) return st;
   if (n_splits == 0 && need > NOALLOC_SCRATCH_BYTES) {
-    // the library's choice of work partitions: take fewer until the partials fit
-    int s = kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, layout->n_q_heads / layout->n_kv_heads, max_seq_len);
-    while (need > NOALLOC_SCRATCH_BYTES && s > 1) {
-      s /= 2;
-      st = kvq_decode_workspace_size(layout, n_seqs, max_seq_len, s, &need);
+    // The library's choice of work partitions needs more than the buffer: take the
+    // largest count below it that fits.  The workspace grows with the count, so a
+    // binary search over [1, auto) finds it (if even one partition does not fit,
+    // the request is refused below).
+    int lo = 1, hi = kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, layout->n_q_heads / layout->n_kv_heads,
+                                           max_seq_len) - 1;
+    int best = 1;
+    while (lo <= hi) {
+      const int mid = lo + (hi - lo) / 2;
+      size_t b = 0;
+      st = kvq_decode_workspace_size(layout, n_seqs, max_seq_len, mid, &b);
       if (st != KVQ_OK) return st;
+      if (b <= NOALLOC_SCRATCH_BYTES) {
+        best = mid;
+        lo = mid + 1;
+      } else {
+        hi = mid - 1;
+      }
     }
-    n_splits = s;
+    n_splits = best;
+    st = kvq_decode_workspace_size(layout, n_seqs, max_seq_len, n_splits, &need);
+    if (st != KVQ_OK) return st;
   }
   char msg[256];
   if (need > NOALLOC_SCRATCH_BYTES) {

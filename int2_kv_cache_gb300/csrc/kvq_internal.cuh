@@ -1,6 +1,8 @@
 // Internal helpers shared by the libkvq translation units (not part of the ABI).
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
 #include <cuda_bf16.h>
@@ -76,6 +78,35 @@ namespace kvq {
 
 // api.cu: record `msg` as this thread's kvq_last_error() text and return `st`.
 kvq_status set_error(kvq_status st, const char* msg);
+
+// api.cu: streaming multiprocessors of the current device (looked up once per
+// device ordinal; 152, a GB300's count, if no device can be queried, which only
+// sizes workspaces on a machine that cannot launch anyway).
+int device_sm_count();
+
+// A kernel's function attributes (its dynamic shared-memory limit) are a
+// per-device setting.  `done` keeps one bit per device ordinal below 64; `setup`
+// runs on the first call made with a device current (larger ordinals run it on
+// every call).  Concurrent first calls may both run it, which is harmless.
+template <typename F>
+inline cudaError_t once_per_device(std::atomic<unsigned long long>& done, F&& setup) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = (dev >= 0 && dev < 64) ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = setup();
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
+// Dynamic shared-memory limit of `kernel`, raised once per device.
+template <typename K>
+inline cudaError_t smem_limit_once(std::atomic<unsigned long long>& done, K kernel, int bytes) {
+  return once_per_device(done, [&] {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  });
+}
 
 // quantize.cu
 cudaError_t launch_key_mean(int n_tok, int n_heads, const void* k, int dtype, float* mu,

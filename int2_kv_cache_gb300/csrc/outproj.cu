@@ -500,17 +500,16 @@ __global__ void __launch_bounds__(OPT_THREADS, opt_ctas_per_sm(NRP)) out_proj_tc
 
 // cuTensorMapEncodeTiled from the driver (no link-time dependency on it).
 static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // a driver entry point is process-wide; the static is initialised once (thread-safe)
+  static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
             cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  }
+      return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+  }();
   return fn;
 }
 
@@ -528,34 +527,19 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, 
          CUDA_SUCCESS;
 }
 
-static int sm_count() {
-  static int n = 0;
-  if (n == 0) {
-    int dev = 0, c = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess && cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
-      n = c;
-    if (n <= 0) n = 152;
-  }
-  return n;
-}
-
 template <int NRP>
 cudaError_t launch_out_proj_tc(int nr, int d_model, int k_dim, const float* x, const void* w, float* y, unsigned* err,
                                cudaStream_t s) {
   constexpr int smem = opt_smem_bytes(NRP);
-  static bool attr_set = false;  // one flag per kernel instance
-  if (!attr_set) {
-    const cudaError_t e =
-        cudaFuncSetAttribute(out_proj_tc_kernel<NRP>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};  // one set of per-device flags per kernel instance
+  const cudaError_t ea = smem_limit_once(attr_set, out_proj_tc_kernel<NRP>, smem);
+  if (ea != cudaSuccess) return ea;
   CUtensorMap tw;
   if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, OPT_BK, OPT_BM)) return cudaErrorNotSupported;
   // K split (the cluster size): about opt_ctas_per_sm CTAs per SM, at most 8, at most one per K stage
   const int n_mt = (d_model + OPT_BM - 1) / OPT_BM;
   const int n_kb = (k_dim + OPT_BK - 1) / OPT_BK;
-  int split = opt_ctas_per_sm(NRP) * sm_count() / n_mt;
+  int split = opt_ctas_per_sm(NRP) * device_sm_count() / n_mt;
   if (split > 8) split = 8;
   if (split > n_kb) split = n_kb;
   if (split < 1) split = 1;

@@ -97,12 +97,9 @@ cudaError_t launch_rotate_heads(int n_rows, int n_heads, int heads_per_rot, cons
   if (warps == 0) return cudaSuccess;
   if (rot.kind == KVQ_ROT_DENSE && x != y) {
     constexpr int smem = (D * D + RH_VB * D) * (int)sizeof(float);
-    static bool attr = false;
-    if (!attr) {
-      const cudaError_t e = cudaFuncSetAttribute(rotate_heads_dense_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (e != cudaSuccess) return e;
-      attr = true;
-    }
+    static std::atomic<unsigned long long> attr{0};  // per device
+    const cudaError_t ea = smem_limit_once(attr, rotate_heads_dense_kernel, smem);
+    if (ea != cudaSuccess) return ea;
     const int n_rot = n_heads / heads_per_rot;
     const int n_vec = n_rows * heads_per_rot;
     rotate_heads_dense_kernel<<<dim3((n_vec + RH_VB - 1) / RH_VB, n_rot), 256, smem, s>>>(
@@ -791,13 +788,9 @@ static cudaError_t launch_append_nondense(const PageGeom& g, int n_seqs, int n_n
     return cudaGetLastError();
   }
   const size_t smem = (size_t)g.n_kv_heads * (1028 + 4 * AF_TOK);
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(append_fast_kernel<AF_LPG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               AF_MAX_HEADS * (1028 + 4 * AF_TOK));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};  // per device
+  const cudaError_t ea = smem_limit_once(attr_set, append_fast_kernel<AF_LPG>, AF_MAX_HEADS * (1028 + 4 * AF_TOK));
+  if (ea != cudaSuccess) return ea;
   append_fast_kernel<AF_LPG><<<dim3((n_new + AF_TOK - 1) / AF_TOK, n_roles), AF_THREADS, smem, s>>>(
       g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
   return cudaGetLastError();
@@ -815,12 +808,9 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
   roles.r[1] = AppendRole{v, rot_v, nullptr, clip_v, 32 * P, 68 * P};
   const dim3 grid((n_new + APPEND_TOK - 1) / APPEND_TOK, g.n_kv_heads, 1);
   const size_t smem = (size_t)D * D * sizeof(float);
-  static bool attr_set = false;
-  if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(append_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<unsigned long long> attr_set{0};  // per device
+  const cudaError_t ea = smem_limit_once(attr_set, append_kernel<true>, (int)smem);
+  if (ea != cudaSuccess) return ea;
   // keys and values may use different rotation kinds: one launch per kind
   const bool kd = rot_k.kind == KVQ_ROT_DENSE, vd = rot_v.kind == KVQ_ROT_DENSE;
   if (!kd && !vd) return launch_append_nondense(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, 2, pool, err, s);

@@ -49,7 +49,7 @@ def check_sampled(g, gpool_np, q, got, seqs):
                          (c.clip_k, c.clip_v), label=f"{c.name} seq {b}")
         kh, vh = oracle.cache.dequantized_sequence(pool_b, c.n_kv_heads, c.page_tokens, c.block_table[b], lens[b])
         ref = oracle.attention.decode_attention(q[b], kh, vh, g.r_k, c.gqa)
-        assert gu.normwise_err(got[b], ref) <= gu.OUT_TOL, (b, gu.normwise_err(got[b], ref))
+        assert gu.out_err(got[b], ref) <= gu.OUT_TOL, (b, gu.out_err(got[b], ref))
 
 
 def test_tiny_single_head_end_to_end():
@@ -73,7 +73,7 @@ def test_tiny_single_head_end_to_end():
     y_o = oracle.output.out_proj(o_ref_q[None], oracle.output.fold_wo(w, g.r_v, 1))
     k, v = c.kv(0)
     y_ref = oracle.output.out_proj(oracle.attention.reference_attention(q[0], k, v, 1)[None], w)
-    assert gu.normwise_err(y, y_o) <= gu.OUT_TOL
+    assert gu.out_err(y, y_o) <= gu.OUT_TOL
     n_gpu, n_ora = oracle.output.nmse(y, y_ref), oracle.output.nmse(y_o, y_ref)
     assert abs(n_gpu - n_ora) <= gu.NMSE_TOL * n_ora
     print(f"tiny: NMSE gpu {n_gpu:.6g} oracle {n_ora:.6g}")
@@ -122,7 +122,7 @@ def test_envelope_selection_then_fresh_queries():
     for i in range(nq):
         y_o = oracle.output.out_proj(oracle.attention.decode_attention(cc.fresh_q[i], kh, vh, r, 1)[None], wfo)
         y_ref = oracle.output.out_proj(oracle.attention.reference_attention(cc.fresh_q[i], cc.k, cc.v, 1)[None], cc.w_o)
-        assert gu.normwise_err(y[i], y_o[0]) <= gu.OUT_TOL
+        assert gu.out_err(y[i], y_o[0]) <= gu.OUT_TOL
         n_gpu.append(oracle.output.nmse(y[i], y_ref[0]))
         n_ora.append(oracle.output.nmse(y_o[0], y_ref[0]))
     n_gpu, n_ora = np.array(n_gpu), np.array(n_ora)

@@ -32,7 +32,7 @@ def test_decode_on_oracle_pool(hq, hkv, page, lengths, rot, dtype, splits):
     g.kvq.kvq_device_check()
     ref = g.oracle_decode(ora_pool, q)
     for b in range(case.n_seqs):
-        err = gu.normwise_err(got[b], ref[b]) if np.abs(ref[b]).max() > 0 else np.abs(got[b]).max()
+        err = gu.out_err(got[b], ref[b]) if np.abs(ref[b]).max() > 0 else np.abs(got[b]).max()
         assert err <= gu.OUT_TOL, (b, err)
         assert np.isfinite(got[b]).all()
     assert np.all(got[np.asarray(lengths) == 0] == 0)
@@ -62,7 +62,7 @@ def test_end_to_end_gpu_write_then_gpu_decode():
     ora_pool, _ = g.oracle_pool()
     ref = g.oracle_decode(ora_pool, q)
     for b in range(case.n_seqs):
-        assert gu.normwise_err(got[b], ref[b]) <= gu.OUT_TOL
+        assert gu.out_err(got[b], ref[b]) <= gu.OUT_TOL
 
 
 def test_bad_sequence_length_is_flagged():

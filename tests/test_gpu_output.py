@@ -43,7 +43,7 @@ def test_out_proj(rows, dm, hq, wdt):
     y = torch.empty(rows, dm, device="cuda")
     kvq.kvq_out_proj(gu.dev(o).reshape(rows, -1), gu.dev(w, wdt), y)
     ref = oracle.output.out_proj(o, w)
-    assert gu.normwise_err(y.cpu().numpy(), ref) <= gu.OUT_TOL
+    assert gu.out_err(y.cpu().numpy(), ref) <= gu.OUT_TOL
 
 
 def test_folded_projection_of_rotated_readout_equals_unrotated():
@@ -77,4 +77,4 @@ def test_out_proj_ragged_k_and_passes(rows, dm, k):
     y = torch.empty(rows, dm, device="cuda")
     kvq.kvq_out_proj(gu.dev(x), gu.dev(w, "bf16"), y)
     ref = x.astype(np.float64) @ w.astype(np.float64).T
-    assert gu.normwise_err(y.cpu().numpy(), ref) <= gu.OUT_TOL
+    assert gu.out_err(y.cpu().numpy(), ref) <= gu.OUT_TOL

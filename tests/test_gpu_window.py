@@ -136,7 +136,7 @@ def test_windowed_decode_matches_the_oracle(hq, hkv, page, lengths, rot, dtype, 
         kh, vh = oracle.cache.dequantized_sequence(ora_pool, hkv, page, case.block_table[b], n)
         wp, wk, wv = oracle.window.read_window(regions[b], n, s, r)
         ref = oracle.window.decode_attention_windowed(q[b], kh, vh, wp, wk, wv, g.r_k, g.r_v, case.gqa, n, s, r)
-        err = gu.normwise_err(got[b], ref)
+        err = gu.out_err(got[b], ref)
         assert np.isfinite(got[b]).all() and err <= gu.OUT_TOL, (b, n, err)
 
 
@@ -173,7 +173,7 @@ def test_end_to_end_windowed_steps():
         kh, vh = oracle.cache.dequantized_sequence(ora_pool, 2, case.page_tokens, case.block_table[b], n)
         wp, wk, wv = oracle.window.read_window(regions[b], n, *sizes)
         ref = oracle.window.decode_attention_windowed(q[b], kh, vh, wp, wk, wv, g.r_k, g.r_v, case.gqa, n, *sizes)
-        assert gu.normwise_err(got[b], ref) <= gu.OUT_TOL
+        assert gu.out_err(got[b], ref) <= gu.OUT_TOL
 
 
 def test_empty_window_is_the_plain_decode_and_splits_agree():
