@@ -7,11 +7,13 @@ heads / 8 KV heads, head dim 128, hidden 4096, bf16 inputs, 16 sequences x
 per-head dense learned-style rotations R = expm(A - A^T), key mean subtracted.
 
 One step = the whole hot path for one decode token of every sequence:
-  1. kvq_quantize_append  -- rotate, centre, clip, quantize, pack and write the new
-                              token's K and V (positions 32,767)
-  2. kvq_decode_attention -- rotated query, split-K attention over 32,768 packed
-                              tokens, log-sum-exp combine
-  3. kvq_out_proj         -- y = o' W_O-bar^T with R_V folded into W_O
+  1. kvq_decode_step -- the query preparation rotates, centres, clips, quantizes,
+                        packs and writes the new token's K and V (position 32,767)
+                        and rotates the query; split-K attention over 32,768 packed
+                        tokens; log-sum-exp combine
+  2. kvq_out_proj    -- y = o' W_O-bar^T with R_V folded into W_O
+(with --window, the append and window copies are separate calls before the
+windowed decode)
 value = sequences x steps / time (decode tokens per second, one layer).
 
 --impl reference times the fp64 oracle (CPU) on a bounded sample of the same
@@ -280,8 +282,9 @@ class DecodeStep:
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
         self.y = torch.empty(n_seqs, self.dm, device=device)
         self.host_y = torch.empty(n_seqs, self.dm).pin_memory()
-        # append (K and V) [+ window copies], query prep + decode + combine, W_O
-        self.launches_per_step = 1 + (1 if self.win else 0) + 3 + 1
+        # without windows: the fused step (query prep with the append, decode, combine) + W_O;
+        # with windows: append (K and V) + window copies, query prep + decode + combine, W_O
+        self.launches_per_step = 3 + 1 if self.win is None else 1 + 1 + 3 + 1
 
     def win_row(self, b):
         """A window struct over sequence b's rows only (for appending one sequence at a time)."""
@@ -290,20 +293,27 @@ class DecodeStep:
         return self.kvq.Window(w.sink_tokens, w.recent_tokens, w.buf[b * per:(b + 1) * per])
 
     def step(self, ev=None):
+        """One decode step.  Without windows: kvq_decode_step (the new token's append fused
+        into the decode call) and the W_O projection.  With windows: the append and the
+        window copies, the windowed decode, the projection.  ev: events [4] recorded
+        before the step, after the append (without windows: at the same point as the
+        first), after the decode and after the projection."""
         kvq = self.kvq
         c = self.case
         if ev is not None:
             ev[0].record()
-        kvq.kvq_quantize_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.table, self.rot_k,
-                                self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
-        if self.win is not None:
-            kvq.kvq_window_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.mu, self.win)
-        if ev is not None:
-            ev[1].record()
         if self.win is None:
-            kvq.kvq_decode_attention(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.pool,
-                                     self.ws, self.o, n_splits=self.splits)
+            if ev is not None:
+                ev[1].record()
+            kvq.kvq_decode_step(self.layout, self.q, self.k_new, self.v_new, self.lens, self.L, self.table, self.rot_k,
+                                self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool, self.ws, self.o,
+                                n_splits=self.splits)
         else:
+            kvq.kvq_quantize_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.table,
+                                    self.rot_k, self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
+            kvq.kvq_window_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.mu, self.win)
+            if ev is not None:
+                ev[1].record()
             kvq.kvq_decode_attention_win(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.rot_v,
                                          self.pool, self.win, self.ws, self.o, n_splits=self.splits)
         if ev is not None:
@@ -311,6 +321,13 @@ class DecodeStep:
         kvq.kvq_out_proj(self.o.reshape(self.B, -1), self.w_fold, self.y)
         if ev is not None:
             ev[3].record()
+
+    def decode_only(self, ev):
+        """kvq_decode_attention alone over the same cache (for the per-phase record)."""
+        ev[0].record()
+        self.kvq.kvq_decode_attention(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.pool,
+                                      self.ws, self.o, n_splits=self.splits)
+        ev[1].record()
 
     def step_e2e(self):
         self.q.copy_(self.host_q, non_blocking=True)
@@ -346,8 +363,11 @@ class DecodeStep:
         # at most 4 * n_ctas + units of them, written once and read once
         pairs = min(4 * self.n_ctas + units, int(hkv * ((lens + 63) // 64).sum()))
         cache = int(lens.sum()) * hkv * 72
+        dense_v = self.case.rot_v.kind == "dense"
         return {
             "kv_cache": cache,
+            # the step's new token: bf16 K and V read, 72 B of codes and meta written, R_V read
+            "step_append": B * hkv * (2 * 256 + 72) + (hkv * 128 * 128 * 4 if dense_v else hkv * 128 * 4),
             "q": B * hq * 128 * 2,
             "block_table": int(((lens + self.case.page_tokens - 1) // self.case.page_tokens).sum()) * 4,
             "rotation": hkv * 128 * 128 * 4,
@@ -404,14 +424,22 @@ def run_gpu(args):
     clk = clocks.stop()
     total_ms = float(np.median(block_ms))
     # per-phase breakdown (separate steps, events around each entry point)
-    n_br = min(args.steps, 200)
+    n_br = max(min(args.steps * len(block_ms), 400), 20)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_br)]
     for i in range(n_br):
         w.step(evs[i])
     barrier()
-    t_app = sum(e[0].elapsed_time(e[1]) for e in evs) / n_br
-    t_dec = sum(e[1].elapsed_time(e[2]) for e in evs) / n_br
-    t_out = sum(e[2].elapsed_time(e[3]) for e in evs) / n_br
+    t_app = float(np.median([e[0].elapsed_time(e[1]) for e in evs]))
+    t_dec = float(np.median([e[1].elapsed_time(e[2]) for e in evs]))
+    t_out = float(np.median([e[2].elapsed_time(e[3]) for e in evs]))
+    t_dec_only = None
+    if window is None:
+        # kvq_decode_attention alone over the same cache (no append), for the record
+        evd = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(n_br)]
+        for i in range(n_br):
+            w.decode_only(evd[i])
+        barrier()
+        t_dec_only = float(np.median([e[0].elapsed_time(e[1]) for e in evd]))
 
     # end to end through the public API with host buffers
     for _ in range(3):
@@ -459,11 +487,15 @@ def run_gpu(args):
                              if window else "none (every token INT2)"),
             "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (w.pool.numel() / 1e6),
         },
-        "kernel_ms": {"quantize_append": t_app, "decode_attention": t_dec, "out_proj": t_out},
+        "kernel_ms": ({"decode_step": t_dec, "out_proj": t_out, "decode_attention_alone": t_dec_only}
+                      if window is None else
+                      {"quantize_append_and_window": t_app, "decode_attention_win": t_dec, "out_proj": t_out}),
         "kv_cache_gbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9,
         "kv_cache_pct_of_peak": {"measured": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / peak,
                                  "nominal_8tbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / NOMINAL_HBM_GBS},
-        "roofline": {"kernel": "kvq_decode_attention (query prep + decode + combine)", "bound": "hbm", "achieved": achieved,
+        "roofline": {"kernel": ("kvq_decode_step (query prep with the new token's append, decode, combine)"
+                                if window is None else "kvq_decode_attention_win (query prep, decode, combine)"),
+                     "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": alg, "bytes": by},
         "e2e": {"value": world * w.B / (e2e_step * 1e-3), "unit": "tokens/s",

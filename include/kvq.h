@@ -201,6 +201,31 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
                                 int n_splits, void* workspace, size_t workspace_bytes,
                                 float* o_rot, kvq_stream stream);
 
+/* One decode step: the quantize-append of each sequence's new token fused with
+ * the decode attention that reads it ("Output-Aware Rotation for INT2 KV-Cache
+ * Quantization", §6 "Efficiency Analysis": the cache-write kernel and the decode
+ * of the rotated INT2 pipeline; Eqs. 4, 20-22, 26, 27).  For every sequence b
+ * with seq_lens[b] >= 1 the token at position seq_lens[b] - 1 is written as
+ * kvq_quantize_append would write it (k_new[b], v_new[b]; same rotations, key
+ * shift and clip ratios, the same bytes), and then o_rot is what
+ * kvq_decode_attention returns over seq_lens[b] tokens.  A sequence of length 0
+ * appends nothing and yields a zero vector.  The query preparation writes the
+ * new tokens, and the decode kernel reads their pages only after it, so the
+ * step is one call with no separate append launch.
+ *   q:            [n_seqs][n_q_heads][128] of dtype
+ *   k_new, v_new: [n_seqs][n_kv_heads][128] of dtype
+ *   mu_rot_k:     float [n_kv_heads][128] (mu R_K) or NULL; clip_k, clip_v in (0, 1]
+ *   pool:         written in place (the new tokens' slots) and read
+ *   workspace:    >= kvq_decode_workspace_size bytes
+ * Other arguments, limits and errors as kvq_decode_attention and
+ * kvq_quantize_append (an out-of-range block id is skipped and flagged). */
+kvq_status kvq_decode_step(const kvq_layout* layout, int n_seqs, const void* q, const void* k_new,
+                           const void* v_new, kvq_dtype dtype, const int32_t* seq_lens, int max_seq_len,
+                           const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v,
+                           const float* mu_rot_k, float clip_k, float clip_v, uint8_t* pool,
+                           int n_splits, void* workspace, size_t workspace_bytes, float* o_rot,
+                           kvq_stream stream);
+
 /* Window copies of appended tokens (see kvq_window).  For every new token of
  * sequence b at position p = start_pos[b] + (t - cu_new[b]) that is a window
  * token at the sequence's new length (p < sink, or p >= start_pos[b] + n_new_b -

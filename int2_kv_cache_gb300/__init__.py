@@ -88,6 +88,8 @@ def lib() -> ctypes.CDLL:
             "kvq_decode_workspace_size": ([lp, i, i, i, ctypes.POINTER(sz)], st),
             "kvq_decode_attention": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, sz, vp, vp], st),
             "kvq_decode_attention_noalloc": ([lp, i, vp, i, vp, i, vp, KvqRot, vp, i, vp, vp], st),
+            "kvq_decode_step": ([lp, i, vp, vp, vp, i, vp, i, vp, KvqRot, KvqRot, vp, f, f, vp, i, vp, sz, vp, vp],
+                                st),
             "kvq_window_append": ([lp, i, i, vp, vp, i, vp, vp, vp, wp, vp], st),
             "kvq_decode_workspace_size_win": ([lp, i, i, i, wp, ctypes.POINTER(sz)], st),
             "kvq_decode_attention_win": ([lp, i, vp, i, vp, i, vp, KvqRot, KvqRot, vp, wp, i, vp, sz, vp, vp], st),
@@ -110,7 +112,7 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mean", "kvq_rotate_heads",
             "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention",
-            "kvq_decode_attention_noalloc", "kvq_window_append", "kvq_decode_workspace_size_win",
+            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_window_append", "kvq_decode_workspace_size_win",
             "kvq_decode_attention_win", "kvq_fold_wo",
             "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse", "kvq_report_workspace_size",
             "kvq_head_error_report")
@@ -226,6 +228,21 @@ def kvq_decode_attention_noalloc(layout: KvqLayout, q, seq_lens, max_seq_len: in
     _check(lib().kvq_decode_attention_noalloc(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _dtype_code(q),
                                               _ptr(seq_lens), max_seq_len, _ptr(block_table), rot_k.c, _ptr(pool),
                                               n_splits, _ptr(o_rot), _stream(stream)))
+
+
+def kvq_decode_step(layout: KvqLayout, q, k_new, v_new, seq_lens, max_seq_len: int, block_table,
+                    rot_k: DeviceRot, rot_v: DeviceRot, mu_rot_k, clip_k: float, clip_v: float, pool, workspace,
+                    o_rot, n_splits: int = 0, stream=None) -> None:
+    """One decode step: each sequence's new token (k_new[b], v_new[b]) is appended at
+    position seq_lens[b] - 1 and the decode attention reads it, in one call."""
+    n_seqs = q.shape[0]
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TypeError("q, k_new and v_new must share a dtype")
+    _check(lib().kvq_decode_step(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _ptr(_contig(k_new, "k_new")),
+                                 _ptr(_contig(v_new, "v_new")), _dtype_code(q), _ptr(seq_lens), max_seq_len,
+                                 _ptr(block_table), rot_k.c, rot_v.c, _ptr(mu_rot_k), clip_k, clip_v, _ptr(pool),
+                                 n_splits, _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                 _ptr(o_rot), _stream(stream)))
 
 
 class Window:

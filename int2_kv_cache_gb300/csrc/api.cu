@@ -293,6 +293,46 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
                                   pool, nullptr, n_splits, workspace, workspace_bytes, o_rot, stream);
 }
 
+kvq_status kvq_decode_step(const kvq_layout* layout, int n_seqs, const void* q, const void* k_new,
+                           const void* v_new, kvq_dtype dtype, const int32_t* seq_lens, int max_seq_len,
+                           const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v, const float* mu_rot_k,
+                           float clip_k, float clip_v, uint8_t* pool, int n_splits, void* workspace,
+                           size_t workspace_bytes, float* o_rot, kvq_stream stream) {
+  KVQ_CHECK(check_layout(layout, true));
+  if (n_seqs < 0) return fail(KVQ_EINVAL, "n_seqs %d < 0", n_seqs);
+  if (!valid_dtype(dtype)) return fail(KVQ_EINVAL, "bad dtype %d", (int)dtype);
+  if (!valid_clip(clip_k) || !valid_clip(clip_v))
+    return fail(KVQ_EINVAL, "clip ratios must lie in (0, 1] (got %g, %g)", clip_k, clip_v);
+  if (max_seq_len < 0 || (long long)max_seq_len > (long long)layout->max_blocks_per_seq * layout->page_tokens)
+    return fail(KVQ_EINVAL, "max_seq_len %d outside [0, max_blocks_per_seq * page_tokens]", max_seq_len);
+  if (n_splits < 0 || n_splits > 8192) return fail(KVQ_EINVAL, "n_splits %d outside [0, 8192]", n_splits);
+  KVQ_CHECK(check_rot(rot_k, "rot_k"));
+  KVQ_CHECK(check_rot(rot_v, "rot_v"));
+  if (n_seqs == 0) return KVQ_OK;
+  KVQ_PTR(q, "q");
+  KVQ_PTR(k_new, "k_new");
+  KVQ_PTR(v_new, "v_new");
+  KVQ_IDX(seq_lens, "seq_lens");
+  KVQ_IDX(block_table, "block_table");
+  KVQ_PTR(pool, "pool");
+  KVQ_PTR(o_rot, "o_rot");
+  KVQ_PTR(workspace, "workspace");
+  if (mu_rot_k && !aligned16(mu_rot_k)) return fail(KVQ_EINVAL, "mu_rot_k is not 16-byte aligned");
+  KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
+  const int gqa = layout->n_q_heads / layout->n_kv_heads;
+  const int s = n_splits ? n_splits : kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, gqa, max_seq_len);
+  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s, false);
+  if (workspace_bytes < need)
+    return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
+  const kvq::StepAppend app{k_new, v_new, (int)dtype, kvq::to_dev(rot_v), mu_rot_k, clip_k, clip_v, pool};
+  cudaError_t e = kvq::launch_decode(geom(layout), layout->n_q_heads, n_seqs, q, dtype, seq_lens, max_seq_len,
+                                     block_table, kvq::to_dev(rot_k), pool, s, workspace, o_rot, err, stream,
+                                     kvq::WinGeom{0, 0, nullptr}, kvq::to_dev(rot_v), &app);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_step");
+}
+
 kvq_status kvq_decode_attention_win(const kvq_layout* layout, int n_seqs, const void* q, kvq_dtype q_dtype,
                                     const int32_t* seq_lens, int max_seq_len, const int32_t* block_table,
                                     kvq_rot rot_k, kvq_rot rot_v, const uint8_t* pool, const kvq_window* win,

@@ -209,7 +209,119 @@ __host__ __device__ constexpr bool v_swapped(int f) { return f == 0 || f >= 5; }
 
 
 // ---------------------------------------------------------------------------
-// Query preparation (Eq. 22), one CTA per (KV head h, sequence b), 256 threads:
+// The new token of a decode step (kvq_decode_step): its key and value groups
+// are quantized and written by the query-preparation CTA of (sequence, KV head),
+// with the decisions of the cache-write kernels (OptR §6 cache-write kernel;
+// Eqs. 4, 20, 21, 27):
+//   x = k R_K - mu R_K (keys) or v R_V (values); lo = c min x, hi = c max x;
+//   scale = fp16((hi - lo)/3), zero = fp16(lo), code = clamp(rint((x - zero)/scale), 0, 3).
+// Dense R: warp w forms the partial x R over rows 16w .. 16w + 15 of R_h in
+// double-float (error-free products and sums; app_df_partial) and one warp adds
+// the 8 partials in a fixed tree and decides exactly (app_df_decide).  A step
+// appends one token per (sequence, head), so the exact path costs little and
+// takes no uncertain second pass (the query preparation gates the whole decode,
+// so its slowest CTA counts).  The key meets the rows of R_K that the query
+// rotation holds in registers; R_V is staged in shared memory by bulk copies
+// issued when the CTA starts.  Identity / signed Hadamard: one warp, certified
+// fp32 or a double-float redo (app_warp).
+// ---------------------------------------------------------------------------
+struct AppSmem {     // per role (key, value)
+  float2 df[8][D];   // each warp's partial x R as (hi, lo)
+  float x[D];        // the input row
+};
+
+__device__ __forceinline__ void app_write(uint8_t* codes, uint8_t* meta, unsigned byte, const QParams& qp, int lane) {
+  codes[lane] = (uint8_t)byte;
+  if (lane == 0) *reinterpret_cast<uint32_t*>(meta) = (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+}
+
+// Every warp: its 16 rows' partial x R in double-float.
+__device__ __forceinline__ void app_df_partial(const float* __restrict__ s_x, const float4 (&rr)[16], int warp,
+                                               int lane, AppSmem& a) {
+  float sh[4] = {0.f, 0.f, 0.f, 0.f}, sl[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 16; ++r) {
+    const float xc = s_x[16 * warp + r];
+    const float rv[4] = {rr[r].x, rr[r].y, rr[r].z, rr[r].w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float p = __fmul_rn(xc, rv[i]);
+      const float pe = __fmaf_rn(xc, rv[i], -p);
+      const DF t = two_sum(sh[i], p);
+      sh[i] = t.hi;
+      sl[i] = __fadd_rn(sl[i], __fadd_rn(t.lo, pe));
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const DF c = df_norm(sh[i], sl[i]);
+    a.df[warp][4 * lane + i] = make_float2(c.hi, c.lo);
+  }
+}
+
+// One warp: adds the double-float partials in a fixed tree, subtracts mu R (if given)
+// and decides exactly.
+__device__ __forceinline__ void app_df_decide(const AppSmem& a, bool has_mu, float4 mu, float clip, uint8_t* codes,
+                                              uint8_t* meta, int lane) {
+  DF x[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    DF q[8];
+#pragma unroll
+    for (int w = 0; w < 8; ++w) q[w] = DF{a.df[w][4 * lane + i].x, a.df[w][4 * lane + i].y};
+    x[i] = df_add(df_add(df_add(q[0], q[1]), df_add(q[2], q[3])), df_add(df_add(q[4], q[5]), df_add(q[6], q[7])));
+  }
+  if (has_mu) {
+    x[0] = df_add_f(x[0], -mu.x); x[1] = df_add_f(x[1], -mu.y);
+    x[2] = df_add_f(x[2], -mu.z); x[3] = df_add_f(x[3], -mu.w);
+  }
+  QParams qp;
+  const unsigned byte = quantize_warp_df(x, clip, qp);
+  app_write(codes, meta, byte, qp, lane);
+}
+
+// One warp, identity or signed Hadamard: certified fp32, else double-float.
+__device__ __forceinline__ void app_warp(const float* __restrict__ s_x, const RotDev& rot, int h,
+                                         const float* __restrict__ mu_rot, float clip, uint8_t* codes, uint8_t* meta,
+                                         int lane) {
+  const float4 v = reinterpret_cast<const float4*>(s_x)[lane];
+  float4 mu = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (mu_rot) mu = __ldg(reinterpret_cast<const float4*>(mu_rot + (size_t)h * D) + lane);
+  float y[4] = {v.x, v.y, v.z, v.w};
+  float E = rotate_f32_bounded(y, rot, h, lane);
+  if (mu_rot) {
+    y[0] = __fsub_rn(y[0], mu.x); y[1] = __fsub_rn(y[1], mu.y);
+    y[2] = __fsub_rn(y[2], mu.z); y[3] = __fsub_rn(y[3], mu.w);
+    // the subtraction's rounding: u (|y| + |mu|), y bounded through E's l1 norm or |x|
+    E += (warp_max(fmaxf(fmaxf(fabsf(v.x) + fabsf(mu.x), fabsf(v.y) + fabsf(mu.y)),
+                         fmaxf(fabsf(v.z) + fabsf(mu.z), fabsf(v.w) + fabsf(mu.w)))) +
+          E * 524288.f) * P2_M22;
+  }
+  QParams qp;
+  unsigned byte = 0u;
+  if (!quantize_warp_certain(y, E, clip, qp, byte)) {
+    DF x[4] = {{v.x, 0.f}, {v.y, 0.f}, {v.z, 0.f}, {v.w, 0.f}};
+    rotate_df_warp(x, rot, h, lane);
+    if (mu_rot) {
+      x[0] = df_add_f(x[0], -mu.x); x[1] = df_add_f(x[1], -mu.y);
+      x[2] = df_add_f(x[2], -mu.z); x[3] = df_add_f(x[3], -mu.w);
+    }
+    byte = quantize_warp_df(x, clip, qp);
+  }
+  app_write(codes, meta, byte, qp, lane);
+}
+
+// Dynamic shared memory of the query preparation with a step's append: R_V staged
+// (dense values only), then the two roles' AppSmem.
+constexpr int QPA_RV_BYTES = D * D * 4;
+__host__ __device__ constexpr int qpa_smem_bytes(bool dense_v) {
+  return (dense_v ? QPA_RV_BYTES : 0) + 2 * (int)sizeof(AppSmem);
+}
+
+// ---------------------------------------------------------------------------
+// Query preparation (Eq. 22), one CTA per (KV head h, sequence b), 256 threads
+// (with a decode step's append it also writes the new token's key and value,
+// see above):
 // q'_j = q[b][h G + j] R_K,h * log2(e)/sqrt(128) for the G query heads of the
 // group, then per head the sum of q' and a power-of-two prescale e_j keeping
 // 256 |q'| well inside the fp16 range, and the B fragments of q'.c.  Also
@@ -217,10 +329,12 @@ __host__ __device__ constexpr bool v_swapped(int f) { return f == 0 || f >= 5; }
 // ---------------------------------------------------------------------------
 constexpr int QP_THREADS = 256;
 
-template <int G, bool DENSE>
+template <int G, bool DENSE, bool APPEND>
 __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_kv_heads, const void* __restrict__ q,
                                                            int q_dtype, RotDev rot, const int32_t* __restrict__ seq_lens,
-                                                           DecWs ws, float* __restrict__ o_rot) {
+                                                           DecWs ws, float* __restrict__ o_rot, PageGeom pg,
+                                                           const int32_t* __restrict__ table, StepAppend app,
+                                                           unsigned* err) {
   constexpr int NT = n_tiles(G);
   constexpr int NW = QP_THREADS / 32;
   pdl_launch_dependents();  // the decode kernel may start its batch scan and first copies
@@ -232,6 +346,52 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
   const int u = b * n_kv_heads + h;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float sc = LOG2E * INV_SQRT_D;
+  // ---- a decode step's new token (APPEND): where it goes, its rows, R_V in flight ----
+  extern __shared__ __align__(128) uint8_t qpa_dyn[];  // APPEND: [R_V (dense values)][AppSmem key][AppSmem value]
+  __shared__ __align__(8) uint64_t rv_bar;
+  const bool dense_v = APPEND && app.rot_v.kind == KVQ_ROT_DENSE;
+  const float4* sRV = reinterpret_cast<const float4*>(qpa_dyn);
+  AppSmem* ak = reinterpret_cast<AppSmem*>(qpa_dyn + (dense_v ? QPA_RV_BYTES : 0));
+  AppSmem* av = ak + 1;
+  int new_len = 0;  // the deciding warps (NW - 1: key, NW - 2: value): seq_lens[b], loaded early
+  float4 mu_k = make_float4(0.f, 0.f, 0.f, 0.f);  // warp NW - 1: its channels of mu R_K
+  if (APPEND) {
+    if (tid == 0 && dense_v) {
+      mbar_init(&rv_bar, 1);
+      fence_mbar_init();
+      mbar_arrive_expect_tx(&rv_bar, QPA_RV_BYTES);
+      fence_proxy_async();
+      const uint8_t* src = reinterpret_cast<const uint8_t*>(app.rot_v.dense + (size_t)h * D * D);
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        bulk_g2s(qpa_dyn + c * (QPA_RV_BYTES / 4), src + c * (QPA_RV_BYTES / 4), QPA_RV_BYTES / 4, &rv_bar);
+    }
+    const size_t e0 = ((size_t)b * n_kv_heads + h) * D;
+    if (warp == NW - 1) {
+      new_len = __ldg(seq_lens + b);
+      reinterpret_cast<float4*>(ak->x)[lane] = load4(app.k, e0 + 4 * lane, app.dtype);
+      if (app.mu_rot_k) mu_k = __ldg(reinterpret_cast<const float4*>(app.mu_rot_k + (size_t)h * D) + lane);
+    }
+    if (warp == NW - 2) {
+      new_len = __ldg(seq_lens + b);
+      reinterpret_cast<float4*>(av->x)[lane] = load4(app.v, e0 + 4 * lane, app.dtype);
+    }
+    if (!DENSE) __syncthreads();  // the dense path's first barrier covers these writes
+  }
+  // The new token's page record (position len - 1; none for an empty sequence, nothing for
+  // a position or block id out of range, which the key's warp flags), by the deciding warps.
+  auto new_record = [&](int& slot) -> uint8_t* {
+    const int len = new_len;
+    if (len < 1 || len > pg.max_blocks * pg.page_tokens) return nullptr;
+    const int pos = len - 1;
+    const int blk = __ldg(table + (size_t)b * pg.max_blocks + pos / pg.page_tokens);
+    if (blk < 0 || blk >= pg.num_blocks) {
+      if (warp == NW - 1 && lane == 0) flag_error(err, ERR_BLOCK_RANGE);
+      return nullptr;
+    }
+    slot = pos % pg.page_tokens;
+    return app.pool + ((size_t)blk * n_kv_heads + h) * pg.record;
+  };
   if (DENSE) {
     for (int i = tid; i < G * D; i += QP_THREADS)
       qv[i / D][i % D] = load1(q, ((size_t)b * n_q_heads + h * G) * D + i, q_dtype);
@@ -251,6 +411,7 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
       }
       reinterpret_cast<float4*>(red[warp][j])[lane] = a;
     }
+    if (APPEND) app_df_partial(ak->x, r, warp, lane, *ak);  // the new key meets the same rows of R_K
     __syncthreads();
     for (int i = tid; i < G * D; i += QP_THREADS) {
       float a = 0.f;
@@ -265,6 +426,43 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
       x.x *= sc; x.y *= sc; x.z *= sc; x.w *= sc;
       reinterpret_cast<float4*>(qr[j])[lane] = x;
     }
+  }
+  if (APPEND) {
+    // values with a dense R_V: every warp its 16 staged rows, in double-float
+    if (dense_v) {
+      if (!mbar_wait_bounded(&rv_bar, 0)) {
+        if (tid == 0) flag_error(err, ERR_TIMEOUT);
+      } else {
+        float4 rv[16];
+#pragma unroll
+        for (int c = 0; c < 16; ++c) rv[c] = sRV[(16 * warp + c) * 32 + lane];
+        app_df_partial(av->x, rv, warp, lane, *av);
+      }
+    }
+    __syncthreads();
+    // the decisions: warp NW - 1 the key, warp NW - 2 the value (dense: the exact
+    // decision on the double-float partials; otherwise the one-warp path)
+    const int P = pg.page_tokens;
+    if (warp == NW - 1) {
+      int slot = 0;
+      uint8_t* rec = new_record(slot);
+      if (rec) {
+        if (DENSE) app_df_decide(*ak, app.mu_rot_k != nullptr, mu_k, app.clip_k, rec + 32 * slot, rec + 64 * P + 4 * slot, lane);
+        else app_warp(ak->x, rot, h, app.mu_rot_k, app.clip_k, rec + 32 * slot, rec + 64 * P + 4 * slot, lane);
+      }
+    }
+    if (warp == NW - 2) {
+      int slot = 0;
+      uint8_t* rec = new_record(slot);
+      if (rec) {
+        if (dense_v)
+          app_df_decide(*av, false, mu_k, app.clip_v, rec + 32 * P + 32 * slot, rec + 68 * P + 4 * slot, lane);
+        else
+          app_warp(av->x, app.rot_v, h, nullptr, app.clip_v, rec + 32 * P + 32 * slot, rec + 68 * P + 4 * slot, lane);
+      }
+    }
+    // the decode kernel reads the pages with bulk copies (the async proxy)
+    asm volatile("fence.proxy.async.global;" ::: "memory");
   }
   __syncthreads();
   for (int j = warp; j < G; j += NW) {
@@ -345,7 +543,7 @@ template <int G, int P, bool WIN>
 __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     PageGeom g, int n_seqs, int n_q_heads, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ table, const uint8_t* __restrict__ pool, DecWs ws,
-    float* __restrict__ o_rot, unsigned* err, WinGeom win) {
+    float* __restrict__ o_rot, unsigned* err, WinGeom win, int step_append) {
   constexpr int NT = n_tiles(G);
   constexpr int NST = DEC_STAGES;
   constexpr int PPC = 32 / P;              // pages per 32-token chunk
@@ -559,15 +757,29 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     else issue_int2(win_first ? f - my_nw : f, sidx);
   };
 
+  // With a step's append (kvq_decode_step) the query preparation writes the new token
+  // into the last page of every sequence: a warp whose first stages include the last
+  // entry of a unit issues them only after that kernel has completed.
+  bool early = true;
+  if (step_append && my_n > 0) {
+    ChunkWalker w = iw;
+    for (int f = 0; f < NST && f < my_n; ++f) {
+      walk_to(w, ga + f);
+      if (ga + f == w.E - 1) early = false;
+    }
+  }
   if (F > 0) {
     if (lane == 0) {
       for (int s = 0; s < NST; ++s) mbar_init(&bars[warp][s], 1);
       fence_mbar_init();
     }
     __syncwarp();
-    for (int f = 0; f < NST && f < F; ++f) issue(f);
+    if (early)
+      for (int f = 0; f < NST && f < F; ++f) issue(f);
   }
   pdl_wait();               // the query fragments and spans come from qprep_kernel
+  if (F > 0 && !early)
+    for (int f = 0; f < NST && f < F; ++f) issue(f);
   pdl_launch_dependents();  // the combine kernel may be scheduled as blocks retire
   if (F <= 0) return;       // no block-level synchronisation follows
 
@@ -1219,18 +1431,30 @@ cudaError_t decode_smem_attr() {
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q, int q_dtype,
                           const int32_t* seq_lens, int max_seq_len, const int32_t* table, RotDev rot_k,
                           const uint8_t* pool, int n_ctas, void* ws_base, float* o_rot, unsigned* err,
-                          cudaStream_t s, WinGeom win, RotDev rot_v) {
+                          cudaStream_t s, WinGeom win, RotDev rot_v, const StepAppend* app) {
   (void)max_seq_len;
   if (n_seqs == 0) return cudaSuccess;
   const int gqa = n_q_heads / g.n_kv_heads;
   const bool windows = win.sink + win.recent > 0;
+  if (app && windows) return cudaErrorInvalidValue;  // the fused step append has no window copies
   DecWs ws;
   decode_ws_layout(ws_base, n_seqs, g.n_kv_heads, gqa, n_ctas, windows, &ws);
   const dim3 qg(g.n_kv_heads, n_seqs);
   const bool dense = rot_k.kind == KVQ_ROT_DENSE;
-#define KVQ_QPREP(GG)                                                                                     \
-  if (dense) qprep_kernel<GG, true><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k, seq_lens, ws, o_rot); \
-  else qprep_kernel<GG, false><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k, seq_lens, ws, o_rot)
+  const StepAppend sa = app ? *app : StepAppend{nullptr, nullptr, 0, RotDev{0, nullptr, nullptr}, nullptr, 1.f, 1.f, nullptr};
+  const int qpa_smem = qpa_smem_bytes(app && app->rot_v.kind == KVQ_ROT_DENSE);
+#define KVQ_QPREP_A(GG, DD)                                                                                   \
+  if (app) {                                                                                                  \
+    static std::atomic<unsigned long long> attr{0};                                                          \
+    const cudaError_t ea = smem_limit_once(attr, qprep_kernel<GG, DD, true>, qpa_smem_bytes(true));           \
+    if (ea != cudaSuccess) return ea;                                                                         \
+    qprep_kernel<GG, DD, true><<<qg, QP_THREADS, qpa_smem, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k,   \
+                                                               seq_lens, ws, o_rot, g, table, sa, err);       \
+  }                                                                                                           \
+  else qprep_kernel<GG, DD, false><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k,       \
+                                                            seq_lens, ws, o_rot, g, table, sa, err)
+#define KVQ_QPREP(GG) \
+  if (dense) { KVQ_QPREP_A(GG, true); } else { KVQ_QPREP_A(GG, false); }
   switch (gqa) {
     case 1: KVQ_QPREP(1); break;
     case 2: KVQ_QPREP(2); break;
@@ -1239,6 +1463,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
     default: return cudaErrorInvalidValue;
   }
 #undef KVQ_QPREP
+#undef KVQ_QPREP_A
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -1258,7 +1483,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
     e = decode_smem_attr<GG, PP, WW>();                                                                   \
     if (e == cudaSuccess)                                                                                 \
       e = cudaLaunchKernelEx(&cfg, decode_split_kernel<GG, PP, WW>, g, n_seqs, n_q_heads, seq_lens, table, pool, \
-                             ws, o_rot, err, win);                                                         \
+                             ws, o_rot, err, win, app ? 1 : 0);                                            \
   } while (0)
 #define KVQ_DEC(GG, PP) \
   if (windows) KVQ_DEC_W(GG, PP, true); else KVQ_DEC_W(GG, PP, false)

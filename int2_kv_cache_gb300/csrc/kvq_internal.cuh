@@ -40,6 +40,19 @@ struct WinGeom {
 constexpr int WIN_REC_TOKENS = 8;
 constexpr int WIN_REC_BYTES = 4096;  // 8 key rows + 8 value rows of 128 bf16
 
+// A decode step's new token (one per sequence, at position seq_lens[b] - 1),
+// quantized and written by the decode's query preparation before the decode
+// kernel reads the pages (kvq_decode_step).  k, v: [n_seqs][n_kv_heads][128].
+struct StepAppend {
+  const void* k;
+  const void* v;
+  int dtype;
+  RotDev rot_v;           // the keys use the decode's rot_k
+  const float* mu_rot_k;  // mu R_K per head, or nullptr
+  float clip_k, clip_v;
+  uint8_t* pool;          // the pool, written in place
+};
+
 struct PageGeom {
   int page_tokens;
   int n_kv_heads;
@@ -135,7 +148,8 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
                           int q_dtype, const int32_t* seq_lens, int max_seq_len,
                           const int32_t* table, RotDev rot_k, const uint8_t* pool, int n_ctas,
                           void* ws, float* o_rot, unsigned* err, cudaStream_t s,
-                          WinGeom win = WinGeom{0, 0, nullptr}, RotDev rot_v = RotDev{0, nullptr, nullptr});
+                          WinGeom win = WinGeom{0, 0, nullptr}, RotDev rot_v = RotDev{0, nullptr, nullptr},
+                          const StepAppend* app = nullptr);
 
 // outproj.cu
 cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, int w_dtype,

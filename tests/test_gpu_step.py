@@ -1,0 +1,122 @@
+"""GPU parity of kvq_decode_step: the decode step with each sequence's new token
+quantized and written inside the decode call ("Output-Aware Rotation for INT2
+KV-Cache Quantization", §6 cache-write kernel and decode; Eqs. 4, 20-22, 26, 27).
+
+The fused step must write exactly the bytes kvq_quantize_append writes and return
+exactly what kvq_decode_attention returns over the extended sequences (same grid,
+so bit for bit), and both must match the fp64 oracle."""
+import numpy as np
+import pytest
+
+import gpu_util as gu
+from int2_kv_cache_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # hq, hkv, page, lengths (after the step), rot, dtype, clips
+    (8, 2, 16, [1, 16, 17, 300, 0, 33], "dense", "bf16", (0.96, 0.92)),
+    (4, 4, 8, [9, 8, 1, 130], "signed_hadamard", "f32", (1.0, 0.9)),
+    (32, 8, 16, [777, 2048], "dense", "bf16", (1.0, 1.0)),
+    (8, 1, 16, [64, 65, 5], "identity", "bf16", (0.9, 0.9)),
+    (40, 10, 16, [1100, 3000, 1025], "dense", "bf16", (1.0, 1.0)),
+]
+
+
+def _inputs(g):
+    """History pools (every token but the last) and the step's new tokens."""
+    c = g.case
+    kv = [c.kv(b) for b in range(c.n_seqs)]
+    hist = np.maximum(g.lengths - 1, 0)
+    pool = g.new_pool()
+    ks, vs, cu, start = [], [], [0], []
+    for b in range(c.n_seqs):
+        ks.append(kv[b][0][:hist[b]])
+        vs.append(kv[b][1][:hist[b]])
+        cu.append(cu[-1] + int(hist[b]))
+        start.append(0)
+    g.kvq.kvq_quantize_append(g.layout, gu.dev(np.concatenate(ks), c.dtype), gu.dev(np.concatenate(vs), c.dtype),
+                              gu.dev_i32(cu), gu.dev_i32(start), g.table, g.rot_k, g.rot_v, g.mu_rot_dev, c.clip_k,
+                              c.clip_v, pool)
+    zero = np.zeros((c.n_kv_heads, 128), np.float32)
+    k_new = np.stack([kv[b][0][g.lengths[b] - 1] if g.lengths[b] else zero for b in range(c.n_seqs)])
+    v_new = np.stack([kv[b][1][g.lengths[b] - 1] if g.lengths[b] else zero for b in range(c.n_seqs)])
+    return pool, k_new, v_new
+
+
+@pytest.mark.parametrize("hq,hkv,page,lengths,rot,dtype,clips", CASES, ids=lambda v: str(v))
+def test_step_equals_append_then_decode_and_the_oracle(hq, hkv, page, lengths, rot, dtype, clips):
+    case = W.decode_case(61, lengths, hq, hkv, 128, rot, dtype, page_tokens=page, clip_k=clips[0], clip_v=clips[1],
+                         spare_blocks=2, n_cal=256)
+    g = gu.GpuCase(case)
+    kvq, torch = g.kvq, g.torch
+    pool_a, k_new, v_new = _inputs(g)
+    pool_b = pool_a.clone()
+    max_len = int(g.lengths.max())
+    q = gu.dev(case.queries(), dtype)
+    kn, vn = gu.dev(k_new, dtype), gu.dev(v_new, dtype)
+    lens = gu.dev_i32(g.lengths)
+    ws = torch.empty(max(kvq.kvq_decode_workspace_size(g.layout, case.n_seqs, max_len), 16), dtype=torch.uint8,
+                     device="cuda")
+    # separate calls: append the new tokens (sequences of length 0 append nothing), then decode
+    has = g.lengths > 0
+    kvq.kvq_quantize_append(g.layout, gu.dev(k_new[has], dtype), gu.dev(v_new[has], dtype),
+                            gu.dev_i32(np.concatenate([[0], np.cumsum(has)])),
+                            gu.dev_i32(np.maximum(g.lengths - 1, 0)), g.table, g.rot_k, g.rot_v, g.mu_rot_dev,
+                            case.clip_k, case.clip_v, pool_a)
+    out_a = torch.full((case.n_seqs, hq, 128), float("nan"), device="cuda")
+    kvq.kvq_decode_attention(g.layout, q, lens, max_len, g.table, g.rot_k, pool_a, ws, out_a)
+    # the fused step
+    out_b = torch.full_like(out_a, float("nan"))
+    kvq.kvq_decode_step(g.layout, q, kn, vn, lens, max_len, g.table, g.rot_k, g.rot_v, g.mu_rot_dev, case.clip_k,
+                        case.clip_v, pool_b, ws, out_b)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    assert torch.equal(pool_a, pool_b)
+    assert torch.equal(out_a, out_b)
+    # and the oracle: pool bytes (with the boundary exemption) and the readout
+    ora_pool, encs = g.oracle_pool()
+    gu.compare_codes(pool_b.cpu().numpy(), ora_pool, hkv, page, case.block_table, g.lengths, encs,
+                     (case.clip_k, case.clip_v), label="step")
+    got = out_b.cpu().numpy()
+    ref = g.oracle_decode(ora_pool, case.queries())
+    for b in range(case.n_seqs):
+        if g.lengths[b] == 0:
+            assert np.all(got[b] == 0)
+        else:
+            assert gu.out_err(got[b], ref[b]) <= gu.OUT_TOL, (b, gu.out_err(got[b], ref[b]))
+
+
+def test_consecutive_steps_walk_across_pages():
+    """Twenty single-token steps on the same pool (lengths cross page boundaries):
+    the pool ends byte-equal to the oracle's encoding of every token."""
+    lengths0 = np.array([5, 30, 1, 250])
+    n_steps = 20
+    final = lengths0 + n_steps - 1
+    case = W.decode_case(62, final, 8, 2, 128, "dense", "bf16", page_tokens=16, clip_k=0.96, clip_v=0.92, n_cal=256)
+    g = gu.GpuCase(case, lengths=lengths0 - 1)
+    kvq, torch = g.kvq, g.torch
+    pool = g.new_pool()
+    g.gpu_append_all(pool)  # history: lengths0 - 1 tokens
+    kv = [case.kv(b) for b in range(case.n_seqs)]
+    ws = torch.empty(kvq.kvq_decode_workspace_size(g.layout, case.n_seqs, int(final.max())), dtype=torch.uint8,
+                     device="cuda")
+    out = torch.empty(case.n_seqs, 8, 128, device="cuda")
+    q = gu.dev(case.queries(), "bf16")
+    for st in range(n_steps):
+        lens = lengths0 + st
+        k_new = np.stack([kv[b][0][lens[b] - 1] for b in range(case.n_seqs)])
+        v_new = np.stack([kv[b][1][lens[b] - 1] for b in range(case.n_seqs)])
+        kvq.kvq_decode_step(g.layout, q, gu.dev(k_new, "bf16"), gu.dev(v_new, "bf16"), gu.dev_i32(lens),
+                            int(lens.max()), g.table, g.rot_k, g.rot_v, g.mu_rot_dev, case.clip_k, case.clip_v, pool,
+                            ws, out)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    g.lengths = final
+    ora_pool, encs = g.oracle_pool()
+    gu.compare_codes(pool.cpu().numpy(), ora_pool, 2, 16, case.block_table, final, encs, (case.clip_k, case.clip_v),
+                     label="steps")
+    ref = g.oracle_decode(ora_pool, case.queries())
+    got = out.cpu().numpy()
+    for b in range(case.n_seqs):
+        assert gu.out_err(got[b], ref[b]) <= gu.OUT_TOL
