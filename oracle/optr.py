@@ -108,12 +108,12 @@ def key_loss(a, r0, q, k, v, w_o, mu, clip: float, lam: float = 1.0, grad: bool 
             p = softmax(a_ref)
             pk = softmax(a_k)
             kl, dkl = kl_term(p, pk)
-            vw = v[: t + 1] @ w_j.T  # [t+1, d_model]: v_s W_j^T
-            e = (pk - p) @ vw
+            vt = v[: t + 1]
+            e = ((pk - p) @ vt) @ w_j.T  # Eq. 13: [sum_s (p^K_s - p_s) v_s] W_j^T
             err, derr = output_error_term(e, dm)
             loss += (kl + lam * err) / n
             if grad:
-                dpk = lam * (vw @ derr)  # d(lam ||e||^2 / dm) / dp^K_s
+                dpk = lam * (vt @ (w_j.T @ derr))  # d(lam ||e||^2 / dm) / dp^K_s = lam v_s . W_j^T derr
                 da = pk * (dpk - pk @ dpk) + dkl  # softmax backward, plus dKL/da^K
                 g_keff[: t + 1] += np.outer(da / n, qq) / np.sqrt(D)
     if not grad:
