@@ -48,7 +48,7 @@ def parse():
     p.add_argument("--steps", type=int, default=2000)
     p.add_argument("--warmup", type=int, default=20)
     p.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
-    p.add_argument("--case", choices=["decode_step", "append_chunk", "append_chunk_dense", "calib", "report"],
+    p.add_argument("--case", choices=["decode_step", "append_chunk", "append_chunk_dense", "calib", "report", "optr"],
                    default="decode_step")
     p.add_argument("--workload", choices=["gqa8b", "long4b", "serve14b"], default="gqa8b",
                    help="decode-step shape: gqa8b (default, the headline), long4b (128K), serve14b (ragged)")
@@ -60,6 +60,7 @@ def parse():
                    help="clip ratios of keys and values, e.g. 0.96,0.92 (Table A); default per workload")
     p.add_argument("--window", default=None, metavar="SINK,RECENT",
                    help="decode step with BF16 sink / recent windows, e.g. 64,256 (default: all tokens INT2)")
+    p.add_argument("--optr-steps", type=int, default=80, help="--case optr: Adam steps per phase (the paper: 80)")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-clocks", action="store_true")
     return p.parse_args()
@@ -739,6 +740,59 @@ def run_report(args):
                       "key_share": [round(float(x), 3) for x in o[1] / (o[1] + o[2])]}), flush=True)
 
 
+def run_optr(args):
+    """OptR gradient calibration (Algorithm 1) of the 14B-class serving layer's heads:
+    each head a 2,560-token training trace and a held-out trace of the same size
+    (the last 64 query positions, 4 query heads), d_model 5,120, clips 0.96 / 0.92,
+    lambda_K = 1, Adam at 0.02 for --optr-steps steps per phase, selection every 20."""
+    import torch
+    import int2_kv_cache_gb300 as kvq
+    from int2_kv_cache_gb300 import workloads as W
+    device = "cuda:0"
+    steps = args.optr_steps
+    n_tok, n_qpos, gqa, dm = 2560, 64, 4, 5120
+    c = W.optr_head(5, n_tok, n_qpos, gqa, dm)
+    t32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device)
+    t64 = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.float64)).to(device)
+    q, k, v = c.train
+    mu = k.mean(axis=0)
+    tr = tuple(t32(x) for x in c.train)
+    ho = tuple(t32(x) for x in c.heldout)
+    ws = torch.empty(kvq.kvq_optr_workspace_size(n_tok, n_qpos, gqa, n_tok, n_qpos), dtype=torch.uint8, device=device)
+    r_k = torch.empty(128, 128, dtype=torch.float64, device=device)
+    r_v = torch.empty_like(r_k)
+    lk = torch.empty(steps, dtype=torch.float64, device=device)
+    lv = torch.empty_like(lk)
+    args_ = (tr, ho, t32(c.w_o), t32(mu), t64(c.r_k0), t64(c.r_v0), W.f32(0.96), W.f32(0.92), 1.0, steps,
+             W.f32(0.02), 20, r_k, r_v, lk, lv, ws)
+    kvq.kvq_optr_calibrate_head(*args_[:9], 2, W.f32(0.02), 20, *args_[12:])  # warm-up (2 steps)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    kvq.kvq_optr_calibrate_head(*args_)
+    e1.record()
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    ms = e0.elapsed_time(e1)
+    # algorithmic fp64 flops of one loss + gradient evaluation (GEMMs, the exponential and its
+    # Frechet derivative at the squarings actually taken are counted from the generator norm)
+    npairs = n_qpos * gqa
+    tok_sum = sum(n_tok - n_qpos + i + 1 for i in range(n_qpos)) * gqa
+    mm = 2.0 * 128 ** 3
+    pair = 10.0 * 128 * tok_sum + 4.0 * 128 * dm * npairs
+    fwd = 18 * mm + 2 * (2.0 * n_tok * 128 * 128) + pair
+    bwd = 2.0 * n_tok * 128 * npairs + 3 * (2.0 * n_tok * 128 * 128) + mm + 3 * 17 * mm
+    flops = steps * 2 * (fwd + bwd)  # both phases (the value pair kernel is cheaper: an upper count)
+    peak = 1250.0  # GFLOP/s, GB300 fp64 (nominal)
+    print(json.dumps({"case": "optr", "workload": (f"OptR Algorithm 1, one KV head of the 14B-class serving layer: "
+                                                   f"{n_tok} tokens, last {n_qpos} positions x {gqa} query heads, "
+                                                   f"d_model {dm}, {steps} + {steps} Adam steps, held-out selection"),
+                      "ms_per_head": ms, "s_per_layer_10_heads": 10 * ms / 1e3,
+                      "final_losses": [float(lk[-1]), float(lv[-1])],
+                      "roofline": {"bound": "alu (fp64)", "achieved_gflops": flops / ms / 1e6, "peak": peak,
+                                   "unit": "GFLOP/s", "frac": flops / ms / 1e6 / peak, "flops": flops}}), flush=True)
+
+
 def main():
     args = parse()
     if args.impl == "reference":
@@ -749,6 +803,8 @@ def main():
         run_report(args)
     elif args.case == "calib":
         run_calib(args)
+    elif args.case == "optr":
+        run_optr(args)
     else:
         run_gpu(args)
 

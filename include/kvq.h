@@ -368,6 +368,62 @@ kvq_status kvq_head_error_report(int n_tok, int n_qpos, int n_kv_heads, int gqa,
                                  const float* mu, float clip_k, float clip_v, double* out,
                                  void* workspace, size_t workspace_bytes, kvq_stream stream);
 
+/* ---- OptR gradient calibration of one KV head ("Output-Aware Rotation for INT2
+ * KV-Cache Quantization", §4.2 Eq. 11, §4.3 Eqs. 12-14, §4.4 Eqs. 15-16, §4.5
+ * Eqs. 17-18, Algorithm 1; §5 implementation details: lambda_K = 1, 80 Adam
+ * steps at learning rate 0.02, selection every 20 steps).
+ * A trace of the head: the queries of its last n_qpos positions (causal: position
+ * t = n_tok - n_qpos + i attends s <= t) and its n_tok keys and values, fp32:
+ *   q [n_qpos][gqa][128], k [n_tok][128], v [n_tok][128]; 1 <= n_tok <= 8192.
+ * w_o: fp32 [d_model][gqa * 128], the W_O columns of the head's query heads
+ * (d_model <= 8192); mu: fp32 [128], the head's (unrotated) key mean, or NULL.
+ * Rotations and generators are fp64 [128][128] row-major (x R for a row x).
+ * All arithmetic is fp64; Q_2's decisions (fp16 scale and zero, codes) follow
+ * kvq_quantize_append's definition with the clip ratio of the role.
+ * The straight-through estimator passes a channel's gradient iff it lies in its
+ * group's clip range [c min, c max] (scale and zero held constant). */
+typedef struct {
+  const float* q;
+  const float* k;
+  const float* v;
+  int n_tok;
+  int n_qpos;
+} kvq_optr_trace;
+
+typedef enum { KVQ_OPTR_KEYS = 0, KVQ_OPTR_VALUES = 1 } kvq_optr_phase;
+
+/* Workspace bytes for a training trace and an optional held-out trace (0, 0 if none). */
+kvq_status kvq_optr_workspace_size(int n_tok, int n_qpos, int n_tok_heldout, int n_qpos_heldout, int gqa,
+                                   size_t* bytes);
+
+/* One objective and its gradient at R = r0 exp(a - a^T):
+ *   KVQ_OPTR_KEYS:   L_K = mean over (t, j) of KL(p_t || p^K_t) + lambda_k ||e_K||^2 / d_model
+ *                    (Eqs. 12-14; p from the raw keys, p^K from Q_2((k - mu) R; clip_k) R^T)
+ *   KVQ_OPTR_VALUES: L_V = mean over (t, j) of ||e_V||^2 / d_model (Eqs. 15-16; the weights p^K
+ *                    from the selected key rotation r_k_sel with clip_k, V~ = Q_2(v R; clip_v) R^T)
+ * loss: device double (written); grad: device double [128][128] = dL/da, or NULL for the loss only.
+ * workspace: >= kvq_optr_workspace_size(n_tok, n_qpos, 0, 0, gqa) bytes. */
+kvq_status kvq_optr_loss_grad(int phase, const kvq_optr_trace* trace, int gqa, int d_model, const float* w_o,
+                              const float* mu, const double* r0, const double* a, const double* r_k_sel,
+                              float clip_k, float clip_v, float lambda_k, double* loss, double* grad,
+                              void* workspace, size_t workspace_bytes, kvq_stream stream);
+
+/* Algorithm 1 for one KV head: `steps` Adam steps (beta 0.9 / 0.999, eps 1e-8, rate lr)
+ * on A_K from 0 for L_K, then `steps` on A_V for L_V under the selected key path.  In
+ * each phase the iterate at step 0 and after every `every` steps (0: none) is a
+ * candidate, scored by the same loss on `heldout` (or on `train` when NULL); the
+ * lowest score wins, ties to the earlier step.
+ *   r_k = r_k0 exp(A_K* - A_K*^T), r_v = r_v0 exp(A_V* - A_V*^T): device double [128][128]
+ *   loss_k, loss_v: device double [steps], the training loss before each step, or NULL
+ * workspace: >= kvq_optr_workspace_size(train sizes, heldout sizes, gqa) bytes.
+ * The call enqueues its kernels on `stream` and returns; a generator whose norm
+ * is too large for the exponential's scaling is flagged (kvq_device_check). */
+kvq_status kvq_optr_calibrate_head(const kvq_optr_trace* train, const kvq_optr_trace* heldout, int gqa, int d_model,
+                                   const float* w_o, const float* mu, const double* r_k0, const double* r_v0,
+                                   float clip_k, float clip_v, float lambda_k, int steps, float lr, int every,
+                                   double* r_k, double* r_v, double* loss_k, double* loss_v, void* workspace,
+                                   size_t workspace_bytes, kvq_stream stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -61,6 +61,11 @@ class KvqRot(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int), ("signs", ctypes.c_void_p), ("dense", ctypes.c_void_p)]
 
 
+class KvqOptrTrace(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("n_tok", ctypes.c_int),
+                ("n_qpos", ctypes.c_int)]
+
+
 class KvqWindow(ctypes.Structure):
     _fields_ = [("sink_tokens", ctypes.c_int), ("recent_tokens", ctypes.c_int), ("buf", ctypes.c_void_p)]
 
@@ -78,6 +83,7 @@ def lib() -> ctypes.CDLL:
         vp, i, f, st, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_int, ctypes.c_size_t
         lp = ctypes.POINTER(KvqLayout)
         wp = ctypes.POINTER(KvqWindow)
+        tp = ctypes.POINTER(KvqOptrTrace)
         sigs = {
             "kvq_last_error": ([], ctypes.c_char_p),
             "kvq_pool_bytes": ([lp], sz),
@@ -101,6 +107,10 @@ def lib() -> ctypes.CDLL:
                                        vp], st),
             "kvq_calib_nmse": ([i, i, i, i, i, vp, vp, vp, i, vp, i, i, ctypes.POINTER(KvqRot), i,
                                 ctypes.POINTER(ctypes.c_float), vp, i, vp, vp, vp, sz, vp], st),
+            "kvq_optr_workspace_size": ([i, i, i, i, i, ctypes.POINTER(sz)], st),
+            "kvq_optr_loss_grad": ([i, tp, i, i, vp, vp, vp, vp, vp, f, f, f, vp, vp, vp, sz, vp], st),
+            "kvq_optr_calibrate_head": ([tp, tp, i, i, vp, vp, vp, vp, f, f, f, i, f, i, vp, vp, vp, vp, vp, sz,
+                                         vp], st),
         }
         for name, (argtypes, restype) in sigs.items():
             fn = getattr(L, name)
@@ -115,7 +125,7 @@ EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mea
             "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_window_append", "kvq_decode_workspace_size_win",
             "kvq_decode_attention_win", "kvq_fold_wo",
             "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse", "kvq_report_workspace_size",
-            "kvq_head_error_report")
+            "kvq_head_error_report", "kvq_optr_workspace_size", "kvq_optr_loss_grad", "kvq_optr_calibrate_head")
 
 
 def _check(status: int) -> None:
@@ -341,3 +351,46 @@ def kvq_head_error_report(q, k, v, w_o, rot_k: DeviceRot, rot_v: DeviceRot, mu, 
                                        _ptr(_contig(w_o, "w_o")), _dtype_code(w_o), rot_k.c, rot_v.c, _ptr(mu),
                                        float(clip_k), float(clip_v), _ptr(out), _ptr(workspace),
                                        workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ---- OptR gradient calibration of one KV head ----
+KVQ_OPTR_KEYS = 0
+KVQ_OPTR_VALUES = 1
+
+
+def _trace(q, k, v):
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        _contig(t, name)
+    return KvqOptrTrace(_ptr(q), _ptr(k), _ptr(v), k.shape[0], q.shape[0])
+
+
+def kvq_optr_workspace_size(n_tok: int, n_qpos: int, gqa: int, n_tok_heldout: int = 0, n_qpos_heldout: int = 0) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().kvq_optr_workspace_size(n_tok, n_qpos, n_tok_heldout, n_qpos_heldout, gqa, ctypes.byref(out)))
+    return int(out.value)
+
+
+def kvq_optr_loss_grad(phase: int, q, k, v, w_o, mu, r0, a, r_k_sel, clip_k: float, clip_v: float, lambda_k: float,
+                       loss, grad, workspace, stream=None) -> None:
+    """One OptR objective (keys: Eq. 14; values: Eq. 16) and dL/dA at R = r0 exp(a - a^T).
+    q [n_qpos][gqa][128], k, v [n_tok][128], w_o [d_model][gqa*128], mu [128] (fp32);
+    r0, a, r_k_sel, grad: fp64 [128][128]; loss: fp64 [1]."""
+    tr = _trace(q, k, v)
+    _check(lib().kvq_optr_loss_grad(phase, ctypes.byref(tr), q.shape[1], w_o.shape[0], _ptr(_contig(w_o, "w_o")),
+                                    _ptr(mu), _ptr(r0), _ptr(a), _ptr(r_k_sel), clip_k, clip_v, lambda_k, _ptr(loss),
+                                    _ptr(grad), _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                    _stream(stream)))
+
+
+def kvq_optr_calibrate_head(train, heldout, w_o, mu, r_k0, r_v0, clip_k: float, clip_v: float, lambda_k: float,
+                            steps: int, lr: float, every: int, r_k, r_v, loss_k, loss_v, workspace,
+                            stream=None) -> None:
+    """Algorithm 1 for one KV head.  train / heldout: (q, k, v) tuples of fp32 tensors (heldout may be None)."""
+    tr = _trace(*train)
+    ho = _trace(*heldout) if heldout is not None else None
+    q = train[0]
+    _check(lib().kvq_optr_calibrate_head(ctypes.byref(tr), ctypes.byref(ho) if ho is not None else None, q.shape[1],
+                                         w_o.shape[0], _ptr(_contig(w_o, "w_o")), _ptr(mu), _ptr(r_k0), _ptr(r_v0),
+                                         clip_k, clip_v, lambda_k, steps, lr, every, _ptr(r_k), _ptr(r_v),
+                                         _ptr(loss_k), _ptr(loss_v), _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(), _stream(stream)))

@@ -333,6 +333,94 @@ kvq_status kvq_decode_step(const kvq_layout* layout, int n_seqs, const void* q, 
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_step");
 }
 
+static kvq_status check_optr_trace(const kvq_optr_trace* t, const char* name, int gqa) {
+  if (!t) return fail(KVQ_EINVAL, "%s is NULL", name);
+  if (t->n_tok < 1 || t->n_tok > 8192) return fail(KVQ_EUNSUPPORTED, "%s: n_tok %d outside [1, 8192]", name, t->n_tok);
+  if (t->n_qpos < 1 || t->n_qpos > t->n_tok)
+    return fail(KVQ_EINVAL, "%s: n_qpos %d outside [1, n_tok]", name, t->n_qpos);
+  if ((long long)t->n_qpos * gqa > 65535) return fail(KVQ_EUNSUPPORTED, "%s: n_qpos * gqa > 65535", name);
+  KVQ_PTR(t->q, "trace q");
+  KVQ_PTR(t->k, "trace k");
+  KVQ_PTR(t->v, "trace v");
+  return KVQ_OK;
+}
+
+static kvq_status check_optr_common(int gqa, int d_model, const float* w_o, const float* mu) {
+  if (gqa < 1 || gqa > 64) return fail(KVQ_EINVAL, "gqa %d outside [1, 64]", gqa);
+  if (d_model < 1 || d_model > 8192) return fail(KVQ_EUNSUPPORTED, "d_model %d outside [1, 8192]", d_model);
+  KVQ_PTR(w_o, "w_o");
+  if (mu && !aligned16(mu)) return fail(KVQ_EINVAL, "mu is not 16-byte aligned");
+  return KVQ_OK;
+}
+
+kvq_status kvq_optr_workspace_size(int n_tok, int n_qpos, int n_tok_heldout, int n_qpos_heldout, int gqa,
+                                   size_t* bytes) {
+  if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");
+  if (n_tok < 1 || n_qpos < 1 || gqa < 1 || n_tok_heldout < 0 || n_qpos_heldout < 0)
+    return fail(KVQ_EINVAL, "bad sizes");
+  *bytes = kvq::optr_workspace_bytes(n_tok, n_qpos, n_tok_heldout, n_qpos_heldout, gqa);
+  return KVQ_OK;
+}
+
+kvq_status kvq_optr_loss_grad(int phase, const kvq_optr_trace* trace, int gqa, int d_model, const float* w_o,
+                              const float* mu, const double* r0, const double* a, const double* r_k_sel,
+                              float clip_k, float clip_v, float lambda_k, double* loss, double* grad,
+                              void* workspace, size_t workspace_bytes, kvq_stream stream) {
+  if (phase != KVQ_OPTR_KEYS && phase != KVQ_OPTR_VALUES) return fail(KVQ_EINVAL, "phase %d", phase);
+  KVQ_CHECK(check_optr_trace(trace, "trace", gqa));
+  KVQ_CHECK(check_optr_common(gqa, d_model, w_o, mu));
+  if (!valid_clip(clip_k) || !valid_clip(clip_v))
+    return fail(KVQ_EINVAL, "clip ratios must lie in (0, 1] (got %g, %g)", clip_k, clip_v);
+  if (!std::isfinite(lambda_k)) return fail(KVQ_EINVAL, "lambda_k is not finite");
+  KVQ_PTR(r0, "r0");
+  KVQ_PTR(a, "a");
+  if (phase == KVQ_OPTR_VALUES) KVQ_PTR(r_k_sel, "r_k_sel");
+  if (!loss || (reinterpret_cast<uintptr_t>(loss) & 7u)) return fail(KVQ_EINVAL, "loss is NULL or not 8-byte aligned");
+  if (grad && !aligned16(grad)) return fail(KVQ_EINVAL, "grad is not 16-byte aligned");
+  KVQ_PTR(workspace, "workspace");
+  const size_t need = kvq::optr_workspace_bytes(trace->n_tok, trace->n_qpos, 0, 0, gqa);
+  if (workspace_bytes < need) return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
+  const kvq::OptrTraceIn tr{trace->q, trace->k, trace->v, trace->n_tok, trace->n_qpos};
+  cudaError_t e = kvq::launch_optr_loss_grad(phase, tr, gqa, d_model, w_o, mu, r0, a, r_k_sel, clip_k, clip_v,
+                                             lambda_k, loss, grad, workspace, err, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_optr_loss_grad");
+}
+
+kvq_status kvq_optr_calibrate_head(const kvq_optr_trace* train, const kvq_optr_trace* heldout, int gqa, int d_model,
+                                   const float* w_o, const float* mu, const double* r_k0, const double* r_v0,
+                                   float clip_k, float clip_v, float lambda_k, int steps, float lr, int every,
+                                   double* r_k, double* r_v, double* loss_k, double* loss_v, void* workspace,
+                                   size_t workspace_bytes, kvq_stream stream) {
+  KVQ_CHECK(check_optr_trace(train, "train", gqa));
+  if (heldout) KVQ_CHECK(check_optr_trace(heldout, "heldout", gqa));
+  KVQ_CHECK(check_optr_common(gqa, d_model, w_o, mu));
+  if (!valid_clip(clip_k) || !valid_clip(clip_v))
+    return fail(KVQ_EINVAL, "clip ratios must lie in (0, 1] (got %g, %g)", clip_k, clip_v);
+  if (!std::isfinite(lambda_k) || !std::isfinite(lr) || !(lr > 0.f)) return fail(KVQ_EINVAL, "bad lambda_k or lr");
+  if (steps < 0 || steps > 100000 || every < 0) return fail(KVQ_EINVAL, "bad steps %d / every %d", steps, every);
+  KVQ_PTR(r_k0, "r_k0");
+  KVQ_PTR(r_v0, "r_v0");
+  KVQ_PTR(r_k, "r_k");
+  KVQ_PTR(r_v, "r_v");
+  if (loss_k && (reinterpret_cast<uintptr_t>(loss_k) & 7u)) return fail(KVQ_EINVAL, "loss_k not 8-byte aligned");
+  if (loss_v && (reinterpret_cast<uintptr_t>(loss_v) & 7u)) return fail(KVQ_EINVAL, "loss_v not 8-byte aligned");
+  KVQ_PTR(workspace, "workspace");
+  const size_t need = kvq::optr_workspace_bytes(train->n_tok, train->n_qpos, heldout ? heldout->n_tok : 0,
+                                                heldout ? heldout->n_qpos : 0, gqa);
+  if (workspace_bytes < need) return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
+  const kvq::OptrTraceIn tr{train->q, train->k, train->v, train->n_tok, train->n_qpos};
+  kvq::OptrTraceIn ho{};
+  if (heldout) ho = kvq::OptrTraceIn{heldout->q, heldout->k, heldout->v, heldout->n_tok, heldout->n_qpos};
+  cudaError_t e = kvq::launch_optr_calibrate(tr, heldout ? &ho : nullptr, gqa, d_model, w_o, mu, r_k0, r_v0, clip_k,
+                                             clip_v, lambda_k, steps, lr, every, r_k, r_v, loss_k, loss_v, workspace,
+                                             err, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_optr_calibrate_head");
+}
+
 kvq_status kvq_decode_attention_win(const kvq_layout* layout, int n_seqs, const void* q, kvq_dtype q_dtype,
                                     const int32_t* seq_lens, int max_seq_len, const int32_t* block_table,
                                     kvq_rot rot_k, kvq_rot rot_v, const uint8_t* pool, const kvq_window* win,

@@ -157,6 +157,25 @@ cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, i
 cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
                             int w_dtype, float* y, unsigned* err, cudaStream_t s);
 
+// optr.cu: OptR calibration of one KV head (fp64)
+struct OptrTraceIn {  // one trace of the head: q [n_qpos][gqa][128], k, v [n_tok][128] (fp32)
+  const float* q;
+  const float* k;
+  const float* v;
+  int n_tok, n_qpos;
+};
+size_t optr_workspace_bytes(int n_tok, int n_qpos, int n_tok_h, int n_qpos_h, int gqa);
+size_t optr_max_smem(int n_tok, int d_model);
+cudaError_t launch_optr_loss_grad(int phase, const OptrTraceIn& tr, int gqa, int d_model, const float* w_o,
+                                  const float* mu, const double* r0, const double* a, const double* r_k_sel,
+                                  float clip_k, float clip_v, float lam, double* loss, double* grad, void* ws,
+                                  unsigned* err, cudaStream_t s);
+cudaError_t launch_optr_calibrate(const OptrTraceIn& tr, const OptrTraceIn* ho, int gqa, int d_model,
+                                  const float* w_o, const float* mu, const double* r_k0, const double* r_v0,
+                                  float clip_k, float clip_v, float lam, int steps, float lr, int every, double* r_k,
+                                  double* r_v, double* loss_k, double* loss_v, void* ws, unsigned* err,
+                                  cudaStream_t s);
+
 // calib.cu
 size_t calib_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint);
 size_t report_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa);

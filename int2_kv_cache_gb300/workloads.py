@@ -368,3 +368,34 @@ def small_calibration(seed: int, n_tok: int, n_qpos: int, n_kv_heads: int, gqa: 
     cands = [make_rot(kd, seed, 700 + i, n_kv_heads) for i, kd in enumerate(kinds)]
     return CalibCase(seed, n_tok, n_qpos, n_kv_heads, gqa, d_model, dtype, k, v, q, w, cands,
                      tuple(f32(c) for c in clips), joint=joint, name="small_calib")
+
+
+@dataclass
+class OptrHeadCase:
+    """One KV head's calibration traces for the OptR gradient calibration: a training
+    trace and a held-out trace (queries at the last n_qpos positions, keys, values),
+    the head's W_O columns, and base rotations R0_K, R0_V (learned-style, fp64)."""
+
+    seed: int
+    gqa: int
+    d_model: int
+    train: tuple  # (q [n_qpos, gqa, 128], k [n_tok, 128], v [n_tok, 128]) float32
+    heldout: tuple
+    w_o: np.ndarray  # [d_model, gqa * 128] float32
+    r_k0: np.ndarray  # [128, 128] float64
+    r_v0: np.ndarray
+
+
+def optr_head(seed: int, n_tok: int, n_qpos: int, gqa: int, d_model: int, a_std: float = 0.05) -> OptrHeadCase:
+    """Synthetic head with the key-outlier profile of the decode workloads (6 offset
+    channels), Student-t value channels, N(0,1) queries, W_O ~ N(0, 1/(gqa 128))."""
+    prof = draw_profile(seed, 1)
+    traces = []
+    for i in range(2):
+        k, v = draw_kv(prof, seed, 7_000_000 + i, n_tok, 1, "f32")
+        q = draw_queries(seed, 7_000_000 + i, (n_qpos, gqa, HEAD_DIM), "f32")
+        traces.append((q, k[:, 0, :].copy(), v[:, 0, :].copy()))
+    w = draw_wo(seed, d_model, gqa * HEAD_DIM, "f32")
+    r_k0 = learned_style_rotation(seed, 900, 1, a_std)[0].astype(np.float64)
+    r_v0 = learned_style_rotation(seed, 901, 1, a_std)[0].astype(np.float64)
+    return OptrHeadCase(seed, gqa, d_model, traces[0], traces[1], w, r_k0, r_v0)
