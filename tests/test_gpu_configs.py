@@ -206,3 +206,59 @@ def test_serve14b_calibration_sampled():
     nm_o, _, ref_o = oracle.calib.calib_sweep(sub.q, sub.k, sub.v, sub.w_o, mats, sub.clips, mu, sub.gqa, False)
     gu.assert_nmse_close(ref, ref_o, "ref")
     gu.assert_nmse_close(nm[sample], nm_o, "serve14b nmse")
+
+
+def test_gqa8b_32k_table_a_windows_sampled():
+    """Table A in full at the 8B-class decode shape: 16 x 32,768 tokens, 8-token pages,
+    clips 0.96 / 0.92, 64 sink + 256 recent BF16 tokens; the whole cache and the window
+    records written by the GPU, the windowed decode over all of it; the oracle re-derives
+    sequences 0 and 15 (INT2 pages, window records, windowed readout)."""
+    import oracle
+    c = W.gqa8b_32k(page_tokens=8, clip_k=0.96, clip_v=0.92)
+    g = gu.GpuCase(c)
+    kvq, torch = g.kvq, g.torch
+    pool = g.new_pool()
+    build_full_cache(g, pool)
+    s_w, r_w = 64, 256
+    mu = oracle.cache.key_mean(c.calibration_keys()).astype(np.float32)
+    mu_dev = gu.dev(mu)
+    per = kvq.Window.buffer_bytes(1, c.n_kv_heads, s_w, r_w)
+    buf = torch.zeros(per * c.n_seqs, dtype=torch.uint8, device="cuda")
+    L = int(c.seq_lens[0])
+    spans = ((0, s_w), (L - r_w, L))
+    for b in range(c.n_seqs):
+        k, v = c.kv(b)
+        row = kvq.Window(s_w, r_w, buf[b * per:(b + 1) * per])
+        for lo, hi in spans:  # the sink, then the recent tokens (window tokens at length L)
+            kvq.kvq_window_append(g.layout, gu.dev(k[lo:hi], "bf16"), gu.dev(v[lo:hi], "bf16"),
+                                  gu.dev_i32([0, hi - lo]), gu.dev_i32([lo]), mu_dev, row)
+    torch.cuda.synchronize()
+    win = kvq.Window(s_w, r_w, buf)
+    ws = torch.empty(kvq.kvq_decode_workspace_size_win(g.layout, c.n_seqs, L, win), dtype=torch.uint8, device="cuda")
+    out = torch.full((c.n_seqs, c.n_q_heads, 128), float("nan"), device="cuda")
+    q = c.queries()
+    kvq.kvq_decode_attention_win(g.layout, gu.dev(q, "bf16"), gu.dev_i32(g.lengths), L, g.table, g.rot_k, g.rot_v,
+                                 pool, win, ws, out)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    got = out.cpu().numpy()
+    assert np.isfinite(got).all()
+    gpool = pool.cpu().numpy()
+    gbuf = buf.cpu().numpy()
+    for b in (0, 15):
+        pool_b, enc = oracle_seq(g, b)
+        lens = [0] * c.n_seqs
+        lens[b] = L
+        encs = [None] * c.n_seqs
+        encs[b] = enc
+        gu.compare_codes(gpool, pool_b, c.n_kv_heads, c.page_tokens, c.block_table, lens, encs, (c.clip_k, c.clip_v),
+                         label=f"table A seq {b}")
+        k, v = c.kv(b)
+        reg = np.zeros((c.n_kv_heads, oracle.window.region_bytes(s_w, r_w)), np.uint8)
+        for lo, hi in spans:
+            oracle.window.write_window(reg, k[lo:hi], v[lo:hi], lo, s_w, r_w, mu)
+        assert np.array_equal(gbuf[b * per:(b + 1) * per].reshape(reg.shape), reg), f"window records of seq {b}"
+        kh, vh = oracle.cache.dequantized_sequence(pool_b, c.n_kv_heads, c.page_tokens, c.block_table[b], L)
+        wp, wk, wv = oracle.window.read_window(reg, L, s_w, r_w)
+        ref = oracle.window.decode_attention_windowed(q[b], kh, vh, wp, wk, wv, g.r_k, g.r_v, c.gqa, L, s_w, r_w)
+        assert gu.out_err(got[b], ref) <= gu.OUT_TOL, (b, gu.out_err(got[b], ref))

@@ -47,3 +47,27 @@ def test_report_matches_the_oracle(seed, n_tok, n_qpos, hkv, gqa, d_model, rk, r
         assert np.array_equal(got[0], got[3])  # the candidate is the plain INT2: identical passes
     pct = 100 * np.sqrt(got[0] / got[3])
     assert np.allclose(pct, rep["rms_pct_of_naive"], rtol=1e-4)
+
+
+def test_report_at_the_serving_calibration_size():
+    """The size `bench.py --case report` runs: the 14B-class calibration trace (2,560
+    tokens, the last 64 positions, 10 KV heads x 4 query heads, d_model 5,120, bf16), two
+    dense candidates as R_K and R_V, centring, Table A's clips.  The GPU reports all ten
+    heads; the oracle recomputes heads 0 and 9 from their slices of the inputs."""
+    import oracle
+    cc = W.serve14b_calibration(n_cand=2)
+    mu = oracle.cache.key_mean(cc.k).astype(np.float32)
+    rot_k, rot_v = cc.cands[:2]
+    clips = (W.f32(0.96), W.f32(0.92))
+    got = run_report(cc, rot_k, rot_v, mu, *clips)
+    assert np.isfinite(got).all()
+    r_k = oracle.rotations.rot_matrices(rot_k, cc.n_kv_heads)
+    r_v = oracle.rotations.rot_matrices(rot_v, cc.n_kv_heads)
+    g, D = cc.gqa, 128
+    for h in (0, 9):
+        qh = cc.q[:, h * g:(h + 1) * g]
+        wh = cc.w_o[:, h * g * D:(h + 1) * g * D]
+        rep = oracle.report.head_error_report(qh, cc.k[:, h:h + 1], cc.v[:, h:h + 1], wh, r_k[h:h + 1],
+                                              r_v[h:h + 1], mu[h:h + 1], clips[0], clips[1], g)
+        for i, name in enumerate(("e", "e_key", "e_val", "e_naive", "y")):
+            gu.assert_nmse_close(got[i][h:h + 1], rep[name], f"head {h} {name}")
