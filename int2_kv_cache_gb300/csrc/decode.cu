@@ -334,7 +334,7 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
                                                            int q_dtype, RotDev rot, const int32_t* __restrict__ seq_lens,
                                                            DecWs ws, float* __restrict__ o_rot, PageGeom pg,
                                                            const int32_t* __restrict__ table, StepAppend app,
-                                                           unsigned* err) {
+                                                           unsigned* err, int n_seqs, int seqs_per_cta) {
   constexpr int NT = n_tiles(G);
   constexpr int NW = QP_THREADS / 32;
   pdl_launch_dependents();  // the decode kernel may start its batch scan and first copies
@@ -342,8 +342,7 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
   __shared__ __align__(16) float qr[G][D];
   __shared__ __align__(16) float red[DENSE ? NW : 1][G][D];
   __shared__ float qe[G];
-  const int h = blockIdx.x, b = blockIdx.y;
-  const int u = b * n_kv_heads + h;
+  const int h = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const float sc = LOG2E * INV_SQRT_D;
   // ---- a decode step's new token (APPEND): where it goes, its rows, R_V in flight ----
@@ -355,8 +354,7 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
   AppSmem* av = ak + 1;
   int new_len = 0;  // the deciding warps (NW - 1: key, NW - 2: value): seq_lens[b], loaded early
   float4 mu_k = make_float4(0.f, 0.f, 0.f, 0.f);  // warp NW - 1: its channels of mu R_K
-  if (APPEND) {
-    if (tid == 0 && dense_v) {
+  if (APPEND && tid == 0 && dense_v) {
       mbar_init(&rv_bar, 1);
       fence_mbar_init();
       mbar_arrive_expect_tx(&rv_bar, QPA_RV_BYTES);
@@ -365,12 +363,28 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
 #pragma unroll
       for (int c = 0; c < 4; ++c)
         bulk_g2s(qpa_dyn + c * (QPA_RV_BYTES / 4), src + c * (QPA_RV_BYTES / 4), QPA_RV_BYTES / 4, &rv_bar);
-    }
+  }
+  if (APPEND && warp == NW - 1 && app.mu_rot_k)
+    mu_k = __ldg(reinterpret_cast<const float4*>(app.mu_rot_k + (size_t)h * D) + lane);
+  // warp w: rows 16w .. 16w + 15 of R_K, lane: columns 4l .. 4l + 3, loaded once for the
+  // CTA's sequences (all row loads in flight at once)
+  float4 r[16];
+  if (DENSE) {
+    const float4* R = reinterpret_cast<const float4*>(rot.dense + (size_t)h * D * D) + lane;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) r[c] = __ldg(R + (size_t)(16 * warp + c) * (D / 4));
+  }
+  // ---- the CTA's sequences: blockIdx.y * seqs_per_cta + si ----
+  for (int si = 0; si < seqs_per_cta; ++si) {
+  const int b = blockIdx.y * seqs_per_cta + si;
+  if (b >= n_seqs) break;
+  const int u = b * n_kv_heads + h;
+  if (si > 0) __syncthreads();  // the previous sequence's readers of the shared buffers are done
+  if (APPEND) {
     const size_t e0 = ((size_t)b * n_kv_heads + h) * D;
     if (warp == NW - 1) {
       new_len = __ldg(seq_lens + b);
       reinterpret_cast<float4*>(ak->x)[lane] = load4(app.k, e0 + 4 * lane, app.dtype);
-      if (app.mu_rot_k) mu_k = __ldg(reinterpret_cast<const float4*>(app.mu_rot_k + (size_t)h * D) + lane);
     }
     if (warp == NW - 2) {
       new_len = __ldg(seq_lens + b);
@@ -396,11 +410,6 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
     for (int i = tid; i < G * D; i += QP_THREADS)
       qv[i / D][i % D] = load1(q, ((size_t)b * n_q_heads + h * G) * D + i, q_dtype);
     __syncthreads();
-    // warp w: rows 16w .. 16w + 15 of R; lane: columns 4l .. 4l + 3 (all row loads in flight at once)
-    const float4* R = reinterpret_cast<const float4*>(rot.dense + (size_t)h * D * D) + lane;
-    float4 r[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) r[c] = __ldg(R + (size_t)(16 * warp + c) * (D / 4));
 #pragma unroll
     for (int j = 0; j < G; ++j) {
       float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -527,6 +536,7 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
   if (tid == 0) ws.span[u] = make_int2(1, 0);
   if (__ldg(seq_lens + b) == 0)  // no cached tokens: the softmax is over nothing, o = 0
     for (int i = tid; i < G * D; i += QP_THREADS) o_rot[((size_t)b * n_q_heads + h * G) * D + i] = 0.f;
+  }
 }
 
 // Position of a warp in the batch's chunk list: unit (sequence b, KV head h)
@@ -1439,7 +1449,11 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   if (app && windows) return cudaErrorInvalidValue;  // the fused step append has no window copies
   DecWs ws;
   decode_ws_layout(ws_base, n_seqs, g.n_kv_heads, gqa, n_ctas, windows, &ws);
-  const dim3 qg(g.n_kv_heads, n_seqs);
+  // query preparation: several sequences of a KV head per CTA when the batch has more units
+  // than fit in one wave of it (two CTAs per SM), so R_K / R_V are loaded once per CTA
+  const int qp_cap = 2 * device_sm_count();
+  const int qp_spc = max(1, min(8, (n_seqs * g.n_kv_heads + qp_cap - 1) / qp_cap));
+  const dim3 qg(g.n_kv_heads, (n_seqs + qp_spc - 1) / qp_spc);
   const bool dense = rot_k.kind == KVQ_ROT_DENSE;
   const StepAppend sa = app ? *app : StepAppend{nullptr, nullptr, 0, RotDev{0, nullptr, nullptr}, nullptr, 1.f, 1.f, nullptr};
   const int qpa_smem = qpa_smem_bytes(app && app->rot_v.kind == KVQ_ROT_DENSE);
@@ -1449,10 +1463,10 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
     const cudaError_t ea = smem_limit_once(attr, qprep_kernel<GG, DD, true>, qpa_smem_bytes(true));           \
     if (ea != cudaSuccess) return ea;                                                                         \
     qprep_kernel<GG, DD, true><<<qg, QP_THREADS, qpa_smem, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k,   \
-                                                               seq_lens, ws, o_rot, g, table, sa, err);       \
+                                                               seq_lens, ws, o_rot, g, table, sa, err, n_seqs, qp_spc); \
   }                                                                                                           \
   else qprep_kernel<GG, DD, false><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k,       \
-                                                            seq_lens, ws, o_rot, g, table, sa, err)
+                                                            seq_lens, ws, o_rot, g, table, sa, err, n_seqs, qp_spc)
 #define KVQ_QPREP(GG) \
   if (dense) { KVQ_QPREP_A(GG, true); } else { KVQ_QPREP_A(GG, false); }
   switch (gqa) {
