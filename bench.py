@@ -11,7 +11,8 @@ One step = the whole hot path for one decode token of every sequence:
                         packs and writes the new token's K and V (position 32,767)
                         and rotates the query; split-K attention over 32,768 packed
                         tokens; log-sum-exp combine
-  2. kvq_out_proj    -- y = o' W_O-bar^T with R_V folded into W_O
+  2. kvq_out_proj_packed -- y = o' W_O-bar^T with R_V folded into W_O (W_O-bar stored in
+                        the projection's box order by kvq_pack_wo)
 (with --window, the append and window copies are separate calls before the
 windowed decode)
 value = sequences x steps / time (decode tokens per second, one layer).
@@ -263,6 +264,9 @@ class DecodeStep:
         # folded W_O (Eqs. 29-31), bf16
         self.w_fold = torch.empty(self.dm, self.hq * 128, dtype=bf, device=device)
         kvq.kvq_fold_wo(t(c.w_o(), bf), self.hq, self.hkv, self.rot_v, self.w_fold)
+        # the projection's box order (one contiguous 16 KB DRAM stream per tensor-core box)
+        self.w_pack = torch.empty(kvq.kvq_wo_packed_bytes(self.dm, self.hq * 128), dtype=torch.uint8, device=device)
+        kvq.kvq_pack_wo(self.w_fold, self.w_pack)
         # step inputs
         kn, vn = zip(*[c.new_kv(b, 1) for b in range(n_seqs)])
         self.host_q = torch.from_numpy(c.queries()).to(bf).pin_memory()
@@ -319,7 +323,7 @@ class DecodeStep:
                                          self.pool, self.win, self.ws, self.o, n_splits=self.splits)
         if ev is not None:
             ev[2].record()
-        kvq.kvq_out_proj(self.o.reshape(self.B, -1), self.w_fold, self.y)
+        kvq.kvq_out_proj_packed(self.o.reshape(self.B, -1), self.w_pack, self.y, self.dm)
         if ev is not None:
             ev[3].record()
 

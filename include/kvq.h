@@ -310,7 +310,28 @@ kvq_status kvq_fold_wo(int d_model, int n_q_heads, int n_kv_heads, const void* w
 kvq_status kvq_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
                         kvq_dtype w_dtype, float* y, kvq_stream stream);
 
-/* Workspace bytes for kvq_calib_nmse. */
+/* The folded W_O in the box order of the projection (the same product as kvq_out_proj with
+ * a bf16 W, for decode-size batches where the weight stream is the cost): W (bf16
+ * [d_model][k_dim], e.g. kvq_fold_wo's output) is stored as one contiguous 16 KB block per
+ * (128-row tile T, 64-column stage c), at (T * ceil(k_dim / 64) + c) * 16 KB; inside a block,
+ * row r (0..127) occupies 128 bytes at r * 128, holding columns 64 c .. 64 c + 63 as eight
+ * 16-byte chunks, chunk j stored at position j ^ (r % 8) (rows past d_model and columns past
+ * k_dim are zero).  Each block is then one bulk copy straight into the tensor cores' operand
+ * layout, one DRAM stream per block instead of 128 rows of 128 bytes.
+ * k_dim must be a multiple of 32 (KVQ_EUNSUPPORTED otherwise). */
+kvq_status kvq_wo_packed_bytes(int d_model, int k_dim, size_t* bytes);
+kvq_status kvq_pack_wo(int d_model, int k_dim, const void* w, void* w_packed, kvq_stream stream);
+
+/* kvq_out_proj with w = the packed W of kvq_pack_wo (bf16): y = x W^T, the same tensor-core
+ * arithmetic and summation order as kvq_out_proj with the row-major bf16 W (equal results).
+ * The packed W is a static weight: the projection starts streaming it while the preceding
+ * kernel on the stream (e.g. the decode's combine) still runs, so w_packed must have been
+ * written before that kernel began (kvq_pack_wo once at set-up; not by the kernel launched
+ * immediately before this call).  x may come from the preceding kernel. */
+kvq_status kvq_out_proj_packed(int n_rows, int d_model, int k_dim, const float* x, const void* w_packed, float* y,
+                               kvq_stream stream);
+
+/* Workspace bytes for kvq_calib_nmse. *//* Workspace bytes for kvq_calib_nmse. */
 kvq_status kvq_calib_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint,
                                     size_t* bytes);
 

@@ -101,6 +101,9 @@ def lib() -> ctypes.CDLL:
             "kvq_decode_attention_win": ([lp, i, vp, i, vp, i, vp, KvqRot, KvqRot, vp, wp, i, vp, sz, vp, vp], st),
             "kvq_fold_wo": ([i, i, i, vp, i, KvqRot, vp, i, vp], st),
             "kvq_out_proj": ([i, i, i, vp, vp, i, vp, vp], st),
+            "kvq_wo_packed_bytes": ([i, i, ctypes.POINTER(sz)], st),
+            "kvq_pack_wo": ([i, i, vp, vp, vp], st),
+            "kvq_out_proj_packed": ([i, i, i, vp, vp, vp, vp], st),
             "kvq_calib_workspace_size": ([i, i, i, i, i, ctypes.POINTER(sz)], st),
             "kvq_report_workspace_size": ([i, i, i, i, ctypes.POINTER(sz)], st),
             "kvq_head_error_report": ([i, i, i, i, i, vp, vp, vp, i, vp, i, KvqRot, KvqRot, vp, f, f, vp, vp, sz,
@@ -124,7 +127,7 @@ EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mea
             "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention",
             "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_window_append", "kvq_decode_workspace_size_win",
             "kvq_decode_attention_win", "kvq_fold_wo",
-            "kvq_out_proj", "kvq_calib_workspace_size", "kvq_calib_nmse", "kvq_report_workspace_size",
+            "kvq_out_proj", "kvq_wo_packed_bytes", "kvq_pack_wo", "kvq_out_proj_packed", "kvq_calib_workspace_size", "kvq_calib_nmse", "kvq_report_workspace_size",
             "kvq_head_error_report", "kvq_optr_workspace_size", "kvq_optr_loss_grad", "kvq_optr_calibrate_head")
 
 
@@ -394,3 +397,22 @@ def kvq_optr_calibrate_head(train, heldout, w_o, mu, r_k0, r_v0, clip_k: float, 
                                          clip_k, clip_v, lambda_k, steps, lr, every, _ptr(r_k), _ptr(r_v),
                                          _ptr(loss_k), _ptr(loss_v), _ptr(workspace),
                                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+# ---- the folded W_O in the projection's box order ----
+def kvq_wo_packed_bytes(d_model: int, k_dim: int) -> int:
+    out = ctypes.c_size_t(0)
+    _check(lib().kvq_wo_packed_bytes(d_model, k_dim, ctypes.byref(out)))
+    return int(out.value)
+
+
+def kvq_pack_wo(w, w_packed, stream=None) -> None:
+    """w: bf16 [d_model][k_dim] (e.g. kvq_fold_wo's output); w_packed: kvq_wo_packed_bytes bytes."""
+    d_model, k_dim = w.shape
+    _check(lib().kvq_pack_wo(d_model, k_dim, _ptr(_contig(w, "w")), _ptr(w_packed), _stream(stream)))
+
+
+def kvq_out_proj_packed(x, w_packed, y, d_model: int, stream=None) -> None:
+    n_rows, k_dim = x.shape
+    _check(lib().kvq_out_proj_packed(n_rows, d_model, k_dim, _ptr(_contig(x, "x")), _ptr(w_packed), _ptr(y),
+                                     _stream(stream)))

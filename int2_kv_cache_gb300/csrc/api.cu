@@ -487,6 +487,38 @@ kvq_status kvq_out_proj(int n_rows, int d_model, int k_dim, const float* x, cons
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_out_proj");
 }
 
+kvq_status kvq_wo_packed_bytes(int d_model, int k_dim, size_t* bytes) {
+  if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");
+  if (d_model < 1 || k_dim < 1) return fail(KVQ_EINVAL, "bad shape d_model %d k_dim %d", d_model, k_dim);
+  if (k_dim % 32 != 0) return fail(KVQ_EUNSUPPORTED, "k_dim %d is not a multiple of 32", k_dim);
+  *bytes = kvq::wo_packed_bytes(d_model, k_dim);
+  return KVQ_OK;
+}
+
+kvq_status kvq_pack_wo(int d_model, int k_dim, const void* w, void* w_packed, kvq_stream stream) {
+  size_t bytes = 0;
+  KVQ_CHECK(kvq_wo_packed_bytes(d_model, k_dim, &bytes));
+  KVQ_PTR(w, "w");
+  KVQ_PTR(w_packed, "w_packed");
+  cudaError_t e = kvq::launch_pack_wo(d_model, k_dim, w, w_packed, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_pack_wo");
+}
+
+kvq_status kvq_out_proj_packed(int n_rows, int d_model, int k_dim, const float* x, const void* w_packed, float* y,
+                               kvq_stream stream) {
+  if (n_rows < 0 || d_model < 1 || k_dim < 1)
+    return fail(KVQ_EINVAL, "bad shape n_rows %d d_model %d k_dim %d", n_rows, d_model, k_dim);
+  if (k_dim % 32 != 0) return fail(KVQ_EUNSUPPORTED, "k_dim %d is not a multiple of 32", k_dim);
+  if (n_rows == 0) return KVQ_OK;
+  KVQ_PTR(x, "x");
+  KVQ_PTR(w_packed, "w_packed");
+  KVQ_PTR(y, "y");
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
+  cudaError_t e = kvq::launch_out_proj_packed(n_rows, d_model, k_dim, x, w_packed, y, err, stream);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_out_proj_packed");
+}
+
 kvq_status kvq_calib_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint,
                                     size_t* bytes) {
   if (!bytes) return fail(KVQ_EINVAL, "bytes is NULL");

@@ -1268,8 +1268,8 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
                                                                            float* __restrict__ o_rot) {
   __shared__ float sm_m[CB_MAX_WARPS], sm_l[CB_MAX_WARPS];
   __shared__ __align__(16) float sm_a[CB_MAX_WARPS][D];
+  pdl_launch_dependents();  // a following projection may start streaming its (static) weights
   pdl_wait();               // the partials come from decode_split_kernel
-  pdl_launch_dependents();  // a following projection may start streaming its weights
   const int u = blockIdx.x, j = blockIdx.y;
   const int nw = blockDim.x >> 5;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1341,8 +1341,8 @@ __global__ void __launch_bounds__(CBW_WARPS * 32) decode_combine_win_kernel(int 
   __shared__ __align__(16) float sW[D];
   __shared__ __align__(16) float sY[D];
   __shared__ float sL, sM;
+  pdl_launch_dependents();  // a following projection may start streaming its (static) weights
   pdl_wait();               // the partials come from decode_split_kernel
-  pdl_launch_dependents();  // a following projection may start streaming its weights
   const int u = blockIdx.x, j = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = u / n_kv_heads, h = u % n_kv_heads;

@@ -156,6 +156,10 @@ cudaError_t launch_fold_wo(int d_model, int n_q_heads, int gqa, const void* w, i
                            RotDev rot_v, void* out, int out_dtype, cudaStream_t s);
 cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
                             int w_dtype, float* y, unsigned* err, cudaStream_t s);
+size_t wo_packed_bytes(int d_model, int k_dim);
+cudaError_t launch_pack_wo(int d_model, int k_dim, const void* w, void* out, cudaStream_t s);
+cudaError_t launch_out_proj_packed(int n_rows, int d_model, int k_dim, const float* x, const void* w_packed, float* y,
+                                   unsigned* err, cudaStream_t s);
 
 // optr.cu: OptR calibration of one KV head (fp64)
 struct OptrTraceIn {  // one trace of the head: q [n_qpos][gqa][128], k, v [n_tok][128] (fp32)

@@ -4,6 +4,8 @@
 // Inference Implementation", Eqs. 29-31: W_O-bar_j = W_O,j R_V,h(j), and
 // (o_j R_V) W_O-bar_j^T = o_j W_O,j^T; Eq. 3: the layer output sums the heads,
 // y = sum_j o_j W_O,j^T = o W_O^T with o the heads concatenated.
+#include <cstring>
+
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -256,8 +258,13 @@ __device__ __forceinline__ void st_cluster_v4(uint32_t addr, float a, float b, f
                : "memory");
 }
 
-template <int NRP>
+// PACKED: W comes pre-tiled (kvq_pack_wo): the box of row tile T and K stage c is the
+// contiguous 16 KB at (T n_kb + c) * 16 KB, already in the shared-memory order a 128-byte
+// swizzled tensor copy would produce, so one bulk copy moves it (one DRAM stream per box
+// instead of 128 rows of 128 bytes).
+template <int NRP, bool PACKED>
 __global__ void __launch_bounds__(OPT_THREADS, opt_ctas_per_sm(NRP)) out_proj_tc_kernel(const __grid_constant__ CUtensorMap tw,
+                                                                     const uint8_t* __restrict__ wpack,
                                                                      const float* __restrict__ x, int n_rows,
                                                                      int d_model, int k_dim, float* __restrict__ y,
                                                                      unsigned* err) {
@@ -321,15 +328,21 @@ __global__ void __launch_bounds__(OPT_THREADS, opt_ctas_per_sm(NRP)) out_proj_tc
 
   if (warp == 0) {
     // ---- W producer ----
-    // W too may come from the preceding kernel (a fold right before the projection)
-    pdl_wait();
+    // A row-major W may come from the preceding kernel (a fold right before the
+    // projection): wait for it.  A packed W is static (written before the preceding
+    // kernel began): stream it while that kernel still runs.
+    if (!PACKED) pdl_wait();
     int issued = 0;
     for (int kb = 0; kb < n_k; ++kb) {
       const int st = kb % SW;
       if (kb >= SW && !warp_wait(&wfree[st], ((kb / SW) - 1) & 1)) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(&wfull[st], OPT_WBYTES);
-        tma_load_2d(wring + st * OPT_WBYTES, &tw, (kb0 + kb) * OPT_BK, n0, &wfull[st]);
+        if (PACKED)
+          bulk_g2s(wring + st * OPT_WBYTES, wpack + ((size_t)blockIdx.x * n_kb + kb0 + kb) * OPT_WBYTES, OPT_WBYTES,
+                   &wfull[st]);
+        else
+          tma_load_2d(wring + st * OPT_WBYTES, &tw, (kb0 + kb) * OPT_BK, n0, &wfull[st]);
       }
       __syncwarp();
       issued = kb + 1;
@@ -527,15 +540,17 @@ static bool encode_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, 
          CUDA_SUCCESS;
 }
 
-template <int NRP>
+template <int NRP, bool PACKED>
 cudaError_t launch_out_proj_tc(int nr, int d_model, int k_dim, const float* x, const void* w, float* y, unsigned* err,
                                cudaStream_t s) {
   constexpr int smem = opt_smem_bytes(NRP);
   static std::atomic<unsigned long long> attr_set{0};  // one set of per-device flags per kernel instance
-  const cudaError_t ea = smem_limit_once(attr_set, out_proj_tc_kernel<NRP>, smem);
+  const cudaError_t ea = smem_limit_once(attr_set, out_proj_tc_kernel<NRP, PACKED>, smem);
   if (ea != cudaSuccess) return ea;
   CUtensorMap tw;
-  if (!encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, OPT_BK, OPT_BM)) return cudaErrorNotSupported;
+  memset(&tw, 0, sizeof(tw));
+  if (!PACKED && !encode_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w, d_model, k_dim, OPT_BK, OPT_BM))
+    return cudaErrorNotSupported;
   // K split (the cluster size): about opt_ctas_per_sm CTAs per SM, at most 8, at most one per K stage
   const int n_mt = (d_model + OPT_BM - 1) / OPT_BM;
   const int n_kb = (k_dim + OPT_BK - 1) / OPT_BK;
@@ -557,29 +572,72 @@ cudaError_t launch_out_proj_tc(int nr, int d_model, int k_dim, const float* x, c
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, out_proj_tc_kernel<NRP>, tw, x, nr, d_model, k_dim, y, err);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, out_proj_tc_kernel<NRP, PACKED>, tw,
+                                           PACKED ? static_cast<const uint8_t*>(w) : nullptr, x, nr, d_model, k_dim,
+                                           y, err);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+template <bool PACKED>
+static cudaError_t out_proj_tc_passes(int n_rows, int d_model, int k_dim, const float* x, const void* w, float* y,
+                                      unsigned* err, cudaStream_t s) {
+  // tensor-core passes of up to 64 activation rows
+  for (int r0 = 0; r0 < n_rows; r0 += 64) {
+    const int nr = n_rows - r0 < 64 ? n_rows - r0 : 64;
+    const float* xr = x + (size_t)r0 * k_dim;
+    float* yr = y + (size_t)r0 * d_model;
+    cudaError_t e;
+    if (nr <= 8) e = launch_out_proj_tc<8, PACKED>(nr, d_model, k_dim, xr, w, yr, err, s);
+    else if (nr <= 16) e = launch_out_proj_tc<16, PACKED>(nr, d_model, k_dim, xr, w, yr, err, s);
+    else if (nr <= 32) e = launch_out_proj_tc<32, PACKED>(nr, d_model, k_dim, xr, w, yr, err, s);
+    else e = launch_out_proj_tc<64, PACKED>(nr, d_model, k_dim, xr, w, yr, err, s);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+// W (bf16 [d_model][k_dim], row-major) -> the packed box order of out_proj_tc_kernel<., true>:
+// thread i writes 16-byte chunk i of the packed buffer: box (row tile T, K stage c), row r,
+// swizzled chunk position jj <- source chunk j = jj ^ (r % 8) (8 bf16 of row T 128 + r,
+// columns 64 c + 8 j ..); zero past d_model or k_dim.
+__global__ void pack_wo_kernel(int d_model, int k_dim, int n_kb, const __nv_bfloat16* __restrict__ w,
+                               uint4* __restrict__ out, long long n_chunks) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_chunks) return;
+  const int jj = (int)(i & 7), r = (int)((i >> 3) & 127);
+  const long long box = i >> 10;
+  const int c = (int)(box % n_kb), T = (int)(box / n_kb);
+  const int j = jj ^ (r & 7);
+  const int row = T * OPT_BM + r, col = c * OPT_BK + 8 * j;
+  uint4 v = make_uint4(0u, 0u, 0u, 0u);
+  if (row < d_model && col < k_dim) v = __ldg(reinterpret_cast<const uint4*>(w + (size_t)row * k_dim + col));
+  out[i] = v;
+}
+
+size_t wo_packed_bytes(int d_model, int k_dim) {
+  return (size_t)((d_model + OPT_BM - 1) / OPT_BM) * ((k_dim + OPT_BK - 1) / OPT_BK) * OPT_WBYTES;
+}
+
+cudaError_t launch_pack_wo(int d_model, int k_dim, const void* w, void* out, cudaStream_t s) {
+  const int n_kb = (k_dim + OPT_BK - 1) / OPT_BK;
+  const long long n_chunks = (long long)wo_packed_bytes(d_model, k_dim) / 16;
+  if (n_chunks == 0) return cudaSuccess;
+  pack_wo_kernel<<<(unsigned)((n_chunks + 255) / 256), 256, 0, s>>>(
+      d_model, k_dim, n_kb, static_cast<const __nv_bfloat16*>(w), static_cast<uint4*>(out), n_chunks);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_out_proj_packed(int n_rows, int d_model, int k_dim, const float* x, const void* w_packed, float* y,
+                                   unsigned* err, cudaStream_t s) {
+  if (n_rows == 0 || d_model == 0) return cudaSuccess;
+  return out_proj_tc_passes<true>(n_rows, d_model, k_dim, x, w_packed, y, err, s);
 }
 
 cudaError_t launch_out_proj(int n_rows, int d_model, int k_dim, const float* x, const void* w,
                             int w_dtype, float* y, unsigned* err, cudaStream_t s) {
   if (n_rows == 0 || d_model == 0) return cudaSuccess;
-  if (w_dtype == KVQ_BF16) {
-    // tensor-core passes of up to 64 activation rows
-    for (int r0 = 0; r0 < n_rows; r0 += 64) {
-      const int nr = n_rows - r0 < 64 ? n_rows - r0 : 64;
-      const float* xr = x + (size_t)r0 * k_dim;
-      float* yr = y + (size_t)r0 * d_model;
-      cudaError_t e;
-      if (nr <= 8) e = launch_out_proj_tc<8>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else if (nr <= 16) e = launch_out_proj_tc<16>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else if (nr <= 32) e = launch_out_proj_tc<32>(nr, d_model, k_dim, xr, w, yr, err, s);
-      else e = launch_out_proj_tc<64>(nr, d_model, k_dim, xr, w, yr, err, s);
-      if (e != cudaSuccess) return e;
-    }
-    return cudaSuccess;
-  }
+  if (w_dtype == KVQ_BF16) return out_proj_tc_passes<false>(n_rows, d_model, k_dim, x, w, y, err, s);
   const dim3 grid((d_model + 31) / 32);
   for (int r0 = 0; r0 < n_rows; r0 += 32) {
     const int nr = n_rows - r0 < 32 ? n_rows - r0 : 32;

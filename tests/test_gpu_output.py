@@ -78,3 +78,44 @@ def test_out_proj_ragged_k_and_passes(rows, dm, k):
     kvq.kvq_out_proj(gu.dev(x), gu.dev(w, "bf16"), y)
     ref = x.astype(np.float64) @ w.astype(np.float64).T
     assert gu.out_err(y.cpu().numpy(), ref) <= gu.OUT_TOL
+
+
+def _unpack(packed, d_model, k_dim):
+    """Read the packed W back (the documented box order) as a [d_model][k_dim] bf16-bit array."""
+    n_kb = (k_dim + 63) // 64
+    n_mt = (d_model + 127) // 128
+    b = packed.reshape(n_mt, n_kb, 128, 8, 8)  # [tile][stage][row][chunk position][8 bf16 bits]
+    out = np.zeros((n_mt * 128, n_kb * 64), np.uint16)
+    r = np.arange(128)
+    for jj in range(8):
+        j = jj ^ (r & 7)  # the source chunk stored at position jj of row r
+        for T in range(n_mt):
+            for c in range(n_kb):
+                for rr in range(128):
+                    out[T * 128 + rr, c * 64 + 8 * j[rr]:c * 64 + 8 * j[rr] + 8] = b[T, c, rr, jj]
+    return out[:d_model, :k_dim]
+
+
+@pytest.mark.parametrize("n_rows,d_model,k_dim", [(16, 4096, 4096), (64, 5120, 5120), (3, 300, 4096), (9, 256, 160),
+                                                  (1, 128, 32)])
+def test_packed_projection_equals_row_major(n_rows, d_model, k_dim):
+    """kvq_pack_wo's box order read back equals W bit for bit, and kvq_out_proj_packed returns
+    exactly what kvq_out_proj returns with the row-major bf16 W (same products, same order)."""
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    gen = np.random.default_rng(d_model + k_dim)
+    w = torch.from_numpy(gen.standard_normal((d_model, k_dim)).astype(np.float32) / np.sqrt(k_dim)).cuda()
+    w = w.to(torch.bfloat16)
+    x = torch.from_numpy(gen.standard_normal((n_rows, k_dim)).astype(np.float32)).cuda()
+    packed = torch.full((kvq.kvq_wo_packed_bytes(d_model, k_dim),), 0x5A, dtype=torch.uint8, device="cuda")
+    kvq.kvq_pack_wo(w, packed)
+    y_rm = torch.empty(n_rows, d_model, device="cuda")
+    y_pk = torch.full_like(y_rm, float("nan"))
+    kvq.kvq_out_proj(x, w, y_rm)
+    kvq.kvq_out_proj_packed(x, packed, y_pk, d_model)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    if d_model * k_dim <= 300 * 4096:
+        got = _unpack(packed.cpu().numpy().view(np.uint16), d_model, k_dim)
+        assert np.array_equal(got, w.view(torch.int16).cpu().numpy().view(np.uint16))
+    assert torch.equal(y_pk, y_rm)
