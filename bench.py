@@ -281,7 +281,7 @@ class DecodeStep:
         self.splits = splits
         ws = kvq.kvq_decode_workspace_size_win(self.layout, n_seqs, ctx, self.win, splits)
         self.ws = torch.empty(ws, dtype=torch.uint8, device=device)
-        # thread blocks of the decode kernel (the library's choice when splits == 0)
+        # work partitions of 4 warps of the decode kernel (the library's choice when splits == 0)
         self.n_ctas = splits or next(s for s in range(1, 8193)
                                      if kvq.kvq_decode_workspace_size_win(self.layout, n_seqs, ctx, self.win, s) == ws)
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
@@ -487,7 +487,7 @@ def run_gpu(args):
         "config": {
             "workload": workload_text(w.case),
             "batch": w.B, "ctx": w.L, "n_q_heads": w.hq, "n_kv_heads": w.hkv, "d_model": w.dm,
-            "decode_ctas": w.n_ctas, "parallelism": f"replicas x{world}",
+            "decode_warps": 4 * w.n_ctas, "parallelism": f"replicas x{world}",
             "bf16_windows": (f"sink {window[0]} + recent {window[1]} tokens per sequence in BF16"
                              if window else "none (every token INT2)"),
             "l2": "inputs larger than L2 (KV pool %.0f MB > 129 MB); no flush" % (w.pool.numel() / 1e6),

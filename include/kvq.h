@@ -183,9 +183,11 @@ kvq_status kvq_decode_workspace_size(const kvq_layout* layout, int n_seqs, int m
  *   p      = softmax(a)
  *   o_rot[b][j] = sum_s p_s (zero_s + scale_s * codeV_s)      (rotated-V basis)
  * The cached tokens of the batch, taken as one list of (sequence, KV head,
- * 32-token chunk) entries, are cut into 4 * n_splits equal contiguous slices
- * (n_splits thread blocks of 4 warps; 0 = the library's choice, one full wave
- * of the GPU).  Each slice yields a partial softmax per (sequence, KV head) it
+ * 32-token chunk) entries, are cut into 4 * n_splits equal contiguous slices,
+ * one per warp (n_splits work partitions of 4 warps; 0 = the library's choice,
+ * one full wave of the GPU, which runs as one thread block per SM; other
+ * counts run as n_splits blocks of 4 warps).  Each slice yields a partial
+ * softmax per (sequence, KV head) it
  * touches, and the partials of a unit are merged by a log-sum-exp combine in
  * slice order, so the result does not depend on timing.  A sequence of
  * length 0 yields a zero vector.  Out-of-range lengths or block ids are

@@ -52,7 +52,7 @@
 namespace kvq {
 
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int DEC_WARPS = 4;
+constexpr int DEC_WARPS = 4;   // warps (slices) per work partition
 constexpr int DEC_STAGES = 3;  // stages of 64 tokens per warp
 // Lazy softmax rescaling: the running sums keep their reference maximum until a
 // chunk's maximum exceeds it by more than TAU (log2 units), so weights stay <= 2^TAU.
@@ -63,7 +63,10 @@ constexpr float LO_SCALE = 2048.f;
 constexpr float LO_UNSCALE = 1.f / 2048.f;
 constexpr int PART = D + 4;  // floats per head in a partial: acc[128], m (log2 units), l, 2 pad (16-byte rows)
 
+// Work partitions of 4 warps resident per SM (register bound: 128 or 170 per thread).
 __host__ __device__ constexpr int ctas_per_sm(int gqa) { return gqa >= 8 ? 3 : 4; }
+// Largest thread block of the decode kernel: every partition of one SM in one block.
+__host__ __device__ constexpr int dec_max_warps(int gqa) { return DEC_WARPS * ctas_per_sm(gqa); }
 __host__ __device__ constexpr int n_tiles(int gqa) { return (gqa + 3) / 4; }
 
 // Workspace regions (each 256-byte aligned):
@@ -546,11 +549,16 @@ struct ChunkWalker {
 };
 
 // ---------------------------------------------------------------------------
-// The decode kernel.  grid = n_ctas, block = 128 (4 independent warps).
+// The decode kernel.  Each warp works through its own slice of the chunk list;
+// the warps are grouped into blocks of nw = blockDim.x / 32 (4 .. dec_max_warps)
+// and only the total number of warps decides the slices (and so the result).
+// A full wave runs as one block per SM: the warps of one block progress at the
+// same rate, while several blocks on one SM finish one after another in the
+// order they arrived, which leaves the SM partly idle at the end.
 // G = query heads per KV head; NT = n-tiles of 8 columns (2 columns per head).
 // ---------------------------------------------------------------------------
 template <int G, int P, bool WIN>
-__global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
+__global__ void __launch_bounds__(dec_max_warps(G) * 32, 1) decode_split_kernel(
     PageGeom g, int n_seqs, int n_q_heads, const int32_t* __restrict__ seq_lens,
     const int32_t* __restrict__ table, const uint8_t* __restrict__ pool, DecWs ws,
     float* __restrict__ o_rot, unsigned* err, WinGeom win, int step_append) {
@@ -574,13 +582,15 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   const int S_w = WIN ? win.sink : 0, R_w = WIN ? win.recent : 0;
   const int n_wrec = (S_w + R_w) / WIN_REC_TOKENS;  // records per (sequence, KV head)
 
-  extern __shared__ __align__(128) uint8_t dyn_smem[];  // [DEC_WARPS][DEC_STAGES][STAGE]
+  constexpr int MAXW = dec_max_warps(G);
+  const int nw = blockDim.x >> 5;  // warps of this block
+  extern __shared__ __align__(128) uint8_t dyn_smem[];  // [nw][DEC_STAGES][STAGE]
   auto stage_ptr = [&](int w, int sidx) { return dyn_smem + (w * DEC_STAGES + sidx) * STAGE; };
-  __shared__ __align__(8) uint64_t bars[DEC_WARPS][DEC_STAGES];
-  __shared__ uint8_t sflag[DEC_WARPS][DEC_STAGES];  // bit p: page p of the staged entry was copied
-  __shared__ int s_sum[DEC_WARPS], s_sumw[DEC_WARPS];
-  __shared__ int s_start[DEC_WARPS][3];   // first sequence of each warp's slice, entries before it, its length
-  __shared__ int s_startw[DEC_WARPS][3];  // the same for the window-record list
+  __shared__ __align__(8) uint64_t bars[MAXW][DEC_STAGES];
+  __shared__ uint8_t sflag[MAXW][DEC_STAGES];  // bit p: page p of the staged entry was copied
+  __shared__ int s_sum[MAXW], s_sumw[MAXW];
+  __shared__ int s_start[MAXW][3];   // first sequence of each warp's slice, entries before it, its length
+  __shared__ int s_startw[MAXW][3];  // the same for the window-record list
 
   // list entries (64-token stages) of a sequence of `len` tokens: INT2 positions [S_w, len - R_w)
   auto n_chunks_of = [&](int len) {
@@ -600,10 +610,10 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   //      the nb_b entries from H_kv * prefix_b + h * nb_b on ----
   // the lengths are kept in the (still unused) stage memory for the second pass
   int* s_len = reinterpret_cast<int*>(dyn_smem);
-  const bool cached = n_seqs <= DEC_WARPS * DEC_STAGES * STAGE / (int)sizeof(int);
+  const bool cached = n_seqs <= nw * DEC_STAGES * STAGE / (int)sizeof(int);
   auto len_of = [&](int b) { return cached ? s_len[b] : __ldg(seq_lens + b); };
   int tot = 0, totw = 0;
-  for (int b = threadIdx.x; b < n_seqs; b += 128) {
+  for (int b = threadIdx.x; b < n_seqs; b += blockDim.x) {
     const int len = __ldg(seq_lens + b);
     if ((len < 0 || len > max_len) && blockIdx.x == 0) flag_error(err, ERR_SEQ_RANGE);
     if (cached) s_len[b] = len;
@@ -620,14 +630,19 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
     s_sumw[warp] = totw;
   }
   __syncthreads();
-  const int T = Hkv * (s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3]);
-  const int n_warps = gridDim.x * DEC_WARPS;
+  int T = 0, Tws = 0;
+  for (int w = 0; w < nw; ++w) {
+    T += s_sum[w];
+    Tws += s_sumw[w];
+  }
+  T *= Hkv;
+  const int n_warps = gridDim.x * nw;
   const int Ww = (T + n_warps - 1) / n_warps;  // entries per warp slice
-  const int gw = blockIdx.x * DEC_WARPS + warp;
+  const int gw = blockIdx.x * nw + warp;
   const int ga = min(T, gw * Ww);
   const int my_n = min(T, ga + Ww) - ga;
   // the window records are split the same way, in a list of their own
-  const int Tw = WIN ? Hkv * (s_sumw[0] + s_sumw[1] + s_sumw[2] + s_sumw[3]) : 0;
+  const int Tw = WIN ? Hkv * Tws : 0;
   const int Wwn = (Tw + n_warps - 1) / n_warps;
   const int gaw = min(Tw, gw * Wwn);
   const int my_nw = min(Tw, gaw + Wwn) - gaw;
@@ -637,7 +652,7 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
   // the first entry of each warp slice of a list (W entries per slice, Ttot in all)
   auto find_starts = [&](auto count, int W, int Ttot, int (*st)[3]) {
     int base = 0;
-    for (int b0 = 0; b0 < n_seqs; b0 += 128) {
+    for (int b0 = 0; b0 < n_seqs; b0 += blockDim.x) {
       const int b = b0 + threadIdx.x;
       const int len = b < n_seqs ? len_of(b) : 0;
       const int n = count(len);
@@ -653,8 +668,8 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
       for (int w = 0; w < warp; ++w) before += s_sum[w];
       const int excl = before + inc - n;
       if (n > 0) {
-        for (int w = 0; w < DEC_WARPS; ++w) {
-          const int gs = (blockIdx.x * DEC_WARPS + w) * W;
+        for (int w = 0; w < nw; ++w) {
+          const int gs = (blockIdx.x * nw + w) * W;
           if (gs < Ttot && gs >= Hkv * excl && gs < Hkv * (excl + n)) {
             st[w][0] = b;
             st[w][1] = excl;
@@ -662,7 +677,7 @@ __global__ void __launch_bounds__(128, ctas_per_sm(G)) decode_split_kernel(
           }
         }
       }
-      base += s_sum[0] + s_sum[1] + s_sum[2] + s_sum[3];
+      for (int w = 0; w < nw; ++w) base += s_sum[w];
       __syncthreads();
     }
   };
@@ -1429,13 +1444,13 @@ __global__ void __launch_bounds__(CBW_WARPS * 32) decode_combine_win_kernel(int 
   }
 }
 
-// Shared-memory ring of the decode kernel: 4 warps x DEC_STAGES stages of 64 tokens.
-constexpr int DEC_SMEM = DEC_WARPS * DEC_STAGES * 2 * 1152 * 2;
+// Shared-memory ring of the decode kernel: per warp DEC_STAGES stages of 64 tokens.
+constexpr int DEC_WARP_SMEM = DEC_STAGES * 2 * 1152 * 2;
 
 template <int G, int P, bool WIN>
 cudaError_t decode_smem_attr() {
   static std::atomic<unsigned long long> done{0};  // one set of per-device flags per kernel instance
-  return smem_limit_once(done, decode_split_kernel<G, P, WIN>, DEC_SMEM);
+  return smem_limit_once(done, decode_split_kernel<G, P, WIN>, dec_max_warps(G) * DEC_WARP_SMEM);
 }
 
 cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const void* q, int q_dtype,
@@ -1481,11 +1496,19 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
-  // the decode kernel is a programmatic dependent of qprep_kernel
+  // The decode kernel is a programmatic dependent of qprep_kernel.  Its 4 * n_ctas
+  // warps run as one block per SM when they fill every SM with a full set of
+  // partitions.  With the step's append, the query preparation holds tens of KB of
+  // shared memory per block while it runs, so the warps of an SM come as two blocks:
+  // the first fits beside a query-preparation block and stages its first copies
+  // while the append still runs.
+  const int n_sm = device_sm_count();
+  const bool per_sm = n_ctas == n_sm * ctas_per_sm(gqa);
+  const int dnw = !per_sm ? DEC_WARPS : app ? dec_max_warps(gqa) / 2 : dec_max_warps(gqa);
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(n_ctas);
-  cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = DEC_SMEM;
+  cfg.gridDim = dim3(DEC_WARPS * n_ctas / dnw);
+  cfg.blockDim = dim3(32 * dnw);
+  cfg.dynamicSmemBytes = dnw * DEC_WARP_SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

@@ -3,8 +3,9 @@ quantized and written inside the decode call ("Output-Aware Rotation for INT2
 KV-Cache Quantization", §6 cache-write kernel and decode; Eqs. 4, 20-22, 26, 27).
 
 The fused step must write exactly the bytes kvq_quantize_append writes and return
-exactly what kvq_decode_attention returns over the extended sequences (same grid,
-so bit for bit), and both must match the fp64 oracle."""
+exactly what kvq_decode_attention returns over the extended sequences (the same
+warp slices, so bit for bit, also at a full wave where the two calls group the
+warps into thread blocks differently), and both must match the fp64 oracle."""
 import numpy as np
 import pytest
 
@@ -20,6 +21,8 @@ CASES = [
     (32, 8, 16, [777, 2048], "dense", "bf16", (1.0, 1.0)),
     (8, 1, 16, [64, 65, 5], "identity", "bf16", (0.9, 0.9)),
     (40, 10, 16, [1100, 3000, 1025], "dense", "bf16", (1.0, 1.0)),
+    # a full wave of the GPU (more than 16 chunks per warp of the default grid)
+    (32, 8, 16, [3072] * 15 + [2900], "dense", "bf16", (0.96, 0.92)),
 ]
 
 
