@@ -31,6 +31,7 @@
 #include <cmath>
 #include <cstdio>
 
+#include "async_copy.cuh"
 #include "kvq_internal.cuh"
 
 namespace kvq {
@@ -44,74 +45,103 @@ constexpr int MAX_SQUARINGS = 40;  // ||S||_1 up to 2^39: beyond that the call r
 // fp64 GEMM: C = alpha op(A) op(B) + beta C, row-major, op = transpose or not.
 // With `skip` non-null and *skip <= step, the kernel copies `copy_src` into C
 // instead (the data-dependent number of squarings of the exponential).
-// 64 x 64 tiles, k-steps of 16, 256 threads with 4 x 4 outputs each.
+//
+// The matrices here are small (128 x 128, or a few thousand rows by 128) and the
+// part's fp64 rate is about two FMAs per clock per SM, so the work is spread over
+// every SM: 16 x 16 output tiles, one output per thread, and when the tiles are
+// fewer than the SMs the K range is split over a cluster of up to 8 blocks.  Each
+// block stores its partial tile into the first block's shared memory (distributed
+// shared memory), which adds them in rank order: the result does not depend on timing.
 // ---------------------------------------------------------------------------
-constexpr int GB = 64, GK = 16;
+constexpr int GT = 16;            // output tile edge
+constexpr int GK = 32;            // k-step staged in shared memory
+constexpr int GEMM_MAX_SPLIT = 8;  // blocks of a cluster splitting K
 
-__global__ void __launch_bounds__(256) gemm64_kernel(int M, int N, int K, double alpha, const double* __restrict__ A,
-                                                     int lda, int ta, const double* __restrict__ B, int ldb, int tb,
-                                                     double beta, double* __restrict__ C, int ldc,
-                                                     const int* __restrict__ skip, int step,
-                                                     const double* __restrict__ copy_src) {
-  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
-  const int m0 = blockIdx.y * GB, n0 = blockIdx.x * GB;
-  if (skip && *skip <= step) {
-    for (int i = tid; i < GB * GB; i += 256) {
-      const int m = m0 + i / GB, n = n0 + i % GB;
-      if (m < M && n < N) C[(size_t)m * ldc + n] = copy_src[(size_t)m * ldc + n];
-    }
+__device__ __forceinline__ unsigned cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Store v at the address of `local` in the shared memory of cluster block `rank`.
+__device__ __forceinline__ void st_cluster_f64(const double* local, unsigned rank, double v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(remote), "d"(v) : "memory");
+}
+
+__global__ void __launch_bounds__(GT * GT) gemm_f64_kernel(int M, int N, int K, double alpha,
+                                                          const double* __restrict__ A, int lda, int ta,
+                                                          const double* __restrict__ B, int ldb, int tb, double beta,
+                                                          double* __restrict__ C, int ldc, int split,
+                                                          const int* __restrict__ skip, int step,
+                                                          const double* __restrict__ copy_src) {
+  __shared__ double As[GK][GT + 1];  // As[k][m]
+  __shared__ double Bs[GK][GT + 1];  // Bs[k][n]
+  __shared__ double red[GEMM_MAX_SPLIT][GT * GT];
+  const int tid = threadIdx.x, tx = tid % GT, ty = tid / GT;
+  const int m0 = blockIdx.y * GT, n0 = blockIdx.x * GT;
+  const int m = m0 + ty, n = n0 + tx;
+  const unsigned rank = split > 1 ? cluster_rank() : 0u;
+  if (skip && *skip <= step) {  // the same decision in every block of the cluster
+    if (rank == 0 && m < M && n < N) C[(size_t)m * ldc + n] = copy_src[(size_t)m * ldc + n];
     return;
   }
-  __shared__ double As[GK][GB + 1];
-  __shared__ double Bs[GK][GB + 1];
-  double acc[4][4] = {};
-  for (int k0 = 0; k0 < K; k0 += GK) {
-    for (int i = tid; i < GB * GK; i += 256) {
-      const int mm = i / GK, kk = i % GK;  // A tile element (m0 + mm, k0 + kk)
-      const int m = m0 + mm, k = k0 + kk;
-      double a = 0.0;
-      if (m < M && k < K) a = ta ? A[(size_t)k * lda + m] : A[(size_t)m * lda + k];
-      As[kk][mm] = a;
-      const int kk2 = i / GB, nn = i % GB;  // B tile element (k0 + kk2, n0 + nn)
-      const int k2 = k0 + kk2, n = n0 + nn;
-      double bv = 0.0;
-      if (k2 < K && n < N) bv = tb ? B[(size_t)n * ldb + k2] : B[(size_t)k2 * ldb + n];
-      Bs[kk2][nn] = bv;
+  // this block's K range
+  const int kc = (K + split - 1) / split;
+  const int k_lo = min(K, (int)rank * kc), k_hi = min(K, k_lo + kc);
+  double acc = 0.0;
+  for (int k0 = k_lo; k0 < k_hi; k0 += GK) {
+    for (int i = tid; i < GT * GK; i += GT * GT) {
+      // element (mm, kk) of the A tile; consecutive threads take consecutive addresses
+      const int mm = ta ? i % GT : i / GK, kk = ta ? i / GT : i % GK;
+      const int am = m0 + mm, ak = k0 + kk;
+      As[kk][mm] = (am < M && ak < k_hi) ? (ta ? A[(size_t)ak * lda + am] : A[(size_t)am * lda + ak]) : 0.0;
+      const int nn = tb ? i / GK : i % GT, kb = tb ? i % GK : i / GT;
+      const int bn = n0 + nn, bk = k0 + kb;
+      Bs[kb][nn] = (bn < N && bk < k_hi) ? (tb ? B[(size_t)bn * ldb + bk] : B[(size_t)bk * ldb + bn]) : 0.0;
     }
     __syncthreads();
-#pragma unroll
-    for (int kk = 0; kk < GK; ++kk) {
-      double a[4], bb[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
-#pragma unroll
-      for (int j = 0; j < 4; ++j) bb[j] = Bs[kk][tx * 4 + j];
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) acc[i][j] = fma(a[i], bb[j], acc[i][j]);
-    }
+#pragma unroll 8
+    for (int kk = 0; kk < GK; ++kk) acc = fma(As[kk][ty], Bs[kk][tx], acc);
     __syncthreads();
   }
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int m = m0 + ty * 4 + i, n = n0 + tx * 4 + j;
-      if (m < M && n < N) {
-        double* c = C + (size_t)m * ldc + n;
-        *c = beta == 0.0 ? alpha * acc[i][j] : fma(alpha, acc[i][j], beta * *c);
-      }
-    }
+  if (split > 1) {
+    cluster_barrier();  // every block of the cluster has started: its shared memory exists
+    if (rank == 0) red[0][tid] = acc;
+    else st_cluster_f64(&red[rank][tid], 0u, acc);
+    cluster_barrier();  // release / acquire: every partial has landed in the first block
+    if (rank != 0) return;
+    acc = red[0][tid];
+    for (int r = 1; r < split; ++r) acc += red[r][tid];
+  }
+  if (m < M && n < N) {
+    double* c = C + (size_t)m * ldc + n;
+    *c = beta == 0.0 ? alpha * acc : fma(alpha, acc, beta * *c);
+  }
 }
 
 cudaError_t gemm64(cudaStream_t s, int M, int N, int K, double alpha, const double* A, int lda, bool ta,
                    const double* B, int ldb, bool tb, double beta, double* C, int ldc, const int* skip = nullptr,
                    int step = 0, const double* copy_src = nullptr) {
-  const dim3 grid((N + GB - 1) / GB, (M + GB - 1) / GB);
-  gemm64_kernel<<<grid, 256, 0, s>>>(M, N, K, alpha, A, lda, ta ? 1 : 0, B, ldb, tb ? 1 : 0, beta, C, ldc, skip, step,
-                                     copy_src);
-  return cudaGetLastError();
+  const int tiles = ((N + GT - 1) / GT) * ((M + GT - 1) / GT);
+  int split = 1;
+  while (tiles * split < device_sm_count() && split < GEMM_MAX_SPLIT && K >= 2 * split * GK) split *= 2;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((N + GT - 1) / GT, (M + GT - 1) / GT, split);
+  cfg.blockDim = dim3(GT * GT);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = split;
+  cfg.attrs = attr;
+  cfg.numAttrs = split > 1 ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, gemm_f64_kernel, M, N, K, alpha, A, lda, ta ? 1 : 0, B, ldb, tb ? 1 : 0, beta, C,
+                            ldc, split, skip, step, copy_src);
 }
 
 // ---------------------------------------------------------------------------
