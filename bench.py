@@ -778,15 +778,17 @@ def run_optr(args):
     torch.cuda.synchronize()
     kvq.kvq_device_check()
     ms = e0.elapsed_time(e1)
-    # algorithmic fp64 flops of one loss + gradient evaluation (GEMMs, the exponential and its
-    # Frechet derivative at the squarings actually taken are counted from the generator norm)
+    # algorithmic fp64 flops of one loss + gradient evaluation: the exponential and its Frechet
+    # derivative (18 + 3 x 17 products of 128 x 128), the effective rows, the causal logits,
+    # C = (p^K - p) V, U = C_j M_j and G = U V^T over the pairs, and the backward products
     npairs = n_qpos * gqa
     tok_sum = sum(n_tok - n_qpos + i + 1 for i in range(n_qpos)) * gqa
     mm = 2.0 * 128 ** 3
-    pair = 10.0 * 128 * tok_sum + 4.0 * 128 * dm * npairs
+    pair = 4.0 * 128 * tok_sum + 2.0 * npairs * 128 * 128
     fwd = 18 * mm + 2 * (2.0 * n_tok * 128 * 128) + pair
-    bwd = 2.0 * n_tok * 128 * npairs + 3 * (2.0 * n_tok * 128 * 128) + mm + 3 * 17 * mm
-    flops = steps * 2 * (fwd + bwd)  # both phases (the value pair kernel is cheaper: an upper count)
+    bwd = 2.0 * 128 * tok_sum + 2.0 * n_tok * 128 * npairs + 3 * (2.0 * n_tok * 128 * 128) + mm + 3 * 17 * mm
+    once = gqa * 2.0 * 128 * 128 * dm + 2 * 2.0 * 128 * tok_sum  # the Gram matrices, both traces' raw logits
+    flops = steps * 2 * (fwd + bwd) + once  # both phases (the value phase is cheaper: an upper count)
     peak = 1250.0  # GFLOP/s, GB300 fp64 (nominal)
     print(json.dumps({"case": "optr", "workload": (f"OptR Algorithm 1, one KV head of the 14B-class serving layer: "
                                                    f"{n_tok} tokens, last {n_qpos} positions x {gqa} query heads, "

@@ -169,7 +169,6 @@ struct OptrTraceIn {  // one trace of the head: q [n_qpos][gqa][128], k, v [n_to
   int n_tok, n_qpos;
 };
 size_t optr_workspace_bytes(int n_tok, int n_qpos, int n_tok_h, int n_qpos_h, int gqa);
-size_t optr_max_smem(int n_tok, int d_model);
 cudaError_t launch_optr_loss_grad(int phase, const OptrTraceIn& tr, int gqa, int d_model, const float* w_o,
                                   const float* mu, const double* r0, const double* a, const double* r_k_sel,
                                   float clip_k, float clip_v, float lam, double* loss, double* grad, void* ws,

@@ -22,6 +22,9 @@
 //   L_exp(S, .)); dL/dA = dL/dS - (dL/dS)^T.
 // Values (Eqs. 15-16) likewise with e_V = [p^K^T (V~ - V)] W_O,j^T under the fixed weights of the
 // selected key rotation, L_V = mean ||e_V||^2 / d_model.
+// e enters only through ||W_j c||^2 = c . M_j c and W_j^T e = M_j c, so the d_model-wide
+// products are replaced by the 128 x 128 Gram matrix M_j = W_j^T W_j of each query head,
+// formed once per call; the other products are fp64 GEMMs over all pairs at once.
 //
 // The exponential and its Frechet derivative use scaling and squaring with a
 // Taylor series: exp(X) = (T(X / 2^s))^(2^s) with ||X / 2^s||_1 <= 1/2 and 18
@@ -72,9 +75,10 @@ __device__ __forceinline__ void st_cluster_f64(const double* local, unsigned ran
   asm volatile("st.shared::cluster.f64 [%0], %1;" ::"r"(remote), "d"(v) : "memory");
 }
 
+template <typename TA, typename TB>  // operand types (fp64, or fp32 widened on load)
 __global__ void __launch_bounds__(GT * GT) gemm_f64_kernel(int M, int N, int K, double alpha,
-                                                          const double* __restrict__ A, int lda, int ta,
-                                                          const double* __restrict__ B, int ldb, int tb, double beta,
+                                                          const TA* __restrict__ A, int lda, int ta,
+                                                          const TB* __restrict__ B, int ldb, int tb, double beta,
                                                           double* __restrict__ C, int ldc, int split,
                                                           const int* __restrict__ skip, int step,
                                                           const double* __restrict__ copy_src) {
@@ -98,10 +102,10 @@ __global__ void __launch_bounds__(GT * GT) gemm_f64_kernel(int M, int N, int K, 
       // element (mm, kk) of the A tile; consecutive threads take consecutive addresses
       const int mm = ta ? i % GT : i / GK, kk = ta ? i / GT : i % GK;
       const int am = m0 + mm, ak = k0 + kk;
-      As[kk][mm] = (am < M && ak < k_hi) ? (ta ? A[(size_t)ak * lda + am] : A[(size_t)am * lda + ak]) : 0.0;
+      As[kk][mm] = (am < M && ak < k_hi) ? (double)(ta ? A[(size_t)ak * lda + am] : A[(size_t)am * lda + ak]) : 0.0;
       const int nn = tb ? i / GK : i % GT, kb = tb ? i % GK : i / GT;
       const int bn = n0 + nn, bk = k0 + kb;
-      Bs[kb][nn] = (bn < N && bk < k_hi) ? (tb ? B[(size_t)bn * ldb + bk] : B[(size_t)bk * ldb + bn]) : 0.0;
+      Bs[kb][nn] = (bn < N && bk < k_hi) ? (double)(tb ? B[(size_t)bn * ldb + bk] : B[(size_t)bk * ldb + bn]) : 0.0;
     }
     __syncthreads();
 #pragma unroll 8
@@ -123,9 +127,10 @@ __global__ void __launch_bounds__(GT * GT) gemm_f64_kernel(int M, int N, int K, 
   }
 }
 
-cudaError_t gemm64(cudaStream_t s, int M, int N, int K, double alpha, const double* A, int lda, bool ta,
-                   const double* B, int ldb, bool tb, double beta, double* C, int ldc, const int* skip = nullptr,
-                   int step = 0, const double* copy_src = nullptr) {
+template <typename TA, typename TB>
+cudaError_t gemm64(cudaStream_t s, int M, int N, int K, double alpha, const TA* A, int lda, bool ta, const TB* B,
+                   int ldb, bool tb, double beta, double* C, int ldc, const int* skip = nullptr, int step = 0,
+                   const double* copy_src = nullptr) {
   const int tiles = ((N + GT - 1) / GT) * ((M + GT - 1) / GT);
   int split = 1;
   while (tiles * split < device_sm_count() && split < GEMM_MAX_SPLIT && K >= 2 * split * GK) split *= 2;
@@ -140,8 +145,8 @@ cudaError_t gemm64(cudaStream_t s, int M, int N, int K, double alpha, const doub
   attr[0].val.clusterDim.z = split;
   cfg.attrs = attr;
   cfg.numAttrs = split > 1 ? 1 : 0;
-  return cudaLaunchKernelEx(&cfg, gemm_f64_kernel, M, N, K, alpha, A, lda, ta ? 1 : 0, B, ldb, tb ? 1 : 0, beta, C,
-                            ldc, split, skip, step, copy_src);
+  return cudaLaunchKernelEx(&cfg, gemm_f64_kernel<TA, TB>, M, N, K, alpha, A, lda, ta ? 1 : 0, B, ldb, tb ? 1 : 0,
+                            beta, C, ldc, split, skip, step, copy_src);
 }
 
 // ---------------------------------------------------------------------------
@@ -297,14 +302,14 @@ __global__ void mask_mul_kernel(int n, const double* __restrict__ src, const dou
 }
 
 // ---------------------------------------------------------------------------
-// Per (query position t, query head j) of the head: one CTA of 256 threads.
-// MODE_KEY_GRAD: the key loss term and dL/da^K (written to da[pair][s], 0 past t);
-// MODE_KEY_LOSS: the loss term only; MODE_WEIGHTS: p^K only (written to da).
-// Query pair index pr = i * G + j <-> position t = n_tok - n_qpos + i.
-// Dynamic shared memory: a_k[n_tok], a_ref[n_tok], e[d_model] (doubles).
+// Row kernels over the (query position, query head) pairs of the head, one CTA of
+// 256 threads per pair: pair pr = i * G + j <-> position t = n_tok - n_qpos + i
+// (causal: a row's entries s > t are zero).  The products around them are fp64
+// GEMMs: logits Q K^T / sqrt(d), C = (P^K - P) V (keys) or P^K (V~ - V) (values),
+// U = C_j M_j with the Gram matrix M_j = W_j^T W_j of the head's W_O columns
+// (so e = W_j c never has to be formed: ||e||^2 = c . M_j c and W_j^T e = M_j c),
+// and G = U V^T.
 // ---------------------------------------------------------------------------
-enum { MODE_KEY_GRAD = 0, MODE_KEY_LOSS = 1, MODE_WEIGHTS = 2 };
-
 __device__ __forceinline__ double block_reduce(double v, double* red, bool is_max) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -320,176 +325,89 @@ __device__ __forceinline__ double block_reduce(double v, double* red, bool is_ma
   return r;
 }
 
-__global__ void __launch_bounds__(256) key_pair_kernel(int mode, int n_tok, int n_qpos, int gqa, int d_model,
-                                                       const double* __restrict__ q,      // [n_qpos * gqa][128]
-                                                       const double* __restrict__ k,      // raw keys [n_tok][128]
-                                                       const double* __restrict__ keff,   // effective keys
-                                                       const double* __restrict__ v,      // [n_tok][128]
-                                                       const float* __restrict__ w_o,     // [d_model][gqa * 128]
-                                                       double lam, double* __restrict__ da,
-                                                       double* __restrict__ loss_pair) {
-  extern __shared__ double dyn[];
-  double* a_k = dyn;
-  double* a_r = dyn + n_tok;
-  double* e = dyn + 2 * n_tok;
-  __shared__ double red[8];
-  __shared__ double s_q[D], s_c[2][D], s_u[D];
-  const int pr = blockIdx.x, j = pr % gqa, i = pr / gqa;
-  const int t = n_tok - n_qpos + i;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int np = n_qpos * gqa;
-  for (int c = tid; c < D; c += 256) s_q[c] = q[(size_t)pr * D + c];
-  __syncthreads();
-  // logits over s <= t: raw keys and effective keys (one warp per token, 4 channels per lane)
-  for (int s = warp; s <= t; s += 8) {
-    double ak = 0.0, ar = 0.0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const int c = 4 * lane + u;
-      ak = fma(keff[(size_t)s * D + c], s_q[c], ak);
-      if (mode != MODE_WEIGHTS) ar = fma(k[(size_t)s * D + c], s_q[c], ar);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      ak += __shfl_xor_sync(0xffffffffu, ak, o);
-      ar += __shfl_xor_sync(0xffffffffu, ar, o);
-    }
-    if (lane == 0) {
-      a_k[s] = ak * INV_SQRT_D64;
-      a_r[s] = ar * INV_SQRT_D64;
-    }
-  }
-  __syncthreads();
-  // log-sum-exp of both
-  double mk = -INFINITY, mr = -INFINITY;
-  for (int s = tid; s <= t; s += 256) {
-    mk = fmax(mk, a_k[s]);
-    mr = fmax(mr, a_r[s]);
-  }
-  mk = block_reduce(mk, red, true);
-  mr = block_reduce(mr, red, true);
-  double sk = 0.0, sr = 0.0;
-  for (int s = tid; s <= t; s += 256) {
-    sk += exp(a_k[s] - mk);
-    if (mode != MODE_WEIGHTS) sr += exp(a_r[s] - mr);
-  }
-  sk = block_reduce(sk, red, false);
-  sr = block_reduce(sr, red, false);
-  const double lk = mk + log(sk), lr = mr + log(sr);  // log of the normalisers
-  if (mode == MODE_WEIGHTS) {
-    for (int s = tid; s < n_tok; s += 256) da[(size_t)pr * n_tok + s] = s <= t ? exp(a_k[s] - lk) : 0.0;
-    return;
-  }
-  // p_s, p^K_s in place (a_r <- p, a_k <- p^K); KL(p || p^K) = sum p (log p - log p^K)
-  double kl = 0.0;
-  for (int s = tid; s <= t; s += 256) {
-    const double lp = a_r[s] - lr, lq = a_k[s] - lk;
-    const double p = exp(lp), pk = exp(lq);
-    kl += p * (lp - lq);
-    a_r[s] = p;
-    a_k[s] = pk;
-  }
-  kl = block_reduce(kl, red, false);
-  // c = sum_s (p^K_s - p_s) v_s  (threads: channel tid & 127, tokens of parity tid >> 7)
-  {
-    const int c = tid & 127, par = tid >> 7;
-    double acc = 0.0;
-    for (int s = par; s <= t; s += 2) acc = fma(a_k[s] - a_r[s], v[(size_t)s * D + c], acc);
-    s_c[par][c] = acc;
-  }
-  __syncthreads();
-  for (int c = tid; c < D; c += 256) s_c[0][c] += s_c[1][c];
-  __syncthreads();
-  // e = W_j c (one warp per output row, 4 channels per lane)
-  const size_t ldw = (size_t)gqa * D;
-  double ee = 0.0;
-  for (int m = warp; m < d_model; m += 8) {
-    const float4 w4 = *reinterpret_cast<const float4*>(w_o + (size_t)m * ldw + (size_t)j * D + 4 * lane);
-    double x = (double)w4.x * s_c[0][4 * lane] + (double)w4.y * s_c[0][4 * lane + 1] +
-               (double)w4.z * s_c[0][4 * lane + 2] + (double)w4.w * s_c[0][4 * lane + 3];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) e[m] = x;
-    ee = fma(x, x, ee);  // every lane holds the full sum; counted once below
-  }
-  ee = block_reduce(lane == 0 ? ee : 0.0, red, false);
-  const double n = (double)np;
-  if (tid == 0) loss_pair[pr] = (kl + lam * ee / d_model) / n;
-  if (mode == MODE_KEY_LOSS) return;
-  // u = (2 lambda / d_model) W_j^T e  (threads: channel tid & 127, rows of parity tid >> 7)
-  {
-    const int c = tid & 127, par = tid >> 7;
-    double acc = 0.0;
-    for (int m = par; m < d_model; m += 2) acc = fma((double)w_o[(size_t)m * ldw + (size_t)j * D + c], e[m], acc);
-    s_c[par][c] = acc;
-  }
-  __syncthreads();
-  for (int c = tid; c < D; c += 256) s_u[c] = (s_c[0][c] + s_c[1][c]) * (2.0 * lam / d_model);
-  __syncthreads();
-  // g_s = v_s . u; dL/da^K_s = p^K_s (g_s - p^K . g) + (p^K_s - p_s), divided by n (the mean)
-  for (int s = warp; s <= t; s += 8) {
-    double g = 0.0;
-#pragma unroll
-    for (int u = 0; u < 4; ++u) g = fma(v[(size_t)s * D + 4 * lane + u], s_u[4 * lane + u], g);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
-    if (lane == 0) e[s] = g;  // e is free again (d_model >= 1 entries were used; reuse as g, n_tok long)
-  }
-  __syncthreads();
-  double pg = 0.0;
-  for (int s = tid; s <= t; s += 256) pg = fma(a_k[s], e[s], pg);
-  pg = block_reduce(pg, red, false);
-  for (int s = tid; s < n_tok; s += 256)
-    da[(size_t)pr * n_tok + s] = s <= t ? (a_k[s] * (e[s] - pg) + (a_k[s] - a_r[s])) / n : 0.0;
+// log-sum-exp of row[0 .. t] (the whole block gets it)
+__device__ __forceinline__ double row_lse(const double* row, int t, double* red) {
+  double m = -INFINITY;
+  for (int s = threadIdx.x; s <= t; s += blockDim.x) m = fmax(m, row[s]);
+  m = block_reduce(m, red, true);
+  double sum = 0.0;
+  for (int s = threadIdx.x; s <= t; s += blockDim.x) sum += exp(row[s] - m);
+  sum = block_reduce(sum, red, false);
+  return m + log(sum);
 }
 
-// Values: per pair, c = sum_s p^K_s dv_s (dv = V~ - V), e = W_j c, loss ||e||^2 / (d_model n),
-// u = (2 / (d_model n)) W_j^T e (the pair's row of U; dL/dv~_s = sum_pairs p^K_s u).
-__global__ void __launch_bounds__(256) value_pair_kernel(int with_grad, int n_tok, int n_qpos, int gqa, int d_model,
-                                                         const double* __restrict__ pk,  // [pairs][n_tok]
-                                                         const double* __restrict__ dv,  // [n_tok][128]
-                                                         const float* __restrict__ w_o, double* __restrict__ u_out,
-                                                         double* __restrict__ loss_pair) {
-  extern __shared__ double dyn[];
-  double* e = dyn;  // [d_model]
+// Causal log-softmax of the raw logits in place: log p_s for s <= t (the reference
+// softmax of Eq. 12, fixed for a trace).
+__global__ void __launch_bounds__(256) log_softmax_rows_kernel(int n_tok, int n_qpos, int gqa, double* __restrict__ a) {
   __shared__ double red[8];
-  __shared__ double s_c[2][D];
-  const int pr = blockIdx.x, j = pr % gqa, i = pr / gqa;
-  const int t = n_tok - n_qpos + i;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const double n = (double)(n_qpos * gqa);
-  {
-    const int c = tid & 127, par = tid >> 7;
-    double acc = 0.0;
-    for (int s = par; s <= t; s += 2) acc = fma(pk[(size_t)pr * n_tok + s], dv[(size_t)s * D + c], acc);
-    s_c[par][c] = acc;
+  const int pr = blockIdx.x, t = n_tok - n_qpos + pr / gqa;
+  double* row = a + (size_t)pr * n_tok;
+  const double lse = row_lse(row, t, red);
+  for (int s = threadIdx.x; s <= t; s += blockDim.x) row[s] -= lse;
+}
+
+// p^K = softmax of the effective-key logits a (Eq. 12).  With weights_out: p^K into it
+// (the value phase's fixed weights).  Otherwise a <- p^K, d <- p^K - p and
+// kl[pr] = sum_{s<=t} p_s (log p_s - log p^K_s) (Eq. 14's first term), p = exp(logp).
+__global__ void __launch_bounds__(256) key_rows_kernel(int n_tok, int n_qpos, int gqa, double* __restrict__ a,
+                                                       const double* __restrict__ logp, double* __restrict__ d,
+                                                       double* __restrict__ kl, double* __restrict__ weights_out) {
+  __shared__ double red[8];
+  const int pr = blockIdx.x, t = n_tok - n_qpos + pr / gqa;
+  double* row = a + (size_t)pr * n_tok;
+  const double lse = row_lse(row, t, red);
+  if (weights_out) {
+    for (int s = threadIdx.x; s < n_tok; s += blockDim.x)
+      weights_out[(size_t)pr * n_tok + s] = s <= t ? exp(row[s] - lse) : 0.0;
+    return;
   }
-  __syncthreads();
-  for (int c = tid; c < D; c += 256) s_c[0][c] += s_c[1][c];
-  __syncthreads();
-  const size_t ldw = (size_t)gqa * D;
-  double ee = 0.0;
-  for (int m = warp; m < d_model; m += 8) {
-    const float4 w4 = *reinterpret_cast<const float4*>(w_o + (size_t)m * ldw + (size_t)j * D + 4 * lane);
-    double x = (double)w4.x * s_c[0][4 * lane] + (double)w4.y * s_c[0][4 * lane + 1] +
-               (double)w4.z * s_c[0][4 * lane + 2] + (double)w4.w * s_c[0][4 * lane + 3];
+  const double* lp = logp + (size_t)pr * n_tok;
+  double* dr = d + (size_t)pr * n_tok;
+  double k = 0.0;
+  for (int s = threadIdx.x; s < n_tok; s += blockDim.x) {
+    if (s <= t) {
+      const double lq = row[s] - lse, pk = exp(lq), p = exp(lp[s]);
+      k += p * (lp[s] - lq);
+      row[s] = pk;
+      dr[s] = pk - p;
+    } else {
+      row[s] = 0.0;
+      dr[s] = 0.0;
+    }
+  }
+  k = block_reduce(k, red, false);
+  if (threadIdx.x == 0) kl[pr] = k;
+}
+
+// lossp[pr] = (kl[pr] + c_pr . u_pr / 2) * scale (kl absent: 0); one warp per pair.
+// With u = (2 lambda / d_model) M_j c, c . u / 2 = lambda ||W_j c||^2 / d_model.
+__global__ void pair_loss_kernel(int np, const double* __restrict__ c, const double* __restrict__ u,
+                                 const double* __restrict__ kl, double scale, double* __restrict__ lossp) {
+  const int pr = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+  if (pr >= np) return;
+  double v = 0.0;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) e[m] = x;
-    ee = fma(x, x, ee);
-  }
-  ee = block_reduce(lane == 0 ? ee : 0.0, red, false);
-  if (tid == 0) loss_pair[pr] = ee / d_model / n;
-  if (!with_grad) return;
-  __syncthreads();
-  {
-    const int c = tid & 127, par = tid >> 7;
-    double acc = 0.0;
-    for (int m = par; m < d_model; m += 2) acc = fma((double)w_o[(size_t)m * ldw + (size_t)j * D + c], e[m], acc);
-    s_c[par][c] = acc;
-  }
-  __syncthreads();
-  for (int c = tid; c < D; c += 256) u_out[(size_t)pr * D + c] = (s_c[0][c] + s_c[1][c]) * (2.0 / d_model / n);
+  for (int i = 0; i < 4; ++i) v = fma(c[(size_t)pr * D + 4 * lane + i], u[(size_t)pr * D + 4 * lane + i], v);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (lane == 0) lossp[pr] = ((kl ? kl[pr] : 0.0) + 0.5 * v) * scale;
+}
+
+// dL/da^K_s = (p^K_s (g_s - p^K . g) + (p^K_s - p_s)) / n for s <= t, 0 beyond
+// (the softmax and KL backward; g = U V^T row).
+__global__ void __launch_bounds__(256) key_grad_rows_kernel(int n_tok, int n_qpos, int gqa,
+                                                            const double* __restrict__ pk,
+                                                            const double* __restrict__ g,
+                                                            const double* __restrict__ logp, double inv_n,
+                                                            double* __restrict__ da) {
+  __shared__ double red[8];
+  const int pr = blockIdx.x, t = n_tok - n_qpos + pr / gqa;
+  const size_t r0 = (size_t)pr * n_tok;
+  double pg = 0.0;
+  for (int s = threadIdx.x; s <= t; s += blockDim.x) pg = fma(pk[r0 + s], g[r0 + s], pg);
+  pg = block_reduce(pg, red, false);
+  for (int s = threadIdx.x; s < n_tok; s += blockDim.x)
+    da[r0 + s] = s <= t ? (pk[r0 + s] * (g[r0 + s] - pg) + (pk[r0 + s] - exp(logp[r0 + s]))) * inv_n : 0.0;
 }
 
 // loss = sum of the per-pair terms in pair order (deterministic); optionally also into hist[idx]
@@ -515,12 +433,15 @@ __global__ void sub_kernel(int n, const double* __restrict__ a, const double* __
 struct OptrTrace {  // one trace, widened to fp64
   int n_tok, n_qpos;
   double *x, *kraw, *vv, *q, *pair;  // x = k - mu; pair: [pairs][n_tok] (dL/da^K, or the fixed weights p^K)
+  double* logp;                      // [pairs][n_tok]: log p of the raw keys (fixed for the trace)
 };
 
 struct OptrWs {
   double *S, *E, *R, *xs, *es, *F, *L, *T, *Dk, *T2, *D2, *F2, *L2, *dR, *dE, *G, *m, *v, *a, *best_a, *outF, *gA;
   double *z, *zq, *mask, *keff, *geff, *dzq;  // [n_tok][128], n_tok the larger trace's
   double *u, *lossp;                         // [pairs][128], [pairs]
+  double *ak, *dm, *cm, *kl;                 // [pairs][n_tok] x 2, [pairs][128], [pairs]
+  double* gram;                              // [gqa][128][128]: M_j = W_j^T W_j
   double* scal;                              // [0] loss, [1] score, [2] best score
   int* nsq;
   OptrTrace tr, ho;                          // training and held-out traces
@@ -535,19 +456,26 @@ size_t optr_ws_layout(void* base, int n_tok, int n_qpos, int n_tok_h, int n_qpos
     off = (off + bytes + 255) & ~size_t(255);
     return at;
   };
-  size_t mats[22], toks[6], tr[5], ho[5];
+  size_t mats[22], toks[6], tr[6], ho[6];
   for (int i = 0; i < 22; ++i) mats[i] = take(NN * sizeof(double));
   for (int i = 0; i < 6; ++i) toks[i] = take(ntm * D * sizeof(double));
   const size_t o_u = take(npm * D * sizeof(double));
   const size_t o_lp = take(npm * sizeof(double));
+  const size_t o_ak = take(npm * ntm * sizeof(double));
+  const size_t o_dm = take(npm * ntm * sizeof(double));
+  const size_t o_cm = take(npm * D * sizeof(double));
+  const size_t o_kl = take(npm * sizeof(double));
+  const size_t o_gram = take((size_t)gqa * NN * sizeof(double));
   const size_t o_sc = take(4 * sizeof(double));
   const size_t o_nsq = take(4 * sizeof(int));
   for (int i = 0; i < 3; ++i) tr[i] = take((size_t)n_tok * D * sizeof(double));
   tr[3] = take(np * D * sizeof(double));
   tr[4] = take(np * n_tok * sizeof(double));
+  tr[5] = take(np * n_tok * sizeof(double));
   for (int i = 0; i < 3; ++i) ho[i] = take((size_t)n_tok_h * D * sizeof(double));
   ho[3] = take(nph * D * sizeof(double));
   ho[4] = take(nph * n_tok_h * sizeof(double));
+  ho[5] = take(nph * n_tok_h * sizeof(double));
   if (o) {
     char* p = static_cast<char*>(base);
     double** mp[22] = {&o->S, &o->E, &o->R, &o->xs, &o->es, &o->F, &o->L, &o->T, &o->Dk, &o->T2, &o->D2,
@@ -557,6 +485,11 @@ size_t optr_ws_layout(void* base, int n_tok, int n_qpos, int n_tok_h, int n_qpos
     for (int i = 0; i < 6; ++i) *tp[i] = reinterpret_cast<double*>(p + toks[i]);
     o->u = reinterpret_cast<double*>(p + o_u);
     o->lossp = reinterpret_cast<double*>(p + o_lp);
+    o->ak = reinterpret_cast<double*>(p + o_ak);
+    o->dm = reinterpret_cast<double*>(p + o_dm);
+    o->cm = reinterpret_cast<double*>(p + o_cm);
+    o->kl = reinterpret_cast<double*>(p + o_kl);
+    o->gram = reinterpret_cast<double*>(p + o_gram);
     o->scal = reinterpret_cast<double*>(p + o_sc);
     o->nsq = reinterpret_cast<int*>(p + o_nsq);
     OptrTrace* t2[2] = {&o->tr, &o->ho};
@@ -569,6 +502,7 @@ size_t optr_ws_layout(void* base, int n_tok, int n_qpos, int n_tok_h, int n_qpos
       t2[k]->vv = reinterpret_cast<double*>(p + offs[k][2]);
       t2[k]->q = reinterpret_cast<double*>(p + offs[k][3]);
       t2[k]->pair = reinterpret_cast<double*>(p + offs[k][4]);
+      t2[k]->logp = reinterpret_cast<double*>(p + offs[k][5]);
     }
   }
   return off;
@@ -635,10 +569,6 @@ cudaError_t effective_rows(const OptrWs& w, const double* X, int n_tok, double c
   return gemm64(s, n_tok, D, D, 1.0, w.zq, D, false, w.R, D, true, 0.0, w.keff, D);
 }
 
-size_t key_pair_smem(int n_tok, int d_model) {
-  return (size_t)(2 * n_tok + (d_model > n_tok ? d_model : n_tok)) * sizeof(double);
-}
-
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -647,8 +577,6 @@ size_t key_pair_smem(int n_tok, int d_model) {
 size_t optr_workspace_bytes(int n_tok, int n_qpos, int n_tok_h, int n_qpos_h, int gqa) {
   return optr_ws_layout(nullptr, n_tok, n_qpos, n_tok_h, n_qpos_h, gqa, nullptr);
 }
-
-size_t optr_max_smem(int n_tok, int d_model) { return key_pair_smem(n_tok, d_model); }
 
 namespace {
 
@@ -662,49 +590,78 @@ cudaError_t widen_trace(const OptrTrace& t, int gqa, const float* q, const float
   return cudaGetLastError();
 }
 
-// dynamic shared memory at the entry points' limits (n_tok, d_model <= 8192)
-constexpr int OPTR_MAX_TOK = 8192, OPTR_MAX_DMODEL = 8192;
-cudaError_t smem_attrs() {
-  static std::atomic<unsigned long long> a1{0}, a2{0};
-  KVQ_TRY(smem_limit_once(a1, key_pair_kernel, (int)key_pair_smem(OPTR_MAX_TOK, OPTR_MAX_DMODEL)));
-  return smem_limit_once(a2, value_pair_kernel, OPTR_MAX_DMODEL * (int)sizeof(double));
+// log p of the raw keys for every pair of trace t (Eq. 12's reference softmax, fixed for the trace)
+cudaError_t raw_logp(const OptrTrace& t, int gqa, cudaStream_t s) {
+  const int np = t.n_qpos * gqa;
+  KVQ_TRY(gemm64(s, np, t.n_tok, D, INV_SQRT_D64, t.q, D, false, t.kraw, D, true, 0.0, t.logp, t.n_tok));
+  log_softmax_rows_kernel<<<np, 256, 0, s>>>(t.n_tok, t.n_qpos, gqa, t.logp);
+  return cudaGetLastError();
+}
+
+// M_j = W_j^T W_j for the head's query heads (W_j: the 128 columns of W_O of query head j)
+cudaError_t gram_of(const OptrWs& w, int gqa, int d_model, const float* w_o, cudaStream_t s) {
+  for (int j = 0; j < gqa; ++j)
+    KVQ_TRY(gemm64(s, D, D, d_model, 1.0, w_o + (size_t)j * D, gqa * D, true, w_o + (size_t)j * D, gqa * D, false, 0.0,
+                   w.gram + (size_t)j * NN, D));
+  return cudaSuccess;
+}
+
+// U_j = alpha C_j M_j for every query head j (rows i * G + j of C and U)
+cudaError_t gram_apply(const OptrWs& w, int n_qpos, int gqa, double alpha, cudaStream_t s) {
+  for (int j = 0; j < gqa; ++j)
+    KVQ_TRY(gemm64(s, n_qpos, D, D, alpha, w.cm + (size_t)j * D, gqa * D, false, w.gram + (size_t)j * NN, D, false, 0.0,
+                   w.u + (size_t)j * D, gqa * D));
+  return cudaSuccess;
 }
 
 // p^K of the rotation in w.R for trace t into t.pair (the value phase's fixed weights)
-cudaError_t key_weights(const OptrWs& w, const OptrTrace& t, int gqa, int d_model, double clip, cudaStream_t s) {
+cudaError_t key_weights(const OptrWs& w, const OptrTrace& t, int gqa, double clip, cudaStream_t s) {
   KVQ_TRY(effective_rows(w, t.x, t.n_tok, clip, s));
   const int np = t.n_qpos * gqa;
-  key_pair_kernel<<<np, 256, key_pair_smem(t.n_tok, d_model), s>>>(MODE_WEIGHTS, t.n_tok, t.n_qpos, gqa, d_model, t.q,
-                                                                   t.kraw, w.keff, t.vv, nullptr, 0.0, t.pair,
-                                                                   w.lossp);
+  KVQ_TRY(gemm64(s, np, t.n_tok, D, INV_SQRT_D64, t.q, D, false, w.keff, D, true, 0.0, w.ak, t.n_tok));
+  key_rows_kernel<<<np, 256, 0, s>>>(t.n_tok, t.n_qpos, gqa, w.ak, nullptr, nullptr, nullptr, t.pair);
   return cudaGetLastError();
 }
 
 // One loss (+ gradient) evaluation of phase 0 (keys) or 1 (values) at generator a with base r0.
 // The loss goes to *loss and, with hist, to hist[idx]; the gradient (dL/dA) to grad when non-null.
-cudaError_t optr_eval(const OptrWs& w, const OptrTrace& t, int gqa, int d_model, const float* w_o, int phase,
-                      const double* r0, const double* a, double clip, double lam, double* loss, double* hist, int idx,
-                      double* grad, unsigned* err, cudaStream_t s) {
+// Needs w.gram (gram_of) and, for keys, t.logp (raw_logp).
+cudaError_t optr_eval(const OptrWs& w, const OptrTrace& t, int gqa, int d_model, int phase, const double* r0,
+                      const double* a, double clip, double lam, double* loss, double* hist, int idx, double* grad,
+                      unsigned* err, cudaStream_t s) {
   const int n_tok = t.n_tok, np = t.n_qpos * gqa;
   const double* X = phase ? t.vv : t.x;
   KVQ_TRY(rotation_of(w, r0, a, err, s));
   KVQ_TRY(effective_rows(w, X, n_tok, clip, s));
   if (phase == 0) {
-    key_pair_kernel<<<np, 256, key_pair_smem(n_tok, d_model), s>>>(grad ? MODE_KEY_GRAD : MODE_KEY_LOSS, n_tok,
-                                                                   t.n_qpos, gqa, d_model, t.q, t.kraw, w.keff, t.vv,
-                                                                   w_o, lam, t.pair, w.lossp);
+    // p^K from the effective keys, C = (p^K - p) V, U = (2 lambda / d_model) C_j M_j
+    KVQ_TRY(gemm64(s, np, n_tok, D, INV_SQRT_D64, t.q, D, false, w.keff, D, true, 0.0, w.ak, n_tok));
+    key_rows_kernel<<<np, 256, 0, s>>>(n_tok, t.n_qpos, gqa, w.ak, t.logp, w.dm, w.kl, nullptr);
+    KVQ_TRY(cudaGetLastError());
+    KVQ_TRY(gemm64(s, np, D, n_tok, 1.0, w.dm, n_tok, false, t.vv, D, false, 0.0, w.cm, D));
+    KVQ_TRY(gram_apply(w, t.n_qpos, gqa, 2.0 * lam / d_model, s));
+    pair_loss_kernel<<<blocks((size_t)np * 32), 256, 0, s>>>(np, w.cm, w.u, w.kl, 1.0 / np, w.lossp);
   } else {
-    sub_kernel<<<blocks((size_t)n_tok * D), 256, 0, s>>>(n_tok * D, w.keff, t.vv, w.dzq);  // dv = V~ - V
-    value_pair_kernel<<<np, 256, (size_t)d_model * sizeof(double), s>>>(grad ? 1 : 0, n_tok, t.n_qpos, gqa, d_model,
-                                                                       t.pair, w.dzq, w_o, w.u, w.lossp);
+    // C = p^K (V~ - V), U = (2 / (d_model n)) C_j M_j
+    sub_kernel<<<blocks((size_t)n_tok * D), 256, 0, s>>>(n_tok * D, w.keff, t.vv, w.dzq);
+    KVQ_TRY(cudaGetLastError());
+    KVQ_TRY(gemm64(s, np, D, n_tok, 1.0, t.pair, n_tok, false, w.dzq, D, false, 0.0, w.cm, D));
+    KVQ_TRY(gram_apply(w, t.n_qpos, gqa, 2.0 / ((double)d_model * np), s));
+    pair_loss_kernel<<<blocks((size_t)np * 32), 256, 0, s>>>(np, w.cm, w.u, nullptr, 1.0, w.lossp);
   }
   KVQ_TRY(cudaGetLastError());
   sum_loss_kernel<<<1, 32, 0, s>>>(np, w.lossp, loss, hist, idx);
   KVQ_TRY(cudaGetLastError());
   if (!grad) return cudaSuccess;
-  // dL/dk~ (keys: DA^T Q / sqrt d, the 1/n already in DA) or dL/dv~ (values: P^T U)
-  if (phase == 0) KVQ_TRY(gemm64(s, n_tok, D, np, INV_SQRT_D64, t.pair, n_tok, true, t.q, D, false, 0.0, w.geff, D));
-  else KVQ_TRY(gemm64(s, n_tok, D, np, 1.0, t.pair, n_tok, true, w.u, D, false, 0.0, w.geff, D));
+  // dL/dk~ (keys: DA^T Q / sqrt d with DA from G = U V^T, the 1/n in DA) or dL/dv~ (values: P^T U)
+  if (phase == 0) {
+    KVQ_TRY(gemm64(s, np, n_tok, D, 1.0, w.u, D, false, t.vv, D, true, 0.0, w.dm, n_tok));
+    key_grad_rows_kernel<<<np, 256, 0, s>>>(n_tok, t.n_qpos, gqa, w.ak, w.dm, t.logp, 1.0 / np, t.pair);
+    KVQ_TRY(cudaGetLastError());
+    KVQ_TRY(gemm64(s, n_tok, D, np, INV_SQRT_D64, t.pair, n_tok, true, t.q, D, false, 0.0, w.geff, D));
+  } else {
+    KVQ_TRY(gemm64(s, n_tok, D, np, 1.0, t.pair, n_tok, true, w.u, D, false, 0.0, w.geff, D));
+  }
   // through k~ = Q(X R) R^T with the straight-through mask: dR = G^T z~ + X^T ((G R) * m)
   KVQ_TRY(gemm64(s, D, D, n_tok, 1.0, w.geff, D, true, w.zq, D, false, 0.0, w.dR, D));
   KVQ_TRY(gemm64(s, n_tok, D, D, 1.0, w.geff, D, false, w.R, D, false, 0.0, w.dzq, D));
@@ -722,27 +679,27 @@ cudaError_t optr_eval(const OptrWs& w, const OptrTrace& t, int gqa, int d_model,
 
 // Adam on A from 0 for `steps` steps, candidates every `every` steps (and step 0), scored on the
 // held-out trace (the training one when absent); the best generator ends in w.best_a.
-cudaError_t optr_phase(const OptrWs& w, bool heldout, int gqa, int d_model, const float* w_o, int phase,
-                       const double* r0, double clip, double lam, int steps, double lr, int every, double* hist,
-                       unsigned* err, cudaStream_t s) {
+cudaError_t optr_phase(const OptrWs& w, bool heldout, int gqa, int d_model, int phase, const double* r0,
+                       double clip, double lam, int steps, double lr, int every, double* hist, unsigned* err,
+                       cudaStream_t s) {
   const OptrTrace& sc = heldout ? w.ho : w.tr;
   fill_kernel<<<blocks(NN), 256, 0, s>>>(NN, 0.0, w.a);
   fill_kernel<<<blocks(NN), 256, 0, s>>>(NN, 0.0, w.m);
   fill_kernel<<<blocks(NN), 256, 0, s>>>(NN, 0.0, w.v);
   KVQ_TRY(cudaGetLastError());
-  KVQ_TRY(optr_eval(w, sc, gqa, d_model, w_o, phase, r0, w.a, clip, lam, w.scal + 1, nullptr, 0, nullptr, err, s));
+  KVQ_TRY(optr_eval(w, sc, gqa, d_model, phase, r0, w.a, clip, lam, w.scal + 1, nullptr, 0, nullptr, err, s));
   select_kernel<<<1, 256, 0, s>>>(w.scal + 1, w.scal + 2, w.a, w.best_a, 1);
   KVQ_TRY(cudaGetLastError());
   const double b1 = 0.9, b2 = 0.999, eps = 1e-8;
   double p1 = 1.0, p2 = 1.0;
   for (int i = 1; i <= steps; ++i) {
-    KVQ_TRY(optr_eval(w, w.tr, gqa, d_model, w_o, phase, r0, w.a, clip, lam, w.scal, hist, i - 1, w.gA, err, s));
+    KVQ_TRY(optr_eval(w, w.tr, gqa, d_model, phase, r0, w.a, clip, lam, w.scal, hist, i - 1, w.gA, err, s));
     p1 *= b1;
     p2 *= b2;
     adam_kernel<<<blocks(NN), 256, 0, s>>>(w.a, w.gA, w.m, w.v, lr, b1, b2, eps, 1.0 - p1, 1.0 - p2);
     KVQ_TRY(cudaGetLastError());
     if (every > 0 && i % every == 0) {
-      KVQ_TRY(optr_eval(w, sc, gqa, d_model, w_o, phase, r0, w.a, clip, lam, w.scal + 1, nullptr, 0, nullptr, err, s));
+      KVQ_TRY(optr_eval(w, sc, gqa, d_model, phase, r0, w.a, clip, lam, w.scal + 1, nullptr, 0, nullptr, err, s));
       select_kernel<<<1, 256, 0, s>>>(w.scal + 1, w.scal + 2, w.a, w.best_a, 0);
       KVQ_TRY(cudaGetLastError());
     }
@@ -758,14 +715,15 @@ cudaError_t launch_optr_loss_grad(int phase, const OptrTraceIn& tr, int gqa, int
                                   unsigned* err, cudaStream_t s) {
   OptrWs w;
   optr_ws_layout(ws, tr.n_tok, tr.n_qpos, 0, 0, gqa, &w);
-  KVQ_TRY(smem_attrs());
   KVQ_TRY(widen_trace(w.tr, gqa, tr.q, tr.k, tr.v, mu, s));
+  KVQ_TRY(gram_of(w, gqa, d_model, w_o, s));
+  if (phase == 0) KVQ_TRY(raw_logp(w.tr, gqa, s));
   if (phase == 1) {  // the fixed weights p^K of the selected key rotation
     KVQ_TRY(cudaMemcpyAsync(w.R, r_k_sel, NN * sizeof(double), cudaMemcpyDeviceToDevice, s));
-    KVQ_TRY(key_weights(w, w.tr, gqa, d_model, clip_k, s));
+    KVQ_TRY(key_weights(w, w.tr, gqa, clip_k, s));
   }
-  return optr_eval(w, w.tr, gqa, d_model, w_o, phase, r0, a, phase ? clip_v : clip_k, lam, loss, nullptr, 0, grad,
-                   err, s);
+  return optr_eval(w, w.tr, gqa, d_model, phase, r0, a, phase ? clip_v : clip_k, lam, loss, nullptr, 0, grad, err,
+                   s);
 }
 
 cudaError_t launch_optr_calibrate(const OptrTraceIn& tr, const OptrTraceIn* ho, int gqa, int d_model,
@@ -775,17 +733,19 @@ cudaError_t launch_optr_calibrate(const OptrTraceIn& tr, const OptrTraceIn* ho, 
                                   cudaStream_t s) {
   OptrWs w;
   optr_ws_layout(ws, tr.n_tok, tr.n_qpos, ho ? ho->n_tok : 0, ho ? ho->n_qpos : 0, gqa, &w);
-  KVQ_TRY(smem_attrs());
   KVQ_TRY(widen_trace(w.tr, gqa, tr.q, tr.k, tr.v, mu, s));
   if (ho) KVQ_TRY(widen_trace(w.ho, gqa, ho->q, ho->k, ho->v, mu, s));
+  KVQ_TRY(gram_of(w, gqa, d_model, w_o, s));
+  KVQ_TRY(raw_logp(w.tr, gqa, s));
+  if (ho) KVQ_TRY(raw_logp(w.ho, gqa, s));
   // keys (Algorithm 1, first loop), then the selected rotation R_K and its weights p^K
-  KVQ_TRY(optr_phase(w, ho != nullptr, gqa, d_model, w_o, 0, r_k0, clip_k, lam, steps, lr, every, loss_k, err, s));
+  KVQ_TRY(optr_phase(w, ho != nullptr, gqa, d_model, 0, r_k0, clip_k, lam, steps, lr, every, loss_k, err, s));
   KVQ_TRY(rotation_of(w, r_k0, w.best_a, err, s));
   KVQ_TRY(cudaMemcpyAsync(r_k, w.R, NN * sizeof(double), cudaMemcpyDeviceToDevice, s));
-  KVQ_TRY(key_weights(w, w.tr, gqa, d_model, clip_k, s));
-  if (ho) KVQ_TRY(key_weights(w, w.ho, gqa, d_model, clip_k, s));
+  KVQ_TRY(key_weights(w, w.tr, gqa, clip_k, s));
+  if (ho) KVQ_TRY(key_weights(w, w.ho, gqa, clip_k, s));
   // values under the selected key path (second loop)
-  KVQ_TRY(optr_phase(w, ho != nullptr, gqa, d_model, w_o, 1, r_v0, clip_v, 0.0, steps, lr, every, loss_v, err, s));
+  KVQ_TRY(optr_phase(w, ho != nullptr, gqa, d_model, 1, r_v0, clip_v, 0.0, steps, lr, every, loss_v, err, s));
   KVQ_TRY(rotation_of(w, r_v0, w.best_a, err, s));
   return cudaMemcpyAsync(r_v, w.R, NN * sizeof(double), cudaMemcpyDeviceToDevice, s);
 }
