@@ -269,12 +269,20 @@ class DecodeStep:
         kvq.kvq_pack_wo(self.w_fold, self.w_pack)
         # step inputs
         kn, vn = zip(*[c.new_kv(b, 1) for b in range(n_seqs)])
-        self.host_q = torch.from_numpy(c.queries()).to(bf).pin_memory()
-        self.host_k = torch.from_numpy(np.concatenate(kn)).to(bf).pin_memory()
-        self.host_v = torch.from_numpy(np.concatenate(vn)).to(bf).pin_memory()
-        self.q = self.host_q.to(device)
-        self.k_new = self.host_k.to(device)
-        self.v_new = self.host_v.to(device)
+        # the step's inputs (q, new K, new V) staged in one pinned buffer: one host->device copy per step
+        parts = [c.queries(), np.concatenate(kn), np.concatenate(vn)]
+        sizes = [x.size for x in parts]
+        self.host_in = torch.empty(sum(sizes), dtype=bf).pin_memory()
+        o = 0
+        for x in parts:
+            self.host_in[o:o + x.size] = torch.from_numpy(np.ascontiguousarray(x).reshape(-1)).to(bf)
+            o += x.size
+        self.dev_in = self.host_in.to(device)
+        views, o = [], 0
+        for x in parts:
+            views.append(self.dev_in[o:o + x.size].view(x.shape))
+            o += x.size
+        self.q, self.k_new, self.v_new = views
         self.cu_new = t(np.arange(n_seqs + 1), torch.int32)
         self.start = t(lens - 1, torch.int32)
         self.lens = t(lens, torch.int32)
@@ -335,9 +343,7 @@ class DecodeStep:
         ev[1].record()
 
     def step_e2e(self):
-        self.q.copy_(self.host_q, non_blocking=True)
-        self.k_new.copy_(self.host_k, non_blocking=True)
-        self.v_new.copy_(self.host_v, non_blocking=True)
+        self.dev_in.copy_(self.host_in, non_blocking=True)
         self.step()
         self.host_y.copy_(self.y, non_blocking=True)
 
@@ -504,7 +510,7 @@ def run_gpu(args):
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": alg, "bytes": by},
         "e2e": {"value": world * w.B / (e2e_step * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": int(w.host_q.numel() * 2 + w.host_k.numel() * 2 + w.host_v.numel() * 2),
+                "h2d_bytes_per_step": int(w.host_in.numel() * 2),
                 "d2h_bytes_per_step": int(w.host_y.numel() * 4)},
         "gpu_launches": w.launches_per_step * args.steps * len(block_ms),
         "clocks": clk,

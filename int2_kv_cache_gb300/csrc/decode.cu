@@ -1271,10 +1271,10 @@ __global__ void __launch_bounds__(dec_max_warps(G) * 32, 1) decode_split_kernel(
 // ---------------------------------------------------------------------------
 // Combine: grid (U, G), nw warps (1..32, from the average partials per unit).
 // o_rot of query head j of unit u is the log-sum-exp merge of the unit's
-// partials (slots k + u, k0 <= k <= k1): the block first takes the maximum M of
-// every slot's m, then warp w sums the slots w, w + nw, ... weighted by
-// 2^(m - M) (independent loads, many in flight), and the warp sums are added in
-// warp order, so the result does not depend on timing.
+// partials (slots k + u, k0 <= k <= k1) in one pass: warp w folds the slots
+// w, w + nw, ... (four at a time, their loads in flight together) into a running
+// state (M, L, A) rescaled when the maximum moves, and the warp states are merged
+// in warp order, so the result does not depend on timing.
 // ---------------------------------------------------------------------------
 constexpr int CB_MAX_WARPS = 32;
 
@@ -1293,27 +1293,32 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
   const int ns = sp.y - sp.x + 1;
   const size_t stride = (size_t)G * PART;  // floats between consecutive slots
   const float* base = ws.part + ((size_t)(sp.x + u) * G + j) * PART;
-  float m = -INFINITY;
-  for (int t = threadIdx.x; t < ns; t += blockDim.x) m = fmaxf(m, __ldcg(base + t * stride + D));
-  m = warp_max(m);
-  if (nw > 1) {
-    if (lane == 0) sm_m[warp] = m;
-    __syncthreads();
-    m = -INFINITY;
-    for (int w = 0; w < nw; ++w) m = fmaxf(m, sm_m[w]);
-  }
-  const float M = m;
+  float M = -INFINITY, l = 0.f;
   float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-  float l = 0.f;
-  if (M != -INFINITY) {
-#pragma unroll 4
-    for (int t = warp; t < ns; t += nw) {
-      const float* pp = base + t * stride;
-      const float2 ml = __ldcg(reinterpret_cast<const float2*>(pp + D));
-      const float4 x = __ldcg(reinterpret_cast<const float4*>(pp) + lane);
-      const float e = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-      l = fmaf(e, ml.y, l);
-      a.x = fmaf(e, x.x, a.x); a.y = fmaf(e, x.y, a.y); a.z = fmaf(e, x.z, a.z); a.w = fmaf(e, x.w, a.w);
+  for (int t0 = warp; t0 < ns; t0 += 4 * nw) {
+    float2 ml[4];
+    float4 x[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int t = t0 + k * nw;
+      ml[k] = make_float2(-INFINITY, 0.f);
+      x[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (t < ns) {
+        ml[k] = __ldcg(reinterpret_cast<const float2*>(base + t * stride + D));
+        x[k] = __ldcg(reinterpret_cast<const float4*>(base + t * stride) + lane);
+      }
+    }
+    const float mn = fmaxf(fmaxf(M, fmaxf(ml[0].x, ml[1].x)), fmaxf(ml[2].x, ml[3].x));
+    if (mn == -INFINITY) continue;  // nothing valid yet (uniform across the warp)
+    const float r = M == -INFINITY ? 0.f : exp2f(M - mn);
+    l *= r;
+    a.x *= r; a.y *= r; a.z *= r; a.w *= r;
+    M = mn;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float e = ml[k].x == -INFINITY ? 0.f : exp2f(ml[k].x - M);
+      l = fmaf(e, ml[k].y, l);
+      a.x = fmaf(e, x[k].x, a.x); a.y = fmaf(e, x[k].y, a.y); a.z = fmaf(e, x[k].z, a.z); a.w = fmaf(e, x[k].w, a.w);
     }
   }
   const int b = u / n_kv_heads, h = u % n_kv_heads;
@@ -1323,15 +1328,22 @@ __global__ void __launch_bounds__(CB_MAX_WARPS * 32) decode_combine_kernel(int n
     dst[lane] = make_float4(a.x * inv, a.y * inv, a.z * inv, a.w * inv);
     return;
   }
-  if (lane == 0) sm_l[warp] = l;
+  if (lane == 0) {
+    sm_m[warp] = M;
+    sm_l[warp] = l;
+  }
   reinterpret_cast<float4*>(sm_a[warp])[lane] = a;
   __syncthreads();
+  float Mt = -INFINITY;
+  for (int w = 0; w < nw; ++w) Mt = fmaxf(Mt, sm_m[w]);
   for (int c = threadIdx.x; c < D; c += blockDim.x) {  // 64 or more threads
     float A = 0.f, L = 0.f;
-    for (int w = 0; w < nw; ++w) {
-      A += sm_a[w][c];
-      L += sm_l[w];
-    }
+    if (Mt != -INFINITY)
+      for (int w = 0; w < nw; ++w) {
+        const float e = sm_m[w] == -INFINITY ? 0.f : exp2f(sm_m[w] - Mt);
+        A = fmaf(e, sm_a[w][c], A);
+        L = fmaf(e, sm_l[w], L);
+      }
     o_rot[((size_t)b * n_q_heads + h * G + j) * D + c] = L > 0.f ? A / L : 0.f;
   }
 }
