@@ -1,3 +1,4 @@
+#include <algorithm>
 // Write path: key mean, per-head rotation of vectors, and the fused
 // rotate -> centre -> clip -> quantize -> pack -> append cache-write kernels.
 //
@@ -321,9 +322,10 @@ __global__ void __launch_bounds__(256, 1) append_kernel(
 // an uncertain decision are listed in shared memory and redone at the end of
 // the CTA, one warp each, in double-float.  Tasks are
 // (token, head) in token-major order, so a warp's four groups are consecutive
-// input rows.  Per CTA: AF_TOK tokens, located once, and per head the sign
+// input rows.  Per CTA: tpc <= AF_TOK tokens, located once, and per head the sign
 // masks and the rotated key mean staged in shared memory.
-// grid = (ceil(n_new / AF_TOK), roles), block = AF_THREADS.
+// grid = (ceil(n_new / tpc), roles), block = AF_THREADS; tpc is chosen so that the CTAs fill
+// whole waves of the GPU (four resident CTAs per SM).
 // ---------------------------------------------------------------------------
 constexpr int AF_TOK = 32;
 constexpr int AF_THREADS = 256;
@@ -363,7 +365,7 @@ __device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
 
 template <int LPG>  // lanes per group: 8 (16 channels each) or 4 (32)
 __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
-    PageGeom g, int n_seqs, int n_new, int dtype, const int32_t* __restrict__ cu_new,
+    PageGeom g, int n_seqs, int n_new, int tpc, int dtype, const int32_t* __restrict__ cu_new,
     const int32_t* __restrict__ start_pos, const int32_t* __restrict__ table, AppendRoles roles,
     uint8_t* __restrict__ pool, unsigned* err) {
   constexpr unsigned FULLM = 0xffffffffu;
@@ -376,8 +378,8 @@ __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
   constexpr float U1 = 6.5e-8f;  // 1.09 u: one rounding, with margin
   const AppendRole ro = blockIdx.y ? roles.r[1] : roles.r[0];
   const int H = g.n_kv_heads;
-  const int t0 = blockIdx.x * AF_TOK;
-  const int nt = min(AF_TOK, n_new - t0);
+  const int t0 = blockIdx.x * tpc;
+  const int nt = min(tpc, n_new - t0);
   const bool had = ro.rot.kind == KVQ_ROT_SIGNED_HADAMARD;
   const bool has_mu = ro.mu_rot != nullptr;
   __shared__ long long s_rec[AF_TOK];
@@ -390,7 +392,7 @@ __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
   float* s_mu = reinterpret_cast<float*>(s_dyn + H * 128);  // [H][128]
   float* s_mumax = s_mu + H * 128;                          // [H]
   int* s_redo = reinterpret_cast<int*>(s_mumax + H);        // [AF_TOK * H]: token << 8 | head
-  if (threadIdx.x < AF_TOK) {
+  if (threadIdx.x < nt) {
     const int t = t0 + threadIdx.x;
     long long rec = -1;
     int slot = 0;
@@ -791,8 +793,12 @@ static cudaError_t launch_append_nondense(const PageGeom& g, int n_seqs, int n_n
   static std::atomic<unsigned long long> attr_set{0};  // per device
   const cudaError_t ea = smem_limit_once(attr_set, append_fast_kernel<AF_LPG>, AF_MAX_HEADS * (1028 + 4 * AF_TOK));
   if (ea != cudaSuccess) return ea;
-  append_fast_kernel<AF_LPG><<<dim3((n_new + AF_TOK - 1) / AF_TOK, n_roles), AF_THREADS, smem, s>>>(
-      g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, pool, err);
+  // tokens per CTA: fill whole waves (four resident CTAs per SM) instead of leaving a partial one
+  const long long slots = 4LL * device_sm_count();
+  const long long waves = ((long long)(n_new + AF_TOK - 1) / AF_TOK * n_roles + slots - 1) / slots;
+  const int tpc = (int)std::min<long long>(AF_TOK, std::max<long long>(1, ((long long)n_new * n_roles + waves * slots - 1) / (waves * slots)));
+  append_fast_kernel<AF_LPG><<<dim3((n_new + tpc - 1) / tpc, n_roles), AF_THREADS, smem, s>>>(
+      g, n_seqs, n_new, tpc, dtype, cu_new, start_pos, table, roles, pool, err);
   return cudaGetLastError();
 }
 
