@@ -23,6 +23,8 @@ CASES = [
     (40, 10, 16, [1100, 3000, 1025], "dense", "bf16", (1.0, 1.0)),
     # a full wave of the GPU (more than 16 chunks per warp of the default grid)
     (32, 8, 16, [3072] * 15 + [2900], "dense", "bf16", (0.96, 0.92)),
+    # 8 query heads per KV head at a full wave: 12-warp blocks (6-warp blocks in the step)
+    (64, 8, 16, [2048] * 15 + [1900], "signed_hadamard", "bf16", (1.0, 0.9)),
 ]
 
 
