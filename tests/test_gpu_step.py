@@ -125,3 +125,73 @@ def test_consecutive_steps_walk_across_pages():
     got = out.cpu().numpy()
     for b in range(case.n_seqs):
         assert gu.out_err(got[b], ref[b]) <= gu.OUT_TOL
+
+
+def _ties(rng, n, hkv):
+    """Rotated groups on, next to and away from the code boundaries (min 0, max
+    3 * step, the rest at k, k + 1/2 and k + 1/2 +- 2^-20 steps), [n][hkv][128]."""
+    y = np.empty((n, hkv, 128))
+    for i in range(n):
+        for h in range(hkv):
+            step = 2.0 ** rng.integers(-4, 2)
+            k = rng.integers(0, 3, 128).astype(np.float64)
+            kind = rng.integers(0, 4, 128)
+            off = np.select([kind == 0, kind == 1, kind == 2],
+                            [0.0, 0.5, 0.5 + 2.0 ** -20 * rng.choice([-1, 1], 128)], rng.uniform(0, 1, 128))
+            v = (k + off) * step
+            v[rng.integers(0, 64)] = 0.0
+            v[64 + rng.integers(0, 64)] = 3.0 * step
+            y[i, h] = np.clip(v, 0.0, 3.0 * step)
+    return y
+
+
+def test_step_with_several_sequences_per_query_block_and_near_ties():
+    """384 (sequence, KV head) units: the query preparation appends for two sequences
+    per block.  The new tokens are built so that their rotated, centred values sit on
+    and next to the code boundaries (x = y R^T + mu with y on the grid, so x R is within
+    fp32 rounding of a midpoint); their codes and fp16 meta must equal the fp64
+    oracle's exactly, the rest of the pool and the readout as in the other cases."""
+    import oracle
+    rng = np.random.default_rng(65)
+    lengths = rng.integers(20, 200, 48)
+    case = W.decode_case(65, lengths, 32, 8, 128, "dense", "f32", page_tokens=16, clip_k=1.0, clip_v=1.0,
+                         spare_blocks=2, n_cal=256)
+    g = gu.GpuCase(case)
+    mu = oracle.cache.key_mean(case.calibration_keys())
+    yk, yv = _ties(rng, case.n_seqs, 8), _ties(rng, case.n_seqs, 8)
+    orig = case.kv
+
+    def kv(b):
+        k, v = orig(b)
+        k, v = k.copy(), v.copy()
+        # y R^T per head (R orthogonal), so that (k - mu) R = y and v R = y up to fp32 rounding
+        k[-1] = (np.einsum("hd,hcd->hc", yk[b], g.r_k) + mu).astype(np.float32)
+        v[-1] = np.einsum("hd,hcd->hc", yv[b], g.r_v).astype(np.float32)
+        return k, v
+
+    case.kv = kv
+    kvq, torch = g.kvq, g.torch
+    pool, k_new, v_new = _inputs(g)
+    max_len = int(g.lengths.max())
+    q = gu.dev(case.queries(), "f32")
+    ws = torch.empty(kvq.kvq_decode_workspace_size(g.layout, case.n_seqs, max_len), dtype=torch.uint8, device="cuda")
+    out = torch.full((case.n_seqs, 32, 128), float("nan"), device="cuda")
+    kvq.kvq_decode_step(g.layout, q, gu.dev(k_new, "f32"), gu.dev(v_new, "f32"), gu.dev_i32(g.lengths), max_len,
+                        g.table, g.rot_k, g.rot_v, g.mu_rot_dev, case.clip_k, case.clip_v, pool, ws, out)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    ora_pool, encs = g.oracle_pool()
+    gpool = pool.cpu().numpy()
+    for b in range(case.n_seqs):
+        n = int(g.lengths[b])
+        for which in ("k", "v"):
+            cg, mg = gu.seq_codes_meta(gpool, 8, 16, case.block_table[b], n, which)
+            co, mo = gu.seq_codes_meta(ora_pool, 8, 16, case.block_table[b], n, which)
+            assert np.array_equal(cg[-1], co[-1]), (b, which, int((cg[-1] != co[-1]).sum()))
+            assert np.array_equal(mg[-1], mo[-1]), (b, which)
+    gu.compare_codes(gpool, ora_pool, 8, 16, case.block_table, g.lengths, encs, (case.clip_k, case.clip_v),
+                     label="step ties")
+    got = out.cpu().numpy()
+    ref = g.oracle_decode(ora_pool, case.queries())
+    for b in range(case.n_seqs):
+        assert gu.out_err(got[b], ref[b]) <= gu.OUT_TOL, (b, gu.out_err(got[b], ref[b]))
