@@ -13,8 +13,8 @@ One step = the whole hot path for one decode token of every sequence:
                         tokens; log-sum-exp combine
   2. kvq_out_proj_packed -- y = o' W_O-bar^T with R_V folded into W_O (W_O-bar stored in
                         the projection's box order by kvq_pack_wo)
-(with --window, the append and window copies are separate calls before the
-windowed decode)
+(with --window, kvq_decode_step_win also writes the new token's BF16 window copy
+and the decode reads the windows)
 value = sequences x steps / time (decode tokens per second, one layer).
 
 --impl reference times the fp64 oracle (CPU) on a bounded sample of the same
@@ -295,9 +295,8 @@ class DecodeStep:
         self.o = torch.empty(n_seqs, self.hq, 128, device=device)
         self.y = torch.empty(n_seqs, self.dm, device=device)
         self.host_y = torch.empty(n_seqs, self.dm).pin_memory()
-        # without windows: the fused step (query prep with the append, decode, combine) + W_O;
-        # with windows: append (K and V) + window copies, query prep + decode + combine, W_O
-        self.launches_per_step = 3 + 1 if self.win is None else 1 + 1 + 3 + 1
+        # the fused step (query prep with the append (and window copy), decode, combine) + W_O
+        self.launches_per_step = 3 + 1
 
     def win_row(self, b):
         """A window struct over sequence b's rows only (for appending one sequence at a time)."""
@@ -306,29 +305,23 @@ class DecodeStep:
         return self.kvq.Window(w.sink_tokens, w.recent_tokens, w.buf[b * per:(b + 1) * per])
 
     def step(self, ev=None):
-        """One decode step.  Without windows: kvq_decode_step (the new token's append fused
-        into the decode call) and the W_O projection.  With windows: the append and the
-        window copies, the windowed decode, the projection.  ev: events [4] recorded
-        before the step, after the append (without windows: at the same point as the
-        first), after the decode and after the projection."""
+        """One decode step: kvq_decode_step (the new token's append fused into the decode
+        call; with windows kvq_decode_step_win, which also writes its window copy) and the
+        W_O projection.  ev: events [4] recorded before the step, before the decode call
+        (the same point), after it and after the projection."""
         kvq = self.kvq
         c = self.case
         if ev is not None:
             ev[0].record()
+            ev[1].record()
         if self.win is None:
-            if ev is not None:
-                ev[1].record()
             kvq.kvq_decode_step(self.layout, self.q, self.k_new, self.v_new, self.lens, self.L, self.table, self.rot_k,
                                 self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool, self.ws, self.o,
                                 n_splits=self.splits)
         else:
-            kvq.kvq_quantize_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.table,
-                                    self.rot_k, self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool)
-            kvq.kvq_window_append(self.layout, self.k_new, self.v_new, self.cu_new, self.start, self.mu, self.win)
-            if ev is not None:
-                ev[1].record()
-            kvq.kvq_decode_attention_win(self.layout, self.q, self.lens, self.L, self.table, self.rot_k, self.rot_v,
-                                         self.pool, self.win, self.ws, self.o, n_splits=self.splits)
+            kvq.kvq_decode_step_win(self.layout, self.q, self.k_new, self.v_new, self.lens, self.L, self.table,
+                                    self.rot_k, self.rot_v, self.mu_rot, self.mu, c.clip_k, c.clip_v, self.pool,
+                                    self.win, self.ws, self.o, n_splits=self.splits)
         if ev is not None:
             ev[2].record()
         kvq.kvq_out_proj_packed(self.o.reshape(self.B, -1), self.w_pack, self.y, self.dm)
@@ -369,6 +362,10 @@ class DecodeStep:
                 "query_fragments_write_read": 2 * units * (2 * frag + g * 16),
                 "partials_write_read": 2 * (pairs + pairs_w) * g * 130 * 4,
                 "o_rot": B * hq * 128 * 4,
+                # the step's new token: bf16 K and V read, 72 B of codes and meta and 512 B of
+                # window row written per head, R_V read
+                "step_append": B * hkv * (2 * 256 + 72 + 512) + (hkv * 128 * 128 * 4
+                                                               if self.case.rot_v.kind == "dense" else hkv * 128 * 4),
             }
         # one partial (acc[128], m, l per query head) per (warp slice, unit) pair:
         # at most 4 * n_ctas + units of them, written once and read once
@@ -440,7 +437,6 @@ def run_gpu(args):
     for i in range(n_br):
         w.step(evs[i])
     barrier()
-    t_app = float(np.median([e[0].elapsed_time(e[1]) for e in evs]))
     t_dec = float(np.median([e[1].elapsed_time(e[2]) for e in evs]))
     t_out = float(np.median([e[2].elapsed_time(e[3]) for e in evs]))
     t_dec_only = None
@@ -500,12 +496,14 @@ def run_gpu(args):
         },
         "kernel_ms": ({"decode_step": t_dec, "out_proj": t_out, "decode_attention_alone": t_dec_only}
                       if window is None else
-                      {"quantize_append_and_window": t_app, "decode_attention_win": t_dec, "out_proj": t_out}),
+                      {"decode_step_win": t_dec, "out_proj": t_out}),
         "kv_cache_gbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9,
         "kv_cache_pct_of_peak": {"measured": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / peak,
                                  "nominal_8tbs": by["kv_cache"] / (t_dec * 1e-3) / 1e9 / NOMINAL_HBM_GBS},
         "roofline": {"kernel": ("kvq_decode_step (query prep with the new token's append, decode, combine)"
-                                if window is None else "kvq_decode_attention_win (query prep, decode, combine)"),
+                                if window is None else
+                                "kvq_decode_step_win (query prep with the new token's append and window copy, "
+                                "decode, combine)"),
                      "bound": "hbm", "achieved": achieved,
                      "peak": peak, "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": traffic, "algorithmic_bytes": alg, "bytes": by},

@@ -267,6 +267,27 @@ kvq_status kvq_decode_attention_win(const kvq_layout* layout, int n_seqs, const 
                                     void* workspace, size_t workspace_bytes, float* o_rot,
                                     kvq_stream stream);
 
+/* One decode step with BF16 sink / recent windows: kvq_decode_step's fused
+ * append and decode, plus the new token's window copy ("Output-Aware Rotation
+ * for INT2 KV-Cache Quantization", §5 implementation details, Table A; §6 the
+ * cache-write kernel and decode).  For every sequence with seq_lens[b] >= 1 the
+ * token at position seq_lens[b] - 1 is written to the pool as kvq_quantize_append
+ * would write it and to the windows as kvq_window_append would (key k - mu_k,
+ * value v, both bf16; sink slot if the position is below sink_tokens, else the
+ * recent ring), and o_rot is then what kvq_decode_attention_win returns over
+ * seq_lens[b] tokens.  One call: the query preparation writes both, and the
+ * decode reads them only after it.
+ *   mu_k:      float [n_kv_heads][128] unrotated key mean for the window keys, or NULL
+ *   win:       the windows (written in place and read); sink + recent may be 0
+ *   workspace: >= kvq_decode_workspace_size_win bytes
+ * Other arguments, limits and errors as kvq_decode_step and kvq_decode_attention_win. */
+kvq_status kvq_decode_step_win(const kvq_layout* layout, int n_seqs, const void* q, const void* k_new,
+                               const void* v_new, kvq_dtype dtype, const int32_t* seq_lens, int max_seq_len,
+                               const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v, const float* mu_rot_k,
+                               const float* mu_k, float clip_k, float clip_v, uint8_t* pool, const kvq_window* win,
+                               int n_splits, void* workspace, size_t workspace_bytes, float* o_rot,
+                               kvq_stream stream);
+
 /* The same decode attention for callers that cannot allocate device memory
  * (the paper has no counterpart; this is a deployment convenience).
  * Serving engines that reserve all device memory up front and forbid allocation

@@ -97,6 +97,8 @@ def lib() -> ctypes.CDLL:
             "kvq_decode_step": ([lp, i, vp, vp, vp, i, vp, i, vp, KvqRot, KvqRot, vp, f, f, vp, i, vp, sz, vp, vp],
                                 st),
             "kvq_window_append": ([lp, i, i, vp, vp, i, vp, vp, vp, wp, vp], st),
+            "kvq_decode_step_win": ([lp, i, vp, vp, vp, i, vp, i, vp, KvqRot, KvqRot, vp, vp, f, f, vp, wp, i, vp, sz,
+                                     vp, vp], st),
             "kvq_decode_workspace_size_win": ([lp, i, i, i, wp, ctypes.POINTER(sz)], st),
             "kvq_decode_attention_win": ([lp, i, vp, i, vp, i, vp, KvqRot, KvqRot, vp, wp, i, vp, sz, vp, vp], st),
             "kvq_fold_wo": ([i, i, i, vp, i, KvqRot, vp, i, vp], st),
@@ -125,7 +127,7 @@ def lib() -> ctypes.CDLL:
 
 EXPORTED = ("kvq_last_error", "kvq_pool_bytes", "kvq_device_check", "kvq_key_mean", "kvq_rotate_heads",
             "kvq_quantize_append", "kvq_decode_workspace_size", "kvq_decode_attention",
-            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_window_append", "kvq_decode_workspace_size_win",
+            "kvq_decode_attention_noalloc", "kvq_decode_step", "kvq_decode_step_win", "kvq_window_append", "kvq_decode_workspace_size_win",
             "kvq_decode_attention_win", "kvq_fold_wo",
             "kvq_out_proj", "kvq_wo_packed_bytes", "kvq_pack_wo", "kvq_out_proj_packed", "kvq_calib_workspace_size", "kvq_calib_nmse", "kvq_report_workspace_size",
             "kvq_head_error_report", "kvq_optr_workspace_size", "kvq_optr_loss_grad", "kvq_optr_calibrate_head")
@@ -291,6 +293,21 @@ def kvq_decode_workspace_size_win(layout: KvqLayout, n_seqs: int, max_seq_len: i
     _check(lib().kvq_decode_workspace_size_win(ctypes.byref(layout), n_seqs, max_seq_len, n_splits, _win_ref(win),
                                                ctypes.byref(out)))
     return int(out.value)
+
+
+def kvq_decode_step_win(layout: KvqLayout, q, k_new, v_new, seq_lens, max_seq_len: int, block_table,
+                        rot_k: DeviceRot, rot_v: DeviceRot, mu_rot_k, mu_k, clip_k: float, clip_v: float, pool,
+                        win: Window | None, workspace, o_rot, n_splits: int = 0, stream=None) -> None:
+    """kvq_decode_step with BF16 windows: the new token is also copied into its window
+    slot (key centred by the unrotated mean mu_k) before the windowed decode reads it."""
+    n_seqs = q.shape[0]
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TypeError("q, k_new and v_new must share a dtype")
+    _check(lib().kvq_decode_step_win(ctypes.byref(layout), n_seqs, _ptr(_contig(q, "q")), _ptr(_contig(k_new, "k_new")),
+                                     _ptr(_contig(v_new, "v_new")), _dtype_code(q), _ptr(seq_lens), max_seq_len,
+                                     _ptr(block_table), rot_k.c, rot_v.c, _ptr(mu_rot_k), _ptr(mu_k), clip_k, clip_v,
+                                     _ptr(pool), _win_ref(win), n_splits, _ptr(workspace),
+                                     workspace.numel() * workspace.element_size(), _ptr(o_rot), _stream(stream)))
 
 
 def kvq_decode_attention_win(layout: KvqLayout, q, seq_lens, max_seq_len: int, block_table, rot_k: DeviceRot,

@@ -293,12 +293,18 @@ kvq_status kvq_decode_attention(const kvq_layout* layout, int n_seqs, const void
                                   pool, nullptr, n_splits, workspace, workspace_bytes, o_rot, stream);
 }
 
-kvq_status kvq_decode_step(const kvq_layout* layout, int n_seqs, const void* q, const void* k_new,
-                           const void* v_new, kvq_dtype dtype, const int32_t* seq_lens, int max_seq_len,
-                           const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v, const float* mu_rot_k,
-                           float clip_k, float clip_v, uint8_t* pool, int n_splits, void* workspace,
-                           size_t workspace_bytes, float* o_rot, kvq_stream stream) {
+}  // extern "C"
+
+static kvq_status decode_step_impl(const char* name, const kvq_layout* layout, int n_seqs, const void* q,
+                                   const void* k_new, const void* v_new, kvq_dtype dtype, const int32_t* seq_lens,
+                                   int max_seq_len, const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v,
+                                   const float* mu_rot_k, float clip_k, float clip_v, uint8_t* pool,
+                                   const kvq_window* win, const float* mu_k, int n_splits, void* workspace,
+                                   size_t workspace_bytes, float* o_rot, kvq_stream stream) {
   KVQ_CHECK(check_layout(layout, true));
+  kvq::WinGeom wg;
+  KVQ_CHECK(check_window(win, &wg));
+  const bool windows = wg.sink + wg.recent > 0;
   if (n_seqs < 0) return fail(KVQ_EINVAL, "n_seqs %d < 0", n_seqs);
   if (!valid_dtype(dtype)) return fail(KVQ_EINVAL, "bad dtype %d", (int)dtype);
   if (!valid_clip(clip_k) || !valid_clip(clip_v))
@@ -318,19 +324,43 @@ kvq_status kvq_decode_step(const kvq_layout* layout, int n_seqs, const void* q, 
   KVQ_PTR(o_rot, "o_rot");
   KVQ_PTR(workspace, "workspace");
   if (mu_rot_k && !aligned16(mu_rot_k)) return fail(KVQ_EINVAL, "mu_rot_k is not 16-byte aligned");
+  if (mu_k && !aligned16(mu_k)) return fail(KVQ_EINVAL, "mu_k is not 16-byte aligned");
   KVQ_CHECK(check_decode_size(layout, n_seqs, max_seq_len));
   const int gqa = layout->n_q_heads / layout->n_kv_heads;
   const int s = n_splits ? n_splits : kvq::decode_auto_ctas(n_seqs, layout->n_kv_heads, gqa, max_seq_len);
-  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s, false);
+  const size_t need = kvq::decode_workspace_bytes(n_seqs, layout->n_kv_heads, gqa, s, windows);
   if (workspace_bytes < need)
     return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
   unsigned* err = nullptr;
   KVQ_CHECK(device_error_word(&err));
-  const kvq::StepAppend app{k_new, v_new, (int)dtype, kvq::to_dev(rot_v), mu_rot_k, clip_k, clip_v, pool};
+  const kvq::StepAppend app{k_new, v_new, (int)dtype, kvq::to_dev(rot_v), mu_rot_k, clip_k, clip_v, pool, wg, mu_k};
   cudaError_t e = kvq::launch_decode(geom(layout), layout->n_q_heads, n_seqs, q, dtype, seq_lens, max_seq_len,
-                                     block_table, kvq::to_dev(rot_k), pool, s, workspace, o_rot, err, stream,
-                                     kvq::WinGeom{0, 0, nullptr}, kvq::to_dev(rot_v), &app);
-  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_decode_step");
+                                     block_table, kvq::to_dev(rot_k), pool, s, workspace, o_rot, err, stream, wg,
+                                     kvq::to_dev(rot_v), &app);
+  return e == cudaSuccess ? KVQ_OK : cuda_fail(e, name);
+}
+
+extern "C" {
+
+kvq_status kvq_decode_step(const kvq_layout* layout, int n_seqs, const void* q, const void* k_new,
+                           const void* v_new, kvq_dtype dtype, const int32_t* seq_lens, int max_seq_len,
+                           const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v, const float* mu_rot_k,
+                           float clip_k, float clip_v, uint8_t* pool, int n_splits, void* workspace,
+                           size_t workspace_bytes, float* o_rot, kvq_stream stream) {
+  return decode_step_impl("kvq_decode_step", layout, n_seqs, q, k_new, v_new, dtype, seq_lens, max_seq_len,
+                          block_table, rot_k, rot_v, mu_rot_k, clip_k, clip_v, pool, nullptr, nullptr, n_splits,
+                          workspace, workspace_bytes, o_rot, stream);
+}
+
+kvq_status kvq_decode_step_win(const kvq_layout* layout, int n_seqs, const void* q, const void* k_new,
+                               const void* v_new, kvq_dtype dtype, const int32_t* seq_lens, int max_seq_len,
+                               const int32_t* block_table, kvq_rot rot_k, kvq_rot rot_v, const float* mu_rot_k,
+                               const float* mu_k, float clip_k, float clip_v, uint8_t* pool, const kvq_window* win,
+                               int n_splits, void* workspace, size_t workspace_bytes, float* o_rot,
+                               kvq_stream stream) {
+  return decode_step_impl("kvq_decode_step_win", layout, n_seqs, q, k_new, v_new, dtype, seq_lens, max_seq_len,
+                          block_table, rot_k, rot_v, mu_rot_k, clip_k, clip_v, pool, win, mu_k, n_splits, workspace,
+                          workspace_bytes, o_rot, stream);
 }
 
 static kvq_status check_optr_trace(const kvq_optr_trace* t, const char* name, int gqa) {

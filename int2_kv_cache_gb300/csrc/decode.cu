@@ -332,7 +332,7 @@ __host__ __device__ constexpr int qpa_smem_bytes(bool dense_v) {
 // ---------------------------------------------------------------------------
 constexpr int QP_THREADS = 256;
 
-template <int G, bool DENSE, bool APPEND>
+template <int G, bool DENSE, bool APPEND, bool WAPP = false>  // WAPP: the append also writes a window row
 __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_kv_heads, const void* __restrict__ q,
                                                            int q_dtype, RotDev rot, const int32_t* __restrict__ seq_lens,
                                                            DecWs ws, float* __restrict__ o_rot, PageGeom pg,
@@ -452,6 +452,32 @@ __global__ void __launch_bounds__(QP_THREADS) qprep_kernel(int n_q_heads, int n_
       }
     }
     __syncthreads();
+    // with BF16 windows, warp 0 writes the new token's window row (the rules of
+    // window_append_kernel: key = bf16(k - mu), value = bf16(v); sink slot p < S, else
+    // recent slot S + p % R)
+    if (WAPP && warp == 0) {
+      const int len = __ldg(seq_lens + b), p = len - 1;
+      const int S = app.win.sink, R = app.win.recent;
+      if (len >= 1 && len <= pg.max_blocks * pg.page_tokens && (p < S || R > 0)) {
+        const int slot = p < S ? p : S + p % R;
+        uint8_t* wrec = app.win.buf + (((size_t)b * n_kv_heads + h) * ((S + R) / WIN_REC_TOKENS) +
+                                       slot / WIN_REC_TOKENS) * WIN_REC_BYTES;
+        const int row = slot % WIN_REC_TOKENS;
+        const int off = row * 256 + (((lane >> 1) ^ row) << 4) + (lane & 1) * 8;
+        float4 x = reinterpret_cast<const float4*>(ak->x)[lane];
+        if (app.mu_win) {
+          const float4 m = __ldg(reinterpret_cast<const float4*>(app.mu_win + (size_t)h * D) + lane);
+          x = make_float4(__fsub_rn(x.x, m.x), __fsub_rn(x.y, m.y), __fsub_rn(x.z, m.z), __fsub_rn(x.w, m.w));
+        }
+        const float4 y = reinterpret_cast<const float4*>(av->x)[lane];
+        const __nv_bfloat162 k01 = __floats2bfloat162_rn(x.x, x.y), k23 = __floats2bfloat162_rn(x.z, x.w);
+        const __nv_bfloat162 v01 = __floats2bfloat162_rn(y.x, y.y), v23 = __floats2bfloat162_rn(y.z, y.w);
+        *reinterpret_cast<uint2*>(wrec + off) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&k01), *reinterpret_cast<const uint32_t*>(&k23));
+        *reinterpret_cast<uint2*>(wrec + 2048 + off) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&v01), *reinterpret_cast<const uint32_t*>(&v23));
+      }
+    }
     // the decisions: warp NW - 1 the key, warp NW - 2 the value (dense: the exact
     // decision on the double-float partials; otherwise the one-warp path)
     const int P = pg.page_tokens;
@@ -783,14 +809,22 @@ __global__ void __launch_bounds__(dec_max_warps(G) * 32, 1) decode_split_kernel(
   };
 
   // With a step's append (kvq_decode_step) the query preparation writes the new token
-  // into the last page of every sequence: a warp whose first stages include the last
-  // entry of a unit issues them only after that kernel has completed.
+  // into the last page of every sequence (and, with windows, into the unit's last
+  // window record): a warp whose first fills include the last entry of a unit in
+  // either list issues them only after that kernel has completed.
   bool early = true;
-  if (step_append && my_n > 0) {
-    ChunkWalker w = iw;
-    for (int f = 0; f < NST && f < my_n; ++f) {
-      walk_to(w, ga + f);
-      if (ga + f == w.E - 1) early = false;
+  if (step_append && F > 0) {
+    ChunkWalker w = iw, w2 = iww;
+    for (int f = 0; f < NST && f < F; ++f) {
+      if (WIN && (win_first ? f < my_nw : f >= my_n)) {
+        const int j = win_first ? f : f - my_n;
+        walk_w(w2, gaw + j);
+        if (gaw + j == w2.E - 1) early = false;
+      } else {
+        const int i = WIN && win_first ? f - my_nw : f;
+        walk_to(w, ga + i);
+        if (ga + i == w.E - 1) early = false;
+      }
     }
   }
   if (F > 0) {
@@ -1473,7 +1507,8 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   if (n_seqs == 0) return cudaSuccess;
   const int gqa = n_q_heads / g.n_kv_heads;
   const bool windows = win.sink + win.recent > 0;
-  if (app && windows) return cudaErrorInvalidValue;  // the fused step append has no window copies
+  if (app && (app->win.sink != win.sink || app->win.recent != win.recent || app->win.buf != win.buf))
+    return cudaErrorInvalidValue;  // the step writes the windows the decode reads
   DecWs ws;
   decode_ws_layout(ws_base, n_seqs, g.n_kv_heads, gqa, n_ctas, windows, &ws);
   // query preparation: several sequences of a KV head per CTA when the batch has more units
@@ -1482,16 +1517,22 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   const int qp_spc = max(1, min(8, (n_seqs * g.n_kv_heads + qp_cap - 1) / qp_cap));
   const dim3 qg(g.n_kv_heads, (n_seqs + qp_spc - 1) / qp_spc);
   const bool dense = rot_k.kind == KVQ_ROT_DENSE;
-  const StepAppend sa = app ? *app : StepAppend{nullptr, nullptr, 0, RotDev{0, nullptr, nullptr}, nullptr, 1.f, 1.f, nullptr};
+  const StepAppend sa = app ? *app
+                            : StepAppend{nullptr, nullptr, 0, RotDev{0, nullptr, nullptr}, nullptr, 1.f, 1.f, nullptr,
+                                         WinGeom{0, 0, nullptr}, nullptr};
   const int qpa_smem = qpa_smem_bytes(app && app->rot_v.kind == KVQ_ROT_DENSE);
-#define KVQ_QPREP_A(GG, DD)                                                                                   \
-  if (app) {                                                                                                  \
+#define KVQ_QPREP_AW(GG, DD, WW)                                                                              \
+  do {                                                                                                        \
     static std::atomic<unsigned long long> attr{0};                                                          \
-    const cudaError_t ea = smem_limit_once(attr, qprep_kernel<GG, DD, true>, qpa_smem_bytes(true));           \
+    const cudaError_t ea = smem_limit_once(attr, qprep_kernel<GG, DD, true, WW>, qpa_smem_bytes(true));       \
     if (ea != cudaSuccess) return ea;                                                                         \
-    qprep_kernel<GG, DD, true><<<qg, QP_THREADS, qpa_smem, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k,   \
-                                                               seq_lens, ws, o_rot, g, table, sa, err, n_seqs, qp_spc); \
-  }                                                                                                           \
+    qprep_kernel<GG, DD, true, WW><<<qg, QP_THREADS, qpa_smem, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k, \
+                                                                   seq_lens, ws, o_rot, g, table, sa, err, n_seqs, \
+                                                                   qp_spc);                                   \
+  } while (0)
+#define KVQ_QPREP_A(GG, DD)                                                                                   \
+  if (app && windows) KVQ_QPREP_AW(GG, DD, true);                                                             \
+  else if (app) KVQ_QPREP_AW(GG, DD, false);                                                                  \
   else qprep_kernel<GG, DD, false><<<qg, QP_THREADS, 0, s>>>(n_q_heads, g.n_kv_heads, q, q_dtype, rot_k,       \
                                                             seq_lens, ws, o_rot, g, table, sa, err, n_seqs, qp_spc)
 #define KVQ_QPREP(GG) \
@@ -1505,6 +1546,7 @@ cudaError_t launch_decode(const PageGeom& g, int n_q_heads, int n_seqs, const vo
   }
 #undef KVQ_QPREP
 #undef KVQ_QPREP_A
+#undef KVQ_QPREP_AW
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 

@@ -51,6 +51,8 @@ struct StepAppend {
   const float* mu_rot_k;  // mu R_K per head, or nullptr
   float clip_k, clip_v;
   uint8_t* pool;          // the pool, written in place
+  WinGeom win;            // BF16 windows (sink + recent = 0: none), written in place
+  const float* mu_win;    // the unrotated key mean that centres window keys, or nullptr
 };
 
 struct PageGeom {

@@ -206,3 +206,82 @@ def test_empty_window_is_the_plain_decode_and_splits_agree():
                                      g.rot_v, pool, win, ws, out, n_splits=sp)
         res.append(out.cpu().numpy())
     assert gu.normwise_err(res[1], res[0]) < 5e-5 and gu.normwise_err(res[2], res[0]) < 5e-5
+
+
+STEP_CASES = [
+    # hq, hkv, page, lengths after the step, rot, dtype, (sink, recent), clips
+    (8, 2, 16, [1, 40, 64, 65, 300, 0, 333], "dense", "bf16", (64, 40), (0.96, 0.92)),
+    (32, 8, 8, [3000] * 6 + [2900], "dense", "bf16", (64, 256), (0.96, 0.92)),
+    (16, 4, 16, [100, 257, 1000], "signed_hadamard", "f32", (64, 0), (1.0, 0.9)),
+    (8, 2, 16, [10, 50, 70], "identity", "bf16", (0, 16), (0.9, 0.9)),
+]
+
+
+@pytest.mark.parametrize("hq,hkv,page,lengths,rot,dtype,win_sizes,clips", STEP_CASES, ids=lambda v: str(v))
+def test_windowed_step_equals_separate_appends_and_the_oracle(hq, hkv, page, lengths, rot, dtype, win_sizes, clips):
+    """kvq_decode_step_win against kvq_quantize_append + kvq_window_append +
+    kvq_decode_attention_win on the same history: pools, window records and outputs
+    equal bit for bit; the readout against the oracle's windowed decode."""
+    import oracle
+    case = W.decode_case(45, lengths, hq, hkv, 128, rot, dtype, page_tokens=page, clip_k=clips[0], clip_v=clips[1],
+                         spare_blocks=2, n_cal=256)
+    g = gu.GpuCase(case)
+    kvq, torch = g.kvq, g.torch
+    mu = _mu(case)
+    full = g.lengths.copy()
+    hist = np.maximum(full - 1, 0)
+    # history: every token but the last, in the pool and the windows
+    g.lengths = hist
+    pool_a = g.new_pool()
+    if hist.sum():
+        g.gpu_append_all(pool_a)
+    win_a = _gpu_window(g, win_sizes)
+    if hist.sum():
+        _append_windows(g, win_a, mu, [])
+    g.lengths = full
+    pool_b = pool_a.clone()
+    win_b = kvq.Window(win_sizes[0], win_sizes[1], win_a.buf.clone())
+    kv = [case.kv(b) for b in range(case.n_seqs)]
+    zero = np.zeros((hkv, 128), np.float32)
+    k_new = np.stack([kv[b][0][full[b] - 1] if full[b] else zero for b in range(case.n_seqs)])
+    v_new = np.stack([kv[b][1][full[b] - 1] if full[b] else zero for b in range(case.n_seqs)])
+    has = full > 0
+    cu = gu.dev_i32(np.concatenate([[0], np.cumsum(has)]))
+    start = gu.dev_i32(hist)
+    kn, vn = gu.dev(k_new, dtype), gu.dev(v_new, dtype)
+    q = gu.dev(case.queries(), dtype)
+    lens = gu.dev_i32(full)
+    max_len = int(full.max())
+    mu_dev = gu.dev(mu)
+    ws = torch.empty(kvq.kvq_decode_workspace_size_win(g.layout, case.n_seqs, max_len, win_a), dtype=torch.uint8,
+                     device="cuda")
+    # separate calls
+    kvq.kvq_quantize_append(g.layout, gu.dev(k_new[has], dtype), gu.dev(v_new[has], dtype), cu, start, g.table,
+                            g.rot_k, g.rot_v, g.mu_rot_dev, case.clip_k, case.clip_v, pool_a)
+    kvq.kvq_window_append(g.layout, gu.dev(k_new[has], dtype), gu.dev(v_new[has], dtype), cu, start, mu_dev, win_a)
+    out_a = torch.full((case.n_seqs, hq, 128), float("nan"), device="cuda")
+    kvq.kvq_decode_attention_win(g.layout, q, lens, max_len, g.table, g.rot_k, g.rot_v, pool_a, win_a, ws, out_a)
+    # the fused step
+    out_b = torch.full_like(out_a, float("nan"))
+    kvq.kvq_decode_step_win(g.layout, q, kn, vn, lens, max_len, g.table, g.rot_k, g.rot_v, g.mu_rot_dev, mu_dev,
+                            case.clip_k, case.clip_v, pool_b, win_b, ws, out_b)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    assert torch.equal(pool_a, pool_b)
+    assert torch.equal(win_a.buf, win_b.buf)
+    assert torch.equal(out_a, out_b)
+    # the oracle: windows of every token, windowed readout over the pool
+    ora_pool, _ = g.oracle_pool()
+    regions = _oracle_windows(g, win_sizes, mu, [np.array([0, n]) for n in full])
+    got = out_b.cpu().numpy()
+    s, r = win_sizes
+    for b in range(case.n_seqs):
+        n = int(full[b])
+        if n == 0:
+            assert np.all(got[b] == 0)
+            continue
+        kh, vh = oracle.cache.dequantized_sequence(ora_pool, hkv, page, case.block_table[b], n)
+        wp, wk, wv = oracle.window.read_window(regions[b], n, s, r)
+        ref = oracle.window.decode_attention_windowed(case.queries()[b], kh, vh, wp, wk, wv, g.r_k, g.r_v, case.gqa,
+                                                      n, s, r)
+        assert gu.out_err(got[b], ref) <= gu.OUT_TOL, (b, n, gu.out_err(got[b], ref))
