@@ -14,7 +14,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OBJDIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libkvq.so")
 SOURCES = ["api.cu", "quantize.cu", "decode.cu", "decode_noalloc.cu", "outproj.cu", "calib.cu", "window.cu",
-           "optr.cu"]
+           "optr.cu", "append_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -25,6 +25,52 @@
 namespace kvq {
 
 // ---------------------------------------------------------------------------
+// Token -> (sequence, position, physical page, slot) with bounds checks.
+// Returns false (and flags) when the token must be skipped.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool locate(int t, int n_seqs, const int32_t* cu_new,
+                                       const int32_t* start_pos, const int32_t* table,
+                                       const PageGeom& g, unsigned* err, long long* rec_index,
+                                       int* slot, int head) {
+  int lo = 0, hi = n_seqs - 1;
+  while (lo < hi) {  // largest b with cu_new[b] <= t
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(cu_new + mid) <= t) lo = mid; else hi = mid - 1;
+  }
+  int b = lo;
+  int base = __ldg(cu_new + b);
+  if (t < base || t >= __ldg(cu_new + b + 1)) { flag_error(err, ERR_SEQ_RANGE); return false; }
+  long long pos = (long long)__ldg(start_pos + b) + (t - base);
+  long long page = pos / g.page_tokens;
+  if (pos < 0 || page >= g.max_blocks) { flag_error(err, ERR_POS_RANGE); return false; }
+  int blk = __ldg(table + (size_t)b * g.max_blocks + page);
+  if (blk < 0 || blk >= g.num_blocks) { flag_error(err, ERR_BLOCK_RANGE); return false; }
+  *rec_index = (long long)blk * g.n_kv_heads + head;
+  *slot = (int)(pos % g.page_tokens);
+  return true;
+}
+
+// One role of a cache write (keys or values): input rows, rotation, rotated key
+// mean (or nullptr), clip ratio and the offsets of its codes and meta in a record.
+struct AppendRole {
+  const void* src;
+  RotDev rot;
+  const float* mu_rot;
+  float clip;
+  int codes_off, meta_off;
+};
+struct AppendRoles {
+  AppendRole r[2];
+};
+
+// Bulk cache write of dense roles on the tensor cores (append_tc.cu): roles.r[0 ..
+// n_roles - 1] must be dense; inputs and pool 16-byte aligned (append_dense_tc_supported).
+bool append_dense_tc_supported(int dtype, const void* k, const void* v, const uint8_t* pool);
+cudaError_t launch_append_dense_tc(const PageGeom& g, int n_seqs, int n_new, int dtype, const int32_t* cu_new,
+                                   const int32_t* start_pos, const int32_t* table, const AppendRoles& roles,
+                                   int n_roles, uint8_t* pool, unsigned* err, cudaStream_t s);
+
+// ---------------------------------------------------------------------------
 // double-float arithmetic (intrinsics keep the compiler from fusing or reordering)
 // ---------------------------------------------------------------------------
 struct DF {
@@ -129,6 +175,38 @@ __device__ __forceinline__ unsigned qcode_df(DF x, const QParams& p) {
   const unsigned b = (d.hi > p.t15 || (d.hi == p.t15 && d.lo >= 0.f)) ? 1u : 0u;  // tie at 1.5 -> 2
   const unsigned c = (d.hi > p.t25 || (d.hi == p.t25 && d.lo > 0.f)) ? 1u : 0u;   // tie at 2.5 -> 2
   return a + b + c;
+}
+
+// Paired fp32 arithmetic of sm_100 (two lanes of a 64-bit register per instruction).
+__device__ __forceinline__ uint64_t f2pk(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2up(uint64_t p) {
+  float2 r;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(p));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
 }
 
 // ---------------------------------------------------------------------------
@@ -346,13 +424,10 @@ __device__ __forceinline__ float rotate_f32_bounded(float y[4], const RotDev& ro
   return l1 * INV_SQRT_D * P2_M19;
 }
 
-// Group decision from d (|d_i - x_i| <= E for every channel of the warp).
-// Returns false (warp-uniform) when some decision is not certain.
-__device__ __forceinline__ bool quantize_warp_certain(const float d[4], float E, float clip, QParams& p,
-                                                      unsigned& byte) {
-  const float mn = warp_min(fminf(fminf(d[0], d[1]), fminf(d[2], d[3])));
-  const float mx = warp_max(fmaxf(fmaxf(d[0], d[1]), fmaxf(d[2], d[3])));
-  // exact min / max lie within E of mn / mx
+// Scale and zero of a group whose exact min and max lie within E of mn and mx:
+// true when both fp16 roundings are certain (p then holds them, as qparams_df
+// would compute them from the exact values); p is filled either way.
+__device__ __forceinline__ bool qparams_certain(float mn, float mx, float E, float clip, QParams& p) {
   const float lo = __fmul_rn(clip, mn), hi = __fmul_rn(clip, mx);
   const float elo = __fmaf_rn(clip, E, fabsf(lo) * P2_M22);
   const float ehi = __fmaf_rn(clip, E, fabsf(hi) * P2_M22);
@@ -369,15 +444,32 @@ __device__ __forceinline__ bool quantize_warp_certain(const float d[4], float E,
   p.t05 = 0.5f * p.s;
   p.t15 = 1.5f * p.s;
   p.t25 = 2.5f * p.s;
+  return ok;
+}
+
+// Code of d (|d - x| <= E) under p; `certain` is cleared when x could take another code.
+__device__ __forceinline__ unsigned qcode_certain(float d, float E, const QParams& p, bool& certain) {
+  const float dz = __fsub_rn(d, p.z);
+  const float eb = __fmaf_rn(fabsf(d) + fabsf(dz), P2_M22, E);
+  certain = fabsf(__fsub_rn(dz, p.t05)) > eb && fabsf(__fsub_rn(dz, p.t15)) > eb && fabsf(__fsub_rn(dz, p.t25)) > eb;
+  return (dz > p.t05 ? 1u : 0u) + (dz > p.t15 ? 1u : 0u) + (dz > p.t25 ? 1u : 0u);
+}
+
+// Group decision from d (|d_i - x_i| <= E for every channel of the warp).
+// Returns false (warp-uniform) when some decision is not certain.
+__device__ __forceinline__ bool quantize_warp_certain(const float d[4], float E, float clip, QParams& p,
+                                                      unsigned& byte) {
+  const float mn = warp_min(fminf(fminf(d[0], d[1]), fminf(d[2], d[3])));
+  const float mx = warp_max(fmaxf(fmaxf(d[0], d[1]), fmaxf(d[2], d[3])));
+  // exact min / max lie within E of mn / mx
+  bool ok = qparams_certain(mn, mx, E, clip, p);
   byte = 0u;
   if (p.s > 0.f) {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const float dz = __fsub_rn(d[i], p.z);
-      const float eb = __fmaf_rn(fabsf(d[i]) + fabsf(dz), P2_M22, E);
-      ok = ok && fabsf(__fsub_rn(dz, p.t05)) > eb && fabsf(__fsub_rn(dz, p.t15)) > eb &&
-           fabsf(__fsub_rn(dz, p.t25)) > eb;
-      const unsigned c = (dz > p.t05 ? 1u : 0u) + (dz > p.t15 ? 1u : 0u) + (dz > p.t25 ? 1u : 0u);
+      bool c_ok;
+      const unsigned c = qcode_certain(d[i], E, p, c_ok);
+      ok = ok && c_ok;
       byte |= c << (2 * i);
     }
   }

@@ -113,32 +113,6 @@ cudaError_t launch_rotate_heads(int n_rows, int n_heads, int heads_per_rot, cons
 }
 
 // ---------------------------------------------------------------------------
-// Token -> (sequence, position, physical page, slot) with bounds checks.
-// Returns false (and flags) when the token must be skipped.
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool locate(int t, int n_seqs, const int32_t* cu_new,
-                                       const int32_t* start_pos, const int32_t* table,
-                                       const PageGeom& g, unsigned* err, long long* rec_index,
-                                       int* slot, int head) {
-  int lo = 0, hi = n_seqs - 1;
-  while (lo < hi) {  // largest b with cu_new[b] <= t
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(cu_new + mid) <= t) lo = mid; else hi = mid - 1;
-  }
-  int b = lo;
-  int base = __ldg(cu_new + b);
-  if (t < base || t >= __ldg(cu_new + b + 1)) { flag_error(err, ERR_SEQ_RANGE); return false; }
-  long long pos = (long long)__ldg(start_pos + b) + (t - base);
-  long long page = pos / g.page_tokens;
-  if (pos < 0 || page >= g.max_blocks) { flag_error(err, ERR_POS_RANGE); return false; }
-  int blk = __ldg(table + (size_t)b * g.max_blocks + page);
-  if (blk < 0 || blk >= g.num_blocks) { flag_error(err, ERR_BLOCK_RANGE); return false; }
-  *rec_index = (long long)blk * g.n_kv_heads + head;
-  *slot = (int)(pos % g.page_tokens);
-  return true;
-}
-
-// ---------------------------------------------------------------------------
 // Cache write: one warp per (token, head) group.  Lane l owns channels 4l..4l+3
 // and hence byte l of the packed group.  x = k R - mu R is formed in
 // double-float (Eq. 20 with the rotation's rounding errors carried), so the
@@ -182,17 +156,6 @@ __device__ __forceinline__ void dense_rotate_df_smem(DF x[4], const float4* __re
     x[i] = df_add(a, b);
   }
 }
-
-struct AppendRole {
-  const void* src;
-  RotDev rot;
-  const float* mu_rot;
-  float clip;
-  int codes_off, meta_off;
-};
-struct AppendRoles {
-  AppendRole r[2];
-};
 
 template <bool DENSE>
 __global__ void __launch_bounds__(256, 1) append_kernel(
@@ -331,37 +294,6 @@ constexpr int AF_TOK = 32;
 constexpr int AF_THREADS = 256;
 constexpr int AF_MAX_HEADS = 192;  // shared-memory staging: 1,156 bytes per head
 constexpr int AF_LPG = 8;          // lanes per group
-
-__device__ __forceinline__ uint64_t f2pk(float a, float b) {
-  uint64_t r;
-  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
-  return r;
-}
-__device__ __forceinline__ float2 f2up(uint64_t p) {
-  float2 r;
-  asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(p));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
-  uint64_t r;
-  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
-  return r;
-}
-__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
-  uint64_t r;
-  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-  return r;
-}
 
 template <int LPG>  // lanes per group: 8 (16 channels each) or 4 (32)
 __global__ void __launch_bounds__(AF_THREADS, 4) append_fast_kernel(
@@ -826,7 +758,10 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
         g, n_seqs, n_new, tb, dtype, cu_new, start_pos, table, roles, pool, err);
     return cudaGetLastError();
   }
+  // chunks beyond a decode step: the tensor-core kernel (the fp32 FMA kernel for unaligned inputs)
+  const bool tc = append_dense_tc_supported(dtype, k, v, pool);
   if (kd && vd) {
+    if (tc) return launch_append_dense_tc(g, n_seqs, n_new, dtype, cu_new, start_pos, table, roles, 2, pool, err, s);
     append_kernel<true><<<dim3(grid.x, grid.y, 2), 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table,
                                                                      roles, pool, err);
     return cudaGetLastError();
@@ -844,7 +779,10 @@ cudaError_t launch_quantize_append(const PageGeom& g, int n_seqs, int n_new, con
                                         g.n_kv_heads, 1),
                                    256, 0, s>>>(g, n_seqs, n_new, dense_step_tokens(n_new, g.n_kv_heads, 1), dtype,
                                                 cu_new, start_pos, table, one, pool, err);
-      else
+      else if (tc) {
+        e = launch_append_dense_tc(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, 1, pool, err, s);
+        if (e != cudaSuccess) return e;
+      } else
         append_kernel<true><<<grid, 256, smem, s>>>(g, n_seqs, n_new, dtype, cu_new, start_pos, table, one, pool, err);
       e = cudaGetLastError();
     } else {

@@ -151,3 +151,63 @@ def test_exact_ties_and_near_ties_match_the_oracle():
         assert np.array_equal(got_m[..., 0], oracle.quant.fp16_bits(s)), which
         assert np.array_equal(got_m[..., 1], oracle.quant.fp16_bits(z)), which
         assert np.array_equal(got_c, codes), (which, int((got_c != codes).sum()))
+
+
+def _signed_permutations(rng, n_heads):
+    """Dense R that are signed permutation matrices: x R is exact in any arithmetic."""
+    r = np.zeros((n_heads, 128, 128), np.float32)
+    for h in range(n_heads):
+        r[h, np.arange(128), rng.permutation(128)] = rng.choice([-1.0, 1.0], 128)
+    return r
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_dense_bulk_append_exact_on_ties(dtype):
+    """More than 128 new tokens with dense R: the tensor-core cache write.  With
+    signed-permutation R the rotated values are exact, and the groups sit on and
+    next to the code and fp16 rounding boundaries, so most groups leave the fp32
+    decision uncertain: scale, zero and codes then come from double-float values
+    of the uncertain elements and must equal the fp64 oracle's bit for bit (ties
+    to even).  300 tokens: two full tiles and a ragged one."""
+    import oracle
+    torch = gu.torch_cuda()
+    kvq = gu.kvq_lib()
+    rng = np.random.default_rng(3141)
+    n_tok, hkv, page = 300, 2, 16
+    k = _tie_groups(rng, n_tok, hkv)
+    v = _tie_groups(rng, n_tok, hkv)
+    if dtype == "bf16":
+        k, v = W.round_bf16(k), W.round_bf16(v)
+    rk, rv = _signed_permutations(rng, hkv), _signed_permutations(rng, hkv)
+    nb = (n_tok + page - 1) // page
+    lay = kvq.make_layout(page, hkv, hkv, nb, nb)
+    pool = torch.zeros(kvq.kvq_pool_bytes(lay), dtype=torch.uint8, device="cuda")
+    dk = kvq.DeviceRot("dense", dense=gu.dev(rk))
+    dv = kvq.DeviceRot("dense", dense=gu.dev(rv))
+    kvq.kvq_quantize_append(lay, gu.dev(k, dtype), gu.dev(v, dtype), gu.dev_i32([0, n_tok]), gu.dev_i32([0]),
+                            gu.dev_i32(np.arange(nb)[None, :]), dk, dv, None, 1.0, 0.9, pool)
+    kvq.kvq_device_check()
+    gpool = pool.cpu().numpy()
+    for which, x, r, clip in (("k", k, rk, 1.0), ("v", v, rv, 0.9)):
+        y = np.einsum("thc,hcd->thd", x.astype(np.float64), r.astype(np.float64))
+        codes, s, z = oracle.quant.quantize_groups(y, clip)
+        got_c, got_m = gu.seq_codes_meta(gpool, hkv, page, np.arange(nb), n_tok, which)
+        assert np.array_equal(got_m[..., 0], oracle.quant.fp16_bits(s)), which
+        assert np.array_equal(got_m[..., 1], oracle.quant.fp16_bits(z)), which
+        assert np.array_equal(got_c, codes), (which, int((got_c != codes).sum()))
+
+
+def test_dense_keys_hadamard_values_bulk_append():
+    """Dense R_K with signed-Hadamard R_V in one call of more than 128 tokens: the
+    tensor-core kernel takes the keys alone, the Walsh-Hadamard kernel the values."""
+    case = W.decode_case(16, [200, 97], 4, 2, 256, "dense", "bf16", page_tokens=8, clip_k=0.95, clip_v=0.9,
+                         spare_blocks=2, n_cal=256)
+    case.rot_v = W.make_rot("signed_hadamard", 16, 7, case.n_kv_heads)
+    g = gu.GpuCase(case)
+    pool = g.new_pool()
+    g.gpu_append_all(pool)
+    g.kvq.kvq_device_check()
+    ora_pool, encs = g.oracle_pool()
+    stats = gu.compare_codes(pool.cpu().numpy(), ora_pool, case.n_kv_heads, 8, case.block_table, g.lengths, encs,
+                             (case.clip_k, case.clip_v), label="dense K / Hadamard V")
+    assert stats["mismatch"] == 0 and stats["meta_mismatch_groups"] == 0, stats
