@@ -7,11 +7,12 @@
 // exact decisions are those of quant_common.cuh (Eq. 4, group 128, fp16 scale
 // and zero).
 //
-// Arithmetic.  Every fp32 R splits exactly into three bf16 limbs,
+// Arithmetic.  Every fp32 R with |R| >= 2^-100 splits exactly into three bf16 limbs,
 //   R = hi + mid + lo, hi = bf16(R), mid = bf16(R - hi), lo = R - hi - mid
 // (round to nearest: |mid| <= 2^-8 |R|, and R - hi - mid has at most 8
 // significant bits, so lo holds it exactly; (lo + mid) + hi gives R back in fp32
-// without rounding).  fp32 inputs x split the same way; bf16 inputs are one limb.
+// without rounding); smaller values are split with an error of at most 2^-134.  fp32
+// inputs x split the same way; bf16 inputs are one limb.
 // The tensor cores take bf16 x bf16 products (exact in fp32) into fp32
 // accumulators in tensor memory.  Their accumulation order and rounding are not
 // documented, so the error bound charges every 128 x 128 x 16 MMA
@@ -26,7 +27,7 @@
 // sum, and (fp32 input) the three dropped limb products of order 2^-24, the
 // rotated value is within 210 u sum_c |x_c| |R_cd| <= 210 u ||x|| ||R_:,d|| of
 // x R (Cauchy-Schwarz), plus 1e-30 for products that could be flushed as
-// subnormals.
+// subnormals and for the split of values below 2^-100.
 //
 // Decisions.  One thread owns one token's group (an accumulator row) and half of
 // its 128 columns (the two warps of a tensor-memory lane quarter share a row).
