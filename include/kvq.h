@@ -354,7 +354,7 @@ kvq_status kvq_pack_wo(int d_model, int k_dim, const void* w, void* w_packed, kv
 kvq_status kvq_out_proj_packed(int n_rows, int d_model, int k_dim, const float* x, const void* w_packed, float* y,
                                kvq_stream stream);
 
-/* Workspace bytes for kvq_calib_nmse. *//* Workspace bytes for kvq_calib_nmse. */
+/* Workspace bytes for kvq_calib_nmse. */
 kvq_status kvq_calib_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int gqa, int joint,
                                     size_t* bytes);
 
@@ -376,7 +376,12 @@ kvq_status kvq_calib_workspace_size(int n_tok, int n_qpos, int n_kv_heads, int g
  *   mu: float [n_kv_heads][128] or NULL
  *   nmse: double [n_cand][n_clip][joint ? 1 : n_kv_heads]; ref: double [joint ? 1 : n_kv_heads]
  *   workspace: >= kvq_calib_workspace_size bytes.
- * Selection (argmin) is left to the caller. */
+ * The quantizer's decisions are exact (double-float rotation, as the cache write); each
+ * candidate's attention is computed by the decode kernels over a page pool of the
+ * quantized trace, one sequence per query position (its causal prefix), so it is scored
+ * with the arithmetic the cache is read with; the reference attention runs in fp32.
+ * gqa must be 1, 2, 4 or 8.  Out-of-range data found on the device sets the error word
+ * (kvq_device_check).  Selection (argmin) is left to the caller. */
 kvq_status kvq_calib_nmse(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model,
                           const void* q, const void* k, const void* v, kvq_dtype dtype,
                           const void* w_o, kvq_dtype w_dtype, int n_cand, const kvq_rot* cand,

@@ -589,8 +589,10 @@ kvq_status kvq_calib_nmse(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_
   if (mu && !aligned16(mu)) return fail(KVQ_EINVAL, "mu is not 16-byte aligned");
   const size_t need = kvq::calib_workspace_bytes(n_tok, n_qpos, n_kv_heads, gqa, joint ? 1 : 0);
   if (workspace_bytes < need) return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
   cudaError_t e = kvq::launch_calib(n_tok, n_qpos, n_kv_heads, gqa, d_model, q, k, v, dtype, w_o, w_dtype,
-                                    n_cand, cand, n_clip, clips, mu, joint ? 1 : 0, nmse, ref, workspace,
+                                    n_cand, cand, n_clip, clips, mu, joint ? 1 : 0, nmse, ref, workspace, err,
                                     stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_calib_nmse");
 }

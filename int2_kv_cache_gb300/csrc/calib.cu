@@ -20,6 +20,13 @@ struct CalibWs {
   float *qf, *qr, *kf, *vf, *xk_hi, *xk_lo, *xv_hi, *xv_lo, *kq, *vq, *o_rot, *o_ref, *o_un, *gram, *part;
   double* gpart;  // [n_groups][(gd / 32)^2] quadratic-form partials
   double* qsum;   // [5][H_q] per-query-head sums of the error report
+  // the sweep's quantized trace as a page pool read by the decode kernels: one
+  // "sequence" per calibration position i (the causal prefix of n_tok - n_qpos + i + 1
+  // tokens), every sequence's block-table row pointing at the same pages
+  uint8_t* pool;
+  int32_t *table, *lens;
+  void* dws;  // decode workspace
+  int n_ctas;
 };
 
 constexpr int CA_SPLIT_MAX = 8;  // key splits of the calibration attention
@@ -35,18 +42,34 @@ static CalibWs carve(void* ws, int n_tok, int n_qpos, int n_kv_heads, int gqa, i
   const size_t gn = (size_t)n_groups * gd * gd;
   const size_t pn = (size_t)CA_SPLIT_MAX * n_qpos * hq * (D + 4);  // attention partials
   const size_t gpn = 2 * (size_t)n_groups * (gd / 32) * (gd / 32);  // doubles, as float pairs
-  const size_t sizes[17] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn, pn, gpn, 2 * 5 * hq};
+  const int n_blk = (n_tok + CALIB_PAGE - 1) / CALIB_PAGE;
+  const int n_ctas = decode_auto_ctas(n_qpos, n_kv_heads, gqa, n_tok);
+  // the pool, block table, lengths and decode workspace, in bytes / 4
+  const size_t pooln = (size_t)n_blk * n_kv_heads * 72 * CALIB_PAGE / 4, tabn = (size_t)n_qpos * n_blk;
+  const size_t dwn = (decode_workspace_bytes(n_qpos, n_kv_heads, gqa, n_ctas) + 3) / 4;
+  const size_t sizes[21] = {qn, qn, kn, kn, kn, kn, kn, kn, kn, kn, qn, qn, qn, gn, pn, gpn, 2 * 5 * hq,
+                            pooln, tabn, (size_t)n_qpos, dwn};
   char* p = static_cast<char*>(ws);
-  float* ptrs[17];
+  float* ptrs[21];
   size_t off = 0;
-  for (int i = 0; i < 17; ++i) {
+  for (int i = 0; i < 21; ++i) {
     ptrs[i] = reinterpret_cast<float*>(p + off);
     off += align_up(sizes[i] * sizeof(float));
   }
   if (total) *total = off;
   return CalibWs{ptrs[0], ptrs[1], ptrs[2], ptrs[3], ptrs[4], ptrs[5], ptrs[6], ptrs[7],
                  ptrs[8], ptrs[9], ptrs[10], ptrs[11], ptrs[12], ptrs[13], ptrs[14],
-                 reinterpret_cast<double*>(ptrs[15]), reinterpret_cast<double*>(ptrs[16])};
+                 reinterpret_cast<double*>(ptrs[15]), reinterpret_cast<double*>(ptrs[16]),
+                 reinterpret_cast<uint8_t*>(ptrs[17]), reinterpret_cast<int32_t*>(ptrs[18]),
+                 reinterpret_cast<int32_t*>(ptrs[19]), ptrs[20], n_ctas};
+}
+
+// Block table (every row 0 .. n_blk - 1) and prefix lengths of the sweep's decode.
+__global__ void calib_pages_kernel(int n_qpos, int n_tok, int n_blk, int32_t* __restrict__ table,
+                                   int32_t* __restrict__ lens) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i < n_qpos * n_blk) table[i] = i % n_blk;
+  if (i < n_qpos) lens[i] = n_tok - n_qpos + i + 1;
 }
 
 static int calib_groups(int n_kv_heads, int joint) { return joint ? 1 : n_kv_heads; }
@@ -483,7 +506,7 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
                          const void* q, const void* k, const void* v, int dtype, const void* w_o,
                          int w_dtype, int n_cand, const kvq_rot* cand, int n_clip,
                          const float* clips, const float* mu, int joint, double* nmse,
-                         double* ref, void* ws, cudaStream_t s) {
+                         double* ref, void* ws, unsigned* err, cudaStream_t s) {
   const int hq = n_kv_heads * gqa;
   const int n_groups = calib_groups(n_kv_heads, joint);
   const int gd = calib_gd(n_kv_heads, gqa, joint);
@@ -517,16 +540,28 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
   };
   out_err(w.o_ref, nullptr, ref);
   KVQ_TRY(cudaSuccess);
+  // the quantized trace is read by the decode kernels: pages of CALIB_PAGE tokens, one
+  // decode "sequence" per calibration position (its causal prefix), all sharing the pages
+  const int n_blk = (n_tok + CALIB_PAGE - 1) / CALIB_PAGE;
+  const PageGeom pg{CALIB_PAGE, n_kv_heads, n_blk, n_blk, 72 * CALIB_PAGE};
+  KVQ_TRY(cudaMemsetAsync(w.pool, 0, (size_t)n_blk * n_kv_heads * 72 * CALIB_PAGE, s));
+  calib_pages_kernel<<<(unsigned)(((long long)n_qpos * n_blk + 255) / 256), 256, 0, s>>>(n_qpos, n_tok, n_blk, w.table,
+                                                                                        w.lens);
+  KVQ_TRY(cudaSuccess);
   for (int i = 0; i < n_cand; ++i) {
     const RotDev r = to_dev(cand[i]);
-    // keys centred (OptR §4.1; attention-equivalent) then rotated; values rotated
+    // keys centred (OptR §4.1; attention-equivalent) then rotated, values rotated: (k - mu) R
+    // in double-float, so the decisions are those of the exact centred values
     KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, k, dtype, mu, r, w.xk_hi, w.xk_lo, s));
     KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, v, dtype, nullptr, r, w.xv_hi, w.xv_lo, s));
-    KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.qf, r, w.qr, false, s));
     for (int c = 0; c < n_clip; ++c) {
-      KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clips[c], w.kq, s));
-      KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clips[c], w.vq, s));
-      KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qr, w.kq, w.vq, w.o_rot, w.part, s));
+      // exact group decisions into the pool, then the decode of every prefix with the
+      // candidate's query rotation (the cache path's own kernels: tensor-core contractions
+      // on the 2-bit codes); o_rot in the rotated value basis
+      KVQ_TRY(launch_quant_to_pool(n_tok, n_kv_heads, w.xk_hi, w.xk_lo, clips[c], 0, w.pool, s));
+      KVQ_TRY(launch_quant_to_pool(n_tok, n_kv_heads, w.xv_hi, w.xv_lo, clips[c], 1, w.pool, s));
+      KVQ_TRY(launch_decode(pg, hq, n_qpos, w.qf, KVQ_F32, w.lens, n_tok, w.table, r, w.pool, w.n_ctas, w.dws, w.o_rot,
+                            err, s));
       KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.o_rot, r, w.o_un, true, s));
       double* slot = nmse + (size_t)(i * n_clip + c) * n_groups;
       out_err(w.o_un, w.o_ref, slot);

@@ -137,6 +137,10 @@ cudaError_t launch_rotate_df(int n_rows, int n_heads, const void* src, int dtype
                              RotDev rot, float* x_hi, float* x_lo, cudaStream_t s);
 cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x_lo, float clip,
                                  float* out, cudaStream_t s);
+// The calibration's private page pool: 16-token pages, records as the decode reads them.
+constexpr int CALIB_PAGE = 16;
+cudaError_t launch_quant_to_pool(int n_tok, int n_kv_heads, const float* x_hi, const float* x_lo, float clip,
+                                 int role, uint8_t* pool, cudaStream_t s);
 
 // window.cu
 cudaError_t launch_window_append(int n_kv_heads, int n_seqs, int n_new, const void* k, const void* v,
@@ -192,6 +196,6 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
                          const void* q, const void* k, const void* v, int dtype, const void* w_o,
                          int w_dtype, int n_cand, const kvq_rot* cand, int n_clip,
                          const float* clips, const float* mu, int joint, double* nmse,
-                         double* ref, void* ws, cudaStream_t s);
+                         double* ref, void* ws, unsigned* err, cudaStream_t s);
 
 }  // namespace kvq

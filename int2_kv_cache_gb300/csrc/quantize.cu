@@ -854,4 +854,35 @@ cudaError_t launch_quant_dequant(int n_groups, const float* x_hi, const float* x
   return cudaGetLastError();
 }
 
+// quant_to_pool: the same exact group decisions as quant_dequant, packed into the
+// records of a private page pool (16-token pages, page t / 16 of the head's record
+// row, slot t % 16; role 0 keys, 1 values) instead of dequantized.  One warp per group.
+__global__ void quant_pool_df_kernel(int n_groups, int n_kv_heads, const float* __restrict__ x_hi,
+                                     const float* __restrict__ x_lo, float clip, int role, uint8_t* __restrict__ pool) {
+  constexpr int P = CALIB_PAGE;
+  const int gi = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (gi >= n_groups) return;
+  const float4 a = reinterpret_cast<const float4*>(x_hi + (size_t)gi * D)[lane];
+  const float4 b = reinterpret_cast<const float4*>(x_lo + (size_t)gi * D)[lane];
+  const DF x[4] = {{a.x, b.x}, {a.y, b.y}, {a.z, b.z}, {a.w, b.w}};
+  QParams qp;
+  const unsigned byte = quantize_warp_df(x, clip, qp);
+  const int t = gi / n_kv_heads, h = gi % n_kv_heads;
+  uint8_t* rec = pool + ((size_t)(t / P) * n_kv_heads + h) * (72 * P);
+  rec[(role ? 32 * P : 0) + GROUP_BYTES * (t % P) + lane] = (uint8_t)byte;
+  if (lane == 0)
+    *reinterpret_cast<uint32_t*>(rec + (role ? 68 * P : 64 * P) + META_BYTES * (t % P)) =
+        (uint32_t)qp.s_bits | ((uint32_t)qp.z_bits << 16);
+}
+
+cudaError_t launch_quant_to_pool(int n_tok, int n_kv_heads, const float* x_hi, const float* x_lo, float clip,
+                                 int role, uint8_t* pool, cudaStream_t s) {
+  const long long n_groups = (long long)n_tok * n_kv_heads;
+  if (n_groups == 0) return cudaSuccess;
+  quant_pool_df_kernel<<<(unsigned)((n_groups * 32 + 255) / 256), 256, 0, s>>>((int)n_groups, n_kv_heads, x_hi, x_lo,
+                                                                                 clip, role, pool);
+  return cudaGetLastError();
+}
+
 }  // namespace kvq
