@@ -283,6 +283,13 @@ class DecodeStep:
             views.append(self.dev_in[o:o + x.size].view(x.shape))
             o += x.size
         self.q, self.k_new, self.v_new = views
+        # the same inputs as views of the pinned host buffer: the end-to-end steps hand these
+        # host pointers to the API (the query preparation reads them over the host link)
+        hv, o = [], 0
+        for x in parts:
+            hv.append(self.host_in[o:o + x.size].view(x.shape))
+            o += x.size
+        self.host_q, self.host_k_new, self.host_v_new = hv
         self.cu_new = t(np.arange(n_seqs + 1), torch.int32)
         self.start = t(lens - 1, torch.int32)
         self.lens = t(lens, torch.int32)
@@ -304,27 +311,31 @@ class DecodeStep:
         per = self.kvq.Window.buffer_bytes(1, self.case.n_kv_heads, w.sink_tokens, w.recent_tokens)
         return self.kvq.Window(w.sink_tokens, w.recent_tokens, w.buf[b * per:(b + 1) * per])
 
-    def step(self, ev=None):
+    def step(self, ev=None, host_io=False):
         """One decode step: kvq_decode_step (the new token's append fused into the decode
         call; with windows kvq_decode_step_win, which also writes its window copy) and the
         W_O projection.  ev: events [4] recorded before the step, before the decode call
-        (the same point), after it and after the projection."""
+        (the same point), after it and after the projection.  host_io: read q and the new
+        K/V from the pinned host buffer and write y into pinned host memory (the kernels
+        move the bytes over the host link themselves)."""
         kvq = self.kvq
         c = self.case
+        q, k_new, v_new, y = ((self.host_q, self.host_k_new, self.host_v_new, self.host_y) if host_io
+                              else (self.q, self.k_new, self.v_new, self.y))
         if ev is not None:
             ev[0].record()
             ev[1].record()
         if self.win is None:
-            kvq.kvq_decode_step(self.layout, self.q, self.k_new, self.v_new, self.lens, self.L, self.table, self.rot_k,
+            kvq.kvq_decode_step(self.layout, q, k_new, v_new, self.lens, self.L, self.table, self.rot_k,
                                 self.rot_v, self.mu_rot, c.clip_k, c.clip_v, self.pool, self.ws, self.o,
                                 n_splits=self.splits)
         else:
-            kvq.kvq_decode_step_win(self.layout, self.q, self.k_new, self.v_new, self.lens, self.L, self.table,
+            kvq.kvq_decode_step_win(self.layout, q, k_new, v_new, self.lens, self.L, self.table,
                                     self.rot_k, self.rot_v, self.mu_rot, self.mu, c.clip_k, c.clip_v, self.pool,
                                     self.win, self.ws, self.o, n_splits=self.splits)
         if ev is not None:
             ev[2].record()
-        kvq.kvq_out_proj_packed(self.o.reshape(self.B, -1), self.w_pack, self.y, self.dm)
+        kvq.kvq_out_proj_packed(self.o.reshape(self.B, -1), self.w_pack, y, self.dm)
         if ev is not None:
             ev[3].record()
 
@@ -336,9 +347,10 @@ class DecodeStep:
         ev[1].record()
 
     def step_e2e(self):
-        self.dev_in.copy_(self.host_in, non_blocking=True)
-        self.step()
-        self.host_y.copy_(self.y, non_blocking=True)
+        """A step whose inputs are in pinned host memory and whose output goes there: the
+        API gets the host pointers, so the query preparation reads q and the new K/V, and
+        the projection writes y, across the host link inside the step (no staging copies)."""
+        self.step(host_io=True)
 
     def decode_bytes(self) -> dict:
         B, hq, hkv = self.B, self.hq, self.hkv
@@ -509,7 +521,9 @@ def run_gpu(args):
                      "traffic": traffic, "algorithmic_bytes": alg, "bytes": by},
         "e2e": {"value": world * w.B / (e2e_step * 1e-3), "unit": "tokens/s",
                 "h2d_bytes_per_step": int(w.host_in.numel() * 2),
-                "d2h_bytes_per_step": int(w.host_y.numel() * 4)},
+                "d2h_bytes_per_step": int(w.host_y.numel() * 4),
+                "transfer": "q and the new K/V read from pinned host memory by the query preparation, y written "
+                            "to pinned host memory by the projection (host pointers through the C ABI)"},
         "gpu_launches": w.launches_per_step * args.steps * len(block_ms),
         "clocks": clk,
     }

@@ -195,3 +195,41 @@ def test_step_with_several_sequences_per_query_block_and_near_ties():
     ref = g.oracle_decode(ora_pool, case.queries())
     for b in range(case.n_seqs):
         assert gu.out_err(got[b], ref[b]) <= gu.OUT_TOL, (b, gu.out_err(got[b], ref[b]))
+
+
+def test_step_and_projection_with_pinned_host_buffers():
+    """The C-ABI takes plain pointers: q and the new K/V in pinned host memory (read by the
+    query preparation over the host link) and y in pinned host memory (written by the
+    projection) give the same pool, o_rot and y as device buffers, bit for bit."""
+    lengths, hq, hkv, d_model = [700, 33, 1, 2048], 8, 2, 256
+    case = W.decode_case(63, lengths, hq, hkv, d_model, "dense", "bf16", page_tokens=16, clip_k=0.96, clip_v=0.92,
+                         spare_blocks=2, n_cal=256)
+    g = gu.GpuCase(case)
+    kvq, torch = g.kvq, g.torch
+    pool_a, k_new, v_new = _inputs(g)
+    pool_b = pool_a.clone()
+    max_len = int(g.lengths.max())
+    q_np = case.queries()
+    q, kn, vn = gu.dev(q_np, "bf16"), gu.dev(k_new, "bf16"), gu.dev(v_new, "bf16")
+    qh, knh, vnh = q.cpu().pin_memory(), kn.cpu().pin_memory(), vn.cpu().pin_memory()
+    lens = gu.dev_i32(g.lengths)
+    ws = torch.empty(max(kvq.kvq_decode_workspace_size(g.layout, case.n_seqs, max_len), 16), dtype=torch.uint8,
+                     device="cuda")
+    w = gu.dev(case.w_o(), "bf16")
+    wp = torch.empty(kvq.kvq_wo_packed_bytes(d_model, hq * 128), dtype=torch.uint8, device="cuda")
+    kvq.kvq_pack_wo(w, wp)
+    o_a = torch.full((case.n_seqs, hq, 128), float("nan"), device="cuda")
+    y_a = torch.full((case.n_seqs, d_model), float("nan"), device="cuda")
+    kvq.kvq_decode_step(g.layout, q, kn, vn, lens, max_len, g.table, g.rot_k, g.rot_v, g.mu_rot_dev, case.clip_k,
+                        case.clip_v, pool_a, ws, o_a)
+    kvq.kvq_out_proj_packed(o_a.reshape(case.n_seqs, -1), wp, y_a, d_model)
+    o_b = torch.full_like(o_a, float("nan"))
+    y_b = torch.full((case.n_seqs, d_model), float("nan")).pin_memory()
+    kvq.kvq_decode_step(g.layout, qh, knh, vnh, lens, max_len, g.table, g.rot_k, g.rot_v, g.mu_rot_dev, case.clip_k,
+                        case.clip_v, pool_b, ws, o_b)
+    kvq.kvq_out_proj_packed(o_b.reshape(case.n_seqs, -1), wp, y_b, d_model)
+    torch.cuda.synchronize()
+    kvq.kvq_device_check()
+    assert torch.equal(pool_a, pool_b)
+    assert torch.equal(o_a, o_b)
+    assert torch.equal(y_a.cpu(), y_b)
