@@ -20,7 +20,11 @@
  *   - All tensor pointers are DEVICE pointers owned by the caller unless the
  *     argument says "host".  The library never allocates device memory; calls
  *     that need scratch take a caller-provided workspace sized by the matching
- *     *_workspace_size function.
+ *     *_workspace_size function.  Exception: the per-step activations may be
+ *     pinned (page-locked, device-mapped) host memory - q, k_new and v_new of
+ *     kvq_decode_attention(_win) and kvq_decode_step(_win), and y of
+ *     kvq_out_proj_packed - which the kernels then read or write across the
+ *     host link themselves (results identical to device buffers).
  *   - Every call is asynchronous on `stream` (NULL = the legacy default stream)
  *     and performs no implicit synchronisation, except kvq_device_check.
  *   - Every tensor is dense, row-major, with the shapes given below.  Pointers
