@@ -233,3 +233,9 @@ def test_step_and_projection_with_pinned_host_buffers():
     assert torch.equal(pool_a, pool_b)
     assert torch.equal(o_a, o_b)
     assert torch.equal(y_a.cpu(), y_b)
+    # the decode alone with the query in host memory
+    o_c, o_d = torch.full_like(o_a, float("nan")), torch.full_like(o_a, float("nan"))
+    kvq.kvq_decode_attention(g.layout, q, lens, max_len, g.table, g.rot_k, pool_a, ws, o_c)
+    kvq.kvq_decode_attention(g.layout, qh, lens, max_len, g.table, g.rot_k, pool_a, ws, o_d)
+    torch.cuda.synchronize()
+    assert torch.equal(o_c, o_d)
