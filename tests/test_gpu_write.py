@@ -70,8 +70,10 @@ def test_identity_rotation_equals_plain_int2_on_gpu():
     assert np.array_equal(mk[..., 0], oracle.quant.fp16_bits(s)) and np.array_equal(mk[..., 1], oracle.quant.fp16_bits(z))
 
 
-def test_out_of_range_block_is_skipped_and_flagged():
-    case = W.decode_case(14, [40], 2, 2, 128, "signed_hadamard", "f32", page_tokens=16, spare_blocks=1)
+@pytest.mark.parametrize("rot,n_tok", [("signed_hadamard", 40), ("dense", 300)])
+def test_out_of_range_block_is_skipped_and_flagged(rot, n_tok):
+    # dense with 300 tokens: the tensor-core cache write locates the tokens of its tiles
+    case = W.decode_case(14, [n_tok], 2, 2, 128, rot, "f32", page_tokens=16, spare_blocks=1)
     case.block_table[0, 1] = case.num_blocks + 5  # page 1 points outside the pool
     g = gu.GpuCase(case)
     pool = g.new_pool()
