@@ -10,6 +10,8 @@
 // matrix, which is exact algebra: with W_h = the W_O columns of the query
 // heads of KV head h and du = o~ - o (unrotated, concatenated over those heads),
 //   ||du W_h^T||^2 = du (W_h^T W_h) du^T.
+#include <algorithm>
+
 #include "quant_common.cuh"
 
 namespace kvq {
@@ -389,55 +391,82 @@ __global__ void __launch_bounds__(256) gram_kernel(int d_model, int total_cols, 
 // tile of M over all positions and adds G o M over the tile in double ->
 // part[group][ri * nt + ci]; gram_reduce_kernel adds the tiles in a fixed order.
 // grid = (gd / 32, gd / 32, n_groups), block = 256.
-__global__ void __launch_bounds__(256) gram_trace_kernel(int n_qpos, int n_groups, int gd,
+// trace(M du^T du) = sum_p du_p M du_p^T for one group (M = W_h^T W_h symmetric), as
+// sum_{p,c} du[p][c] Z[p][c] with Z = du M: a block takes 64 columns of Z and a K range
+// of `kspan` channels (both linear in Z, so ranges add), streams du[:, k] and M[k][c] through
+// shared memory 64 x 64 at a time, and dots its Z tile with du[:, c] in double.
+// grid = (gd / 64, ceil(gd / kspan), n_groups), block = 256 (thread: 4 x 4 of the tile).
+constexpr int GT_T = 64;
+__global__ void __launch_bounds__(256) gram_trace_kernel(int n_qpos, int n_groups, int gd, int kspan,
                                                          const float* __restrict__ a,
                                                          const float* __restrict__ b,
                                                          const float* __restrict__ gram,
                                                          double* __restrict__ part) {
-  __shared__ float sr[64][33], sc[64][33];  // du of 64 positions at the tile's rows / columns
+  __shared__ float sdu[GT_T][GT_T + 1];  // du[p0 + p][k0 + k]
+  __shared__ __align__(16) float smat[GT_T][GT_T + 4];  // M[k0 + k][c0 + c]
   __shared__ double sred[8];
-  const int ci = blockIdx.x, ri = blockIdx.y, grp = blockIdx.z, tid = threadIdx.x;
-  const int tx = tid & 31, ty = tid >> 5;  // column tx, rows ty + 8 i
-  const int r0 = 32 * ri, c0 = 32 * ci;
-  float m[4] = {0.f, 0.f, 0.f, 0.f};
-  for (int p0 = 0; p0 < n_qpos; p0 += 64) {
-    for (int i = tid; i < 64 * 32; i += 256) {
-      const int pp = i >> 5, k = i & 31, qi = p0 + pp;
-      float xr = 0.f, xc = 0.f;
-      if (qi < n_qpos) {
-        const size_t base = ((size_t)qi * n_groups + grp) * gd;
-        xr = b ? a[base + r0 + k] - b[base + r0 + k] : a[base + r0 + k];
-        xc = b ? a[base + c0 + k] - b[base + c0 + k] : a[base + c0 + k];
-      }
-      sr[pp][k] = xr;
-      sc[pp][k] = xc;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int pp = 0; pp < 64; ++pp) {
-      const float xc = sc[pp][tx];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) m[i] = fmaf(sr[pp][ty + 8 * i], xc, m[i]);
-    }
-    __syncthreads();
-  }
+  const int ct = blockIdx.x, ks = blockIdx.y, grp = blockIdx.z, tid = threadIdx.x;
+  const int tx = tid & 15, ty = tid >> 4;
+  const int c0 = GT_T * ct, kb0 = ks * kspan, kb1 = min(gd, kb0 + kspan);
+  const float* mg = gram + (size_t)grp * gd * gd;
+  auto du_at = [&](int p, int k) {
+    const size_t i = ((size_t)p * n_groups + grp) * gd + k;
+    return b ? a[i] - b[i] : a[i];
+  };
   double acc = 0.0;
+  for (int p0 = 0; p0 < n_qpos; p0 += GT_T) {
+    float z[4][4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
-    acc += (double)m[i] * (double)gram[((size_t)grp * gd + r0 + ty + 8 * i) * gd + c0 + tx];
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) z[i][j] = 0.f;
+    for (int k0 = kb0; k0 < kb1; k0 += GT_T) {
+      for (int i = tid; i < GT_T * GT_T; i += 256) {
+        const int r = i >> 6, k = i & 63;
+        sdu[r][k] = (p0 + r < n_qpos && k0 + k < kb1) ? du_at(p0 + r, k0 + k) : 0.f;
+        smat[r][k] = k0 + r < kb1 ? mg[(size_t)(k0 + r) * gd + c0 + k] : 0.f;
+      }
+      __syncthreads();
+#pragma unroll 8
+      for (int k = 0; k < GT_T; ++k) {
+        const float4 m4 = *reinterpret_cast<const float4*>(&smat[k][4 * tx]);
+        const float mv[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float d = sdu[4 * ty + i][k];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) z[i][j] = fmaf(d, mv[j], z[i][j]);
+        }
+      }
+      __syncthreads();
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int p = p0 + 4 * ty + i;
+      if (p < n_qpos)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc += (double)z[i][j] * (double)du_at(p, c0 + 4 * tx + j);
+    }
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if (tx == 0) sred[ty] = acc;
+  if ((tid & 31) == 0) sred[tid >> 5] = acc;
   __syncthreads();
   if (tid == 0) {
     double t = 0.0;
     for (int i = 0; i < 8; ++i) t += sred[i];
-    part[((size_t)grp * gridDim.y + ri) * gridDim.x + ci] = t;
+    part[((size_t)grp * gridDim.y + ks) * gridDim.x + ct] = t;
   }
 }
 
-// out[g] = sum of part[g][:] (n_tiles values): 256 strided partial sums, then a
-// fixed tree (deterministic).  One block per group.
+// K span of the trace blocks: about two blocks per SM over all groups, at least 64 channels.
+static int gram_kspan(int gd, int n_groups) {
+  const int tiles = gd / GT_T;
+  int ksplit = (2 * device_sm_count() + tiles * n_groups - 1) / (tiles * n_groups);
+  ksplit = std::max(1, std::min(ksplit, gd / GT_T));
+  return ((gd + ksplit - 1) / ksplit + GT_T - 1) / GT_T * GT_T;
+}
+
 __global__ void __launch_bounds__(256) gram_reduce_kernel(int n_tiles, const double* __restrict__ part,
                                                           double* __restrict__ out) {
   __shared__ double sh[256];
@@ -534,8 +563,10 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
       proj_err_kernel<<<dim3(n_qpos, n_groups), 256, form_smem, s>>>(n_qpos, n_groups, gd, d_model, a, b, w_o,
                                                                      w_dtype, dst);
     else {
-      gram_trace_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(n_qpos, n_groups, gd, a, b, w.gram, w.gpart);
-      gram_reduce_kernel<<<n_groups, 256, 0, s>>>((gd / 32) * (gd / 32), w.gpart, dst);
+      const int ksp = gram_kspan(gd, n_groups), nks = (gd + ksp - 1) / ksp;
+      gram_trace_kernel<<<dim3(gd / GT_T, nks, n_groups), 256, 0, s>>>(n_qpos, n_groups, gd, ksp, a, b, w.gram,
+                                                                       w.gpart);
+      gram_reduce_kernel<<<n_groups, 256, 0, s>>>((gd / GT_T) * nks, w.gpart, dst);
     }
   };
   out_err(w.o_ref, nullptr, ref);
@@ -619,8 +650,10 @@ cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, i
       proj_err_kernel<<<dim3(n_qpos, n_groups), 256, (size_t)gd * sizeof(float), s>>>(n_qpos, n_groups, gd, d_model,
                                                                                    a, b, w_o, w_dtype, dst);
     else {
-      gram_trace_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(n_qpos, n_groups, gd, a, b, w.gram, w.gpart);
-      gram_reduce_kernel<<<n_groups, 256, 0, s>>>((gd / 32) * (gd / 32), w.gpart, dst);
+      const int ksp = gram_kspan(gd, n_groups), nks = (gd + ksp - 1) / ksp;
+      gram_trace_kernel<<<dim3(gd / GT_T, nks, n_groups), 256, 0, s>>>(n_qpos, n_groups, gd, ksp, a, b, w.gram,
+                                                                       w.gpart);
+      gram_reduce_kernel<<<n_groups, 256, 0, s>>>((gd / GT_T) * nks, w.gpart, dst);
     }
   };
   double* e_tot = w.qsum;
