@@ -529,6 +529,8 @@ def run_gpu(args):
     }
     # the prefill-chunk quantize-append (4 x 4,096 tokens, 4B-class layer), its own roofline
     line["append_chunk"] = append_chunk_measure(device, False, 50, 5, min_s=0.25)
+    # the same chunk with dense learned rotations (8B-class layer): the tensor-core cache write
+    line["append_chunk_dense"] = append_chunk_measure(device, True, 20, 3, min_s=0.25)
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w.case, budget_s=12.0)
     print(json.dumps(line), flush=True)
@@ -676,14 +678,21 @@ def append_chunk_measure(device: str, dense: bool, steps: int, warmup: int, min_
     bytes_ = n_seq * 4096 * 8 * (2 * 256 + 72) + rot_bytes + 8 * 128 * 4
     peak, kind = peaks()
     achieved = bytes_ / ms / 1e6
-    return {"workload": (f"prefill-chunk quantize-append: {n_seq} sequences x 4,096 new tokens, Hkv 8, d 128, bf16 K/V, "
-                         + ("dense expm(A-A^T) rotations, clip 1" if dense else "signed-Hadamard rotations, clip 0.9")
-                         + ", 16-token pages"),
-            "ms": ms, "tokens": n_seq * 4096, "blocks": len(blocks),
-            "l2": "inputs cycled over 3 copies (%.0f MB > 129 MB L2)" % (3 * 2 * k.numel() * 2 / 1e6),
-            "roofline": {"kernel": "kvq_quantize_append (prefill chunk)", "bound": "hbm", "achieved": achieved,
-                         "peak": peak, "peak_kind": kind, "unit": "GB/s", "frac": achieved / peak,
-                         "algorithmic_bytes": bytes_}}
+    out = {"workload": (f"prefill-chunk quantize-append: {n_seq} sequences x 4,096 new tokens, Hkv 8, d 128, bf16 K/V, "
+                        + ("dense expm(A-A^T) rotations, clip 1" if dense else "signed-Hadamard rotations, clip 0.9")
+                        + ", 16-token pages"),
+           "ms": ms, "tokens": n_seq * 4096, "blocks": len(blocks),
+           "l2": "inputs cycled over 3 copies (%.0f MB > 129 MB L2)" % (3 * 2 * k.numel() * 2 / 1e6),
+           "roofline": {"kernel": "kvq_quantize_append (prefill chunk)", "bound": "hbm", "achieved": achieved,
+                        "peak": peak, "peak_kind": kind, "unit": "GB/s", "frac": achieved / peak,
+                        "algorithmic_bytes": bytes_}}
+    if dense:
+        # the rotation x R_h on the tensor cores: one 128 x 128 x 128 product per (role, head, 128-token
+        # tile), done as three exact bf16 limb products of R (bf16 K/V are one limb)
+        flops = 2 * 8 * (n_seq * 4096) * 128 * 128 * 2
+        out["tensor"] = {"algorithmic_gflop": flops / 1e9, "limb_products": 3,
+                         "tflops_algorithmic": flops / ms / 1e9, "tflops_issued": 3 * flops / ms / 1e9}
+    return out
 
 
 def run_append_chunk(args):
