@@ -29,27 +29,31 @@
 // x R (Cauchy-Schwarz), plus 1e-30 for products that could be flushed as
 // subnormals and for the split of values below 2^-100.
 //
-// Decisions.  One thread owns one token's group (an accumulator row) and half of
-// its 128 columns (the two warps of a tensor-memory lane quarter share a row).
-// Scale and zero are taken from the fp32 min and max when certain under that
-// bound (qparams_certain); otherwise the columns that could hold the exact min or
-// max (within 2E of the fp32 extremes) are evaluated in double-float and the
-// exact min and max decide (qparams_df).  Codes are then taken in fp32 where
-// certain (qcode_certain) and from a double-float value where not (qcode_df).  A
-// double-float value x_t R_:,d - mu_d is evaluated by the whole warp (lane l
-// takes channels 4l..4l+3, from the staged bf16 limbs of x and R, exact products
-// by FMA, compensated sums, a shuffle tree), so an uncertain element costs about
-// 150 warp instructions instead of a whole group's double-float rotation.  The
-// result equals the decision on the exact x R - mu R except within ~1e-12
-// (relative) of a rounding boundary, like the double-float path elsewhere.
+// Decisions.  One thread owns a quarter of one token's group: an accumulator row
+// and 32 of its columns (the four warps of a tensor-memory lane quarter share a
+// row and meet at named barriers to combine the row's extremes).  Scale and zero
+// are taken from the fp32 min and max when certain under that bound
+// (qparams_certain), codes by the scaled distance of (y - z) / s to the nearest
+// half-integer.  Where a decision is uncertain, the elements that can decide it
+// (for scale and zero: the columns within 2E of the fp32 extremes, which hold the
+// exact arg-min and arg-max) are evaluated again by the whole warp from the staged
+// bf16 limbs of x and R (lane l takes channels 4l..4l+3): first in fp32 (an FMA
+// chain and a shuffle tree, 9 u sum_c |x_c R_cd|), then, where still uncertain, in
+// double-float (exact products by FMA, compensated sums), deciding with
+// qparams_df / qcode_df.  An uncertain element costs about 50 (fp32) or 150
+// (double-float) warp instructions instead of a whole group's double-float
+// rotation.  The result equals the decision on the exact x R - mu R except within
+// ~1e-12 (relative) of a rounding boundary, like the double-float path elsewhere.
 //
 // Schedule.  One CTA per SM (tensor memory: 512 columns), persistent over units
 // (role, KV head, 128-token tile), ordered so that consecutive units share R_h:
 //   stage R_h's limbs (B operand, [d][c], 128-byte swizzle) when the head changes;
-//   load the tile's x (A operand, [token][c]) and locate its tokens' pages;
+//   the tile's x (A operand, [token][c]): bf16 by asynchronous copies one unit
+//   ahead into a second buffer, fp32 loaded and split here; the tokens' pages located;
 //   one thread issues the 24 (bf16) or 48 (fp32) MMAs and commits them to an
-//   mbarrier; all threads wait (bounded), read the accumulators and decide.
-// grid = min(units, SMs), block = 256.
+//   mbarrier; all threads wait (bounded) and read the accumulators, after which the
+//   next unit's MMAs are issued (same head) while this unit's decisions are taken.
+// grid = min(units, SMs), block = 512.
 #include <algorithm>
 
 #include "quant_common.cuh"
