@@ -629,9 +629,11 @@ kvq_status kvq_head_error_report(int n_tok, int n_qpos, int n_kv_heads, int gqa,
   if (mu && !aligned16(mu)) return fail(KVQ_EINVAL, "mu is not 16-byte aligned");
   const size_t need = kvq::report_workspace_bytes(n_tok, n_qpos, n_kv_heads, gqa);
   if (workspace_bytes < need) return fail(KVQ_EINVAL, "workspace %zu bytes < %zu required", workspace_bytes, need);
+  unsigned* err = nullptr;
+  KVQ_CHECK(device_error_word(&err));
   cudaError_t e = kvq::launch_head_report(n_tok, n_qpos, n_kv_heads, gqa, d_model, q, k, v, dtype, w_o, w_dtype,
                                           kvq::to_dev(rot_k), kvq::to_dev(rot_v), mu, clip_k, clip_v, out,
-                                          workspace, stream);
+                                          workspace, err, stream);
   return e == cudaSuccess ? KVQ_OK : cuda_fail(e, "kvq_head_error_report");
 }
 

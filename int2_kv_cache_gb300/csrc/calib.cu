@@ -630,7 +630,7 @@ __global__ void group_sum_kernel(int n_rows, int n_groups, int per, const double
 cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model, const void* q,
                                const void* k, const void* v, int dtype, const void* w_o, int w_dtype, RotDev rot_k,
                                RotDev rot_v, const float* mu, float clip_k, float clip_v, double* out, void* ws,
-                               cudaStream_t s) {
+                               unsigned* err, cudaStream_t s) {
   const int hq = n_kv_heads * gqa;
   const int n_groups = hq, gd = D;
   CalibWs w = carve(ws, n_tok, n_qpos, n_kv_heads, gqa, n_groups, gd, nullptr);
@@ -661,18 +661,28 @@ cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, i
   double* e_val = w.qsum + 2 * hq;
   double* e_naive = w.qsum + 3 * hq;
   double* y_ref = w.qsum + 4 * hq;
+  // the passes with INT2 keys and values read a page pool of the quantized trace with the
+  // decode kernels (one sequence per position, as in the sweep)
+  const int n_blk = (n_tok + CALIB_PAGE - 1) / CALIB_PAGE;
+  const PageGeom pg{CALIB_PAGE, n_kv_heads, n_blk, n_blk, 72 * CALIB_PAGE};
+  KVQ_TRY(cudaMemsetAsync(w.pool, 0, (size_t)n_blk * n_kv_heads * 72 * CALIB_PAGE, s));
+  calib_pages_kernel<<<(unsigned)(((long long)n_qpos * n_blk + 255) / 256), 256, 0, s>>>(n_qpos, n_tok, n_blk, w.table,
+                                                                                        w.lens);
+  KVQ_TRY(cudaSuccess);
   // reference
   KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qf, w.kf, w.vf, w.o_ref, w.part, s));
   out_err(w.o_ref, nullptr, y_ref);
   // candidate: keys centred and rotated by R_K, values rotated by R_V, both INT2
   KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, k, dtype, mu, rot_k, w.xk_hi, w.xk_lo, s));
   KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, v, dtype, nullptr, rot_v, w.xv_hi, w.xv_lo, s));
-  KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.qf, rot_k, w.qr, false, s));
-  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clip_k, w.kq, s));
-  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clip_v, w.vq, s));
-  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qr, w.kq, w.vq, w.o_rot, w.part, s));
+  KVQ_TRY(launch_quant_to_pool(n_tok, n_kv_heads, w.xk_hi, w.xk_lo, clip_k, 0, w.pool, s));
+  KVQ_TRY(launch_quant_to_pool(n_tok, n_kv_heads, w.xv_hi, w.xv_lo, clip_v, 1, w.pool, s));
+  KVQ_TRY(launch_decode(pg, hq, n_qpos, w.qf, KVQ_F32, w.lens, n_tok, w.table, rot_k, w.pool, w.n_ctas, w.dws,
+                        w.o_rot, err, s));
   KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.o_rot, rot_v, w.o_un, true, s));  // o~ (unrotated)
   out_err(w.o_un, w.o_ref, e_tot);
+  KVQ_TRY(launch_rotate_heads(n_qpos, hq, gqa, w.qf, rot_k, w.qr, false, s));
+  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clip_k, w.kq, s));
   // keys only: the candidate's weights p~ with the exact values (unrotated basis)
   KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qr, w.kq, w.vf, w.o_rot, w.part, s));
   out_err(w.o_rot, w.o_ref, e_key);
@@ -680,9 +690,10 @@ cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, i
   // plain per-group INT2: identity rotations, no centring, the same clips
   KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, k, dtype, nullptr, ident, w.xk_hi, w.xk_lo, s));
   KVQ_TRY(launch_rotate_df(n_tok, n_kv_heads, v, dtype, nullptr, ident, w.xv_hi, w.xv_lo, s));
-  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xk_hi, w.xk_lo, clip_k, w.kq, s));
-  KVQ_TRY(launch_quant_dequant(n_tok * n_kv_heads, w.xv_hi, w.xv_lo, clip_v, w.vq, s));
-  KVQ_TRY(launch_calib_attn(n_tok, n_qpos, n_kv_heads, gqa, w.qf, w.kq, w.vq, w.o_rot, w.part, s));
+  KVQ_TRY(launch_quant_to_pool(n_tok, n_kv_heads, w.xk_hi, w.xk_lo, clip_k, 0, w.pool, s));
+  KVQ_TRY(launch_quant_to_pool(n_tok, n_kv_heads, w.xv_hi, w.xv_lo, clip_v, 1, w.pool, s));
+  KVQ_TRY(launch_decode(pg, hq, n_qpos, w.qf, KVQ_F32, w.lens, n_tok, w.table, ident, w.pool, w.n_ctas, w.dws,
+                        w.o_rot, err, s));
   out_err(w.o_rot, w.o_ref, e_naive);
   group_sum_kernel<<<blocks(5 * n_kv_heads), 256, 0, s>>>(5, n_kv_heads, gqa, w.qsum, out);
   return cudaGetLastError();

@@ -191,7 +191,7 @@ size_t report_workspace_bytes(int n_tok, int n_qpos, int n_kv_heads, int gqa);
 cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model, const void* q,
                                const void* k, const void* v, int dtype, const void* w_o, int w_dtype, RotDev rot_k,
                                RotDev rot_v, const float* mu, float clip_k, float clip_v, double* out, void* ws,
-                               cudaStream_t s);
+                               unsigned* err, cudaStream_t s);
 cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_model,
                          const void* q, const void* k, const void* v, int dtype, const void* w_o,
                          int w_dtype, int n_cand, const kvq_rot* cand, int n_clip,
