@@ -357,40 +357,63 @@ static cudaError_t launch_calib_attn(int n_tok, int n_qpos, int n_kv_heads, int 
 
 // Gram matrices G_g = W_g^T W_g for head groups g of gd = cols columns each.
 // w: [d_model][n_groups * gd]; gram: [n_groups][gd][gd].  32x32 tiles.
+// Gram blocks G_g = W_g^T W_g (gd x gd) of the W_O columns of each scored group g:
+// a block takes a 64 x 64 tile (thread: 4 x 4), K = d_model in chunks of 32 rows of W
+// staged in shared memory as fp32.  grid = (gd / 64, gd / 64, n_groups), block = 256.
+constexpr int GR_T = 64, GR_K = 32;
 __global__ void __launch_bounds__(256) gram_kernel(int d_model, int total_cols, int gd,
                                                    const void* __restrict__ w, int w_dtype,
                                                    float* __restrict__ gram) {
-  __shared__ float A[32][33], B[32][33];
+  __shared__ __align__(16) float A[GR_K][GR_T + 4], B[GR_K][GR_T + 4];
   const int grp = blockIdx.z;
-  const int a0 = blockIdx.y * 32, b0 = blockIdx.x * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // ty 0..7
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-  const size_t col0 = (size_t)grp * gd;
-  for (int n0 = 0; n0 < d_model; n0 += 32) {
-    for (int i = ty; i < 32; i += 8) {
-      const int n = n0 + i;
-      A[i][tx] = n < d_model ? load1(w, (size_t)n * total_cols + col0 + a0 + tx, w_dtype) : 0.f;
-      B[i][tx] = n < d_model ? load1(w, (size_t)n * total_cols + col0 + b0 + tx, w_dtype) : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 8
-    for (int i = 0; i < 32; ++i) {
-      const float bv = B[i][tx];
+  const int a0 = blockIdx.y * GR_T, b0 = blockIdx.x * GR_T;
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  float acc[4][4];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) acc[r] = fmaf(A[i][ty + 8 * r], bv, acc[r]);
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
+  const size_t col0 = (size_t)grp * gd;
+  // the next chunk's elements are loaded into registers while the current one is multiplied
+  // thread: row tid / 8 of the chunk, columns 8 (tid % 8) .. + 7 of both tiles
+  static_assert(GR_K * GR_T == 256 * 8, "one row segment of 8 columns per thread and tile");
+  const int fr = tid >> 3, fc = 8 * (tid & 7);
+  float4 na[2], nb[2];
+  auto fetch = [&](int n0) {
+    const int n = n0 + fr;
+    const size_t row = (size_t)n * total_cols + col0;
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+    na[0] = n < d_model ? load4(w, row + a0 + fc, w_dtype) : z;
+    na[1] = n < d_model ? load4(w, row + a0 + fc + 4, w_dtype) : z;
+    nb[0] = n < d_model ? load4(w, row + b0 + fc, w_dtype) : z;
+    nb[1] = n < d_model ? load4(w, row + b0 + fc + 4, w_dtype) : z;
+  };
+  fetch(0);
+  for (int n0 = 0; n0 < d_model; n0 += GR_K) {
+    *reinterpret_cast<float4*>(&A[fr][fc]) = na[0];
+    *reinterpret_cast<float4*>(&A[fr][fc + 4]) = na[1];
+    *reinterpret_cast<float4*>(&B[fr][fc]) = nb[0];
+    *reinterpret_cast<float4*>(&B[fr][fc + 4]) = nb[1];
+    __syncthreads();
+    if (n0 + GR_K < d_model) fetch(n0 + GR_K);
+#pragma unroll 8
+    for (int r = 0; r < GR_K; ++r) {
+      const float4 av = *reinterpret_cast<const float4*>(&A[r][4 * ty]);
+      const float4 bv = *reinterpret_cast<const float4*>(&B[r][4 * tx]);
+      const float ar[4] = {av.x, av.y, av.z, av.w}, br[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(ar[i], br[j], acc[i][j]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int r = 0; r < 4; ++r)
-    gram[((size_t)grp * gd + a0 + ty + 8 * r) * gd + b0 + tx] = acc[r];
+  for (int i = 0; i < 4; ++i)
+    *reinterpret_cast<float4*>(gram + ((size_t)grp * gd + a0 + 4 * ty + i) * gd + b0 + 4 * tx) =
+        make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
 }
 
-// sum over positions p of du_p G du_p^T (du = a - b, or a when b == NULL) as
-// trace(G M) with M = sum_p du_p^T du_p: block (ri, ci, group) forms the 32 x 32
-// tile of M over all positions and adds G o M over the tile in double ->
-// part[group][ri * nt + ci]; gram_reduce_kernel adds the tiles in a fixed order.
-// grid = (gd / 32, gd / 32, n_groups), block = 256.
 // trace(M du^T du) = sum_p du_p M du_p^T for one group (M = W_h^T W_h symmetric), as
 // sum_{p,c} du[p][c] Z[p][c] with Z = du M: a block takes 64 columns of Z and a K range
 // of `kspan` channels (both linear in Z, so ranges add), streams du[:, k] and M[k][c] through
@@ -552,7 +575,7 @@ cudaError_t launch_calib(int n_tok, int n_qpos, int n_kv_heads, int gqa, int d_m
   // ||du W^T||^2: directly when d_model <= gd, else through the group's Gram matrix
   const bool direct = d_model <= gd;
   if (!direct)
-    gram_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype, w.gram);
+    gram_kernel<<<dim3(gd / GR_T, gd / GR_T, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype, w.gram);
   zero_f64_kernel<<<1, 256, 0, s>>>(ref, n_groups);
   const int n_out = n_cand * n_clip * n_groups;
   zero_f64_kernel<<<(n_out + 255) / 256, 256, 0, s>>>(nmse, n_out);
@@ -644,7 +667,8 @@ cudaError_t launch_head_report(int n_tok, int n_qpos, int n_kv_heads, int gqa, i
   zero_f64_kernel<<<1, 256, 0, s>>>(w.qsum, 5 * hq);
   KVQ_TRY(cudaSuccess);
   const bool direct = d_model <= gd;
-  if (!direct) gram_kernel<<<dim3(gd / 32, gd / 32, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype, w.gram);
+  if (!direct)
+    gram_kernel<<<dim3(gd / GR_T, gd / GR_T, n_groups), 256, 0, s>>>(d_model, hq * D, gd, w_o, w_dtype, w.gram);
   auto out_err = [&](const float* a, const float* b, double* dst) {
     if (direct)
       proj_err_kernel<<<dim3(n_qpos, n_groups), 256, (size_t)gd * sizeof(float), s>>>(n_qpos, n_groups, gd, d_model,
