@@ -213,3 +213,21 @@ def test_dense_keys_hadamard_values_bulk_append():
     stats = gu.compare_codes(pool.cpu().numpy(), ora_pool, case.n_kv_heads, 8, case.block_table, g.lengths, encs,
                              (case.clip_k, case.clip_v), label="dense K / Hadamard V")
     assert stats["mismatch"] == 0 and stats["meta_mismatch_groups"] == 0, stats
+
+
+@pytest.mark.parametrize("dtype,lengths", [("f32", [5000, 4999]), ("bf16", [3000, 2900, 3100])])
+def test_dense_bulk_append_many_units_per_cta(dtype, lengths):
+    """More (role, head, 128-token tile) units than SMs: every persistent CTA of the
+    tensor-core cache write takes several units, restages R when the head changes and
+    (bf16) copies the next tile's rows while the current one is decided; codes and meta
+    equal the oracle's."""
+    case = W.decode_case(17, lengths, 8, 4, 256, "dense", dtype, page_tokens=16, clip_k=0.9, clip_v=0.96,
+                         spare_blocks=2, n_cal=256)
+    g = gu.GpuCase(case)
+    pool = g.new_pool()
+    g.gpu_append_all(pool)
+    g.kvq.kvq_device_check()
+    ora_pool, encs = g.oracle_pool()
+    stats = gu.compare_codes(pool.cpu().numpy(), ora_pool, case.n_kv_heads, 16, case.block_table, g.lengths, encs,
+                             (case.clip_k, case.clip_v), label=f"dense {dtype} many units")
+    assert stats["mismatch"] == 0 and stats["meta_mismatch_groups"] == 0, stats
